@@ -1,0 +1,374 @@
+"""Plain float64 definitions of every step on the MHLA forward path.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): nothing on the product
+path imports this module.
+
+Conventions
+-----------
+* ``q, k, v``: arrays ``[B, H, N, d]`` (any float dtype; widened to float64).
+* ``mixing``: ``[H, M, M]``; row ``i`` is the query block, column ``b`` the
+  KV block (MHLA paper §4.1 "multi-head mixing" and §4.2, where entry (i, j)
+  is the affinity of query block i to the summary of block j).
+* blocks are contiguous token ranges of ``block_size`` tokens,
+  ``M = N / block_size`` (MHLA paper §4.1 splits the sequence into M
+  non-overlapping blocks; the contiguous 1-D reading is the one this library
+  implements).
+* ``eps`` is added to the denominator after mixing, as the Linear Attention
+  notes do in both of their code examples (§四 and §五).
+
+Every function is a direct transcription of the formula it cites, written
+for a reader to check by eye; there is no blocking, fusion or reordering
+beyond what that formula states.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+# What pins each function to something other than itself
+# (tests/test_oracle_pins.py holds the pins).
+PIN_STATUS = {
+    "phi": "closed-form values at 0, +1, -1, continuity, positivity",
+    "mhla_block_form": "token-level expansion (brute N x N), closed form at Q=K=0, "
+                       "identity / all-ones / row-scaled mixing, token permutation",
+    "mhla_token_expansion": "closed form at Q=K=0, hand-derived golden fixture, rank bounds",
+    "mhla_attention_matrix": "rank <= d for all-ones mixing, generic rank = sum_b min(n_b, d)",
+    "global_linear_attention": "equals MHLA with M=1 and with all-ones mixing; golden fixture",
+    "causal_recurrent": "hand-derived golden fixture; equals masked brute force",
+    "causal_chunked": "equals recurrence and brute force for C in {1, 16, 64, N} and ragged C",
+    "causal_bruteforce": "hand-derived golden fixture; last row equals non-causal global LA",
+    "causal_mhla_chunked": "equals its masked brute force; all-ones mixing equals causal LA",
+    "causal_mhla_bruteforce": "all-ones mixing equals causal_bruteforce; golden fixture",
+    "decode_steps": "equals rows of the causal forward on prefix+steps; final state = sum phi(k) v^T",
+    "rala_forward": "brute form; closed forms at Q=0 and K=0; softmax weights sum to 1",
+    "rala_bruteforce": "closed forms at Q=0 and K=0; hand-derived golden fixture",
+    "numerical_rank": "diagonal matrices of known rank",
+}
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def phi(x):
+    """Feature map phi(x) = ELU(x) + 1, i.e. x + 1 for x > 0 and exp(x) otherwise.
+
+    Linear Attention notes §二 (first listed kernel choice, "ELU(x)+1") and
+    its code examples; RALA notes "核函数选择" (kernel choice Elu(.)+1).  ELU
+    with alpha = 1, so both branches meet at phi(0) = 1.
+    """
+    x = _f64(x)
+    return np.where(x > 0.0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def block_of(n_tokens: int, block_size: int) -> np.ndarray:
+    """b(t): index of the contiguous block holding token t (MHLA paper §4.2)."""
+    return np.arange(n_tokens) // block_size
+
+
+def _check_blocks(n, block_size, mixing):
+    if block_size <= 0 or n % block_size != 0:
+        raise ValueError("N must be a positive multiple of block_size")
+    m = n // block_size
+    mixing = _f64(mixing)
+    if mixing.shape[-2:] != (m, m):
+        raise ValueError(f"mixing must be [H, {m}, {m}]")
+    return m, mixing
+
+
+def mhla_block_form(q, k, v, mixing, block_size, eps=1e-6):
+    """MHLA forward in its block form.  Returns ``(Y, den)``.
+
+    MHLA paper §4.1:
+      * local KV summary and normaliser of block b:
+        S_b = sum_{j in b} phi(K_j) V_j^T  (d x d),  z_b = sum_{j in b} phi(K_j);
+      * multi-head mixing for query block i:
+        S~_i = sum_b m_{i,b} S_b,  z~_i = sum_b m_{i,b} z_b;
+      * output for a query q in block i:
+        o = phi(q)^T S~_i / (phi(q)^T z~_i)   (+ eps, Linear Attention notes §五).
+
+    ``den`` is phi(q)^T z~_i + eps for every token, shape [B, H, N].
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    m, mix = _check_blocks(n, block_size, mixing)
+    kb = phi(k).reshape(bsz, nh, m, block_size, d)
+    vb = v.reshape(bsz, nh, m, block_size, d)
+    # S_b[c, e] = sum_j phi(k_j)_c v_j,e ; z_b[c] = sum_j phi(k_j)_c
+    s = np.einsum("bhmjc,bhmje->bhmce", kb, vb)
+    z = kb.sum(axis=3)
+    # S~_i = sum_b m_{i,b} S_b ; z~_i = sum_b m_{i,b} z_b  (one matrix per head)
+    s_mix = np.einsum("hib,zhbce->zhice", mix, s)
+    z_mix = np.einsum("hib,zhbc->zhic", mix, z)
+    qb = phi(q).reshape(bsz, nh, m, block_size, d)
+    num = np.einsum("bhitc,bhice->bhite", qb, s_mix)
+    den = np.einsum("bhitc,bhic->bhit", qb, z_mix) + eps
+    y = num / den[..., None]
+    return y.reshape(bsz, nh, n, d), den.reshape(bsz, nh, n)
+
+
+def mhla_attention_matrix(q1, k1, mixing1, block_size):
+    """Explicit MHLA attention matrix of one head, [N, N].
+
+    MHLA paper §4.2 (token-level effect, eq. 5) and §4.3: the score of query
+    t on key s is m_{b(t), b(s)} * phi(q_t)^T phi(k_s).  ``q1, k1``: [N, d];
+    ``mixing1``: [M, M].
+    """
+    q1, k1 = _f64(q1), _f64(k1)
+    n = q1.shape[0]
+    _, mix = _check_blocks(n, block_size, mixing1)
+    bt = block_of(n, block_size)
+    kernel = phi(q1) @ phi(k1).T          # phi(q_t)^T phi(k_s)
+    return mix[bt[:, None], bt[None, :]] * kernel
+
+
+def mhla_token_expansion(q, k, v, mixing, block_size, eps=1e-6):
+    """MHLA forward written token by token (brute force, O(N^2)).  Returns ``(Y, den)``.
+
+    MHLA paper §4.2 eq. 5 and App. B: phi(q)^T S~_i = sum_t m_{i,b(t)}
+    (phi(q)^T phi(K_t)) V_t^T, and the normaliser is the same sum without
+    V_t.  For every (batch, head) this builds the N x N score matrix A and
+    returns Y_t = sum_s A_ts v_s / (sum_s A_ts + eps).  Small inputs only.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    _, mix = _check_blocks(n, block_size, mixing)
+    y = np.empty_like(v)
+    den = np.empty((bsz, nh, n))
+    for b in range(bsz):
+        for h in range(nh):
+            a = mhla_attention_matrix(q[b, h], k[b, h], mix[h], block_size)
+            den[b, h] = a.sum(axis=1) + eps
+            y[b, h] = (a @ v[b, h]) / den[b, h][:, None]
+    return y, den
+
+
+def global_linear_attention(q, k, v, eps=1e-6):
+    """Non-causal global linear attention.  Returns ``(Y, den)``.
+
+    Linear Attention notes §三 and §五 (parallel form): KV = phi(K)^T V
+    (d x d), z = sum_j phi(K_j), Y = phi(Q) KV / (phi(Q) z + eps).  MHLA paper
+    §3.1 gives the same G and z as the single global summary.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    qf, kf = phi(q), phi(k)
+    kv = np.einsum("...jc,...je->...ce", kf, v)
+    z = kf.sum(axis=-2)
+    num = np.einsum("...tc,...ce->...te", qf, kv)
+    den = np.einsum("...tc,...c->...t", qf, z) + eps
+    return num / den[..., None], den
+
+
+def causal_recurrent(q, k, v, eps=1e-6):
+    """Causal linear attention by its recurrence.  Returns ``(Y, den)``.
+
+    Linear Attention notes §四: S_t = S_{t-1} + phi(k_t) v_t^T,
+    z_t = z_{t-1} + phi(k_t), out_t = phi(q_t)^T S_t / (phi(q_t)^T z_t + eps);
+    the state is updated before it is read, so token t sees itself.
+    Works on any leading batch dimensions; loops over tokens in Python.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    *lead, n, d = q.shape
+    s = np.zeros((*lead, d, d))
+    z = np.zeros((*lead, d))
+    y = np.empty_like(v)
+    den = np.empty((*lead, n))
+    for t in range(n):
+        qt, kt, vt = phi(q[..., t, :]), phi(k[..., t, :]), v[..., t, :]
+        s = s + kt[..., :, None] * vt[..., None, :]
+        z = z + kt
+        num = np.einsum("...c,...ce->...e", qt, s)
+        dn = np.einsum("...c,...c->...", qt, z) + eps
+        y[..., t, :] = num / dn[..., None]
+        den[..., t] = dn
+    return y, den
+
+
+def causal_bruteforce(q, k, v, eps=1e-6):
+    """Causal linear attention from the explicit masked N x N matrix.  Returns ``(Y, den)``.
+
+    Linear Attention notes §三 (out_i = sum_j phi(q_i)^T phi(k_j) v_j over the
+    normaliser) with the causal mask of the Attention tutorial ("Mask"): only
+    the strictly upper triangle (future keys) is removed, the diagonal stays.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n = q.shape[-2]
+    a = np.einsum("...tc,...sc->...ts", phi(q), phi(k))
+    a = a * np.tril(np.ones((n, n)))
+    den = a.sum(axis=-1) + eps
+    return np.einsum("...ts,...se->...te", a, v) / den[..., None], den
+
+
+def causal_chunked(q, k, v, chunk, eps=1e-6):
+    """Chunkwise-parallel causal linear attention.  Returns ``(Y, den)``.
+
+    MHLA paper App. C: for chunk i, the output is the inter-chunk term
+    phi(Q_i) S^global_{i-1} plus the intra-chunk term (phi(Q_i) phi(K_i)^T) V_i,
+    then S^global_i = S^global_{i-1} + S_i.  The intra-chunk scores keep the
+    lower triangle including the diagonal (Attention tutorial "Mask"), and the
+    normaliser is built the same way with eps (Linear Attention notes §四).
+    The last chunk may be shorter than ``chunk``.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    *lead, n, d = q.shape
+    if chunk <= 0:
+        raise ValueError("chunk must be positive")
+    p = np.zeros((*lead, d, d))     # S^global of all previous chunks
+    zeta = np.zeros((*lead, d))     # sum of phi(K) over all previous chunks
+    y = np.empty_like(v)
+    den = np.empty((*lead, n))
+    for c0 in range(0, n, chunk):
+        c1 = min(c0 + chunk, n)
+        qc, kc, vc = phi(q[..., c0:c1, :]), phi(k[..., c0:c1, :]), v[..., c0:c1, :]
+        length = c1 - c0
+        intra = np.einsum("...tc,...sc->...ts", qc, kc) * np.tril(np.ones((length, length)))
+        num = np.einsum("...tc,...ce->...te", qc, p) + np.einsum("...ts,...se->...te", intra, vc)
+        dn = np.einsum("...tc,...c->...t", qc, zeta) + intra.sum(axis=-1) + eps
+        y[..., c0:c1, :] = num / dn[..., None]
+        den[..., c0:c1] = dn
+        p = p + np.einsum("...sc,...se->...ce", kc, vc)
+        zeta = zeta + kc.sum(axis=-2)
+    return y, den
+
+
+def causal_mhla_chunked(q, k, v, mixing, block_size, eps=1e-6):
+    """Causal MHLA with a lower-triangular mixing matrix, chunk = block.  Returns ``(Y, den)``.
+
+    MHLA paper §4.2 ("chunkwise-parallel form": mixed prefix summary
+    S~_i = sum_{b<=i} m_{i,b} S_b) and App. C.  App. C's printed formula is
+    garbled; the reading implemented is
+      H_i = phi(Q_i) (sum_{b<i} m_{i,b} S_b) + m_{i,i} tril(phi(Q_i) phi(K_i)^T) V_i
+    with the normaliser built the same way plus eps.  Entries of ``mixing``
+    above the diagonal are ignored (the paper masks them).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    m, mix = _check_blocks(n, block_size, mixing)
+    qb = phi(q).reshape(bsz, nh, m, block_size, d)
+    kb = phi(k).reshape(bsz, nh, m, block_size, d)
+    vb = v.reshape(bsz, nh, m, block_size, d)
+    s = np.einsum("bhmjc,bhmje->bhmce", kb, vb)
+    z = kb.sum(axis=3)
+    tri = np.tril(np.ones((block_size, block_size)))
+    y = np.empty((bsz, nh, m, block_size, d))
+    den = np.empty((bsz, nh, m, block_size))
+    for i in range(m):
+        w_prev = mix[:, i, :i]                                   # [H, i]
+        s_prev = np.einsum("hb,zhbce->zhce", w_prev, s[:, :, :i])
+        z_prev = np.einsum("hb,zhbc->zhc", w_prev, z[:, :, :i])
+        intra = np.einsum("zhtc,zhsc->zhts", qb[:, :, i], kb[:, :, i]) * tri
+        intra = intra * mix[:, i, i][None, :, None, None]
+        num = np.einsum("zhtc,zhce->zhte", qb[:, :, i], s_prev) + \
+            np.einsum("zhts,zhse->zhte", intra, vb[:, :, i])
+        dn = np.einsum("zhtc,zhc->zht", qb[:, :, i], z_prev) + intra.sum(axis=-1) + eps
+        y[:, :, i] = num / dn[..., None]
+        den[:, :, i] = dn
+    return y.reshape(bsz, nh, n, d), den.reshape(bsz, nh, n)
+
+
+def causal_mhla_bruteforce(q, k, v, mixing, block_size, eps=1e-6):
+    """Causal MHLA from the explicit masked, mixed N x N score matrix.  Returns ``(Y, den)``.
+
+    Score of query t on key s: m_{b(t), b(s)} phi(q_t)^T phi(k_s) for s <= t
+    (MHLA paper §4.2 eq. 5 restricted by the causal mask of the Attention
+    tutorial), zero otherwise.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    _, mix = _check_blocks(n, block_size, mixing)
+    tri = np.tril(np.ones((n, n)))
+    y = np.empty_like(v)
+    den = np.empty((bsz, nh, n))
+    for b in range(bsz):
+        for h in range(nh):
+            a = mhla_attention_matrix(q[b, h], k[b, h], mix[h], block_size) * tri
+            den[b, h] = a.sum(axis=1) + eps
+            y[b, h] = (a @ v[b, h]) / den[b, h][:, None]
+    return y, den
+
+
+def decode_steps(s0, z0, qs, ks, vs, eps=1e-6):
+    """Recurrent decode: T single-token steps from state (S, z).
+
+    Linear Attention notes §四 (and §八: the state is a fixed-size d x d
+    "KV cache"): per step S <- S + phi(k) v^T, z <- z + phi(k), then
+    out = phi(q)^T S / (phi(q)^T z + eps).  ``s0``: [..., d, d] with
+    S[c, e] = sum phi(k)_c v_e; ``z0``: [..., d]; ``qs, ks, vs``: [T, ..., d].
+    Returns ``(outs [T, ..., d], dens [T, ...], S_T, z_T)``.
+    """
+    s, z = _f64(s0).copy(), _f64(z0).copy()
+    qs, ks, vs = _f64(qs), _f64(ks), _f64(vs)
+    outs = np.empty_like(vs)
+    dens = np.empty(vs.shape[:-1])
+    for t in range(qs.shape[0]):
+        qt, kt = phi(qs[t]), phi(ks[t])
+        s = s + kt[..., :, None] * vs[t][..., None, :]
+        z = z + kt
+        dn = np.einsum("...c,...c->...", qt, z) + eps
+        outs[t] = np.einsum("...c,...ce->...e", qt, s) / dn[..., None]
+        dens[t] = dn
+    return outs, dens, s, z
+
+
+def _rala_weights(q1, k1):
+    """Softmax weights alpha_j of one (batch, head): RALA notes, KV buffer rank augmentation.
+
+    Q_g is the mean of the raw queries over all tokens; alpha = softmax over
+    tokens j of Q_g^T phi(K_j).  The maximum is subtracted before exp, which
+    leaves alpha unchanged in exact arithmetic.
+    """
+    q_g = q1.mean(axis=0)
+    logits = phi(k1) @ q_g
+    e = np.exp(logits - logits.max())
+    return e / e.sum()
+
+
+def rala_forward(q, k, v, x, w):
+    """Rank-augmented linear attention (RALA) forward.  Returns Y [B, H, N, d].
+
+    RALA notes, "关键设计" (key designs):
+      1. KV buffer rank augmentation: Q_g = mean_i Q_i,
+         alpha_j = softmax_j(Q_g^T phi(K_j)), B = sum_j alpha_j phi(K_j)^T V_j;
+      2. output rank augmentation: Y_i = phi_X(X_i) * (phi(Q_i) B) (Hadamard
+         product), with phi_X the linear map X W; ``x``: [B, N, Cx] shared by
+         all heads of a sample, ``w``: [Cx, d] shared by all heads.
+    No normaliser and no eps appear in the notes' output formula.
+    """
+    q, k, v, x, w = _f64(q), _f64(k), _f64(v), _f64(x), _f64(w)
+    bsz, nh, n, d = q.shape
+    y = np.empty_like(v)
+    for b in range(bsz):
+        gate = x[b] @ w                                   # [N, d]
+        for h in range(nh):
+            alpha = _rala_weights(q[b, h], k[b, h])
+            buf = np.einsum("j,jc,je->ce", alpha, phi(k[b, h]), v[b, h])
+            y[b, h] = gate * (phi(q[b, h]) @ buf)
+    return y
+
+
+def rala_bruteforce(q, k, v, x, w):
+    """RALA written token by token: Y_t = (X W)_t * sum_s alpha_s (phi(q_t)^T phi(k_s)) v_s.
+
+    Same definitions as ``rala_forward`` (RALA notes, key designs 1 and 2)
+    with the d x d buffer B expanded into its token sum.  Small inputs only.
+    """
+    q, k, v, x, w = _f64(q), _f64(k), _f64(v), _f64(x), _f64(w)
+    bsz, nh, n, d = q.shape
+    y = np.empty_like(v)
+    for b in range(bsz):
+        gate = x[b] @ w
+        for h in range(nh):
+            alpha = _rala_weights(q[b, h], k[b, h])
+            scores = (phi(q[b, h]) @ phi(k[b, h]).T) * alpha[None, :]
+            y[b, h] = gate * (scores @ v[b, h])
+    return y
+
+
+def numerical_rank(a, rtol=None):
+    """Numerical rank: singular values above max(shape) * eps * sigma_max (default tolerance)."""
+    a = _f64(a)
+    sv = np.linalg.svd(a, compute_uv=False)
+    if sv.size == 0 or sv[0] == 0.0:
+        return 0
+    tol = (max(a.shape) * np.finfo(np.float64).eps if rtol is None else rtol) * sv[0]
+    return int((sv > tol).sum())

@@ -1,0 +1,312 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each test fixes an oracle function against a hand-derived fixture, a closed
+form, an invariant stated by the source pages, or a second, differently
+written definition (block form against token expansion, recurrence against
+chunked form against masked brute force).  These run on the CPU only.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import WORKLOADS, make_mhla_inputs, normal, uniform
+
+TOL = 1e-12
+
+
+def close(a, b, tol=TOL):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    scale = max(1.0, float(np.max(np.abs(b))) if b.size else 1.0)
+    return a.shape == b.shape and float(np.max(np.abs(a - b))) <= tol * scale
+
+
+def load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+def as4(x):
+    """[N, d] fixture array -> [1, 1, N, d]."""
+    return np.asarray(x, dtype=np.float64)[None, None]
+
+
+# ---------------------------------------------------------------- phi
+def test_phi_closed_forms():
+    assert oracle.phi(0.0) == 1.0
+    assert oracle.phi(1.0) == 2.0
+    assert oracle.phi(2.5) == 3.5
+    assert math.isclose(oracle.phi(-1.0), math.exp(-1.0), rel_tol=0, abs_tol=1e-16)
+    assert math.isclose(oracle.phi(-math.log(2.0)), 0.5, rel_tol=1e-15)
+    assert oracle.phi(-800.0) == 0.0
+    # continuity at 0 and positivity everywhere (a positive feature map, Linear Attention notes §二)
+    assert abs(oracle.phi(1e-12) - oracle.phi(-1e-12)) < 1e-11
+    x = np.linspace(-30, 30, 10001)
+    assert np.all(oracle.phi(x) > 0)
+    assert np.all(np.diff(oracle.phi(x)) > 0)
+
+
+# ------------------------------------------------------- golden fixtures
+def test_golden_linear_attention(golden_dir):
+    for name in ("linear_attention_d1.json", "linear_attention_d2_eps.json"):
+        fx = load(golden_dir, name)
+        q, k, v, eps = as4(fx["q"]), as4(fx["k"]), as4(fx["v"]), fx["eps"]
+        n = q.shape[2]
+        y, den = oracle.global_linear_attention(q, k, v, eps)
+        assert close(y[0, 0], fx["noncausal_y"]) and close(den[0, 0], fx["noncausal_den"]), name
+        one = np.ones((1, 1, 1))
+        y, den = oracle.mhla_block_form(q, k, v, one, n, eps)
+        assert close(y[0, 0], fx["noncausal_y"]) and close(den[0, 0], fx["noncausal_den"]), name
+        y, den = oracle.mhla_token_expansion(q, k, v, one, n, eps)
+        assert close(y[0, 0], fx["noncausal_y"]) and close(den[0, 0], fx["noncausal_den"]), name
+        for fn in (oracle.causal_recurrent, oracle.causal_bruteforce):
+            y, den = fn(q, k, v, eps)
+            assert close(y[0, 0], fx["causal_y"]) and close(den[0, 0], fx["causal_den"]), (name, fn)
+        y, den = oracle.causal_chunked(q, k, v, 1, eps)
+        assert close(y[0, 0], fx["causal_y"]) and close(den[0, 0], fx["causal_den"]), name
+        # decode: one prefix token, then one step
+        s0 = oracle.phi(k[0, 0, 0])[:, None] * v[0, 0, 0][None, :]
+        outs, dens, _, _ = oracle.decode_steps(s0, oracle.phi(k[0, 0, 0]), q[0, 0, 1:], k[0, 0, 1:],
+                                               v[0, 0, 1:], eps)
+        assert close(outs[0], fx["causal_y"][1]) and close(dens[0], fx["causal_den"][1]), name
+
+
+def test_golden_mhla_two_blocks(golden_dir):
+    fx = load(golden_dir, "mhla_two_blocks_d1.json")
+    q, k, v, eps = as4(fx["q"]), as4(fx["k"]), as4(fx["v"]), fx["eps"]
+    mix = np.asarray(fx["mixing"])[None]
+    for fn in (oracle.mhla_block_form, oracle.mhla_token_expansion):
+        y, den = fn(q, k, v, mix, fx["block_size"], eps)
+        assert close(y[0, 0], fx["noncausal_y"]) and close(den[0, 0], fx["noncausal_den"]), fn
+    for fn in (oracle.causal_mhla_chunked, oracle.causal_mhla_bruteforce):
+        y, den = fn(q, k, v, mix, fx["block_size"], eps)
+        assert close(y[0, 0], fx["causal_y"]) and close(den[0, 0], fx["causal_den"]), fn
+
+
+def test_golden_rala(golden_dir):
+    fx = load(golden_dir, "rala_d1.json")
+    q, k, v = as4(fx["q"]), as4(fx["k"]), as4(fx["v"])
+    x, w = np.asarray(fx["x"])[None], np.asarray(fx["w"])
+    for fn in (oracle.rala_forward, oracle.rala_bruteforce):
+        assert close(fn(q, k, v, x, w)[0, 0], fx["y"]), fn
+
+
+# ------------------------------------------- two definitions of MHLA agree
+@pytest.fixture(scope="module")
+def tiny():
+    wl = WORKLOADS["tiny"]
+    return wl, make_mhla_inputs(wl)
+
+
+def test_block_form_equals_token_expansion_tiny(tiny):
+    wl, x = tiny
+    y1, d1 = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block, 1e-6)
+    y2, d2 = oracle.mhla_token_expansion(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block, 1e-6)
+    assert close(y1, y2, 1e-11) and close(d1, d2, 1e-11)
+    # the tiny workload's mixing is genuinely asymmetric, so a transposed m is caught here
+    assert np.max(np.abs(x["mixing64"][0] - x["mixing64"][0].T)) > 0.05
+
+
+def test_closed_form_constant_features():
+    """Q = K = 0 gives phi = 1, so every score is d and Y_t is a mixed block mean of V.
+
+    Y_t = d * sum_b m_{i,b} sum_{s in b} v_s / (d * sum_b m_{i,b} n_b + eps),
+    written here from block sums of V alone (no phi, S or z).
+    """
+    n, d, nb, eps = 48, 3, 12, 0.37
+    m = n // nb
+    v = normal(7, 1, (1, 2, n, d))
+    mix = uniform(7, 2, (2, m, m)) + 0.1
+    zero = np.zeros_like(v)
+    block_sums = v.reshape(1, 2, m, nb, d).sum(axis=3)            # [1, 2, M, d]
+    expect = np.empty_like(v)
+    for h in range(2):
+        for t in range(n):
+            i = t // nb
+            num = d * (mix[h, i][:, None] * block_sums[0, h]).sum(axis=0)
+            expect[0, h, t] = num / (d * mix[h, i].sum() * nb + eps)
+    for fn in (oracle.mhla_block_form, oracle.mhla_token_expansion):
+        y, _ = fn(zero, zero, v, mix, nb, eps)
+        assert close(y, expect, 1e-12), fn
+
+
+def test_m1_and_all_ones_mixing_equal_global_linear_attention(tiny):
+    wl, x = tiny
+    q, k, v = x["q64"], x["k64"], x["v64"]
+    ref, dref = oracle.global_linear_attention(q, k, v, 1e-6)
+    y, den = oracle.mhla_block_form(q, k, v, np.ones((1, 1, 1)), wl.N, 1e-6)
+    assert close(y, ref, 1e-12) and close(den, dref, 1e-12)
+    y, den = oracle.mhla_block_form(q, k, v, np.ones((1, wl.M, wl.M)), wl.block, 1e-6)
+    assert close(y, ref, 1e-12) and close(den, dref, 1e-12)
+
+
+def test_identity_mixing_is_blockwise_linear_attention(tiny):
+    wl, x = tiny
+    q, k, v = x["q64"], x["k64"], x["v64"]
+    y, _ = oracle.mhla_block_form(q, k, v, np.eye(wl.M)[None], wl.block, 1e-6)
+    for b in range(wl.M):
+        sl = slice(b * wl.block, (b + 1) * wl.block)
+        ref, _ = oracle.global_linear_attention(q[..., sl, :], k[..., sl, :], v[..., sl, :], 1e-6)
+        assert close(y[..., sl, :], ref, 1e-12)
+
+
+def test_row_scaling_of_mixing_leaves_output_unchanged(tiny):
+    """The output is a ratio (MHLA paper §4.1), so scaling row i of m by c > 0 cancels when eps = 0."""
+    wl, x = tiny
+    q, k, v, mix = x["q64"], x["k64"], x["v64"], x["mixing64"]
+    scaled = mix * np.array([0.5, 3.0, 7.0, 0.01])[None, :, None]
+    y1, _ = oracle.mhla_block_form(q, k, v, mix, wl.block, 0.0)
+    y2, _ = oracle.mhla_block_form(q, k, v, scaled, wl.block, 0.0)
+    assert close(y1, y2, 1e-12)
+
+
+def test_permutation_inside_a_block(tiny):
+    """Summaries are sums over a block, so permuting the tokens of block 1 permutes only block 1's outputs."""
+    wl, x = tiny
+    q, k, v, mix = x["q64"], x["k64"], x["v64"], x["mixing64"]
+    perm = np.arange(wl.N)
+    sl = np.arange(wl.block, 2 * wl.block)
+    perm[sl] = sl[::-1]
+    y1, _ = oracle.mhla_block_form(q, k, v, mix, wl.block, 1e-6)
+    y2, _ = oracle.mhla_block_form(q[..., perm, :], k[..., perm, :], v[..., perm, :], mix, wl.block, 1e-6)
+    assert close(y2, y1[..., perm, :], 1e-12)
+
+
+# ------------------------------------------------------------- rank pins
+def test_rank_of_linear_attention_matrix_is_at_most_d(tiny):
+    """MHLA paper §3.2: rank(phi(Q) phi(K)^T) <= d whatever N is."""
+    wl, x = tiny
+    a = oracle.mhla_attention_matrix(x["q64"][0, 0], x["k64"][0, 0], np.ones((wl.M, wl.M)), wl.block)
+    assert a.shape == (wl.N, wl.N)
+    assert oracle.numerical_rank(a) == wl.d
+
+
+def test_rank_of_mhla_matrix_reaches_sum_of_block_ranks(tiny):
+    """MHLA paper §4.3: rank(A_MHLA) <= min(n, sum_b min(n_b, d)), attained for generic mixing."""
+    wl, x = tiny
+    a = oracle.mhla_attention_matrix(x["q64"][0, 0], x["k64"][0, 0], x["mixing64"][0], wl.block)
+    bound = min(wl.N, wl.M * min(wl.block, wl.d))
+    assert bound == 64
+    assert oracle.numerical_rank(a) == bound
+
+
+def test_numerical_rank_on_known_matrices():
+    assert oracle.numerical_rank(np.diag([3.0, 2.0, 1.0, 0.0, 0.0])) == 3
+    assert oracle.numerical_rank(np.zeros((4, 4))) == 0
+    assert oracle.numerical_rank(np.outer(np.arange(1, 6), np.arange(1, 4))) == 1
+
+
+# ----------------------------------------------------------- causal pins
+@pytest.fixture(scope="module")
+def causal_small():
+    q = normal(11, 1, (2, 2, 96, 8), 0.4)
+    k = normal(11, 2, (2, 2, 96, 8), 0.4)
+    v = normal(11, 3, (2, 2, 96, 8))
+    return q, k, v
+
+
+def test_causal_three_ways(causal_small):
+    q, k, v = causal_small
+    ref, dref = oracle.causal_bruteforce(q, k, v, 1e-6)
+    y, den = oracle.causal_recurrent(q, k, v, 1e-6)
+    assert close(y, ref, 1e-11) and close(den, dref, 1e-11)
+    for c in (1, 16, 32, 96, 40):        # 40: ragged last chunk
+        y, den = oracle.causal_chunked(q, k, v, c, 1e-6)
+        assert close(y, ref, 1e-11) and close(den, dref, 1e-11), c
+
+
+def test_causal_last_token_sees_everything(causal_small):
+    q, k, v = causal_small
+    y, den = oracle.causal_recurrent(q, k, v, 1e-6)
+    g, dg = oracle.global_linear_attention(q, k, v, 1e-6)
+    assert close(y[..., -1, :], g[..., -1, :], 1e-12) and close(den[..., -1], dg[..., -1], 1e-12)
+
+
+def test_causal_mhla_chunked_equals_bruteforce(causal_small):
+    q, k, v = causal_small
+    mix = np.tril(uniform(3, 4, (2, 4, 4)) + 0.05)
+    y1, d1 = oracle.causal_mhla_chunked(q, k, v, mix, 24, 1e-6)
+    y2, d2 = oracle.causal_mhla_bruteforce(q, k, v, mix, 24, 1e-6)
+    assert close(y1, y2, 1e-11) and close(d1, d2, 1e-11)
+    # entries above the diagonal are ignored
+    y3, _ = oracle.causal_mhla_chunked(q, k, v, mix + np.triu(np.ones((4, 4)), 1)[None], 24, 1e-6)
+    assert close(y3, y1, 1e-12)
+
+
+def test_causal_mhla_all_ones_is_causal_linear_attention(causal_small):
+    q, k, v = causal_small
+    ref, dref = oracle.causal_recurrent(q, k, v, 1e-6)
+    for fn in (oracle.causal_mhla_chunked, oracle.causal_mhla_bruteforce):
+        y, den = fn(q, k, v, np.ones((2, 4, 4)), 24, 1e-6)
+        assert close(y, ref, 1e-11) and close(den, dref, 1e-11), fn
+
+
+def test_decode_continues_the_causal_sequence(causal_small):
+    """P prefix tokens then T decode steps give rows P..P+T-1 of the causal forward."""
+    q, k, v = causal_small
+    p = 64
+    ref, dref = oracle.causal_bruteforce(q, k, v, 1e-6)
+    kf = oracle.phi(k[..., :p, :])
+    s0 = np.einsum("bhjc,bhje->bhce", kf, v[..., :p, :])
+    z0 = kf.sum(axis=2)
+    steps = lambda x: np.moveaxis(x[..., p:, :], 2, 0)  # noqa: E731  [T, B, H, d]
+    outs, dens, s_t, z_t = oracle.decode_steps(s0, z0, steps(q), steps(k), steps(v), 1e-6)
+    assert close(np.moveaxis(outs, 0, 2), ref[..., p:, :], 1e-11)
+    assert close(np.moveaxis(dens, 0, 2), dref[..., p:], 1e-11)
+    # the final state is the summary of the whole sequence, as the block form computes it
+    whole = oracle.mhla_block_form(q, k, v, np.ones((2, 1, 1)), 96, 1e-6)[1]
+    assert close(np.einsum("bhtc,bhc->bht", oracle.phi(q), z_t) + 1e-6, whole, 1e-12)
+
+
+# ------------------------------------------------------------- RALA pins
+@pytest.fixture(scope="module")
+def rala_small():
+    q = normal(5, 1, (2, 2, 40, 8), 8 ** -0.5)
+    k = normal(5, 2, (2, 2, 40, 8), 8 ** -0.5)
+    v = normal(5, 3, (2, 2, 40, 8), 8 ** -0.5)
+    x = normal(5, 5, (2, 40, 16))
+    w = normal(5, 6, (16, 8), 0.25)
+    return q, k, v, x, w
+
+
+def test_rala_forward_equals_bruteforce(rala_small):
+    q, k, v, x, w = rala_small
+    assert close(oracle.rala_forward(q, k, v, x, w), oracle.rala_bruteforce(q, k, v, x, w), 1e-11)
+
+
+def test_rala_zero_queries_weight_all_keys_equally(rala_small):
+    """Q = 0 gives Q_g = 0, so alpha_j = 1/N and phi(Q) = 1: Y_t = (XW)_t * mean_s (sum_c phi(k_s)_c) v_s."""
+    _, k, v, x, w = rala_small
+    q = np.zeros_like(k)
+    y = oracle.rala_forward(q, k, v, x, w)
+    ksum = oracle.phi(k).sum(axis=-1)                                  # [B, H, N]
+    mean = (ksum[..., None] * v).mean(axis=2)                          # [B, H, d]
+    expect = np.einsum("bnc,cd->bnd", x, w)[:, None] * mean[:, :, None, :]
+    assert close(y, expect, 1e-12)
+
+
+def test_rala_zero_keys_give_mean_value(rala_small):
+    """K = 0 gives phi(K) = 1 and equal logits, so B has every row equal to mean(V)."""
+    q, _, v, x, w = rala_small
+    k = np.zeros_like(q)
+    y = oracle.rala_bruteforce(q, k, v, x, w)
+    qsum = oracle.phi(q).sum(axis=-1)                                  # [B, H, N]
+    expect = np.einsum("bnc,cd->bnd", x, w)[:, None] * (qsum[..., None] * v.mean(axis=2)[:, :, None, :])
+    assert close(y, expect, 1e-12)
+
+
+def test_rala_one_dominant_key(rala_small):
+    """One key far above the rest takes all the softmax weight: B = phi(k*) v*^T, so with Q = 1
+    (phi(Q) = 2) Y_t = (XW)_t * 2 d (1 + 30) v*."""
+    _, _, v, x, w = rala_small
+    q = np.ones_like(v)
+    k = np.zeros_like(v)
+    k[..., 7, :] = 30.0
+    d = v.shape[-1]
+    expect = np.einsum("bnc,cd->bnd", x, w)[:, None] * (2.0 * d * 31.0 * v[..., 7, :])[:, :, None, :]
+    for fn in (oracle.rala_forward, oracle.rala_bruteforce):
+        assert close(fn(q, k, v, x, w), expect, 1e-12), fn
