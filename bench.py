@@ -1,0 +1,566 @@
+"""Benchmark of the MHLA forward hot path on one or more GPUs (one process per GPU).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dit] [--impl ours|reference]
+
+A step is one pass of the hot path over one batch of the workload: one
+``mhla_forward`` (non-causal MHLA: summaries, mixing, output) for the default
+DiT-S/2-like workload (B=8, H=6, N=4096, d=64, M=16 blocks of 256, bf16).
+Inputs are generated on the device from the seeded streams of ``workloads``
+and are resident in HBM before timing starts.  To keep L2 (129 MB on GB300)
+from serving the inputs, the steps rotate over R copies of the inputs and
+outputs whose total exceeds 3x L2.  The K timed steps are captured in CUDA
+graphs and timed with CUDA events on the launching stream; per-step events
+inside the graph give the average kernel duration used for the roofline.
+
+The JSON line also carries ``e2e`` (the same metric through the C ABI with
+the inputs copied from pinned host memory and the output read back every
+step), ``roofline``, ``cpu_baseline`` (the float64 oracle on a bounded sample
+on this host), ``clocks`` (nvidia-smi samples during the timed region) and
+``gpu_launches``.
+
+With ``--impl reference`` the float64 CPU oracle is the reference arm: each
+step runs it on a bounded sample of the same workload (rank 0 only).
+
+Under torchrun (N > 1) each rank runs its own copy of the workload on its own
+GPU (independent problems, no data-path collective, weak scaling); the time
+is the maximum over ranks and ``value`` counts the tokens of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MHLA fwd tokens/s (B*H*N) at N=4096,d=64 bf16; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def workload_bytes(wl):
+    """Algorithmic HBM bytes of one step: every input read once, every output written once."""
+    eb = 2 if wl.dtype == "bf16" else 4
+    t = wl.B * wl.H * wl.N * wl.d * eb
+    if wl.kind in ("mhla", "causal"):
+        mix = wl.H * wl.M * wl.M * 4 if wl.kind == "mhla" else 0
+        return 4 * t + mix
+    if wl.kind == "decode":
+        units = wl.B * wl.H
+        return units * (2 * (wl.d * wl.d + wl.d) * 4 + 4 * wl.d * eb)
+    if wl.kind == "rala":
+        cx = wl.extra["cx"]
+        return 4 * t + wl.B * wl.N * cx * eb + cx * wl.d * eb
+    raise ValueError(wl.kind)
+
+
+def tokens_per_step(wl):
+    return wl.B * wl.H if wl.kind == "decode" else wl.B * wl.H * wl.N
+
+
+def describe(wl):
+    s = f"{wl.name}: B{wl.B} H{wl.H} N{wl.N} d{wl.d} {wl.dtype}"
+    if wl.kind == "mhla":
+        s += f" M{wl.M} (blocks of {wl.block})"
+    elif wl.kind == "causal":
+        s += f" causal chunk {wl.block}"
+    elif wl.kind == "decode":
+        s = f"{wl.name}: {wl.B}x{wl.H} units d{wl.d} {wl.dtype}, one recurrent step, fp32 state"
+    elif wl.kind == "rala":
+        s += f" cx{wl.extra['cx']}"
+    return s
+
+
+def parse_traffic(kernel_name):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged since."""
+    import glob
+    src = source_digest()
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read()
+        m_k = re.search(r"^bench_kernel:\s*(\S+)", text, re.M)
+        m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        m_s = re.search(r"^source_sha256:\s*([0-9a-f]+)", text, re.M)
+        if m_k and m_t and m_s and m_k.group(1) == kernel_name and m_s.group(1) == src:
+            return float(m_t.group(1))
+    return None
+
+
+def source_digest():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "token_level_head_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        used = inside or [r for r in rows if t0 - 0.25 <= r[0] <= t1 + 0.25]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in used for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": reasons, "samples": len(used),
+                "window": "timed region" if inside else "timed region +-0.25 s"}
+
+
+# --------------------------------------------------------------- runners
+class Runner:
+    """Device buffers and the per-step call of one workload (R rotating sets)."""
+
+    def __init__(self, wl, device, l2_bytes):
+        import torch
+        from token_level_head_gb300 import binding
+        import workloads
+
+        self.wl, self.binding, self.torch = wl, binding, torch
+        self.device = device
+        step_bytes = workload_bytes(wl)
+        self.R = max(1, min(16, math.ceil(3 * l2_bytes / step_bytes)))
+        if wl.kind == "decode":
+            self.R = 1  # the recurrent state is carried from one step to the next
+        self.sets = []
+        if wl.kind in ("mhla", "causal"):
+            base = workloads.mhla_device(wl, device)
+            causal = wl.kind == "causal"
+            self.ws = binding.new_workspace(binding.mhla_workspace_bytes(wl.B, wl.H, wl.N, wl.d, wl.block,
+                                                                         int(causal)), device)
+            for r in range(self.R):
+                s = {k: (v if r == 0 else v.clone()) for k, v in base.items()}
+                s["y"] = torch.empty_like(s["q"])
+                self.sets.append(s)
+        elif wl.kind == "rala":
+            base = workloads.rala_device(wl, device)
+            cx = wl.extra["cx"]
+            self.ws = binding.new_workspace(binding.rala_workspace_bytes(wl.B, wl.H, wl.N, wl.d, cx), device)
+            for r in range(self.R):
+                s = {k: (v if r == 0 else v.clone()) for k, v in base.items()}
+                s["y"] = torch.empty_like(s["q"])
+                self.sets.append(s)
+        elif wl.kind == "decode":
+            dev = workloads.decode_device(wl, device, steps=64)
+            kf = dev["prefix_k"].float()
+            kf = torch.where(kf > 0, kf + 1, torch.exp(kf))
+            S = torch.einsum("pbhc,pbhe->bhce", kf, dev["prefix_v"].float()).contiguous()
+            z = kf.sum(dim=0).contiguous()
+            self.sets.append({"steps": dev, "S": S, "z": z,
+                              "out": torch.empty(wl.B, wl.H, wl.d, dtype=dev["step_q"].dtype, device=device)})
+            self.ws = None
+        self.step_index = 0
+
+    def step(self, i):
+        self._call(self.sets[i % self.R], i)
+
+    def _call(self, s, i):
+        wl, b = self.wl, self.binding
+        if wl.kind == "mhla":
+            b.mhla_forward(s["q"], s["k"], s["v"], s["mixing"], s["y"], wl.block, workspace=self.ws)
+        elif wl.kind == "causal":
+            b.mhla_forward_causal(s["q"], s["k"], s["v"], None, s["y"], wl.block, workspace=self.ws)
+        elif wl.kind == "rala":
+            b.rala_forward(s["q"], s["k"], s["v"], s["x"], s["w"], s["y"], workspace=self.ws)
+        elif wl.kind == "decode":
+            st = s["steps"]
+            t = i % st["step_q"].shape[0]
+            b.linattn_decode_step(st["step_q"][t], st["step_k"][t], st["step_v"][t], s["S"], s["z"], s["out"])
+
+    # ---- end to end: host inputs -> device -> forward -> host output
+    def e2e_setup(self):
+        torch = self.torch
+        s = self.sets[0]
+        if self.wl.kind == "decode":
+            st = s["steps"]
+            self.h_in = {k: st[k][:8].cpu().pin_memory() for k in ("step_q", "step_k", "step_v")}
+            self.h_out = torch.empty_like(s["out"], device="cpu").pin_memory()
+            return
+        names = ["q", "k", "v"] + (["x"] if self.wl.kind == "rala" else [])
+        self.h_in = {n: s[n].cpu().pin_memory() for n in names}
+        self.h_out = torch.empty_like(s["y"], device="cpu").pin_memory()
+
+    def e2e_step(self, i):
+        s = self.sets[0]
+        wl = self.wl
+        if wl.kind == "decode":
+            st = s["steps"]
+            t = i % 8
+            for n in ("step_q", "step_k", "step_v"):
+                st[n][t].copy_(self.h_in[n][t], non_blocking=True)
+            self.binding.linattn_decode_step(st["step_q"][t], st["step_k"][t], st["step_v"][t], s["S"], s["z"], s["out"])
+            self.h_out.copy_(s["out"], non_blocking=True)
+            return
+        for n, h in self.h_in.items():
+            s[n].copy_(h, non_blocking=True)
+        self._call(s, i)
+        self.h_out.copy_(s["y"], non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = sum(t[:1].numel() * t.element_size() if self.wl.kind == "decode" else t.numel() * t.element_size()
+                  for t in self.h_in.values())
+        return h2d, self.h_out.numel() * self.h_out.element_size()
+
+
+def capture(torch, runner, steps, first, with_events):
+    """CUDA graph of `steps` consecutive steps starting at step index `first`; optional per-step events."""
+    g = torch.cuda.CUDAGraph()
+    events = None
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        if with_events:
+            try:
+                events = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(steps + 1)]
+            except TypeError:
+                events = None
+        with torch.cuda.graph(g, stream=stream):
+            if events:
+                events[0].record()
+            for i in range(steps):
+                runner.step(first + i)
+                if events:
+                    events[i + 1].record()
+    torch.cuda.current_stream().wait_stream(stream)
+    return g, events
+
+
+# ------------------------------------------------------------ our arm
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    from token_level_head_gb300 import binding
+    from token_level_head_gb300.build import build_library
+
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        build_library()
+    if world > 1:
+        dist.barrier()
+    binding.load()
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+    runner = Runner(wl, device, l2)
+
+    # eager warm-up (lazy initialisation), then capture
+    for i in range(max(1, args.warmup)):
+        runner.step(i)
+    torch.cuda.synchronize()
+    launches0 = binding.mhla_launch_count()
+    chunk = min(args.steps, 64 * runner.R)
+    chunk -= chunk % runner.R if chunk >= runner.R else 0
+    chunk = max(chunk, 1)
+    g, events = capture(torch, runner, chunk, 0, True)
+    per_step_kernels = (binding.mhla_launch_count() - launches0) / chunk
+    rem = args.steps % chunk
+    g_rem = capture(torch, runner, rem, 0, False)[0] if rem else None
+    n_chunks = args.steps // chunk
+    g_warm = capture(torch, runner, max(args.warmup, 1), 0, False)[0]
+    torch.cuda.synchronize()
+
+    g_warm.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record()
+    for _ in range(n_chunks):
+        g.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if rank == 0:
+        time.sleep(0.2)
+        sampler.stop()
+    step_ms = None
+    if events:
+        durs = [events[i].elapsed_time(events[i + 1]) for i in range(chunk)]
+        step_ms = sum(durs) / len(durs)
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    # end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        runner.e2e_setup()
+        k_e2e = max(3, min(args.steps, 50))
+        for i in range(2):
+            runner.e2e_step(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record()
+        for i in range(k_e2e):
+            runner.e2e_step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d, d2h = runner.e2e_bytes()
+        e2e = {"value": world * tokens_per_step(wl) * k_e2e / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e,
+               "ms_per_step": e_ms / k_e2e}
+
+    if rank != 0:
+        return None
+    alg = workload_bytes(wl)
+    peak, peak_src = hbm_peak()
+    kernel_ms = step_ms if step_ms is not None else elapsed_ms / args.steps
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    path = binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"),
+                                     torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
+    kernel_name = f"{wl.kind}_{path}"
+    value = world * tokens_per_step(wl) * args.steps / (elapsed_ms / 1e3)
+    line = {
+        "metric": METRIC if wl.name == "dit" else f"{wl.name} tokens/s",
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded SplitMix64 normal inputs, generated on the device)",
+        "config": {"workload": describe(wl), "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
+                   "block_size": wl.block, "M": wl.M, "parallelism": f"independent replicas x{world}",
+                   "l2": f"inputs larger than L2: {runner.R} rotating input/output sets of "
+                         f"{alg / 1e6:.1f} MB (L2 {l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA graphs, CUDA events on the launching stream",
+                   "path": path},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": parse_traffic(kernel_name),
+                     "kernel": kernel_name, "kernels_per_step": per_step_kernels,
+                     "alg_bytes_per_launch": alg, "launch_ms": kernel_ms, "peak_source": peak_src,
+                     "frac_of_nominal_8TBps": achieved / 8000.0},
+        "gpu_launches": int(round(per_step_kernels * args.steps)),
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
+    return line
+
+
+# ------------------------------------------------------ oracle (CPU) arm
+def _oracle_sample(wl, n_units):
+    """Prepares one bounded sample of the workload for the oracle; returns (fn, tokens, description)."""
+    import numpy as np
+    import oracle
+    import workloads
+
+    if wl.kind in ("mhla", "causal"):
+        heads = [(i // wl.H % wl.B, i % wl.H) for i in range(n_units)]
+        x = workloads.mhla_host(wl, heads=heads)
+        if wl.kind == "mhla":
+            fn = lambda: oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)  # noqa: E731
+        else:
+            fn = lambda: oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)  # noqa: E731
+        return fn, n_units * wl.N, f"{n_units} of {wl.B * wl.H} (batch, head) slices, all {wl.N} tokens"
+    if wl.kind == "decode":
+        units = list(range(n_units))
+        host = workloads.decode_host(wl, units, steps=1)
+        s0 = np.zeros((n_units, wl.d, wl.d))
+        z0 = np.zeros((n_units, wl.d))
+        fn = lambda: oracle.decode_steps(s0, z0, host["step_q64"], host["step_k64"], host["step_v64"])  # noqa: E731
+        return fn, n_units, f"{n_units} of {wl.B * wl.H} units, one step"
+    if wl.kind == "rala":
+        host = workloads.rala_host(wl, list(range(n_units)))
+        fn = lambda: oracle.rala_forward(host["q64"], host["k64"], host["v64"], host["x64"], host["w64"])  # noqa: E731
+        return fn, n_units * wl.H * wl.N, f"{n_units} of {wl.B} samples (all heads)"
+    raise ValueError(wl.kind)
+
+
+def _default_sample_units(wl):
+    return {"mhla": max(1, min(wl.B * wl.H, 8)), "causal": 2, "decode": 256, "rala": 2}[wl.kind]
+
+
+def cpu_baseline(wl, budget_s=10.0, n_units=None):
+    """The oracle as it stands, single-threaded, on a bounded sample, repeated for ~budget_s seconds."""
+    code = (
+        "import json, sys, time; sys.path.insert(0, %r)\n"
+        "import bench, workloads\n"
+        "wl = workloads.WORKLOADS[%r]\n"
+        "fn, tokens, desc = bench._oracle_sample(wl, %d)\n"
+        "fn()\n"
+        "t0 = time.perf_counter(); n = 0\n"
+        "while True:\n"
+        "    fn(); n += 1\n"
+        "    if time.perf_counter() - t0 >= %f: break\n"
+        "dt = time.perf_counter() - t0\n"
+        "print(json.dumps({'value': n * tokens / dt, 'reps': n, 'seconds': dt, 'desc': desc}))\n"
+    ) % (ROOT, wl.name, n_units or _default_sample_units(wl), budget_s)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if res.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {res.stderr.strip()[-300:]}"}
+    r = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": r["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{r['desc']}; float64 numpy oracle, 1 thread, {r['reps']} reps in {r['seconds']:.1f} s"}
+
+
+def run_reference(args, wl, rank):
+    """Reference arm: the CPU oracle, each step a bounded sample of the workload (rank 0 only)."""
+    if rank != 0:
+        return None
+    import multiprocessing  # noqa: F401  (no pool: the oracle runs in this process, single-threaded)
+    n_units = _default_sample_units(wl)
+    fn, tokens, desc = _oracle_sample(wl, n_units)
+    t0 = time.perf_counter()
+    fn()
+    per = time.perf_counter() - t0
+    budget = 150.0
+    while n_units > 1 and per * (args.steps + args.warmup) > budget:
+        n_units = max(1, n_units // 2)
+        fn, tokens, desc = _oracle_sample(wl, n_units)
+        t0 = time.perf_counter()
+        fn()
+        per = time.perf_counter() - t0
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    dt = time.perf_counter() - t0
+    value = tokens * args.steps / dt
+    return {
+        "impl": "reference",
+        "metric": METRIC if wl.name == "dit" else f"{wl.name} tokens/s",
+        "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 normal inputs)",
+        "config": {"workload": describe(wl), "B": wl.B, "H": wl.H, "N": wl.N, "d": wl.d,
+                   "block_size": wl.block, "M": wl.M},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{desc} per step; float64 numpy oracle, 1 thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="dit")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, wl, rank)
+    else:
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl")
+        line = run_ours(args, wl, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

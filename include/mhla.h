@@ -1,0 +1,159 @@
+/*
+ * mhla.h — C ABI of the GB300 (sm_103a) token-level multi-head linear
+ * attention (MHLA) forward library.
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [MHLA]  "MHLA: Restoring Expressivity of Linear Attention via Token-Level
+ *           Multi-Head" — §4.1 (local KV summaries, multi-head mixing,
+ *           output), §4.2 (token-level form, chunkwise-parallel causal form),
+ *           App. C (causal chunked linear attention and causal inference).
+ *   [LA]    "Linear Attention（线性注意力）笔记" — §二 (phi = ELU + 1),
+ *           §四 (recurrent form, eps in the denominator), §五 (parallel form).
+ *   [MASK]  "4. Attention" tutorial — "Mask": the causal mask removes only
+ *           the future (strict upper triangle).
+ *   [RALA]  "Breaking the Low-Rank Dilemma of Linear Attention" notes — key
+ *           designs 1 (KV buffer rank augmentation) and 2 (output rank
+ *           augmentation).
+ *
+ * Conventions shared by every entry point
+ *   - phi(x) = ELU(x) + 1 = (x > 0 ? x + 1 : exp(x))            [LA §二]
+ *   - Q, K, V, Y are dense row-major [B, H, N, d] (d innermost); the (b, h)
+ *     slices are independent problems.  d must be 16, 32, 64 or 128.
+ *   - dtype: MHLA_F32 (fp32 in/out, fp32 arithmetic) or MHLA_BF16 (bf16
+ *     in/out, fp32 accumulation; summaries, normalisers and decode state are
+ *     fp32).  Outputs have the input dtype.
+ *   - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte
+ *     aligned; the caller owns all memory, including the workspace.  The
+ *     library allocates nothing and keeps no per-call state outside the
+ *     workspace; calls are asynchronous on `stream` (a cudaStream_t, 0 = the
+ *     legacy default stream) and do not synchronise the host.
+ *   - Argument errors are detected on the host before any launch and return
+ *     MHLA_ERR_INVALID_ARG (or MHLA_ERR_UNSUPPORTED for valid but
+ *     unimplemented combinations) without touching device memory.  Launch
+ *     failures return MHLA_ERR_CUDA.  Sizes with B*H*N == 0 are a no-op.
+ *   - Workspace: at least the size returned by the matching *_workspace_bytes
+ *     query, 256-byte aligned.  Before its FIRST use a workspace must be
+ *     zero-filled (e.g. cudaMemsetAsync); the library leaves it ready for the
+ *     next call.  Calls that share a workspace must not overlap on the GPU.
+ *     A workspace may be reused across shapes as long as it is big enough.
+ *   - Device-side waits (between the summary, mixing and output stages of
+ *     one launch) are bounded; if one gives up, the output is incomplete and
+ *     MHLA_ERR_TIMEOUT is latched in the workspace; mhla_query_status()
+ *     reports it.
+ */
+#ifndef MHLA_GB300_H
+#define MHLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MHLA_OK = 0,
+  MHLA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, aliasing, small workspace */
+  MHLA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  MHLA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MHLA_ERR_TIMEOUT = 4       /* a bounded device-side wait gave up (latched in the workspace) */
+} mhla_status;
+
+typedef enum { MHLA_F32 = 0, MHLA_BF16 = 1 } mhla_dtype;
+
+/* Which kernel family mhla_forward / mhla_forward_causal would run. */
+typedef enum { MHLA_PATH_NONE = 0, MHLA_PATH_SIMT = 1, MHLA_PATH_TCGEN05 = 2 } mhla_path;
+
+/* Workspace bytes for mhla_forward (causal = 0) or mhla_forward_causal
+ * (causal = 1, block_size = chunk) with these sizes; 0 if the sizes are
+ * invalid.  Valid for both dtypes. */
+size_t mhla_workspace_bytes(int B, int H, int N, int d, int block_size, int causal);
+
+/* MHLA forward, non-causal ([MHLA] §4.1; eps as in [LA] §五).
+ *   Blocks are the M = N / block_size contiguous token ranges of block_size
+ *   tokens.  For each (b, h) and block j:
+ *     S_j = sum_{t in j} phi(K_t) V_t^T  (d x d, S_j[c][e]),  z_j = sum_{t in j} phi(K_t)
+ *   for each query block i:  S~_i = sum_j m[h][i][j] S_j,   z~_i = sum_j m[h][i][j] z_j
+ *   for token t in block i:  Y_t = phi(Q_t) S~_i / (phi(Q_t) . z~_i + eps)
+ *   q, k, v : [B, H, N, d] (dtype dt)            — inputs
+ *   mixing  : [H, M, M] fp32, row i = query block — input; not inspected
+ *             (non-negative rows are the caller's contract, [MHLA] §4.2)
+ *   y       : [B, H, N, d] (dtype dt)            — output, must not overlap q, k, v
+ *   den_out : [B, H, N] fp32 or NULL             — optional output of the denominator
+ *   block_size divides N; M = 1 is global linear attention ([LA] §五).
+ *   causal  : 0 for the form above; 1 computes causal MHLA exactly as
+ *             mhla_forward_causal(..., mixing, ..., chunk = block_size).
+ *   eps     : finite, >= 0 (1e-6 in [LA]). */
+mhla_status mhla_forward(const void* q, const void* k, const void* v, const float* mixing,
+                         void* y, float* den_out, int B, int H, int N, int d, int block_size,
+                         int causal, mhla_dtype dt, float eps, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* Causal chunked forward ([MHLA] App. C with the [MASK] convention and the
+ * [LA] §四 normaliser).  Chunks are contiguous ranges of `chunk` tokens
+ * (chunk divides N).  For token t in chunk i:
+ *   mixing == NULL (plain causal linear attention):
+ *     Y_t = [phi(Q_t) P_i + sum_{s in i, s<=t} (phi(Q_t).phi(K_s)) V_s]
+ *         / [phi(Q_t) . zeta_i + sum_{s in i, s<=t} phi(Q_t).phi(K_s) + eps]
+ *     with P_i = sum_{j<i} S_j, zeta_i = sum_{j<i} z_j (exclusive prefixes);
+ *     equal to the recurrence S_t = S_{t-1} + phi(k_t) v_t^T of [LA] §四.
+ *   mixing != NULL ([H, M, M] fp32, M = N / chunk; causal MHLA, [MHLA] §4.2
+ *     chunkwise form): P_i = sum_{j<i} m[h][i][j] S_j, zeta_i likewise, and
+ *     the intra-chunk sums are scaled by m[h][i][i]; entries above the
+ *     diagonal are ignored.
+ *   Other arguments as in mhla_forward. */
+mhla_status mhla_forward_causal(const void* q, const void* k, const void* v, const float* mixing,
+                                void* y, float* den_out, int B, int H, int N, int d, int chunk,
+                                mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* One recurrent decode step for B*H independent (batch, head) states
+ * ([LA] §四; the fixed-size state of [LA] §八; [MHLA] App. C inference).
+ *   q, k, v : [B, H, d] (dtype dt)       — this step's token
+ *   S       : [B, H, d, d] fp32, in/out — S[c][e] = sum over past tokens of phi(k)_c v_e
+ *   z       : [B, H, d] fp32, in/out    — sum over past tokens of phi(k)
+ *   out     : [B, H, d] (dtype dt)      — output; must not overlap the inputs or the state
+ *   den_out : [B, H] fp32 or NULL
+ *   Order: S += phi(k) v^T; z += phi(k); out = phi(q) S / (phi(q) . z + eps),
+ *   i.e. the token attends to itself.  No workspace. */
+mhla_status linattn_decode_step(const void* q, const void* k, const void* v, float* S, float* z,
+                                void* out, float* den_out, int B, int H, int d, mhla_dtype dt,
+                                float eps, void* stream);
+
+/* Workspace bytes for rala_forward; 0 if the sizes are invalid. */
+size_t rala_workspace_bytes(int B, int H, int N, int d, int cx);
+
+/* Rank-augmented linear attention forward ([RALA] key designs 1 and 2).
+ * For each (b, h):
+ *   Q_g = (1/N) sum_t Q_t (raw queries);  l_j = Q_g . phi(K_j);
+ *   alpha = softmax_j(l);  Bkv = sum_j alpha_j phi(K_j) V_j^T  (d x d);
+ *   G = X_b W  ([N, d], shared by the heads of sample b);
+ *   Y_t = G_t * (phi(Q_t) Bkv)   (elementwise product; no normaliser).
+ *   q, k, v : [B, H, N, d] (dtype dt);  x : [B, N, cx] (dtype dt);
+ *   w : [cx, d] (dtype dt);  y : [B, H, N, d] (dtype dt).
+ *   cx must be a multiple of 16 and at most 256. */
+mhla_status rala_forward(const void* q, const void* k, const void* v, const void* x,
+                         const void* w, void* y, int B, int H, int N, int d, int cx,
+                         mhla_dtype dt, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Kernel family mhla_forward would use for these arguments (no launch). */
+mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
+                            mhla_dtype dt);
+
+/* Synchronises `stream`, then returns MHLA_ERR_TIMEOUT if a device-side wait
+ * in a call that used this workspace gave up (and clears the flag), MHLA_OK
+ * otherwise, or MHLA_ERR_CUDA if the synchronisation or read failed. */
+mhla_status mhla_query_status(void* workspace, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* mhla_status_string(mhla_status s);
+
+/* Number of kernels this library has launched (or captured into a graph) in
+ * this process since it was loaded; a diagnostic counter. */
+unsigned long long mhla_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHLA_GB300_H */

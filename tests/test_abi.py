@@ -1,0 +1,131 @@
+"""The C-ABI library builds, loads, exports every declared symbol and rejects bad arguments.
+
+Runs without a GPU: every call below fails host-side validation (or is an
+empty no-op) before the library touches CUDA.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from token_level_head_gb300 import binding
+from token_level_head_gb300.build import INCLUDE, build_library
+
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+F32, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(INCLUDE, "mhla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)) - {"if"})
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "mhla_forward" in names and "linattn_decode_step" in names and "rala_forward" in names
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in binding.EXPORTED, name
+
+
+def test_status_strings(lib):
+    for s in range(5):
+        assert binding.status_string(s)
+    assert binding.status_string(99) == "unknown status"
+
+
+def test_workspace_queries(lib):
+    assert binding.mhla_workspace_bytes(8, 6, 4096, 64, 256) > 0
+    assert binding.mhla_workspace_bytes(8, 6, 4096, 48, 256) == 0       # d not supported
+    assert binding.mhla_workspace_bytes(8, 6, 4096, 64, 300) == 0       # block does not divide N
+    assert binding.mhla_workspace_bytes(8, 6, 4096, 64, 0) == 0
+    small = binding.mhla_workspace_bytes(1, 1, 4096, 64, 256)
+    big = binding.mhla_workspace_bytes(2, 1, 4096, 64, 256)
+    assert 0 < small < big
+    assert binding.rala_workspace_bytes(64, 2, 3136, 32, 64) > 0
+    assert binding.rala_workspace_bytes(64, 2, 3136, 32, 60) == 0       # cx not a multiple of 16
+
+
+P = 1 << 20  # fake, 256-byte-aligned "device" addresses; never dereferenced
+
+
+def fwd(lib, q=P, k=2 * P, v=3 * P, mix=4 * P, y=5 * P, den=None, B=1, H=1, N=256, d=64,
+        block=64, causal=0, dt=BF16, eps=1e-6, ws=8 * P, wsb=1 << 30):
+    return lib.mhla_forward(q, k, v, mix, y, den, B, H, N, d, block, causal, dt, eps, ws, wsb, None)
+
+
+def test_forward_argument_errors(lib):
+    assert fwd(lib, d=48) == INVALID
+    assert fwd(lib, block=100) == INVALID
+    assert fwd(lib, block=0) == INVALID
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, dt=7) == INVALID
+    assert fwd(lib, eps=-1.0) == INVALID
+    assert fwd(lib, eps=float("nan")) == INVALID
+    assert fwd(lib, eps=float("inf")) == INVALID
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, y=None) == INVALID
+    assert fwd(lib, mix=None) == INVALID                    # non-causal MHLA needs the mixing
+    assert fwd(lib, q=P + 8) == INVALID                     # misaligned
+    assert fwd(lib, den=P * 40 + 4) == INVALID              # misaligned den_out
+    assert fwd(lib, y=P + 4096) == INVALID                  # y overlaps q
+    assert fwd(lib, y=P) == INVALID                         # y aliases q
+    assert fwd(lib, ws=None) == INVALID
+    assert fwd(lib, ws=8 * P + 16) == INVALID               # workspace not 256-aligned
+    assert fwd(lib, wsb=16) == INVALID                      # workspace too small
+    assert fwd(lib, causal=2) == INVALID
+
+
+def test_empty_inputs_are_a_no_op(lib):
+    assert fwd(lib, B=0) == OK
+    assert fwd(lib, N=0, q=None, k=None, v=None, y=None) == OK
+    assert lib.mhla_forward_causal(None, None, None, None, None, None, 0, 4, 128, 64, 64, BF16,
+                                   1e-6, None, 0, None) == OK
+    assert lib.linattn_decode_step(None, None, None, None, None, None, None, 0, 16, 64, BF16, 1e-6,
+                                   None) == OK
+    assert lib.rala_forward(None, None, None, None, None, None, 3, 2, 0, 32, 64, BF16, None, 0,
+                            None) == OK
+
+
+def test_decode_argument_errors(lib):
+    def dec(q=P, k=2 * P, v=3 * P, S=4 * P, z=6 * P, out=7 * P, B=2, H=2, d=64, dt=BF16, eps=1e-6):
+        return lib.linattn_decode_step(q, k, v, S, z, out, None, B, H, d, dt, eps, None)
+    assert dec(d=24) == INVALID
+    assert dec(S=None) == INVALID
+    assert dec(z=4 * P + 64) == INVALID                    # z inside S
+    assert dec(out=P) == INVALID                           # out aliases q
+    assert dec(eps=-0.5) == INVALID
+    assert dec(q=P + 2) == INVALID
+
+
+def test_rala_argument_errors(lib):
+    def rala(cx=64, d=32, ws=8 * P, wsb=1 << 30, y=6 * P, x=4 * P):
+        return lib.rala_forward(P, 2 * P, 3 * P, x, 5 * P, y, 2, 2, 3136, d, cx, BF16, ws, wsb, None)
+    assert rala(cx=60) == INVALID
+    assert rala(cx=512) == INVALID
+    assert rala(d=20) == INVALID
+    assert rala(wsb=8) == INVALID
+    assert rala(y=P) == INVALID
+    assert rala(cx=256, d=128) == UNSUPPORTED
+
+
+def test_forward_path_query(lib):
+    assert binding.PATH_NAMES[lib.mhla_forward_path(1, 1, 256, 16, 64, 0, F32)] == "simt"
+    assert binding.PATH_NAMES[lib.mhla_forward_path(1, 1, 256, 48, 64, 0, F32)] == "none"
+
+
+def test_query_status_rejects_null(lib):
+    assert lib.mhla_query_status(None, None) == INVALID
+
+
+def test_launch_counter_starts_readable(lib):
+    assert isinstance(binding.mhla_launch_count(), int)

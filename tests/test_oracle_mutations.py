@@ -11,7 +11,7 @@ import pytest
 import oracle
 import oracle.mhla_oracle as om
 import test_oracle_pins as pins
-from workloads import WORKLOADS, make_mhla_inputs
+from workloads import WORKLOADS, mhla_host
 
 
 def _fails(fn, *args):
@@ -78,6 +78,6 @@ def test_causal_mask_without_diagonal_is_caught(monkeypatch, golden_dir):
 def test_block_offset_error_is_caught(monkeypatch):
     """An off-by-one block index (b(t) shifted by one token) breaks the two-definition agreement."""
     wl = WORKLOADS["tiny"]
-    x = make_mhla_inputs(wl)
+    x = mhla_host(wl)
     monkeypatch.setattr(om, "block_of", lambda n, bs: np.minimum((np.arange(n) + 1) // bs, n // bs - 1))
     _fails(pins.test_block_form_equals_token_expansion_tiny, (wl, x))

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
-from workloads import WORKLOADS, make_mhla_inputs, normal, uniform
+from workloads import WORKLOADS, mhla_host, normal, uniform
 
 TOL = 1e-12
 
@@ -99,7 +99,7 @@ def test_golden_rala(golden_dir):
 @pytest.fixture(scope="module")
 def tiny():
     wl = WORKLOADS["tiny"]
-    return wl, make_mhla_inputs(wl)
+    return wl, mhla_host(wl)
 
 
 def test_block_form_equals_token_expansion_tiny(tiny):

@@ -1,0 +1,335 @@
+"""GPU parity: the CUDA library through its C ABI against the float64 oracle.
+
+Same seeded inputs on both sides (the oracle gets the dtype-rounded values).
+Small shapes are compared element by element in full; the full-size
+workloads run in the launch configuration the bench times and are compared
+on sampled (batch, head) slices the oracle computes one by one, plus
+properties checked over the whole output (finite, positive denominators).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (TOL_Y, assert_close_den, assert_close_y, rel, slice_rel, to_device, to_f64,
+                      torch_dtype)
+from token_level_head_gb300 import binding
+from token_level_head_gb300.build import build_library
+from workloads import (WORKLOADS, bf16_bits, bf16_bits_to_f64, decode_device, decode_host,
+                       mhla_device, mhla_host, normal, rala_device, rala_host, uniform)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build_library()
+    return binding.load()
+
+
+def rounded(x64, dtype):
+    """(device tensor, float64 values) of x64 rounded to dtype."""
+    if dtype == "bf16":
+        bits = bf16_bits(x64)
+        return to_device(bits), bf16_bits_to_f64(bits)
+    f = np.asarray(x64, np.float32)
+    return to_device(f), f.astype(np.float64)
+
+
+def rand_inputs(seed, shape, dtype, scale=None):
+    d = shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    out = {}
+    for i, name in enumerate("qkv"):
+        out[name], out[name + "64"] = rounded(normal(seed, i + 1, shape, scale), dtype)
+    return out
+
+
+def rand_mixing(seed, h, m, lower=False):
+    u = uniform(seed, 9, (h, m, m)) + 0.05
+    if lower:
+        u = np.tril(u)
+    mix = (u / u.sum(axis=-1, keepdims=True)).astype(np.float32)
+    return torch.from_numpy(mix).cuda(), mix.astype(np.float64)
+
+
+def forward(q, k, v, mix, block, causal=0, eps=1e-6):
+    y = torch.empty_like(q)
+    den = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    binding.mhla_forward(q, k, v, mix, y, block, causal=causal, eps=eps, den_out=den)
+    torch.cuda.synchronize()
+    return to_f64(y), to_f64(den)
+
+
+def forward_causal(q, k, v, mix, chunk, eps=1e-6):
+    y = torch.empty_like(q)
+    den = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    binding.mhla_forward_causal(q, k, v, mix, y, chunk, eps=eps, den_out=den)
+    torch.cuda.synchronize()
+    return to_f64(y), to_f64(den)
+
+
+# ------------------------------------------------------------ non-causal MHLA
+def test_tiny_workload_fp32():
+    wl = WORKLOADS["tiny"]
+    x = mhla_host(wl)
+    q, k, v = (to_device(x[n]) for n in "qkv")
+    mix = to_device(x["mixing"])
+    y, den = forward(q, k, v, mix, wl.block)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
+    brute, dbrute = oracle.mhla_token_expansion(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
+    assert_close_y(y, ref, "f32")
+    assert_close_y(y, brute, "f32")
+    assert_close_den(den, dref, "f32")
+    assert_close_den(den, dbrute, "f32")
+
+
+SMALL = [  # B, H, N, d, block
+    (2, 3, 192, 16, 64),
+    (1, 2, 96, 32, 48),
+    (1, 1, 128, 64, 1),
+    (2, 2, 512, 64, 128),
+    (1, 2, 256, 128, 256),
+    (1, 3, 384, 64, 384),
+    (3, 1, 1024, 64, 256),
+    (1, 2, 768, 32, 256),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "x".join(map(str, s)))
+def test_small_shapes(shape, dtype):
+    B, H, N, d, block = shape
+    x = rand_inputs(100 + N + d, (B, H, N, d), dtype)
+    mix_t, mix64 = rand_mixing(7 + block, H, N // block)
+    y, den = forward(x["q"], x["k"], x["v"], mix_t, block)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block)
+    assert_close_y(y, ref, dtype)
+    assert_close_den(den, dref, dtype)
+
+
+def test_extreme_values_fp32():
+    """Large |Q|, |K| exercise both branches of phi far from 0 (exp underflow, big linear values)."""
+    B, H, N, d, block = 1, 2, 256, 32, 64
+    x = rand_inputs(31, (B, H, N, d), "f32", scale=6.0)
+    mix_t, mix64 = rand_mixing(3, H, N // block)
+    y, den = forward(x["q"], x["k"], x["v"], mix_t, block, eps=0.0)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block, eps=0.0)
+    assert_close_y(y, ref, "f32")
+    assert_close_den(den, dref, "f32")
+
+
+@pytest.mark.parametrize("name", ["dit"])
+def test_full_workload_all_heads(name):
+    wl = WORKLOADS[name]
+    dev = mhla_device(wl)
+    y, den = forward(dev["q"], dev["k"], dev["v"], dev["mixing"], wl.block)
+    x = mhla_host(wl)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
+    assert_close_y(y, ref, wl.dtype)
+    assert_close_den(den, dref, wl.dtype)
+
+
+@pytest.mark.parametrize("name", ["hires", "hires_m1"])
+def test_full_workload_sampled_heads(name):
+    wl = WORKLOADS[name]
+    dev = mhla_device(wl)
+    y, den = forward(dev["q"], dev["k"], dev["v"], dev["mixing"], wl.block)
+    assert np.all(np.isfinite(y)) and np.all(den > 0)
+    heads = [(0, 1), (0, 4)]
+    x = mhla_host(wl, heads=heads)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
+    for i, (b, h) in enumerate(heads):
+        assert_close_y(y[b, h][None, None], ref[0, i][None, None], wl.dtype, what=f"Y[{b},{h}]")
+        assert_close_den(den[b, h], dref[0, i], wl.dtype, what=f"den[{b},{h}]")
+
+
+def test_m1_equals_all_ones_mixing():
+    """Global linear attention two ways on the GPU path: M = 1, and all-ones mixing over M = 8 blocks."""
+    x = rand_inputs(55, (1, 2, 1024, 64), "bf16")
+    y1, d1 = forward(x["q"], x["k"], x["v"], torch.ones(2, 1, 1, device="cuda"), 1024)
+    y8, d8 = forward(x["q"], x["k"], x["v"], torch.ones(2, 8, 8, device="cuda"), 128)
+    ref, dref = oracle.global_linear_attention(x["q64"], x["k64"], x["v64"])
+    for y, den in ((y1, d1), (y8, d8)):
+        assert_close_y(y, ref, "bf16")
+        assert_close_den(den, dref, "bf16")
+
+
+def test_deterministic():
+    wl = WORKLOADS["dit"]
+    dev = mhla_device(wl)
+    outs = []
+    for _ in range(2):
+        y = torch.empty_like(dev["q"])
+        binding.mhla_forward(dev["q"], dev["k"], dev["v"], dev["mixing"], y, wl.block)
+        torch.cuda.synchronize()
+        outs.append(y.view(torch.int16).clone())
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_empty_batch_is_a_no_op():
+    q = torch.empty(0, 2, 256, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(q)
+    ws = binding.new_workspace(256, "cuda")
+    binding.mhla_forward(q, q, q, torch.ones(2, 4, 4, device="cuda"), y, 64, workspace=ws)
+    assert binding.mhla_query_status(ws) == 0
+
+
+# --------------------------------------------------------------------- causal
+CAUSAL = [  # B, H, N, d, chunk
+    (2, 2, 256, 16, 64),
+    (1, 2, 384, 64, 128),
+    (1, 1, 256, 32, 16),
+    (1, 2, 512, 64, 512),
+    (2, 1, 256, 128, 128),
+    (1, 1, 64, 64, 1),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", CAUSAL, ids=lambda s: "x".join(map(str, s)))
+def test_causal_small(shape, dtype):
+    B, H, N, d, chunk = shape
+    x = rand_inputs(200 + N + d, (B, H, N, d), dtype)
+    y, den = forward_causal(x["q"], x["k"], x["v"], None, chunk)
+    ref, dref = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], chunk)
+    assert_close_y(y, ref, dtype)
+    assert_close_den(den, dref, dtype)
+    if N <= 256:
+        brute, dbrute = oracle.causal_bruteforce(x["q64"], x["k64"], x["v64"])
+        assert_close_y(y, brute, dtype)
+        assert_close_den(den, dbrute, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_causal_mhla_with_mixing(dtype):
+    B, H, N, d, chunk = 1, 2, 256, 32, 64
+    x = rand_inputs(77, (B, H, N, d), dtype)
+    mix_t, mix64 = rand_mixing(5, H, N // chunk, lower=True)
+    y, den = forward_causal(x["q"], x["k"], x["v"], mix_t, chunk)
+    ref, dref = oracle.causal_mhla_bruteforce(x["q64"], x["k64"], x["v64"], mix64, chunk)
+    assert_close_y(y, ref, dtype)
+    assert_close_den(den, dref, dtype)
+    # mhla_forward(causal=1) is the same computation
+    y2, den2 = forward(x["q"], x["k"], x["v"], mix_t, chunk, causal=1)
+    assert np.array_equal(y2, y) and np.array_equal(den2, den)
+
+
+def test_causal_full_workload_sampled_heads():
+    wl = WORKLOADS["causal"]
+    dev = mhla_device(wl)
+    y, den = forward_causal(dev["q"], dev["k"], dev["v"], None, wl.block)
+    assert np.all(np.isfinite(y)) and np.all(den > 0)
+    heads = [(0, 0), (2, 9), (3, 15)]
+    x = mhla_host(wl, heads=heads)
+    ref, dref = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)
+    for i, (b, h) in enumerate(heads):
+        assert_close_y(y[b, h][None, None], ref[0, i][None, None], wl.dtype, what=f"Y[{b},{h}]")
+        assert_close_den(den[b, h], dref[0, i], wl.dtype, what=f"den[{b},{h}]")
+
+
+# --------------------------------------------------------------------- decode
+def decode_run(S, z, qs, ks, vs, eps=1e-6):
+    """Runs T steps on the GPU; returns per-step outputs and denominators (float64)."""
+    outs, dens = [], []
+    for t in range(qs.shape[0]):
+        out = torch.empty_like(qs[t])
+        den = torch.empty(qs.shape[1:-1], dtype=torch.float32, device=qs.device)
+        binding.linattn_decode_step(qs[t], ks[t], vs[t], S, z, out, eps=eps, den_out=den)
+        outs.append(out)
+        dens.append(den)
+    torch.cuda.synchronize()
+    return to_f64(torch.stack(outs)), to_f64(torch.stack(dens))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_decode_small(d, dtype):
+    B, H, T, P = 3, 5, 12, 40
+    pk = normal(9, 1, (P, B, H, d), d ** -0.5)
+    pv = normal(9, 2, (P, B, H, d), d ** -0.5)
+    kf = oracle.phi(pk)
+    s0 = np.einsum("pbhc,pbhe->bhce", kf, pv).astype(np.float32)
+    z0 = kf.sum(axis=0).astype(np.float32)
+    steps = {n: rounded(normal(9, 3 + i, (T, B, H, d), d ** -0.5), dtype) for i, n in enumerate("qkv")}
+    S, z = torch.from_numpy(s0).cuda(), torch.from_numpy(z0).cuda()
+    outs, dens = decode_run(S, z, steps["q"][0], steps["k"][0], steps["v"][0])
+    ref, dref, s_t, z_t = oracle.decode_steps(s0, z0, steps["q"][1], steps["k"][1], steps["v"][1])
+    assert_close_y(outs.reshape(T * B, H, d)[:, :, None], ref.reshape(T * B, H, d)[:, :, None], dtype)
+    assert_close_den(dens, dref, dtype)
+    assert_close_y(to_f64(S), s_t, "f32", what="state S")
+    assert rel(to_f64(z), z_t) < 1e-5
+
+
+def test_decode_full_workload_sampled_units():
+    wl = WORKLOADS["decode"]
+    B, H, d = wl.B, wl.H, wl.d
+    dev = decode_device(wl)
+    # initial state: the prefix summary.  Computed on the device by torch for
+    # every unit, then overwritten by the oracle's value for the checked units.
+    kf = torch.where(dev["prefix_k"].float() > 0, dev["prefix_k"].float() + 1, torch.exp(dev["prefix_k"].float()))
+    S = torch.einsum("pbhc,pbhe->bhce", kf, dev["prefix_v"].float()).contiguous()
+    z = kf.sum(dim=0).contiguous()
+    units = [0, 1234, B * H - 1]
+    host = decode_host(wl, units)
+    s0 = np.einsum("puc,pue->uce", oracle.phi(host["prefix_k64"]), host["prefix_v64"]).astype(np.float32)
+    z0 = oracle.phi(host["prefix_k64"]).sum(axis=0).astype(np.float32)
+    Sf, zf = S.view(B * H, d, d), z.view(B * H, d)
+    for i, u in enumerate(units):
+        Sf[u] = torch.from_numpy(s0[i]).cuda()
+        zf[u] = torch.from_numpy(z0[i]).cuda()
+    T = wl.N
+    outs = torch.empty(T, len(units), d, dtype=torch.float32, device="cuda")
+    dens = torch.empty(T, len(units), dtype=torch.float32, device="cuda")
+    sel = torch.tensor(units, device="cuda")
+    out = torch.empty(B, H, d, dtype=torch.bfloat16, device="cuda")
+    den = torch.empty(B, H, dtype=torch.float32, device="cuda")
+    for t in range(T):
+        binding.linattn_decode_step(dev["step_q"][t], dev["step_k"][t], dev["step_v"][t], S, z, out,
+                                    den_out=den)
+        outs[t] = out.view(B * H, d)[sel].float()
+        dens[t] = den.view(B * H)[sel]
+    torch.cuda.synchronize()
+    ref, dref, s_t, _ = oracle.decode_steps(s0, z0, host["step_q64"], host["step_k64"], host["step_v64"])
+    assert_close_y(to_f64(outs).transpose(1, 0, 2)[:, None], ref.transpose(1, 0, 2)[:, None], "bf16")
+    assert_close_den(to_f64(dens), dref, "bf16")
+    assert_close_y(to_f64(Sf[sel])[:, None], s_t[:, None], "f32", what="state S")
+
+
+# ----------------------------------------------------------------------- RALA
+RALA = [  # B, H, N, d, cx
+    (2, 2, 200, 16, 32),
+    (1, 2, 256, 32, 64),
+    (2, 1, 600, 64, 16),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", RALA, ids=lambda s: "x".join(map(str, s)))
+def test_rala_small(shape, dtype):
+    B, H, N, d, cx = shape
+    x = rand_inputs(300 + N, (B, H, N, d), dtype)
+    xt, x64 = rounded(normal(301, 5, (B, N, cx)), dtype)
+    wt, w64 = rounded(normal(301, 6, (cx, d), cx ** -0.5), dtype)
+    y = torch.empty_like(x["q"])
+    binding.rala_forward(x["q"], x["k"], x["v"], xt, wt, y)
+    torch.cuda.synchronize()
+    ref = oracle.rala_forward(x["q64"], x["k64"], x["v64"], x64, w64)
+    assert_close_y(to_f64(y), ref, dtype)
+
+
+def test_rala_full_workload_sampled_batches():
+    wl = WORKLOADS["rala"]
+    dev = rala_device(wl)
+    y = torch.empty_like(dev["q"])
+    binding.rala_forward(dev["q"], dev["k"], dev["v"], dev["x"], dev["w"], y)
+    torch.cuda.synchronize()
+    y = to_f64(y)
+    assert np.all(np.isfinite(y))
+    batches = [0, 33, 63]
+    host = rala_host(wl, batches)
+    ref = oracle.rala_forward(host["q64"], host["k64"], host["v64"], host["x64"], host["w64"])
+    assert_close_y(y[batches], ref, wl.dtype)

@@ -1,0 +1,170 @@
+"""ctypes binding of the C ABI in ``include/mhla.h`` — argument marshalling only.
+
+Every function here has the name of the C entry point it calls, takes torch
+CUDA tensors, passes their device pointers, sizes and the current CUDA stream
+to the library, and raises :class:`MhlaError` on a non-OK status.  All work
+runs in the library's CUDA kernels; there is no fallback: if the library is
+missing or CUDA is unavailable the call fails.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+MHLA_OK, MHLA_ERR_INVALID_ARG, MHLA_ERR_UNSUPPORTED, MHLA_ERR_CUDA, MHLA_ERR_TIMEOUT = range(5)
+MHLA_F32, MHLA_BF16 = 0, 1
+PATH_NAMES = {0: "none", 1: "simt", 2: "tcgen05"}
+
+_lib = None
+
+_vp, _sz, _i, _f = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_float
+
+_SIGNATURES = {
+    "mhla_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "mhla_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "mhla_forward_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "linattn_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "rala_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "rala_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
+    "mhla_forward_path": (_i, [_i, _i, _i, _i, _i, _i, _i]),
+    "mhla_query_status": (_i, [_vp, _vp]),
+    "mhla_status_string": (ctypes.c_char_p, [_i]),
+    "mhla_launch_count": (ctypes.c_ulonglong, []),
+}
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class MhlaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def load(path: str = LIB_PATH):
+    """Loads the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"MHLA CUDA library not built at {path}; call __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().mhla_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != MHLA_OK:
+        raise MhlaError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return MHLA_F32
+    if t.dtype == torch.bfloat16:
+        return MHLA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def mhla_workspace_bytes(B: int, H: int, N: int, d: int, block_size: int, causal: int = 0) -> int:
+    return int(load().mhla_workspace_bytes(B, H, N, d, block_size, causal))
+
+
+def rala_workspace_bytes(B: int, H: int, N: int, d: int, cx: int) -> int:
+    return int(load().rala_workspace_bytes(B, H, N, d, cx))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """Zero-filled uint8 device buffer of ``nbytes`` (the library needs it zeroed before first use)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def mhla_forward_path(B, H, N, d, block_size, causal, dtype) -> str:
+    dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
+    return PATH_NAMES[int(load().mhla_forward_path(B, H, N, d, block_size, causal, dt))]
+
+
+def mhla_forward(q, k, v, mixing, y, block_size, *, causal=0, eps=1e-6, den_out=None,
+                 workspace=None, stream=None):
+    """Non-causal (or, with causal=1, causal) MHLA forward; q/k/v/y [B, H, N, d], mixing [H, M, M] fp32."""
+    _need_cuda(q, k, v, mixing, y, den_out, workspace)
+    B, H, N, d = q.shape
+    if workspace is None:
+        workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, block_size, causal), q.device)
+    st = load().mhla_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                             B, H, N, d, block_size, causal, _dtype(q), eps, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("mhla_forward", st)
+    return y
+
+
+def mhla_forward_causal(q, k, v, mixing, y, chunk, *, eps=1e-6, den_out=None, workspace=None,
+                        stream=None):
+    """Causal chunked forward; mixing None = plain causal linear attention."""
+    _need_cuda(q, k, v, mixing, y, den_out, workspace)
+    B, H, N, d = q.shape
+    if workspace is None:
+        workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, chunk, 1), q.device)
+    st = load().mhla_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                    B, H, N, d, chunk, _dtype(q), eps, _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("mhla_forward_causal", st)
+    return y
+
+
+def linattn_decode_step(q, k, v, S, z, out, *, eps=1e-6, den_out=None, stream=None):
+    """One recurrent decode step; q/k/v/out [B, H, d], S [B, H, d, d] fp32, z [B, H, d] fp32 (updated)."""
+    _need_cuda(q, k, v, S, z, out, den_out)
+    B, H, d = q.shape
+    st = load().linattn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out),
+                                    _ptr(den_out), B, H, d, _dtype(q), eps, _stream(stream))
+    _check("linattn_decode_step", st)
+    return out
+
+
+def rala_forward(q, k, v, x, w, y, *, workspace=None, stream=None):
+    """Rank-augmented linear attention; q/k/v/y [B, H, N, d], x [B, N, cx], w [cx, d]."""
+    _need_cuda(q, k, v, x, w, y, workspace)
+    B, H, N, d = q.shape
+    cx = x.shape[-1]
+    if workspace is None:
+        workspace = new_workspace(rala_workspace_bytes(B, H, N, d, cx), q.device)
+    st = load().rala_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(x), _ptr(w), _ptr(y), B, H, N, d, cx,
+                             _dtype(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(stream))
+    _check("rala_forward", st)
+    return y
+
+
+def mhla_query_status(workspace, stream=None) -> int:
+    return int(load().mhla_query_status(_ptr(workspace), _stream(stream)))
+
+
+def mhla_launch_count() -> int:
+    return int(load().mhla_launch_count())

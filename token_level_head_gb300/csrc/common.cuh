@@ -1,0 +1,31 @@
+// Device helpers shared by the kernels of the MHLA library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mhla.h"
+
+namespace mhla {
+
+// phi(x) = ELU(x) + 1: x + 1 for x > 0, exp(x) otherwise
+// ("Linear Attention notes" §二, first kernel choice).
+__device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Status word at the start of every workspace: bit 0 = a bounded wait gave up.
+struct WorkspaceHeader {
+  unsigned int status;
+  unsigned int pad[63];  // keeps what follows 256-byte aligned
+};
+
+}  // namespace mhla

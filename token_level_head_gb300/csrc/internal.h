@@ -1,0 +1,41 @@
+// Internal host-side interfaces between the C-ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "mhla.h"
+
+namespace mhla {
+
+// Counts every kernel launch (or graph-captured launch) issued by the library.
+void note_launch(int n = 1);
+
+// How the non-causal / causal MHLA work is split into summary partials.
+struct MhlaShape {
+  int B, H, N, d, block;  // block = block_size (non-causal) or chunk (causal)
+  int heads() const { return B * H; }
+  int M() const { return N / block; }
+};
+
+// Mixing modes of the summary-mixing stage.
+enum MixMode {
+  MIX_FULL = 0,         // S~_i = sum_j m_ij S_j                (non-causal MHLA)
+  MIX_STRICT_LOWER = 1, // S~_i = sum_{j<i} m_ij S_j            (causal MHLA)
+  MIX_PREFIX = 2        // S~_i = sum_{j<i} S_j                 (plain causal linear attention)
+};
+
+// ---- SIMT path (fp32 mode, and every shape the tensor-core path does not take)
+size_t simt_mhla_workspace(const MhlaShape& s);
+cudaError_t simt_mhla_launch(const MhlaShape& s, mhla_dtype dt, const void* q, const void* k,
+                             const void* v, const float* mixing, void* y, float* den_out,
+                             float eps, MixMode mode, void* ws, cudaStream_t st);
+cudaError_t simt_decode_launch(int units, int d, mhla_dtype dt, const void* q, const void* k,
+                               const void* v, float* S, float* z, void* out, float* den_out,
+                               float eps, cudaStream_t st);
+size_t simt_rala_workspace(int B, int H, int N, int d, int cx);
+cudaError_t simt_rala_launch(int B, int H, int N, int d, int cx, mhla_dtype dt, const void* q,
+                             const void* k, const void* v, const void* x, const void* w, void* y,
+                             void* ws, cudaStream_t st);
+
+}  // namespace mhla

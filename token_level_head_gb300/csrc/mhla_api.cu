@@ -1,0 +1,198 @@
+// C-ABI entry points: argument validation, workspace plans and dispatch.
+// The operations and their sources are documented in include/mhla.h.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mhla {
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+
+bool valid_d(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t dtype_bytes(mhla_dtype dt) { return dt == MHLA_F32 ? 4 : 2; }
+
+// [a, a+an) and [b, b+bn) overlap?
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return an != 0 && bn != 0 && x < y + bn && y < x + an;
+}
+
+bool dims_ok(int B, int H, int N) { return B >= 0 && H >= 0 && N >= 0; }
+
+size_t elems(int B, int H, int N, int d) { return (size_t)B * H * N * d; }
+
+mhla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA; }
+
+size_t mhla_ws(int B, int H, int N, int d, int block) {
+  MhlaShape s{B, H, N, d, block};
+  return simt_mhla_workspace(s);
+}
+
+// Shared validation of the Q/K/V/Y/den/workspace arguments of the MHLA entries.
+mhla_status check_mhla(const void* q, const void* k, const void* v, const void* y,
+                       const float* den_out, int B, int H, int N, int d, int block,
+                       mhla_dtype dt, float eps, const void* ws, size_t ws_bytes) {
+  if (!dims_ok(B, H, N) || !valid_d(d)) return MHLA_ERR_INVALID_ARG;
+  if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return MHLA_ERR_INVALID_ARG;
+  if (block <= 0 || (N > 0 && N % block != 0)) return MHLA_ERR_INVALID_ARG;
+  if ((size_t)B * H * N == 0) return MHLA_OK;
+  if (!q || !k || !v || !y) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y)) return MHLA_ERR_INVALID_ARG;
+  if (den_out && !aligned16(den_out)) return MHLA_ERR_INVALID_ARG;
+  const size_t tb = elems(B, H, N, d) * dtype_bytes(dt);
+  if (overlap(y, tb, q, tb) || overlap(y, tb, k, tb) || overlap(y, tb, v, tb))
+    return MHLA_ERR_INVALID_ARG;
+  if (den_out) {
+    const size_t db = (size_t)B * H * N * sizeof(float);
+    if (overlap(den_out, db, q, tb) || overlap(den_out, db, k, tb) || overlap(den_out, db, v, tb) ||
+        overlap(den_out, db, y, tb))
+      return MHLA_ERR_INVALID_ARG;
+  }
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MHLA_ERR_INVALID_ARG;
+  if (ws_bytes < mhla_ws(B, H, N, d, block)) return MHLA_ERR_INVALID_ARG;
+  return MHLA_OK;
+}
+
+}  // namespace
+}  // namespace mhla
+
+using namespace mhla;
+
+extern "C" {
+
+size_t mhla_workspace_bytes(int B, int H, int N, int d, int block_size, int causal) {
+  (void)causal;
+  if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0)) return 0;
+  return mhla_ws(B, H, N, d, block_size);
+}
+
+mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
+                            mhla_dtype dt) {
+  (void)causal;
+  if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0) ||
+      (dt != MHLA_F32 && dt != MHLA_BF16))
+    return MHLA_PATH_NONE;
+  return MHLA_PATH_SIMT;
+}
+
+static mhla_status run_mhla(const void* q, const void* k, const void* v, const float* mixing,
+                            void* y, float* den_out, int B, int H, int N, int d, int block,
+                            MixMode mode, mhla_dtype dt, float eps, void* ws, size_t ws_bytes,
+                            void* stream) {
+  mhla_status st = check_mhla(q, k, v, y, den_out, B, H, N, d, block, dt, eps, ws, ws_bytes);
+  if (st != MHLA_OK || (size_t)B * H * N == 0) return st;
+  if (mode != MIX_PREFIX && (!mixing || !aligned16(mixing))) return MHLA_ERR_INVALID_ARG;
+  MhlaShape s{B, H, N, d, block};
+  return from_cuda(simt_mhla_launch(s, dt, q, k, v, mixing, y, den_out, eps, mode, ws,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+mhla_status mhla_forward(const void* q, const void* k, const void* v, const float* mixing,
+                         void* y, float* den_out, int B, int H, int N, int d, int block_size,
+                         int causal, mhla_dtype dt, float eps, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (causal != 0 && causal != 1) return MHLA_ERR_INVALID_ARG;
+  if (causal)
+    return mhla_forward_causal(q, k, v, mixing, y, den_out, B, H, N, d, block_size, dt, eps,
+                               workspace, workspace_bytes, stream);
+  return run_mhla(q, k, v, mixing, y, den_out, B, H, N, d, block_size, MIX_FULL, dt, eps,
+                  workspace, workspace_bytes, stream);
+}
+
+mhla_status mhla_forward_causal(const void* q, const void* k, const void* v, const float* mixing,
+                                void* y, float* den_out, int B, int H, int N, int d, int chunk,
+                                mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return run_mhla(q, k, v, mixing, y, den_out, B, H, N, d, chunk,
+                  mixing ? MIX_STRICT_LOWER : MIX_PREFIX, dt, eps, workspace, workspace_bytes,
+                  stream);
+}
+
+mhla_status linattn_decode_step(const void* q, const void* k, const void* v, float* S, float* z,
+                                void* out, float* den_out, int B, int H, int d, mhla_dtype dt,
+                                float eps, void* stream) {
+  if (B < 0 || H < 0 || !valid_d(d)) return MHLA_ERR_INVALID_ARG;
+  if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return MHLA_ERR_INVALID_ARG;
+  const size_t units = (size_t)B * H;
+  if (units == 0) return MHLA_OK;
+  if (!q || !k || !v || !S || !z || !out) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) || !aligned16(z) ||
+      !aligned16(out) || (den_out && !aligned16(den_out)))
+    return MHLA_ERR_INVALID_ARG;
+  const size_t vb = units * d * dtype_bytes(dt), sb = units * d * d * sizeof(float),
+               zb = units * d * sizeof(float);
+  if (overlap(out, vb, q, vb) || overlap(out, vb, k, vb) || overlap(out, vb, v, vb) ||
+      overlap(out, vb, S, sb) || overlap(out, vb, z, zb) || overlap(S, sb, z, zb) ||
+      overlap(S, sb, q, vb) || overlap(S, sb, k, vb) || overlap(S, sb, v, vb))
+    return MHLA_ERR_INVALID_ARG;
+  if (units > 0x7fffffffu) return MHLA_ERR_UNSUPPORTED;
+  return from_cuda(simt_decode_launch((int)units, d, dt, q, k, v, S, z, out, den_out, eps,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t rala_workspace_bytes(int B, int H, int N, int d, int cx) {
+  if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256) return 0;
+  return simt_rala_workspace(B, H, N, d, cx);
+}
+
+mhla_status rala_forward(const void* q, const void* k, const void* v, const void* x,
+                         const void* w, void* y, int B, int H, int N, int d, int cx,
+                         mhla_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256)
+    return MHLA_ERR_INVALID_ARG;
+  if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
+  if ((size_t)B * H * N == 0) return MHLA_OK;
+  if (!q || !k || !v || !x || !w || !y) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(x) || !aligned16(w) ||
+      !aligned16(y))
+    return MHLA_ERR_INVALID_ARG;
+  if ((size_t)cx * d > 16384) return MHLA_ERR_UNSUPPORTED;
+  const size_t tb = elems(B, H, N, d) * dtype_bytes(dt);
+  const size_t xb = (size_t)B * N * cx * dtype_bytes(dt), wb = (size_t)cx * d * dtype_bytes(dt);
+  if (overlap(y, tb, q, tb) || overlap(y, tb, k, tb) || overlap(y, tb, v, tb) ||
+      overlap(y, tb, x, xb) || overlap(y, tb, w, wb))
+    return MHLA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHLA_ERR_INVALID_ARG;
+  if (workspace_bytes < simt_rala_workspace(B, H, N, d, cx)) return MHLA_ERR_INVALID_ARG;
+  return from_cuda(simt_rala_launch(B, H, N, d, cx, dt, q, k, v, x, w, y, workspace,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+mhla_status mhla_query_status(void* workspace, void* stream) {
+  if (!workspace) return MHLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MHLA_ERR_CUDA;
+  unsigned int flag = 0;
+  auto* hdr = static_cast<WorkspaceHeader*>(workspace);
+  if (cudaMemcpy(&flag, &hdr->status, sizeof(flag), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MHLA_ERR_CUDA;
+  if (flag == 0) return MHLA_OK;
+  const unsigned int zero = 0;
+  if (cudaMemcpy(&hdr->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MHLA_ERR_CUDA;
+  return MHLA_ERR_TIMEOUT;
+}
+
+const char* mhla_status_string(mhla_status s) {
+  switch (s) {
+    case MHLA_OK: return "ok";
+    case MHLA_ERR_INVALID_ARG: return "invalid argument";
+    case MHLA_ERR_UNSUPPORTED: return "unsupported argument combination";
+    case MHLA_ERR_CUDA: return "CUDA error";
+    case MHLA_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+unsigned long long mhla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

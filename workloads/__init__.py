@@ -9,12 +9,25 @@ neither of them.
 from .gen import (  # noqa: F401
     SEED_BASE,
     TID,
-    normal,
-    uniform,
     bf16_bits,
-    bf16_round,
     bf16_bits_to_f64,
+    bf16_round,
+    normal,
+    normal_at,
+    normal_device,
     row_softmax_mixing,
+    uniform,
+    uniform_at,
     uniform_row_normalised_mixing,
 )
-from .configs import WORKLOADS, Workload, make_mhla_inputs, make_rala_inputs, make_decode_inputs  # noqa: F401
+from .configs import (  # noqa: F401
+    WORKLOADS,
+    Workload,
+    decode_device,
+    decode_host,
+    make_mixing,
+    mhla_device,
+    mhla_host,
+    rala_device,
+    rala_host,
+)

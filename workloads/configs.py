@@ -5,6 +5,11 @@ datasets and trained weights behind them are not needed for a forward-path
 kernel): DiT-S/2-like 64x64 latent token grids, a 256x256 high-resolution
 token grid, long causal sequences with recurrent decode, and the 56x56
 rank-augmented vision stage.  Seeds are ``SEED_BASE + index``.
+
+``*_host`` functions return numpy arrays (device representation plus the
+float64 values the oracle consumes) for the whole workload or a listed
+subset; ``*_device`` functions return the full workload as torch tensors
+generated on a device from the same streams.
 """
 
 from __future__ import annotations
@@ -13,8 +18,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, normal,
-                  row_softmax_mixing, uniform_row_normalised_mixing)
+from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, normal, normal_at,
+                  normal_device, row_softmax_mixing, uniform_row_normalised_mixing)
 
 
 @dataclass(frozen=True)
@@ -24,7 +29,7 @@ class Workload:
     kind: str               # "mhla" | "causal" | "decode" | "rala"
     B: int
     H: int
-    N: int
+    N: int                  # tokens (decode: number of steps)
     d: int
     block: int = 0          # MHLA block size, or causal chunk
     dtype: str = "bf16"     # "f32" | "bf16"
@@ -73,86 +78,118 @@ def _as_dtype(x64: np.ndarray, dtype: str):
     return f, f.astype(np.float64)
 
 
-def _heads_tensor(wl: Workload, tid: int, scale: float, heads, n: int, d: int, lead=None):
-    """[B, H, n, d] tensor, or only the listed (b, h) slices stacked as [1, len(heads), n, d]."""
-    if heads is None:
-        return normal(wl.seed, tid, (wl.B, wl.H, n, d), scale)
-    per = n * d
-    out = np.empty((1, len(heads), n, d))
-    for i, (b, h) in enumerate(heads):
-        out[0, i] = normal(wl.seed, tid, (n, d), scale, offset=(b * wl.H + h) * per)
-    return out
+def _torch_dtype(dtype: str):
+    import torch
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
 
 
 def make_mixing(wl: Workload) -> np.ndarray:
-    """[H, M, M] float64 mixing matrix of a workload (rows: query blocks)."""
+    """[H, M, M] float64 mixing matrix of a workload (rows: query blocks), already float32-exact."""
     if wl.mixing == "uniform_rows":
-        return uniform_row_normalised_mixing(wl.seed, wl.H, wl.M)
-    if wl.mixing == "softmax_diag2":
-        return row_softmax_mixing(wl.seed, wl.H, wl.M, diag_boost=2.0)
-    if wl.mixing == "softmax":
-        return row_softmax_mixing(wl.seed, wl.H, wl.M)
-    if wl.mixing == "ones":
-        return np.ones((wl.H, wl.M, wl.M))
-    raise ValueError(f"workload {wl.name} has no mixing")
+        m = uniform_row_normalised_mixing(wl.seed, wl.H, wl.M)
+    elif wl.mixing == "softmax_diag2":
+        m = row_softmax_mixing(wl.seed, wl.H, wl.M, diag_boost=2.0)
+    elif wl.mixing == "softmax":
+        m = row_softmax_mixing(wl.seed, wl.H, wl.M)
+    elif wl.mixing == "ones":
+        m = np.ones((wl.H, wl.M, wl.M))
+    else:
+        raise ValueError(f"workload {wl.name} has no mixing")
+    return m.astype(np.float32).astype(np.float64)
 
 
-def make_mhla_inputs(wl: Workload, heads=None) -> dict:
-    """Q, K, V (and mixing for MHLA) of an MHLA or causal workload.
+# ------------------------------------------------------------ MHLA / causal
+def mhla_host(wl: Workload, heads=None) -> dict:
+    """Q, K, V (and mixing) of an MHLA or causal workload, on the host.
 
-    Returns device representations (``q, k, v``: float32 or uint16 bf16 bits;
-    ``mixing``: float32 [H, M, M]) and the float64 values the oracle consumes
-    (``q64, k64, v64, mixing64``).  With ``heads`` = list of (b, h), only
-    those slices are generated, as [1, len(heads), N, d] (mixing rows follow
+    ``q, k, v``: float32 arrays or uint16 bf16 bits; ``q64, k64, v64``: the
+    float64 values the oracle consumes; ``mixing`` (float32 [H, M, M]) and
+    ``mixing64`` for MHLA workloads.  With ``heads`` = list of (b, h) only
+    those slices are produced, as [1, len(heads), N, d] (mixing rows follow
     the listed heads).
     """
     out = {}
+    per = wl.N * wl.d
     for name in ("q", "k", "v"):
-        x = _heads_tensor(wl, TID[name], wl.scale, heads, wl.N, wl.d)
+        if heads is None:
+            x = normal(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), wl.scale)
+        else:
+            x = np.stack([normal(wl.seed, TID[name], (wl.N, wl.d), wl.scale, offset=(b * wl.H + h) * per)
+                          for b, h in heads])[None]
         out[name], out[name + "64"] = _as_dtype(x, wl.dtype)
-    if wl.kind == "mhla":
+    if wl.mixing != "none":
         mix = make_mixing(wl)
         if heads is not None:
             mix = mix[[h for _, h in heads]]
+        out["mixing64"] = mix
         out["mixing"] = mix.astype(np.float32)
-        out["mixing64"] = out["mixing"].astype(np.float64)
     return out
 
 
-def make_decode_inputs(wl: Workload, units=None, steps=None) -> dict:
-    """Prefix K, V and per-step q, k, v of the decode workload.
+def mhla_device(wl: Workload, device="cuda") -> dict:
+    """The full MHLA / causal workload as device tensors (same values as :func:`mhla_host`)."""
+    import torch
+    dt = _torch_dtype(wl.dtype)
+    out = {name: normal_device(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), wl.scale, device=device, dtype=dt)
+           for name in ("q", "k", "v")}
+    if wl.mixing != "none":
+        out["mixing"] = torch.from_numpy(make_mixing(wl).astype(np.float32)).to(device)
+    return out
 
-    Shapes: ``prefix_k/v`` [P, U, d] and ``step_q/k/v`` [T, U, d] where the U
-    = B*H (batch x head) units are flattened; ``units`` restricts to a list of
-    unit indices.  Step t of unit u is element (t, u) of the step tensors.
+
+# ------------------------------------------------------------------ decode
+def _decode_index(u_all: int, d: int, steps, units) -> np.ndarray:
+    t = np.asarray(steps, dtype=np.uint64)[:, None, None]
+    u = np.asarray(units, dtype=np.uint64)[None, :, None]
+    c = np.arange(d, dtype=np.uint64)[None, None, :]
+    return (t * np.uint64(u_all * d) + u * np.uint64(d) + c)
+
+
+def decode_host(wl: Workload, units, steps=None) -> dict:
+    """Prefix K, V and per-step q, k, v of the decode workload for the listed units.
+
+    The U = B*H (batch x head) units are flattened; a tensor of T rows is
+    [T, U, d] with element (t, u, c) at flat index (t * U + u) * d + c.
+    Returns [P or T, len(units), d] arrays (device representation and
+    float64 values).
     """
     u_all = wl.B * wl.H
-    units = list(range(u_all)) if units is None else list(units)
     steps = wl.N if steps is None else steps
     p = wl.extra["prefix"]
     out = {}
-    for name, tid, length in (("prefix_k", TID["prefix_k"], p), ("prefix_v", TID["prefix_v"], p),
-                              ("step_q", TID["step_q"], steps), ("step_k", TID["step_k"], steps),
-                              ("step_v", TID["step_v"], steps)):
-        arr = np.empty((length, len(units), wl.d))
-        for t in range(length):
-            row = normal(wl.seed, tid, (u_all, wl.d), wl.scale, offset=t * u_all * wl.d)
-            arr[t] = row[units]
-        out[name], out[name + "64"] = _as_dtype(arr, wl.dtype)
+    for name, length in (("prefix_k", p), ("prefix_v", p), ("step_q", steps), ("step_k", steps),
+                         ("step_v", steps)):
+        idx = _decode_index(u_all, wl.d, range(length), units)
+        x = normal_at(wl.seed, TID[name], idx.reshape(-1), wl.scale).reshape(idx.shape)
+        out[name], out[name + "64"] = _as_dtype(x, wl.dtype)
     return out
 
 
-def make_rala_inputs(wl: Workload, batches=None) -> dict:
-    """Q, K, V [B, H, N, d], X [B, N, Cx], W [Cx, d] of the rank-augmented workload.
+def decode_device(wl: Workload, device="cuda", steps=None) -> dict:
+    """Full decode workload on a device: prefix_k/v [P, B, H, d], step_q/k/v [T, B, H, d]."""
+    steps = wl.N if steps is None else steps
+    p = wl.extra["prefix"]
+    dt = _torch_dtype(wl.dtype)
+    out = {}
+    for name, length in (("prefix_k", p), ("prefix_v", p), ("step_q", steps), ("step_k", steps),
+                         ("step_v", steps)):
+        out[name] = normal_device(wl.seed, TID[name], (length, wl.B, wl.H, wl.d), wl.scale,
+                                  device=device, dtype=dt)
+    return out
+
+
+# -------------------------------------------------------------------- RALA
+def rala_host(wl: Workload, batches=None) -> dict:
+    """Q, K, V [B', H, N, d], X [B', N, Cx], W [Cx, d] of the rank-augmented workload.
 
     Q, K, V ~ N(0, 1/d); X ~ N(0, 1); W ~ N(0, 1/Cx).  ``batches`` restricts
-    to a list of batch indices.
+    to a list of batch indices (B' = len(batches)).
     """
     cx = wl.extra["cx"]
     batches = list(range(wl.B)) if batches is None else list(batches)
     out = {}
+    per = wl.H * wl.N * wl.d
     for name in ("q", "k", "v"):
-        per = wl.H * wl.N * wl.d
         arr = np.stack([normal(wl.seed, TID[name], (wl.H, wl.N, wl.d), wl.scale, offset=b * per)
                         for b in batches])
         out[name], out[name + "64"] = _as_dtype(arr, wl.dtype)
@@ -161,4 +198,14 @@ def make_rala_inputs(wl: Workload, batches=None) -> dict:
     out["x"], out["x64"] = _as_dtype(x, wl.dtype)
     w = normal(wl.seed, TID["w"], (cx, wl.d), cx ** -0.5)
     out["w"], out["w64"] = _as_dtype(w, wl.dtype)
+    return out
+
+
+def rala_device(wl: Workload, device="cuda") -> dict:
+    cx = wl.extra["cx"]
+    dt = _torch_dtype(wl.dtype)
+    out = {name: normal_device(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), wl.scale, device=device, dtype=dt)
+           for name in ("q", "k", "v")}
+    out["x"] = normal_device(wl.seed, TID["x"], (wl.B, wl.N, cx), 1.0, device=device, dtype=dt)
+    out["w"] = normal_device(wl.seed, TID["w"], (cx, wl.d), cx ** -0.5, device=device, dtype=dt)
     return out
