@@ -136,6 +136,30 @@ mhla_status rala_forward(const void* q, const void* k, const void* v, const void
                          const void* w, void* y, int B, int H, int N, int d, int cx,
                          mhla_dtype dt, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Scratch held by mhla_forward_noalloc on every GPU that loads the library. */
+#define MHLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
+
+/* Non-causal MHLA forward that allocates nothing and takes no workspace.
+ * The paper has no counterpart: this exists for callers that cannot obtain
+ * device memory for a workspace (no allocator is available to them, or they
+ * must not allocate after start-up, e.g. inside a host framework that owns a
+ * fixed memory pool).  The result is that of mhla_forward(..., causal = 0,
+ * ...) computed by the SIMT kernels; all arguments mean the same.
+ *   Scratch: a file-scope device array of MHLA_NOALLOC_SCRATCH_BYTES per GPU,
+ *   reserved when the library is loaded and held until the process exits.
+ *   Sizes whose scratch need exceeds it return MHLA_ERR_UNSUPPORTED before
+ *   any launch (the DiT-like B8 H6 N4096 d64 M16 case needs 25.2 MB).
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   outside any stream capture.
+ *   Every call uses the same array; nothing in it needs to start at zero,
+ *   but calls whose kernels overlap on the GPU (other streams, other host
+ *   threads) race on it and must be serialised by the caller.
+ *   Errors as for mhla_forward; no cudaMalloc/cudaFree is ever called. */
+mhla_status mhla_forward_noalloc(const void* q, const void* k, const void* v, const float* mixing,
+                                 void* y, float* den_out, int B, int H, int N, int d,
+                                 int block_size, mhla_dtype dt, float eps, void* stream);
+
 /* Kernel family mhla_forward would use for these arguments (no launch). */
 mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
                             mhla_dtype dt);

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     load,
     mhla_forward,
     mhla_forward_causal,
+    mhla_forward_noalloc,
     mhla_forward_path,
     mhla_launch_count,
     mhla_query_status,

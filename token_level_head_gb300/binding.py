@@ -35,6 +35,7 @@ _SIGNATURES = {
     "mhla_query_status": (_i, [_vp, _vp]),
     "mhla_status_string": (ctypes.c_char_p, [_i]),
     "mhla_launch_count": (ctypes.c_ulonglong, []),
+    "mhla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -159,6 +160,20 @@ def rala_forward(q, k, v, x, w, y, *, workspace=None, stream=None):
                              _dtype(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream))
     _check("rala_forward", st)
+    return y
+
+
+def mhla_forward_noalloc(q, k, v, mixing, y, block_size, *, eps=1e-6, den_out=None, stream=None):
+    """Non-causal MHLA forward with no workspace: for callers that cannot allocate device memory.
+
+    The library keeps a fixed 32 MiB scratch array per GPU for it; calls that
+    overlap on the GPU share that array and must not run concurrently.
+    """
+    _need_cuda(q, k, v, mixing, y, den_out)
+    B, H, N, d = q.shape
+    st = load().mhla_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                     B, H, N, d, block_size, _dtype(q), eps, _stream(stream))
+    _check("mhla_forward_noalloc", st)
     return y
 
 
