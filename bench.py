@@ -177,7 +177,7 @@ class ClockSampler:
 class Runner:
     """Device buffers and the per-step call of one workload (R rotating sets)."""
 
-    def __init__(self, wl, device, l2_bytes):
+    def __init__(self, wl, device, l2_bytes, sets=0):
         import torch
         from token_level_head_gb300 import binding
         import workloads
@@ -185,7 +185,7 @@ class Runner:
         self.wl, self.binding, self.torch = wl, binding, torch
         self.device = device
         step_bytes = workload_bytes(wl)
-        self.R = max(1, min(16, math.ceil(3 * l2_bytes / step_bytes)))
+        self.R = sets if sets > 0 else max(1, min(16, math.ceil(3 * l2_bytes / step_bytes)))
         if wl.kind == "decode":
             self.R = 1  # the recurrent state is carried from one step to the next
         self.sets = []
@@ -307,7 +307,7 @@ def run_ours(args, wl, rank, world, local_rank):
     binding.load()
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
-    runner = Runner(wl, device, l2)
+    runner = Runner(wl, device, l2, args.sets)
 
     # eager warm-up (lazy initialisation), then capture
     for i in range(max(1, args.warmup)):
@@ -540,6 +540,8 @@ def main(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--sets", type=int, default=0,
+                   help="rotating input sets (default: enough to exceed 3x L2); 1 for small profiler captures")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")

@@ -111,6 +111,52 @@ def test_small_shapes(shape, dtype):
     assert_close_den(den, dref, dtype)
 
 
+TC_SHAPES = [  # bf16, d = 64, blocks of whole 128-token tiles: the tcgen05 kernel
+    (1, 1, 128, 64, 128),     # one chunk, M = 1
+    (2, 3, 2048, 64, 128),    # M = 16, one chunk per block
+    (1, 2, 4096, 64, 4096),   # M = 1 with 32 chunks (split block sums)
+    (1, 1, 8192, 64, 128),    # M = 64, one chunk per block
+    (3, 5, 640, 64, 128),     # odd head count, M = 5
+    (2, 1, 1536, 64, 512),    # 4 chunks per block
+]
+
+
+@pytest.mark.parametrize("shape", TC_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tcgen05_shapes(shape):
+    B, H, N, d, block = shape
+    assert binding.mhla_forward_path(B, H, N, d, block, 0, torch.bfloat16) == "tcgen05"
+    x = rand_inputs(400 + N + B * H, (B, H, N, d), "bf16")
+    mix_t, mix64 = rand_mixing(11 + block, H, N // block)
+    y, den = forward(x["q"], x["k"], x["v"], mix_t, block)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block)
+    assert_close_y(y, ref, "bf16")
+    assert_close_den(den, dref, "bf16")
+
+
+def test_bench_workloads_take_the_tensor_core_path():
+    for name in ("dit", "hires", "hires_m1"):
+        wl = WORKLOADS[name]
+        assert binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block, 0, torch.bfloat16) == "tcgen05"
+
+
+def test_workspace_reuse_across_shapes_and_paths():
+    """One zero-filled workspace, reused by SIMT and tcgen05 calls of different sizes, stays valid."""
+    shapes = [(2, 2, 512, 64, 128, "bf16"), (1, 2, 256, 16, 64, "f32"), (4, 6, 1024, 64, 256, "bf16"),
+              (1, 1, 256, 64, 128, "bf16"), (4, 6, 1024, 64, 256, "bf16")]
+    big = max(binding.mhla_workspace_bytes(B, H, N, d, blk) for B, H, N, d, blk, _ in shapes)
+    ws = binding.new_workspace(big, "cuda")
+    for i, (B, H, N, d, blk, dt) in enumerate(shapes):
+        x = rand_inputs(500 + i, (B, H, N, d), dt)
+        mix_t, mix64 = rand_mixing(13 + i, H, N // blk)
+        y = torch.empty_like(x["q"])
+        den = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+        binding.mhla_forward(x["q"], x["k"], x["v"], mix_t, y, blk, den_out=den, workspace=ws)
+        assert binding.mhla_query_status(ws) == 0
+        ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, blk)
+        assert_close_y(to_f64(y), ref, dt)
+        assert_close_den(to_f64(den), dref, dt)
+
+
 def test_extreme_values_fp32():
     """Large |Q|, |K| exercise both branches of phi far from 0 (exp underflow, big linear values)."""
     B, H, N, d, block = 1, 2, 256, 32, 64

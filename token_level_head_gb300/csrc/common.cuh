@@ -28,4 +28,15 @@ struct WorkspaceHeader {
   unsigned int pad[63];  // keeps what follows 256-byte aligned
 };
 
+// Every workspace starts with the header and a fixed counter region used by
+// the persistent kernels (ticket, finished, two per-head counters for up to
+// kMaxCounterHeads heads).  The kernels leave these counters at zero when
+// they exit and no kernel writes data into the region, so a workspace that
+// was zero-filled once stays valid for any later call, shape or path.
+constexpr int kMaxCounterHeads = 65536;
+constexpr size_t kCounterOffset = sizeof(WorkspaceHeader);
+constexpr size_t kWorkspacePrefix =
+    ((sizeof(WorkspaceHeader) + (2 + 2 * (size_t)kMaxCounterHeads) * sizeof(unsigned)) + 255) &
+    ~size_t(255);
+
 }  // namespace mhla

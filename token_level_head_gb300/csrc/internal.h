@@ -25,6 +25,13 @@ enum MixMode {
   MIX_PREFIX = 2        // S~_i = sum_{j<i} S_j                 (plain causal linear attention)
 };
 
+// ---- tcgen05 path (bf16, d = 64, blocks of whole 128-token tiles)
+bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
+size_t tc_mhla_workspace(const MhlaShape& s);
+cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
+                           const float* mixing, void* y, float* den_out, float eps, MixMode mode,
+                           void* ws, cudaStream_t st);
+
 // ---- SIMT path (fp32 mode, and every shape the tensor-core path does not take)
 size_t simt_mhla_workspace(const MhlaShape& s);
 cudaError_t simt_mhla_launch(const MhlaShape& s, mhla_dtype dt, const void* q, const void* k,

@@ -32,7 +32,9 @@ mhla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MHLA_OK : MHLA_
 
 size_t mhla_ws(int B, int H, int N, int d, int block) {
   MhlaShape s{B, H, N, d, block};
-  return simt_mhla_workspace(s);
+  const size_t a = simt_mhla_workspace(s);
+  const size_t b = tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0;
+  return a > b ? a : b;
 }
 
 // Shared validation of the Q/K/V/Y/den/workspace arguments of the MHLA entries.
@@ -76,11 +78,11 @@ size_t mhla_workspace_bytes(int B, int H, int N, int d, int block_size, int caus
 
 mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
                             mhla_dtype dt) {
-  (void)causal;
   if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0) ||
-      (dt != MHLA_F32 && dt != MHLA_BF16))
+      (dt != MHLA_F32 && dt != MHLA_BF16) || (causal != 0 && causal != 1))
     return MHLA_PATH_NONE;
-  return MHLA_PATH_SIMT;
+  const MhlaShape s{B, H, N, d, block_size};
+  return tc_mhla_supported(s, dt, causal ? MIX_PREFIX : MIX_FULL) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
 
 static mhla_status run_mhla(const void* q, const void* k, const void* v, const float* mixing,
@@ -91,6 +93,9 @@ static mhla_status run_mhla(const void* q, const void* k, const void* v, const f
   if (st != MHLA_OK || (size_t)B * H * N == 0) return st;
   if (mode != MIX_PREFIX && (!mixing || !aligned16(mixing))) return MHLA_ERR_INVALID_ARG;
   MhlaShape s{B, H, N, d, block};
+  if (tc_mhla_supported(s, dt, mode))
+    return from_cuda(tc_mhla_launch(s, q, k, v, mixing, y, den_out, eps, mode, ws,
+                                    static_cast<cudaStream_t>(stream)));
   return from_cuda(simt_mhla_launch(s, dt, q, k, v, mixing, y, den_out, eps, mode, ws,
                                     static_cast<cudaStream_t>(stream)));
 }

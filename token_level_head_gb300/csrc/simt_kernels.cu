@@ -232,7 +232,7 @@ SimtPlan simt_plan(const MhlaShape& s) {
   p.P = s.block / p.chunk;
   p.parts = s.N / p.chunk;
   const size_t heads = (size_t)s.heads(), dd = (size_t)s.d * s.d;
-  size_t off = sizeof(WorkspaceHeader);
+  size_t off = kWorkspacePrefix;
   p.off_spart = off; off = align256(off + heads * p.parts * dd * sizeof(float));
   p.off_zpart = off; off = align256(off + heads * p.parts * s.d * sizeof(float));
   p.off_smix = off;  off = align256(off + heads * s.M() * dd * sizeof(float));
@@ -492,7 +492,7 @@ RalaPlan rala_plan(int B, int H, int N, int d) {
   RalaPlan p;
   p.ntiles = (N + kRalaTile - 1) / kRalaTile;
   const size_t heads = (size_t)B * H;
-  size_t off = sizeof(WorkspaceHeader);
+  size_t off = kWorkspacePrefix;
   p.off_qpart = off; off = align256(off + heads * p.ntiles * d * sizeof(float));
   p.off_bpart = off; off = align256(off + heads * p.ntiles * (size_t)d * d * sizeof(float));
   p.off_m = off;     off = align256(off + heads * p.ntiles * sizeof(float));
