@@ -7,24 +7,29 @@
 //   Y_t = phi(Q_t) S~_i / (phi(Q_t) . z~_i + eps)                           (output)
 // with phi = ELU + 1 and eps from "Linear Attention notes" §四/§五.
 //
-// Work is split into units handed out by a global ticket counter:
-//   SUM (head, 128-token chunk): TMA K, V tiles -> phi(K) in smem -> one
-//       tcgen05.mma chain D = V^T phi(K) (M = N = 64, K = 128) gives the
-//       chunk's S^T partial in TMEM; z partial by a CUDA-core reduction.
-//       fp32 partials to L2, one contiguous 128-byte row per thread.
-//   MIX (head, slice of the 64*64+64 summary entries): sums the partials of
-//       each block and mixes them for every query block; writes S~ (bf16, in
-//       the K-major layout the output MMA reads) and z~ (fp32).  Four entries
-//       per thread (float4), G threads per 4-entry vector chosen on the host.
-//       The MIX units of head h are placed in the ticket order a few heads
-//       after its SUM units, so they run while other CTAs keep streaming.
-//   OUT (head, 128-token tile): TMA Q tile -> phi(Q) in smem and the fp32
-//       denominator phi(Q) . z~ on CUDA cores -> tcgen05.mma (M = 128,
-//       N = 64, K = 64) against S~ -> divide in registers -> bf16 -> TMA store.
-// A unit only ever waits (bounded) on units with smaller tickets, which are
-// held by running CTAs, so there is no deadlock whatever the residency.
-// Each CTA prefetches the next unit's TMA inputs as soon as its tensor-core
-// work has consumed the current ones.
+// One CTA per SM (cooperative launch), 16 warps, a SUM pass, a MIX phase and
+// an OUT pass; every hand-over inside a CTA is an mbarrier ring:
+//   warp 0      TMA producer: the CTA's SUM chunks (K and V tiles), then its
+//               OUT chunks (Q tile at once; S~ tile and z~ of the chunk's block
+//               once every CTA has finished the MIX phase)
+//   warps 8-15  phi: phi in place on each K / Q tile, 16 rows a warp; for an
+//               OUT chunk also the fp32 denominator phi(Q_t) . z~ + eps
+//   warp 1      MMA issuer (one thread): SUM  D = [V^T ; 1] phi(K)  (M 128,
+//               N 64, K 128): rows 0-63 are the chunk's S^T, rows 64-127 its z;
+//               OUT  D = phi(Q) S~  (M 128, N 64, K 64); four TMEM accumulators
+//   warps 4-7   epilogue, one TMEM lane quadrant each: SUM -> the chunk's
+//               partial (S^T bf16, z fp32) to global; OUT -> Y = D / den in
+//               bf16, TMA store of the warp's 32 rows
+//   warps 2-15  MIX phase, between the passes, behind a grid barrier on all
+//               SUM partials: each CTA takes a range of summary rows (64 rows
+//               of S^T and the z row per head), sums the chunk partials of each
+//               block and mixes the block sums for every query block; writes
+//               S~^T (bf16, the K-major layout the OUT MMA reads) and z~ (fp32),
+//               then arrives at a second grid barrier
+// Chunks go to CTAs with stride gridDim.x.  The producer keeps loading Q tiles
+// during the MIX phase, so HBM stays busy across it.  The grid barriers need
+// every CTA resident (one per SM, cooperative launch).  All waits are bounded:
+// on time-out the kernel sets the status word and winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,487 +44,601 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
-constexpr int kTile = 128;                   // tokens per SUM / OUT unit
-constexpr int kD = 64;                       // head dimension of this kernel
-constexpr int kTileBytes = kTile * kD * 2;   // 16 KB bf16 tile
-constexpr int kSTileBytes = kD * kD * 2;     // 8 KB bf16 S~ tile
-constexpr int kEnt = kD * kD + kD;           // summary entries: S^T (e*64 + c), then z
-constexpr int kCtasPerSm = 3;
-constexpr uint32_t kTmemCols = 64;
-constexpr uint32_t kSpinBudget = 1u << 24;
-constexpr int kMixBytes = 16384;             // MIX staging: at most 1024 float4
+constexpr int kThreads = 512;
+constexpr int kTile = 128;                  // tokens per chunk
+constexpr int kD = 64;                      // head dimension of this kernel
+constexpr int kTileBytes = kTile * kD * 2;  // 16 KB bf16 tile
+constexpr int kStageBytes = 2 * kTileBytes; // SUM: K, V.  OUT: Q, S~^T (8 KB), z~ (256 B)
+constexpr int kSTile = kD * kD * 2;         // 8 KB S~^T tile
+constexpr int kNA = 4;                      // TMEM accumulators, 64 columns each
+constexpr uint32_t kTmemCols = kNA * 64;
+constexpr int kMixRows = kD + 1;            // MIX rows per head: 64 of S^T, then z
+constexpr uint64_t kWaitLimitNs = 500000000ull;  // a wait gives up after 0.5 s
 
-enum { UNIT_SUM = 0, UNIT_MIX = 1, UNIT_OUT = 2 };
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpMix = 2, kWarpEpi = 4, kWarpPhi = 8;
+constexpr int kMixThreads = (16 - kWarpMix) * 32;  // warps 2-15 run the MIX phase
+constexpr int kPhiWarps = 8;
+constexpr int kBarMix = 1;                  // named barrier of the MIX phase (0 is __syncthreads)
 
-struct Params {
-  CUtensorMap tm_q, tm_k, tm_v, tm_y;  // [heads*N rows][64] bf16, box 64 x 128
-  CUtensorMap tm_s;                    // S~ [heads*M*64 rows][64] bf16, box 64 x 64
-  const float* mixing;                 // [H][M][M]
-  float* s_part;                       // [heads][C][64 e][64 c]
-  float* z_part;                       // [heads][C][64]
-  __nv_bfloat16* s_mix;                // [heads][M][64 e][64 c]
-  float* z_mix;                        // [heads][M][64]
-  float* den_out;                      // [heads][N] or null
-  unsigned* ctr;                       // ticket, finished, sum_done[heads], mix_done[heads]
-  unsigned* status;
-  int heads, H, N, M, C, cpb;          // C = chunks per head, cpb = chunks per block
-  int L, I, T1, total;                 // lag (heads), MIX items per head, tickets before OUT, all
-  int G, nvec, split;                  // MIX: threads per vector, vectors per item, threads per block (G >= M)
-  float eps;
-  int mode;                            // MixMode
-};
+constexpr int kMaxNS = 5;
 
 struct Small {
-  float zt[kD];              // z~ of the current OUT tile (bulk-copied; 16-byte aligned)
-  float den_half[2][kTile];
-  float zred[8][kD];
-  uint64_t bar_in, bar_s, bar_mma;
+  uint64_t full[kMaxNS], ready[kMaxNS], empty[kMaxNS];
+  uint64_t acc_full[kNA], acc_empty[kNA];
   uint32_t tbase;
-  int next;
-  int flag;
-  int s_ticket;              // OUT ticket whose S~ / z~ loads are already in flight on bar_s
-  int s_inflight;            // 1 while a bar_s load has been issued and not yet waited for
+  int abort;
+  int last;
+  int prod_q, mma_q;
 };
 
+// Dynamic shared memory, from a 1024-byte aligned base: input ring, ones
+// tile, Y staging (4 warps x 4 KB; during the MIX phase, with the 16 KB after
+// it, the transposed mixing matrix of up to MAXM blocks), den per accumulator
+// and the barriers.
+template <int MAXM>
+struct Layout {
+  static constexpr int NS = 5;                            // stages of the input ring
+  static constexpr int kOffOnes = NS * kStageBytes;       // 16 KB of bf16 ones (A rows 64..127 of SUM)
+  static constexpr int kOffY = kOffOnes + kTileBytes;     // Y staging / mixing matrix
+  static constexpr int kOffDen = kOffY + 32768;           // kNA x 128 fp32
+  static constexpr int kOffSmall = kOffDen + kNA * kTile * 4;
+  static constexpr size_t kBytes = 1024 + kOffSmall + sizeof(Small);
+  static_assert(MAXM * MAXM * 4 <= 32768, "mixing matrix staging");
+  static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+struct Params {
+  CUtensorMap tm_q, tm_k, tm_v;  // [heads*N rows][64] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap tm_y;              // same tensor shape, box 64 x 32
+  const float* mixing;           // [H][M][M], m[h][i][b]
+  __nv_bfloat16* ps;             // chunk partial S^T: [heads * C][64 e][64 c]
+  float* pz;                     // chunk partial z: [heads * C][64]
+  uint8_t* smix;                 // S~^T tiles: [heads * M] x 8 KB, K-major, 128-byte swizzle
+  float* zmix;                   // z~: [heads * M][64]
+  float* den_out;                // [heads * N] or null
+  unsigned* ctr;                 // [1] finished CTAs, [2 + h] chunks summarised, [2 + kMax + h] rows mixed
+  unsigned* status;
+  int heads, H, N, M, C, cpb, TS;  // C = chunks per head, cpb = chunks per block, TS = heads * C
+  float eps;
+};
+
+// ------------------------------------------------------------------ waits
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ bool wait_geq(const unsigned* p, unsigned target) {
-  for (uint32_t it = 0; it < kSpinBudget; ++it) {
-    if (ld_acquire(p) >= target) return true;
-    __nanosleep(it < 16 ? 32 : 256);
-  }
-  return false;
-}
-
-// Every thread waits (bounded) and the CTA agrees on the outcome, so a time-out
-// can never leave some threads at a barrier the others skipped.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity) {
-  return __syncthreads_and(mbar_wait(bar, parity) ? 1 : 0) != 0;
-}
-
-__device__ __forceinline__ float phi_fast(float x) { return x > 0.f ? x + 1.f : __expf(x); }
-
-struct Unit {
-  int kind, h, idx;
-};
-
-// Ticket order: rounds r = 0 .. heads+L-1, round r = [SUM units of head r]
-// [MIX items of head r-L], then every OUT unit head by head.  A MIX item of
-// head h only waits for SUM units of head h and an OUT unit only for MIX
-// items of its head: always smaller tickets.
-__device__ __forceinline__ Unit decode(const Params& p, int t) {
-  Unit u;
-  if (t >= p.T1) {
-    const int o = t - p.T1;
-    u.kind = UNIT_OUT;
-    u.h = o / p.C;
-    u.idx = o - u.h * p.C;
-    return u;
-  }
-  const int head_sum = p.L * p.C;
-  if (t < head_sum) {
-    u.kind = UNIT_SUM;
-    u.h = t / p.C;
-    u.idx = t - u.h * p.C;
-    return u;
-  }
-  const int t2 = t - head_sum;
-  const int mid = (p.heads - p.L) * (p.C + p.I);
-  if (t2 < mid) {
-    const int r = t2 / (p.C + p.I), off = t2 - r * (p.C + p.I);
-    if (off < p.C) {
-      u.kind = UNIT_SUM;
-      u.h = p.L + r;
-      u.idx = off;
-    } else {
-      u.kind = UNIT_MIX;
-      u.h = r;
-      u.idx = off - p.C;
-    }
-    return u;
-  }
-  const int t3 = t2 - mid;
-  u.kind = UNIT_MIX;
-  u.h = p.heads - p.L + t3 / p.I;
-  u.idx = t3 - (u.h - (p.heads - p.L)) * p.I;
-  return u;
-}
-
-// Thread 0: S~ tile and z~ of OUT ticket t (its head's mixing is complete).
-__device__ __forceinline__ void issue_mix_loads(const Params& p, int t, uint8_t* regC, Small* sh) {
-  const Unit u = decode(p, t);
-  const int blk = (u.idx * kTile) / (p.N / p.M);
-  const size_t sidx = (size_t)u.h * p.M + blk;
-  fence_proxy_async_global();
-  mbar_arrive_expect_tx(&sh->bar_s, kSTileBytes + kD * 4);
-  tma_load_2d(regC, &p.tm_s, 0, (int)(sidx * kD), &sh->bar_s);
-  bulk_load_1d(sh->zt, p.z_mix + sidx * kD, kD * 4, &sh->bar_s);
-  sh->s_ticket = t;
-  sh->s_inflight = 1;
-}
-
-// Thread 0: issues the TMA loads a unit needs at its start (none for MIX);
-// for an OUT unit also its S~ / z~ if that head's mixing is already done.
-__device__ __forceinline__ void issue_inputs(const Params& p, int t, uint8_t* regA, uint8_t* regB,
-                                             uint8_t* regC, Small* sh) {
-  const Unit u = decode(p, t);
-  const int row = u.h * p.N + u.idx * kTile;
-  if (u.kind == UNIT_SUM) {
-    mbar_arrive_expect_tx(&sh->bar_in, 2 * kTileBytes);
-    tma_load_2d(regA, &p.tm_k, 0, row, &sh->bar_in);
-    tma_load_2d(regB, &p.tm_v, 0, row, &sh->bar_in);
-  } else if (u.kind == UNIT_OUT) {
-    mbar_arrive_expect_tx(&sh->bar_in, kTileBytes);
-    tma_load_2d(regA, &p.tm_q, 0, row, &sh->bar_in);
-    if (ld_acquire(&p.ctr[2 + p.heads + u.h]) >= (unsigned)p.I) issue_mix_loads(p, t, regC, sh);
-  }
-}
-
-__device__ __forceinline__ bool has_inputs(const Params& p, int t) {
-  return t < p.total && decode(p, t).kind != UNIT_MIX;
-}
-
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ float4 f4add(float4 a, float4 b) {
-  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// One MIX item of head h: summary entries [item*4*nvec, +4*nvec) (S^T entries
-// e*64 + c first, then the 64 z entries) for every query block i:
-//   T_b = sum of the chunk partials of block b,   out_i = sum_b w_ib T_b
-// with w_ib = m_ib (MIX_FULL), m_ib for b < i (MIX_STRICT_LOWER) or 1 for
-// b < i (MIX_PREFIX).  Thread (g, v): vector v = 4 consecutive entries,
-// g = one of the G threads sharing it.
-__device__ void mix_item(const Params& p, int h, int item, float4* sT, Small* sh) {
-  if (threadIdx.x == 0) sh->flag = wait_geq(&p.ctr[2 + h], (unsigned)p.C) ? 1 : 0;
-  __syncthreads();
-  if (!sh->flag) {
-    if (threadIdx.x == 0) atomicOr(p.status, 1u);
-    return;
+// Every thread of named barrier `id` (n threads) contributes `pred`; all get the AND.
+__device__ __forceinline__ bool group_and(int id, int n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ int aborted(Small* sh) { return *reinterpret_cast<volatile int*>(&sh->abort); }
+__device__ __forceinline__ void set_abort(Small* sh) { *reinterpret_cast<volatile int*>(&sh->abort) = 1; }
+
+// mbarrier phase wait.  The waiting thread sleeps in the barrier unit (it
+// issues nothing while suspended); false once kWaitLimitNs has passed (and
+// then the CTA aborts) or as soon as another role has aborted.
+__device__ __noinline__ bool bwait(uint64_t* bar, uint32_t parity, Small* sh) {
+  if (mbar_try_wait_ns(bar, parity, 1000)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_ns(bar, parity, 1000)) return true;
+    if (aborted(sh)) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
-  const int nvec = p.nvec, G = p.G, M = p.M, cpb = p.cpb, split = p.split;
-  const int g = threadIdx.x / nvec, v = threadIdx.x - g * nvec;
-  const int ent = (item * nvec + v) * 4;
-  const bool live = ent < kEnt;
-  const size_t chunk0 = (size_t)h * p.C;
-  const float* base = ent < kD * kD ? p.s_part + (chunk0 << 12) + ent : p.z_part + chunk0 * kD + (ent - kD * kD);
-  const size_t cstride = ent < kD * kD ? (size_t)kD * kD : (size_t)kD;   // floats between chunks
-  if (live) {  // phase 1: block sums (split == 0) or partial block sums (split > 0)
-    if (split == 0) {
-      for (int b = g; b < M; b += G) {
-        const float4* src = reinterpret_cast<const float4*>(base + (size_t)b * cpb * cstride);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int c = 0; c < cpb; ++c) acc = f4add(acc, __ldcg(src + c * (cstride / 4)));
-        sT[b * nvec + v] = acc;
+  set_abort(sh);
+  return false;
+}
+
+// Short wait (10 ms at most) used only while winding down after an abort.
+__device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_ns(bar, parity, 1000))
+    if (globaltimer_ns() - t0 > 10000000ull) return;
+}
+
+// Global counter wait (acquire): false after kWaitLimitNs or on abort.
+__device__ __noinline__ bool gwait(const unsigned* p, unsigned target, Small* sh) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(200);
+    if (ld_acquire(p) >= target) return true;
+    if (aborted(sh)) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+  }
+  set_abort(sh);
+  return false;
+}
+
+// ------------------------------------------------------------------ phi
+// phi(x) = exp(min(x, 0)) + max(x, 0): x + 1 for x > 0 (exp(0) = 1 exactly),
+// exp(x) otherwise; exp through the hardware base-2 exponential.
+__device__ __forceinline__ float phi_f(float x) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(x, 0.f) * 1.4426950408889634f));
+  return e + fmaxf(x, 0.f);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t phi2(uint32_t w) {
+  return pack_bf16(phi_f(__uint_as_float(w << 16)), phi_f(__uint_as_float(w & 0xffff0000u)));
+}
+
+// phi of 8 bf16 values in place; returns sum_j phi(x_j) z[j] in fp32.
+__device__ __forceinline__ float phi8_dot(uint4& x, const float* z) {
+  uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  float a = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = phi_f(__uint_as_float(w[j] << 16));
+    const float hi = phi_f(__uint_as_float(w[j] & 0xffff0000u));
+    a = fmaf(lo, z[2 * j], a);
+    a = fmaf(hi, z[2 * j + 1], a);
+    w[j] = pack_bf16(lo, hi);
+  }
+  x = make_uint4(w[0], w[1], w[2], w[3]);
+  return a;
+}
+
+// ------------------------------------------------------------------ roles
+// Producer (one thread).  Returns the number of stages it filled.  The OUT
+// stages' Q tiles are loaded as soon as a stage is free; their S~ / z~ loads
+// wait for the MIX phase of every CTA (grid barrier 2).
+template <class L>
+__device__ bool mix_ready(const Params& p, bool& ready) {
+  if (!ready && ld_acquire(&p.ctr[3]) >= gridDim.x) {
+    fence_proxy_async_global();  // S~ / z~ were written by generic stores of other CTAs
+    ready = true;
+  }
+  return ready;
+}
+
+template <class L>
+__device__ void issue_mix_loads(const Params& p, uint8_t* sm, Small* sh, int q, int g) {
+  constexpr int kNS = L::NS;
+  const int s = q % kNS;
+  uint8_t* st = sm + s * kStageBytes;
+  const size_t blk = (size_t)(g / p.C) * p.M + (g % p.C) / p.cpb;
+  bulk_load_1d(st + kTileBytes, p.smix + blk * kSTile, kSTile, &sh->full[s]);
+  bulk_load_1d(st + kTileBytes + kSTile, p.zmix + blk * kD, kD * 4, &sh->full[s]);
+}
+
+template <class L>
+__device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
+  constexpr int kNS = L::NS;
+  int q = 0;
+  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
+    const int s = q % kNS;
+    if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
+    uint8_t* st = sm + s * kStageBytes;
+    mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
+    tma_load_2d(st, &p.tm_k, 0, g * kTile, &sh->full[s]);
+    tma_load_2d(st + kTileBytes, &p.tm_v, 0, g * kTile, &sh->full[s]);
+  }
+  // OUT pass.  qm = first OUT stage without its S~ / z~ loads.
+  int qm = q;
+  int gm = blockIdx.x;  // chunk of stage qm
+  bool ready = false;
+  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
+    const int s = q % kNS;
+    if (q >= kNS) {
+      // wait for the stage; until the MIX phase is done, keep checking for it,
+      // since the stages ahead cannot drain without their S~ / z~
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait_ns(&sh->empty[s], ((q / kNS) - 1) & 1, 500)) {
+        if (!ready && mix_ready<L>(p, ready)) {
+          for (; qm < q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
+        }
+        if (aborted(sh)) return q;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          set_abort(sh);
+          return q;
+        }
+      }
+    }
+    uint8_t* st = sm + s * kStageBytes;
+    mbar_arrive_expect_tx(&sh->full[s], kTileBytes + kSTile + kD * 4);
+    tma_load_2d(st, &p.tm_q, 0, g * kTile, &sh->full[s]);
+    if (mix_ready<L>(p, ready)) {
+      for (; qm <= q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
+    }
+  }
+  // every OUT stage still needs its S~ / z~ before the consumers can finish
+  const uint64_t t0 = globaltimer_ns();
+  while (qm < q) {
+    if (mix_ready<L>(p, ready)) {
+      for (; qm < q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
+      break;
+    }
+    if (aborted(sh)) return q;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_abort(sh);
+      return q;
+    }
+    __nanosleep(200);
+  }
+  return q;
+}
+
+// phi warp w (0..7): rows 16w .. 16w+15 of every tile of one pass (0 SUM,
+// 1 OUT); q counts the stages across both passes.
+template <class L>
+__device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lane, int pass, int& q) {
+  constexpr int kNS = L::NS;
+  float* den = reinterpret_cast<float*>(sm + L::kOffDen);
+  // 16-byte piece w*128 + lane + 32i of a tile holds row 16w + (lane>>3) + 4i;
+  // physical piece lane&7 is logical piece (lane&7) ^ (row&7) (128-byte swizzle)
+  const int r0 = lane >> 3;
+  const int g0 = (lane & 7) ^ r0, g1 = (lane & 7) ^ (r0 + 4);
+  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
+    const int s = q % kNS;
+    if (!bwait(&sh->full[s], (q / kNS) & 1, sh)) return;
+    uint8_t* st = sm + s * kStageBytes;
+    uint4* t4 = reinterpret_cast<uint4*>(st) + w * 128 + lane;
+    uint4 x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = t4[32 * i];
+    if (pass == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[i].x = phi2(x[i].x);
+        x[i].y = phi2(x[i].y);
+        x[i].z = phi2(x[i].z);
+        x[i].w = phi2(x[i].w);
+        t4[32 * i] = x[i];
       }
     } else {
-      const int b = g / split, sub = g - b * split, per = cpb / split;
-      const float4* src = reinterpret_cast<const float4*>(base + ((size_t)b * cpb + (size_t)sub * per) * cstride);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int c = 0; c < per; ++c) acc = f4add(acc, __ldcg(src + c * (cstride / 4)));
-      sT[g * nvec + v] = acc;
-    }
-  }
-  __syncthreads();
-  if (live) {  // phase 2: mix
-    const float* mh = p.mixing + (size_t)(h % p.H) * M * M;
-    for (int i = g; i < M; i += G) {
-      const int bend = p.mode == MIX_FULL ? M : i;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (int b = 0; b < bend; ++b) {
-        float4 tb;
-        if (split == 0) {
-          tb = sT[b * nvec + v];
-        } else {
-          tb = sT[(b * split) * nvec + v];
-          for (int s2 = 1; s2 < split; ++s2) tb = f4add(tb, sT[(b * split + s2) * nvec + v]);
-        }
-        const float w = p.mode == MIX_PREFIX ? 1.f : __ldg(mh + (size_t)i * M + b);
-        acc.x = fmaf(w, tb.x, acc.x);
-        acc.y = fmaf(w, tb.y, acc.y);
-        acc.z = fmaf(w, tb.z, acc.z);
-        acc.w = fmaf(w, tb.w, acc.w);
+      const int a = q % kNA;
+      // den[a] is free once the epilogue of the chunk kNA earlier has read it
+      if (q >= kNA && !bwait(&sh->acc_empty[a], ((q / kNA) - 1) & 1, sh)) return;
+      const float4* zt = reinterpret_cast<const float4*>(st + kTileBytes + kSTile);
+      float z0[8], z1[8];
+      {
+        const float4 u0 = zt[2 * g0], u1 = zt[2 * g0 + 1], v0 = zt[2 * g1], v1 = zt[2 * g1 + 1];
+        z0[0] = u0.x; z0[1] = u0.y; z0[2] = u0.z; z0[3] = u0.w;
+        z0[4] = u1.x; z0[5] = u1.y; z0[6] = u1.z; z0[7] = u1.w;
+        z1[0] = v0.x; z1[1] = v0.y; z1[2] = v0.z; z1[3] = v0.w;
+        z1[4] = v1.x; z1[5] = v1.y; z1[6] = v1.z; z1[7] = v1.w;
       }
-      if (ent < kD * kD) {
-        uint2 packed;
-        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&packed);
-        h2[0] = __floats2bfloat162_rn(acc.x, acc.y);
-        h2[1] = __floats2bfloat162_rn(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(p.s_mix + (((size_t)h * M + i) << 12) + ent) = packed;
-      } else {
-        *reinterpret_cast<float4*>(p.z_mix + ((size_t)h * M + i) * kD + (ent - kD * kD)) = acc;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float dsum = phi8_dot(x[i], (i & 1) ? z1 : z0);
+        t4[32 * i] = x[i];
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 1);
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 2);
+        dsum += __shfl_xor_sync(0xffffffffu, dsum, 4);
+        if ((lane & 7) == 0) den[a * kTile + w * 16 + r0 + 4 * i] = dsum + p.eps;
       }
     }
+    fence_proxy_async_smem();  // phi tile -> tensor core reads
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->ready[s]);
   }
-  fence_proxy_async_global();  // S~ is read later through TMA (async proxy)
-  __syncthreads();
-  if (threadIdx.x == 0) red_release_add(&p.ctr[2 + p.heads + h], 1u);
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) mhla_tc_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* regA = sm;                                   // K or Q tile
-  uint8_t* regB = sm + kTileBytes;                      // V tile or Y staging
-  uint8_t* regC = sm + 2 * kTileBytes;                  // S~ tile
-  float4* sT = reinterpret_cast<float4*>(sm + 2 * kTileBytes + kSTileBytes);   // MIX staging
-  Small* sh = reinterpret_cast<Small*>(sm + 2 * kTileBytes + kSTileBytes + kMixBytes);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// MMA issuer (one thread).  Returns the number of chunks it issued.
+template <class L>
+__device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem) {
+  constexpr int kNS = L::NS;
+  const uint32_t ones = smem_u32(sm + L::kOffOnes);
+  // SUM: A = V tile (MN-major) with the ones tile as M rows 64..127, B = phi(K)
+  // (MN-major).  OUT: A = phi(Q) (K-major), B = S~^T (K-major).
+  const uint32_t idesc_sum = idesc_bf16_f32(128, 64, 1, 1);
+  const uint32_t idesc_out = idesc_bf16_f32(128, 64, 0, 0);
+  int q = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
+      const int s = q % kNS, a = q % kNA;
+      if (q >= kNA && !bwait(&sh->acc_empty[a], ((q / kNA) - 1) & 1, sh)) return q;
+      if (!bwait(&sh->ready[s], (q / kNS) & 1, sh)) return q;
+      tc_fence_after();
+      const uint32_t st = smem_u32(sm + s * kStageBytes);
+      const uint32_t dst = tmem + (uint32_t)(a * 64);
+      if (pass == 0) {
+        const uint32_t v0 = st + kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          mma_bf16(dst, smem_desc(v0 + k * 2048, ones - v0, 1024), smem_desc(st + k * 2048, 8192, 1024),
+                   idesc_sum, k > 0);
+      } else {
+        const uint32_t b0 = st + kTileBytes;
+#pragma unroll
+        for (int k = 0; k < kD / 16; ++k)
+          mma_bf16(dst, smem_desc(st + 32 * k, 16, 1024), smem_desc(b0 + 32 * k, 16, 1024), idesc_out, k > 0);
+      }
+      mma_commit(&sh->empty[s]);     // the stage is free once these MMAs have read it
+      mma_commit(&sh->acc_full[a]);  // and the accumulator is ready
+    }
+  }
+  return q;
+}
 
+// Epilogue warp for TMEM lane quadrant qd, one pass (0 SUM, 1 OUT); q counts
+// the chunks across both passes, nst the Y stores.
+template <class L>
+__device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, int qd, int lane, int pass, int& q,
+                         int& nst) {
+  const float* den = reinterpret_cast<const float*>(sm + L::kOffDen);
+  uint8_t* yb = sm + L::kOffY + qd * 4096;
+  {
+    for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
+      const int a = q % kNA;
+      if (!bwait(&sh->acc_full[a], (q / kNA) & 1, sh)) return;
+      tc_fence_after();
+      const uint32_t ta = tmem + (uint32_t)(a * 64) + ((uint32_t)(qd * 32) << 16);
+      float v[64];
+      if (pass == 0) {
+        if (qd < 3) {
+          tmem_ld16(ta, v);
+          tmem_ld16(ta + 16, v + 16);
+          tmem_ld16(ta + 32, v + 32);
+          tmem_ld16(ta + 48, v + 48);
+          tmem_ld_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
+        if (qd < 2) {
+          // row e = 32 qd + lane of the chunk's S^T: 64 bf16, one 128-byte row
+          uint4* dst = reinterpret_cast<uint4*>(p.ps + ((size_t)g * kD + qd * 32 + lane) * kD);
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            dst[c] = make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                                pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+        } else if (qd == 2 && lane == 0) {
+          // rows 64..127 all hold z; lane 0 writes it
+          float4* dst = reinterpret_cast<float4*>(p.pz + (size_t)g * kD);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        }
+      } else {
+        tmem_ld16(ta, v);
+        tmem_ld16(ta + 16, v + 16);
+        tmem_ld16(ta + 32, v + 32);
+        tmem_ld16(ta + 48, v + 48);
+        tmem_ld_wait();
+        const int row = qd * 32 + lane;
+        const float dn = den[a * kTile + row];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
+        if (p.den_out != nullptr) p.den_out[(size_t)g * kTile + row] = dn;
+        const float r = 1.f / dn;
+        if (lane == 0 && nst >= 1) tma_store_wait_read0();  // the previous store has read yb
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(yb + swz128(lane, 8 * c)) =
+              make_uint4(pack_bf16(v[8 * c] * r, v[8 * c + 1] * r), pack_bf16(v[8 * c + 2] * r, v[8 * c + 3] * r),
+                         pack_bf16(v[8 * c + 4] * r, v[8 * c + 5] * r), pack_bf16(v[8 * c + 6] * r, v[8 * c + 7] * r));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tm_y, yb, 0, g * kTile + qd * 32);
+          tma_store_commit();
+        }
+        ++nst;
+      }
+    }
+  }
+}
+
+// MIX phase, run by warps 2-15 of every CTA (448 threads) between the SUM and
+// OUT passes.  It starts with a grid barrier on every CTA's SUM partials and
+// ends by arriving at a second one that the producers wait on before loading
+// S~ / z~.  A CTA mixes the contiguous range [blockIdx.x R / G, (blockIdx.x+1)
+// R / G) of the R = heads x 65 summary rows (64 rows of S^T, then z); thread
+// t works on entry t % 64 of row t / 64 of each group of 7 rows: it sums the
+// chunk partials of each block (loads straight from L2) and mixes the block
+// sums for every query block.  Returns false after an abort.
+template <int MAXM>
+__device__ bool mix_phase(const Params& p, uint8_t* sm, Small* sh, int t) {
+  using L = Layout<MAXM>;
+  constexpr int kRowsPerRound = kMixThreads / kD;  // 7
+  constexpr int kBatch = MAXM <= 32 ? 32 : 16;     // slot values loaded at once
+  const unsigned G = gridDim.x;
+  // grid barrier 1: every CTA's SUM partials are stored
+  named_bar(kBarMix, kMixThreads);
+  bool ok = true;
+  if (t == 0) {
+    red_release_add(&p.ctr[2], 1u);
+    ok = gwait(&p.ctr[2], G, sh);
+  }
+  if (!group_and(kBarMix, kMixThreads, ok && !aborted(sh))) return false;
+
+  float* wt = reinterpret_cast<float*>(sm + L::kOffY);  // wT[b * MAXM + i] = m[i][b] of head cur_hh
+  const int R = p.heads * kMixRows;
+  const int r0 = (int)((long long)blockIdx.x * R / G), r1 = (int)((long long)(blockIdx.x + 1) * R / G);
+  const int c = t % kD, rr = t / kD;
+  int cur_hh = -1;
+  for (int u = r0; u < r1;) {
+    const int h = u / kMixRows;
+    const int hend = min(r1, (h + 1) * kMixRows);
+    const int hh = h % p.H;
+    if (hh != cur_hh) {
+      named_bar(kBarMix, kMixThreads);
+      const float* mw = p.mixing + (size_t)hh * p.M * p.M;
+      for (int j = t; j < MAXM * MAXM; j += kMixThreads) {
+        const int b = j / MAXM, i = j % MAXM;
+        wt[j] = (b < p.M && i < p.M) ? __ldcg(mw + i * p.M + b) : 0.f;
+      }
+      named_bar(kBarMix, kMixThreads);
+      cur_hh = hh;
+    }
+    for (int base = u; base < hend; base += kRowsPerRound) {
+      const int row = base + rr;
+      if (row >= hend) continue;
+      const int e = row - h * kMixRows;  // 0..63: row e of S^T; 64: z
+      const size_t part0 = (size_t)h * p.C;  // first chunk partial of head h
+      float acc[MAXM];
+#pragma unroll
+      for (int i = 0; i < MAXM; ++i) acc[i] = 0.f;
+      float T = 0.f;
+      int xin = 0, b = 0;
+      for (int x0 = 0; x0 < p.C; x0 += kBatch) {
+        const int n = min(kBatch, p.C - x0);
+        float val[kBatch];
+        if (e < kD) {
+          const unsigned short* src =
+              reinterpret_cast<const unsigned short*>(p.ps) + (part0 + x0) * (kD * kD) + e * kD + c;
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k)
+            val[k] = k < n ? __uint_as_float((uint32_t)__ldcg(src + (size_t)k * (kD * kD)) << 16) : 0.f;
+        } else {
+          const float* src = p.pz + (part0 + x0) * kD + c;
+#pragma unroll
+          for (int k = 0; k < kBatch; ++k) val[k] = k < n ? __ldcg(src + (size_t)k * kD) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          if (k >= n) break;
+          T += val[k];
+          if (++xin == p.cpb) {
+            const float4* w4 = reinterpret_cast<const float4*>(wt + b * MAXM);
+#pragma unroll
+            for (int i = 0; i < MAXM / 4; ++i) {
+              const float4 m4 = w4[i];
+              acc[4 * i] = fmaf(m4.x, T, acc[4 * i]);
+              acc[4 * i + 1] = fmaf(m4.y, T, acc[4 * i + 1]);
+              acc[4 * i + 2] = fmaf(m4.z, T, acc[4 * i + 2]);
+              acc[4 * i + 3] = fmaf(m4.w, T, acc[4 * i + 3]);
+            }
+            T = 0.f;
+            xin = 0;
+            ++b;
+          }
+        }
+      }
+      if (e < kD) {
+#pragma unroll
+        for (int i = 0; i < MAXM; ++i)
+          if (i < p.M)
+            *reinterpret_cast<__nv_bfloat16*>(p.smix + ((size_t)h * p.M + i) * kSTile + swz128(e, c)) =
+                __float2bfloat16_rn(acc[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < MAXM; ++i)
+          if (i < p.M) p.zmix[((size_t)h * p.M + i) * kD + c] = acc[i];
+      }
+    }
+    u = hend;
+  }
+  // grid barrier 2 (arrival only): this CTA's rows are stored; the producers
+  // wait for all CTAs before loading S~ / z~
+  named_bar(kBarMix, kMixThreads);
+  if (t == 0) red_release_add(&p.ctr[3], 1u);
+  return true;
+}
+
+template <int MAXM>
+__global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_constant__ Params p) {
+  using L = Layout<MAXM>;
+  constexpr int kNS = L::NS;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  Small* sh = reinterpret_cast<Small*>(sm + L::kOffSmall);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    sh->s_ticket = -1;
-    sh->s_inflight = 0;
-    mbar_init(&sh->bar_in, 1);
-    mbar_init(&sh->bar_s, 1);
-    mbar_init(&sh->bar_mma, 1);
+    for (int s = 0; s < kNS; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->ready[s], kPhiWarps);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < kNA; ++a) {
+      mbar_init(&sh->acc_full[a], 1);
+      mbar_init(&sh->acc_empty[a], 4);
+    }
+    sh->abort = 0;
+    sh->prod_q = 0;
+    sh->mma_q = 0;
     fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&sh->tbase, kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProd && lane == 0) {
     prefetch_tmap(&p.tm_q);
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_y);
-    prefetch_tmap(&p.tm_s);
   }
-  if (warp == 0) {
-    tmem_alloc(&sh->tbase, kTmemCols);
-    tmem_relinquish();
-  }
+  for (int i = tid; i < kTileBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sm + L::kOffOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tbase;
 
-  uint32_t ph_in = 0, ph_s = 0, ph_mma = 0;
-  bool pend_in = false, pend_s = false;  // TMA loads issued and not yet waited for
-  bool abort = false;
-
-  if (tid == 0) {
-    const int t0 = (int)atomicAdd(&p.ctr[0], 1u);
-    sh->next = t0;
-    if (t0 < p.total) issue_inputs(p, t0, regA, regB, regC, sh);
+  if (warp == kWarpProd) {
+    if (lane == 0) sh->prod_q = producer<L>(p, sm, sh);
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    if (lane == 0) sh->mma_q = mma_issuer<L>(p, sm, sh, tmem);
+    __syncwarp();
+  } else {
+    // warps 2-15: SUM pass (phi and epilogue warps), MIX phase (all), OUT pass
+    int q = 0, nst = 0;
+    if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 0, q);
+    else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 0, q, nst);
+    if (mix_phase<MAXM>(p, sm, sh, tid - kWarpMix * 32)) {
+      if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, q);
+      else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 1, q, nst);
+    }
+    if (warp >= kWarpEpi && warp < kWarpPhi && lane == 0) tma_store_wait_all0();
   }
   __syncthreads();
-  int t = sh->next;
-  pend_in = has_inputs(p, t);
 
-  // SUM: D = V^T phi(K) = S^T (A = V^T, B = phi(K): both MN-major views of the token-major tiles)
-  const uint32_t idesc_sum = idesc_bf16_f32(64, 64, 1, 1);
-  // OUT: D = phi(Q) S~ (A = phi(Q), B = S~ stored e rows x c cols: both K-major)
-  const uint32_t idesc_out = idesc_bf16_f32(128, 64, 0, 0);
-
-  while (t < p.total && !abort) {
-    const Unit u = decode(p, t);
-    // the next ticket is taken now; its loads are issued once this unit's inputs are consumed
-    unsigned nt_reg = 0;
-    if (tid == 0) nt_reg = atomicAdd(&p.ctr[0], 1u);
-    if (u.kind == UNIT_SUM) {
-      // ---------------------------------------------------------------- SUM
-      if (!cta_wait(&sh->bar_in, ph_in)) { abort = true; break; }
-      ph_in ^= 1;
-      pend_in = false;
-      {  // phi(K) in place (bf16) and the fp32 z partial of this chunk
-        const int j = tid & 7;
-        float zacc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) zacc[e] = 0.f;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const int r = (tid >> 3) + 32 * s;
-          uint4* ptr = reinterpret_cast<uint4*>(regA + swz128(r, j * 8));
-          uint4 raw = *ptr;
-          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h2[e]);
-            const float a = phi_fast(f.x), b = phi_fast(f.y);
-            zacc[2 * e] += a;
-            zacc[2 * e + 1] += b;
-            h2[e] = __floats2bfloat162_rn(a, b);
-          }
-          *ptr = raw;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float v = zacc[e];
-          v += __shfl_xor_sync(0xffffffffu, v, 8);
-          v += __shfl_xor_sync(0xffffffffu, v, 16);
-          if (lane < 8) sh->zred[warp][lane * 8 + e] = v;
-        }
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid < kD) {
-        float z = 0.f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) z += sh->zred[w][tid];
-        p.z_part[((size_t)u.h * p.C + u.idx) * kD + tid] = z;
-      }
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t k0 = smem_u32(regA), v0 = smem_u32(regB);
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          mma_bf16(tmem, smem_desc(v0 + k * 2048, 8192, 1024), smem_desc(k0 + k * 2048, 8192, 1024),
-                   idesc_sum, k > 0);
-        mma_commit(&sh->bar_mma);
-      }
-      if (!cta_wait(&sh->bar_mma, ph_mma)) { abort = true; break; }
-      ph_mma ^= 1;
-      tc_fence_after();
-      if (tid == 0) {  // K, V consumed: issue the next unit's loads
-        sh->next = (int)nt_reg;
-        if ((int)nt_reg < p.total) issue_inputs(p, (int)nt_reg, regA, regB, regC, sh);
-      }
-      {  // epilogue: D row e (M = 64: TMEM lane 32*(e/16) + e%16) = S^T[e][0..63]
-        const int q = warp & 3, half = warp >> 2;
-        float v[32];
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + half * 32;
-        tmem_ld16(ta, v);
-        tmem_ld16(ta + 16, v + 16);
-        tmem_ld_wait();
-        if (lane < 16) {
-          const int e = 16 * q + lane;
-          float4* dst = reinterpret_cast<float4*>(p.s_part + (((size_t)u.h * p.C + u.idx) << 12) + e * kD + half * 32);
-#pragma unroll
-          for (int j4 = 0; j4 < 8; ++j4) dst[j4] = make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]);
-        }
-      }
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) red_release_add(&p.ctr[2 + u.h], 1u);  // publish this chunk's partial
-      t = sh->next;
-      pend_in = has_inputs(p, t);
-    } else if (u.kind == UNIT_MIX) {
-      // ---------------------------------------------------------------- MIX
-      if (tid == 0) {
-        sh->next = (int)nt_reg;
-        if ((int)nt_reg < p.total) issue_inputs(p, (int)nt_reg, regA, regB, regC, sh);
-      }
-      __syncthreads();
-      t = sh->next;
-      pend_in = has_inputs(p, t);
-      mix_item(p, u.h, u.idx, sT, sh);
-    } else {
-      // ---------------------------------------------------------------- OUT
-      if (tid == 0 && sh->s_ticket != t) {
-        const int ok = wait_geq(&p.ctr[2 + p.heads + u.h], (unsigned)p.I) ? 1 : 0;
-        sh->flag = ok;
-        if (ok) issue_mix_loads(p, t, regC, sh);
-        else atomicOr(p.status, 1u);
-      } else if (tid == 0) {
-        sh->flag = 1;
-      }
-      __syncthreads();
-      if (!sh->flag) { abort = true; break; }
-      pend_s = true;
-      if (!cta_wait(&sh->bar_in, ph_in)) { abort = true; break; }
-      ph_in ^= 1;
-      pend_in = false;
-      if (!cta_wait(&sh->bar_s, ph_s)) { abort = true; break; }  // S~ tile and z~ have landed
-      ph_s ^= 1;
-      pend_s = false;
-      if (tid == 0) sh->s_inflight = 0;
-      const int q = warp & 3, half = warp >> 2, r = 32 * q + lane;
-      {  // phi(Q) in place; partial denominator over this thread's 32 columns
-        float dpart = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int jc = half * 4 + jj;
-          uint4* ptr = reinterpret_cast<uint4*>(regA + swz128(r, jc * 8));
-          uint4 raw = *ptr;
-          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 f = __bfloat1622float2(h2[e]);
-            const float a = phi_fast(f.x), b = phi_fast(f.y);
-            dpart = fmaf(a, sh->zt[jc * 8 + 2 * e], dpart);
-            dpart = fmaf(b, sh->zt[jc * 8 + 2 * e + 1], dpart);
-            h2[e] = __floats2bfloat162_rn(a, b);
-          }
-          *ptr = raw;
-        }
-        sh->den_half[half][r] = dpart;
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t a0 = smem_u32(regA), b0 = smem_u32(regC);
-#pragma unroll
-        for (int k = 0; k < kD / 16; ++k)
-          mma_bf16(tmem, smem_desc(a0 + 32 * k, 16, 1024), smem_desc(b0 + 32 * k, 16, 1024), idesc_out,
-                   k > 0);
-        mma_commit(&sh->bar_mma);
-      }
-      if (!cta_wait(&sh->bar_mma, ph_mma)) { abort = true; break; }
-      ph_mma ^= 1;
-      tc_fence_after();
-      const float den = sh->den_half[0][r] + sh->den_half[1][r] + p.eps;
-      if (tid == 0) {  // Q and S~ consumed: prefetch; then make sure the last Y store has left regB
-        sh->next = (int)nt_reg;
-        if ((int)nt_reg < p.total) issue_inputs(p, (int)nt_reg, regA, regB, regC, sh);
-        tma_store_wait_read0();
-      }
-      __syncthreads();
-      {  // epilogue: row r, columns half*32 .. +32
-        float v[32];
-        const uint32_t ta = tmem + ((uint32_t)(32 * q) << 16) + half * 32;
-        tmem_ld16(ta, v);
-        tmem_ld16(ta + 16, v + 16);
-        tmem_ld_wait();
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          uint4 raw;
-          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&raw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) h2[e] = __floats2bfloat162_rn(v[jj * 8 + 2 * e] * inv, v[jj * 8 + 2 * e + 1] * inv);
-          *reinterpret_cast<uint4*>(regB + swz128(r, (half * 4 + jj) * 8)) = raw;
-        }
-        if (half == 0 && p.den_out != nullptr) p.den_out[(size_t)u.h * p.N + u.idx * kTile + r] = den;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        tma_store_2d(&p.tm_y, regB, 0, u.h * p.N + u.idx * kTile);
-        tma_store_commit();
-      }
-      t = sh->next;
-      pend_in = has_inputs(p, t);
-    }
-  }
-
-  // ------------------------------------------------------------------ drain
-  if (tid == 0) {
-    if (abort) atomicOr(p.status, 1u);
-    if (pend_in) mbar_wait(&sh->bar_in, ph_in);
-    if (pend_s || sh->s_inflight) mbar_wait(&sh->bar_s, ph_s);
-    tma_store_wait_all0();
+  // Wind down.  On the normal path every wait below is already satisfied; after
+  // an abort they let TMA loads and MMAs still in flight finish first.
+  if (tid == 0 && aborted(sh)) {
+    const int nq = sh->prod_q;
+    for (int q = nq > kNS ? nq - kNS : 0; q < nq; ++q) drain_wait(&sh->full[q % kNS], (q / kNS) & 1);
+    const int mq = sh->mma_q;
+    if (mq > 0) drain_wait(&sh->acc_full[(mq - 1) % kNA], ((mq - 1) / kNA) & 1);
+    atomicOr(p.status, 1u);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+
+  // The last CTA out leaves the counters at zero for the next call.
   if (tid == 0) {
     __threadfence();
-    const unsigned f = atomicAdd(&p.ctr[1], 1u);
-    if (f == gridDim.x - 1) {  // last CTA: every other CTA is done with the counters; reset them
-      p.ctr[0] = 0;
-      for (int i = 0; i < 2 * p.heads; ++i) p.ctr[2 + i] = 0;
-      __threadfence();
-      p.ctr[1] = 0;
-    }
+    sh->last = atomicAdd(&p.ctr[1], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (sh->last && tid == 0) {
+    __threadfence();
+    p.ctr[2] = 0;
+    p.ctr[3] = 0;
+    p.ctr[1] = 0;
   }
 }
 
@@ -528,17 +647,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
-    void* p = nullptr;
+    void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   });
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// [rows][64] bf16, box 64 x box_rows, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
@@ -552,7 +672,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 
 struct TcPlan {
   int C, M, cpb;
-  size_t off_ctr, off_spart, off_zpart, off_smix, off_zmix, total;
+  size_t off_ps, off_pz, off_smix, off_zmix, total;
 };
 
 inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -563,46 +683,13 @@ TcPlan tc_plan(const MhlaShape& s) {
   p.M = s.M();
   p.cpb = s.block / kTile;
   const size_t heads = (size_t)s.heads();
-  p.off_ctr = kCounterOffset;
   size_t off = kWorkspacePrefix;
-  p.off_spart = off; off = a256(off + heads * p.C * (size_t)kD * kD * sizeof(float));
-  p.off_zpart = off; off = a256(off + heads * p.C * (size_t)kD * sizeof(float));
-  p.off_smix = off;  off = a256(off + heads * p.M * (size_t)kD * kD * 2);
-  p.off_zmix = off;  off = a256(off + heads * p.M * (size_t)kD * sizeof(float));
+  p.off_ps = off;   off = a256(off + heads * p.C * (size_t)kD * kD * 2);
+  p.off_pz = off;   off = a256(off + heads * p.C * (size_t)kD * sizeof(float));
+  p.off_smix = off; off = a256(off + heads * p.M * (size_t)kSTile);
+  p.off_zmix = off; off = a256(off + heads * p.M * (size_t)kD * sizeof(float));
   p.total = off;
   return p;
-}
-
-// MIX work split: G threads share each 4-entry vector (G * nvec = 256).
-// Constraints: per-thread chunk loads <= 32 (latency), block sums fit the
-// 16 KB staging (M <= 4 G when G < M), and when G >= M the G/M threads of a
-// block split its chunks evenly.  Among valid G, minimise the estimated total
-// MIX time: items per head x (fixed cost + load latency + mixing work).
-bool choose_mix_split(int M, int cpb, int* G_out, int* split_out) {
-  long best = -1;
-  for (int G = 1; G <= kThreads; G *= 2) {
-    const int nvec = kThreads / G;
-    int split = 0, loads = 0, work = 0;
-    if (G < M) {
-      if (M > 4 * G) continue;
-      loads = ((M + G - 1) / G) * cpb;
-      work = ((M + G - 1) / G) * M;
-    } else {
-      if (G % M != 0 || cpb % (G / M) != 0) continue;
-      split = G / M;
-      loads = cpb / split;
-      work = M * split;
-    }
-    if (loads > 32) continue;
-    const long items = (kEnt + 4 * nvec - 1) / (4 * nvec);
-    const long cost = items * (400 + 50 * (long)loads + work);
-    if (best < 0 || cost < best) {
-      best = cost;
-      *G_out = G;
-      *split_out = split;
-    }
-  }
-  return best >= 0;
 }
 
 int sm_count() {
@@ -612,6 +699,28 @@ int sm_count() {
   return n;
 }
 
+template <int MAXM>
+cudaError_t launch_t(const Params& p, int grid, cudaStream_t st) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(mhla_tc_kernel<MAXM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)Layout<MAXM>::kBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<MAXM>::kBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mhla_tc_kernel<MAXM>, p);
+}
+
 }  // namespace
 
 bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
@@ -619,9 +728,7 @@ bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
   if (s.block % kTile != 0 || s.N % kTile != 0) return false;
   if ((long long)s.heads() * s.N >= (1ll << 31)) return false;
   if (s.heads() > kMaxCounterHeads) return false;
-  if (s.M() > 64) return false;
-  int G = 0, split = 0;
-  return choose_mix_split(s.M(), s.block / kTile, &G, &split);
+  return s.M() <= 64;
 }
 
 size_t tc_mhla_workspace(const MhlaShape& s) { return tc_plan(s).total; }
@@ -629,21 +736,21 @@ size_t tc_mhla_workspace(const MhlaShape& s) { return tc_plan(s).total; }
 cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
                            const float* mixing, void* y, float* den_out, float eps, MixMode mode,
                            void* ws, cudaStream_t st) {
+  (void)mode;
   const TcPlan pl = tc_plan(s);
   char* w = static_cast<char*>(ws);
   Params p;
   const uint64_t rows = (uint64_t)s.heads() * s.N;
-  if (!make_map(&p.tm_q, q, rows, kTile) || !make_map(&p.tm_k, k, rows, kTile) ||
-      !make_map(&p.tm_v, v, rows, kTile) || !make_map(&p.tm_y, y, rows, kTile) ||
-      !make_map(&p.tm_s, w + pl.off_smix, (uint64_t)s.heads() * pl.M * kD, kD))
+  if (!make_map_2d(&p.tm_q, q, rows, kTile) || !make_map_2d(&p.tm_k, k, rows, kTile) ||
+      !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32))
     return cudaErrorInvalidValue;
   p.mixing = mixing;
-  p.s_part = reinterpret_cast<float*>(w + pl.off_spart);
-  p.z_part = reinterpret_cast<float*>(w + pl.off_zpart);
-  p.s_mix = reinterpret_cast<__nv_bfloat16*>(w + pl.off_smix);
-  p.z_mix = reinterpret_cast<float*>(w + pl.off_zmix);
+  p.ps = reinterpret_cast<__nv_bfloat16*>(w + pl.off_ps);
+  p.pz = reinterpret_cast<float*>(w + pl.off_pz);
+  p.smix = reinterpret_cast<uint8_t*>(w + pl.off_smix);
+  p.zmix = reinterpret_cast<float*>(w + pl.off_zmix);
   p.den_out = den_out;
-  p.ctr = reinterpret_cast<unsigned*>(w + pl.off_ctr);
+  p.ctr = reinterpret_cast<unsigned*>(w + kCounterOffset);
   p.status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
   p.heads = s.heads();
   p.H = s.H;
@@ -651,31 +758,20 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   p.M = pl.M;
   p.C = pl.C;
   p.cpb = pl.cpb;
-  if (!choose_mix_split(p.M, p.cpb, &p.G, &p.split)) return cudaErrorInvalidValue;
-  p.nvec = kThreads / p.G;
-  p.I = (kEnt + 4 * p.nvec - 1) / (4 * p.nvec);
+  p.TS = s.heads() * pl.C;
+  p.eps = eps;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid_cap = sms * kCtasPerSm;
-  // MIX items of head h go L heads after its SUM units: about two grids of tickets later
-  int L = (2 * grid_cap + p.C + p.I - 1) / (p.C + p.I) + 1;
-  p.L = L < p.heads ? L : p.heads;
-  p.T1 = p.heads * (p.C + p.I);
-  p.total = p.T1 + p.heads * p.C;
-  p.eps = eps;
-  p.mode = (int)mode;
-  const int grid = p.total < grid_cap ? p.total : grid_cap;
-  const size_t smem = 1024 + 2 * kTileBytes + kSTileBytes + kMixBytes + sizeof(Small);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mhla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  mhla_tc_kernel<<<grid, kThreads, smem, st>>>(p);
+  const int grid = p.TS < sms ? p.TS : sms;
+  cudaError_t e;
+  if (p.M <= 16)
+    e = launch_t<16>(p, grid, st);
+  else if (p.M <= 32)
+    e = launch_t<32>(p, grid, st);
+  else
+    e = launch_t<64>(p, grid, st);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mhla
