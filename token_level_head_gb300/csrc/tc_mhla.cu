@@ -51,7 +51,7 @@ constexpr int kTileBytes = kTile * kD * 2;  // 16 KB bf16 tile
 constexpr int kStageBytes = 2 * kTileBytes; // SUM: K, V.  OUT: Q, S~^T (8 KB), z~ (256 B)
 constexpr int kSTile = kD * kD * 2;         // 8 KB S~^T tile
 constexpr int kNA = 4;                      // TMEM accumulators, 64 columns each
-constexpr uint32_t kTmemCols = kNA * 64;
+constexpr uint32_t kTmemCols = 512;         // SUM / OUT use the first kNA x 64 columns, MIX all
 constexpr int kMixRows = kD + 1;            // MIX rows per head: 64 of S^T, then z
 constexpr uint64_t kWaitLimitNs = 500000000ull;  // a wait gives up after 0.5 s
 
@@ -59,12 +59,14 @@ constexpr int kWarpProd = 0, kWarpMma = 1, kWarpMix = 2, kWarpEpi = 4, kWarpPhi 
 constexpr int kMixThreads = (16 - kWarpMix) * 32;  // warps 2-15 run the MIX phase
 constexpr int kPhiWarps = 8;
 constexpr int kBarMix = 1;                  // named barrier of the MIX phase (0 is __syncthreads)
+constexpr int kBarZ = 2;                    // named barrier of warps 2-3 (z rows)
 
 constexpr int kMaxNS = 5;
 
 struct Small {
   uint64_t full[kMaxNS], ready[kMaxNS], empty[kMaxNS];
   uint64_t acc_full[kNA], acc_empty[kNA];
+  uint64_t mixf[2], mixe[2];  // MIX accumulators: TMEM columns [256 j, 256 j + 256)
   uint32_t tbase;
   int abort;
   int last;
@@ -90,15 +92,20 @@ struct Layout {
 struct Params {
   CUtensorMap tm_q, tm_k, tm_v;  // [heads*N rows][64] bf16, box 64 x 128, 128-byte swizzle
   CUtensorMap tm_y;              // same tensor shape, box 64 x 32
+  CUtensorMap tm_p;              // chunk partials [heads*C rows][4096] bf16, box 64 x C (tensor-core MIX)
+  CUtensorMap tm_w;              // MIX weights [H*128 rows][64] bf16, box 64 x 128 (tensor-core MIX)
   const float* mixing;           // [H][M][M], m[h][i][b]
   __nv_bfloat16* ps;             // chunk partial S^T: [heads * C][64 e][64 c]
   float* pz;                     // chunk partial z: [heads * C][64]
   uint8_t* smix;                 // S~^T tiles: [heads * M] x 8 KB, K-major, 128-byte swizzle
   float* zmix;                   // z~: [heads * M][64]
+  __nv_bfloat16* wts;            // MIX weight tiles: [H][128 rows][64] bf16 (see build_mix_weights)
   float* den_out;                // [heads * N] or null
-  unsigned* ctr;                 // [1] finished CTAs, [2 + h] chunks summarised, [2 + kMax + h] rows mixed
+  unsigned* ctr;                 // [1] finished CTAs, [2] SUM barrier, [3] MIX barrier
   unsigned* status;
   int heads, H, N, M, C, cpb, TS;  // C = chunks per head, cpb = chunks per block, TS = heads * C
+  int tc_mix;                    // 1: S^T rows mixed on the tensor cores (C % 16 == 0, C <= 64)
+  int XS;                        // tensor-core MIX units: heads * 64 (0 without tc_mix)
   float eps;
 };
 
@@ -204,6 +211,28 @@ __device__ __forceinline__ float phi8_dot(uint4& x, const float* z) {
   return a;
 }
 
+// ------------------------------------------------------------------ MIX stages
+// The tensor-core MIX units of a CTA are the contiguous range [u0, u1) of the
+// heads x 64 (head, row e of S^T) pairs.  A ring stage carries n <=
+// mix_per_stage(C) consecutive units of one head: their chunk-partial boxes
+// (C slots x 64 entries, C x 128 bytes each) from offset 0 and the head's
+// 128-row weight tile (row i: m[i][x / cpb] over the C slots x) at 16 KB.
+// MMA: D (128 x 64 n) = W (128 x C) . [boxes] (C x 64 n), fp32 in TMEM.
+// With M <= 32 the weight rows are repeated in every 32-row quarter, so each
+// TMEM lane quadrant holds all M query blocks and epilogue warp k reads unit
+// k's 64 columns from its own quadrant; otherwise rows 0..M-1 hold them once
+// and each unit is its own N = 64 MMA chain.
+constexpr int kMixWOff = 16384;
+constexpr int kMixWRows = 128;
+__device__ __forceinline__ int mix_per_stage(int C) { return min(4, kMixWOff / (C * kD * 2)); }
+__host__ __device__ __forceinline__ bool mix_rep(int M) { return M <= 32; }
+__device__ __forceinline__ int mix_u0(const Params& p) { return (int)((long long)blockIdx.x * p.XS / gridDim.x); }
+__device__ __forceinline__ int mix_u1(const Params& p) { return (int)((long long)(blockIdx.x + 1) * p.XS / gridDim.x); }
+// units in the stage that starts at unit u
+__device__ __forceinline__ int mix_stage_units(const Params& p, int u, int u1) {
+  return min(min(mix_per_stage(p.C), u1 - u), (u / kD + 1) * kD - u);
+}
+
 // ------------------------------------------------------------------ roles
 // Producer (one thread).  Returns the number of stages it filled.  The OUT
 // stages' Q tiles are loaded as soon as a stage is free; their S~ / z~ loads
@@ -230,14 +259,43 @@ __device__ void issue_mix_loads(const Params& p, uint8_t* sm, Small* sh, int q, 
 template <class L>
 __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
   constexpr int kNS = L::NS;
+  const uint64_t once = policy_evict_first();  // Q, K, V are read once
   int q = 0;
   for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
     const int s = q % kNS;
     if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
     uint8_t* st = sm + s * kStageBytes;
     mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
-    tma_load_2d(st, &p.tm_k, 0, g * kTile, &sh->full[s]);
-    tma_load_2d(st + kTileBytes, &p.tm_v, 0, g * kTile, &sh->full[s]);
+    tma_load_2d_hint(st, &p.tm_k, 0, g * kTile, &sh->full[s], once);
+    tma_load_2d_hint(st + kTileBytes, &p.tm_v, 0, g * kTile, &sh->full[s], once);
+    // pull the chunk one ring ahead into L2, so its load finds it there
+    const int gp = g + kNS * (int)gridDim.x;
+    if (gp < p.TS) {
+      tma_prefetch_2d(&p.tm_k, 0, gp * kTile);
+      tma_prefetch_2d(&p.tm_v, 0, gp * kTile);
+    }
+  }
+  // and the first OUT chunks' Q tiles, which wait behind the MIX phase
+  for (int k = 0; k < kNS; ++k) {
+    const int gp = blockIdx.x + k * (int)gridDim.x;
+    if (gp < p.TS) tma_prefetch_2d(&p.tm_q, 0, gp * kTile);
+  }
+  // MIX units (head h, row e of S^T): the chunk partials' row e and the head's
+  // weights, once every CTA has stored its partials (grid barrier 1)
+  const int u1 = mix_u1(p);
+  if (p.tc_mix && mix_u0(p) < u1) {
+    if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
+    fence_proxy_async_global();  // partials and weights were written by generic stores
+    for (int u = mix_u0(p); u < u1; ++q) {
+      const int s = q % kNS;
+      if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
+      uint8_t* st = sm + s * kStageBytes;
+      const int n = mix_stage_units(p, u, u1), h = u / kD;
+      mbar_arrive_expect_tx(&sh->full[s], n * p.C * kD * 2 + kMixWRows * kD * 2);
+      for (int k = 0; k < n; ++k) tma_load_2d(st + k * p.C * kD * 2, &p.tm_p, (u % kD + k) * kD, h * p.C, &sh->full[s]);
+      tma_load_2d(st + kMixWOff, &p.tm_w, 0, (h % p.H) * kMixWRows, &sh->full[s]);
+      u += n;
+    }
   }
   // OUT pass.  qm = first OUT stage without its S~ / z~ loads.
   int qm = q;
@@ -262,7 +320,11 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
     }
     uint8_t* st = sm + s * kStageBytes;
     mbar_arrive_expect_tx(&sh->full[s], kTileBytes + kSTile + kD * 4);
-    tma_load_2d(st, &p.tm_q, 0, g * kTile, &sh->full[s]);
+    tma_load_2d_hint(st, &p.tm_q, 0, g * kTile, &sh->full[s], once);
+    {
+      const int gp = g + kNS * (int)gridDim.x;
+      if (gp < p.TS) tma_prefetch_2d(&p.tm_q, 0, gp * kTile);
+    }
     if (mix_ready<L>(p, ready)) {
       for (; qm <= q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
     }
@@ -285,18 +347,18 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
 }
 
 // phi warp w (0..7): rows 16w .. 16w+15 of every tile of one pass (0 SUM,
-// 1 OUT); q counts the stages across both passes.
+// 1 OUT); qs counts ring stages, qa accumulators (units), over all passes.
 template <class L>
-__device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lane, int pass, int& q) {
+__device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lane, int pass, int& qs, int& qa) {
   constexpr int kNS = L::NS;
   float* den = reinterpret_cast<float*>(sm + L::kOffDen);
   // 16-byte piece w*128 + lane + 32i of a tile holds row 16w + (lane>>3) + 4i;
   // physical piece lane&7 is logical piece (lane&7) ^ (row&7) (128-byte swizzle)
   const int r0 = lane >> 3;
   const int g0 = (lane & 7) ^ r0, g1 = (lane & 7) ^ (r0 + 4);
-  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
-    const int s = q % kNS;
-    if (!bwait(&sh->full[s], (q / kNS) & 1, sh)) return;
+  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qs, ++qa) {
+    const int s = qs % kNS;
+    if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return;
     uint8_t* st = sm + s * kStageBytes;
     uint4* t4 = reinterpret_cast<uint4*>(st) + w * 128 + lane;
     uint4 x[4];
@@ -312,9 +374,9 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
         t4[32 * i] = x[i];
       }
     } else {
-      const int a = q % kNA;
-      // den[a] is free once the epilogue of the chunk kNA earlier has read it
-      if (q >= kNA && !bwait(&sh->acc_empty[a], ((q / kNA) - 1) & 1, sh)) return;
+      const int a = qa % kNA;
+      // den[a] is free once the epilogue of the unit kNA earlier has read it
+      if (qa >= kNA && !bwait(&sh->acc_empty[a], ((qa / kNA) - 1) & 1, sh)) return;
       const float4* zt = reinterpret_cast<const float4*>(st + kTileBytes + kSTile);
       float z0[8], z1[8];
       {
@@ -340,6 +402,22 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
   }
 }
 
+// phi warps during the MIX units: nothing to transform, the stage is handed on.
+template <class L>
+__device__ void phi_passthrough(const Params& p, Small* sh, int lane, int& qs, int& qa) {
+  constexpr int kNS = L::NS;
+  const int u1 = mix_u1(p);
+  for (int u = mix_u0(p); u < u1; ++qs) {
+    const int n = mix_stage_units(p, u, u1);
+    const int s = qs % kNS;
+    if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->ready[s]);
+    u += n;
+  }
+  (void)qa;
+}
+
 // MMA issuer (one thread).  Returns the number of chunks it issued.
 template <class L>
 __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem) {
@@ -347,34 +425,68 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
   const uint32_t ones = smem_u32(sm + L::kOffOnes);
   // SUM: A = V tile (MN-major) with the ones tile as M rows 64..127, B = phi(K)
   // (MN-major).  OUT: A = phi(Q) (K-major), B = S~^T (K-major).
+  // MIX: A = weight tile (K-major, M 128), B = chunk-partial boxes (MN-major).
   const uint32_t idesc_sum = idesc_bf16_f32(128, 64, 1, 1);
   const uint32_t idesc_out = idesc_bf16_f32(128, 64, 0, 0);
-  int q = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
-      const int s = q % kNS, a = q % kNA;
-      if (q >= kNA && !bwait(&sh->acc_empty[a], ((q / kNA) - 1) & 1, sh)) return q;
-      if (!bwait(&sh->ready[s], (q / kNS) & 1, sh)) return q;
+  const uint32_t idesc_mix = idesc_bf16_f32(128, 64, 0, 1);
+  int qs = 0, qa = 0;
+  for (int pass = 0; pass < 3; ++pass) {
+    if (pass == 1) {
+      // MIX stages: TMEM columns [256 (j % 2), +256) for MIX stage j
+      const int u1 = mix_u1(p);
+      const bool rep4 = mix_rep(p.M);
+      int j = 0;
+      for (int u = mix_u0(p); u < u1; ++qs, ++j) {
+        const int n = mix_stage_units(p, u, u1);
+        const int s = qs % kNS, half = j & 1;
+        if (!bwait(&sh->ready[s], (qs / kNS) & 1, sh)) return qa;
+        if (j >= 2 && !bwait(&sh->mixe[half], ((j >> 1) - 1) & 1, sh)) return qa;
+        tc_fence_after();
+        const uint32_t st = smem_u32(sm + s * kStageBytes);
+        const uint64_t da = smem_desc(st + kMixWOff, 16, 1024);
+        const uint32_t dst = tmem + (uint32_t)(256 * half);
+        if (rep4) {
+          // one chain, N = 64 n: the boxes are the N chunks, C x 128 bytes apart
+          const uint64_t db = smem_desc(st, p.C * kD * 2, 1024);
+          const uint32_t idesc = idesc_bf16_f32(128, 64 * n, 0, 1);
+          for (int kk = 0; kk < p.C / 16; ++kk) mma_bf16(dst, da + kk * (32 >> 4), db + kk * (2048 >> 4), idesc, kk > 0);
+        } else {
+          for (int k = 0; k < n; ++k) {
+            const uint64_t db = smem_desc(st + k * p.C * kD * 2, 8192, 1024);
+            for (int kk = 0; kk < p.C / 16; ++kk)
+              mma_bf16(dst + 64 * k, da + kk * (32 >> 4), db + kk * (2048 >> 4), idesc_mix, kk > 0);
+          }
+        }
+        mma_commit(&sh->mixf[half]);
+        mma_commit(&sh->empty[s]);  // the stage is free once these MMAs have read it
+        u += n;
+      }
+      continue;
+    }
+    for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qs, ++qa) {
+      const int s = qs % kNS, a = qa % kNA;
+      if (qa >= kNA && !bwait(&sh->acc_empty[a], ((qa / kNA) - 1) & 1, sh)) return qa;
+      if (!bwait(&sh->ready[s], (qs / kNS) & 1, sh)) return qa;
       tc_fence_after();
       const uint32_t st = smem_u32(sm + s * kStageBytes);
       const uint32_t dst = tmem + (uint32_t)(a * 64);
+      // descriptors built once per stage; a K step only moves the start
+      // address field (bytes >> 4 in the low bits)
       if (pass == 0) {
         const uint32_t v0 = st + kTileBytes;
+        const uint64_t da = smem_desc(v0, ones - v0, 1024), db = smem_desc(st, 8192, 1024);
 #pragma unroll
-        for (int k = 0; k < kTile / 16; ++k)
-          mma_bf16(dst, smem_desc(v0 + k * 2048, ones - v0, 1024), smem_desc(st + k * 2048, 8192, 1024),
-                   idesc_sum, k > 0);
+        for (int k = 0; k < kTile / 16; ++k) mma_bf16(dst, da + k * (2048 >> 4), db + k * (2048 >> 4), idesc_sum, k > 0);
       } else {
-        const uint32_t b0 = st + kTileBytes;
+        const uint64_t da = smem_desc(st, 16, 1024), db = smem_desc(st + kTileBytes, 16, 1024);
 #pragma unroll
-        for (int k = 0; k < kD / 16; ++k)
-          mma_bf16(dst, smem_desc(st + 32 * k, 16, 1024), smem_desc(b0 + 32 * k, 16, 1024), idesc_out, k > 0);
+        for (int k = 0; k < kD / 16; ++k) mma_bf16(dst, da + k * (32 >> 4), db + k * (32 >> 4), idesc_out, k > 0);
       }
       mma_commit(&sh->empty[s]);     // the stage is free once these MMAs have read it
       mma_commit(&sh->acc_full[a]);  // and the accumulator is ready
     }
   }
-  return q;
+  return qa;
 }
 
 // Epilogue warp for TMEM lane quadrant qd, one pass (0 SUM, 1 OUT); q counts
@@ -384,6 +496,44 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
                          int& nst) {
   const float* den = reinterpret_cast<const float*>(sm + L::kOffDen);
   uint8_t* yb = sm + L::kOffY + qd * 4096;
+  const uint64_t once = policy_evict_first();  // Y is written once
+  if (pass == 2) {
+    // MIX stages (see the MMA issuer): with M <= 32 warp qd takes unit qd of the
+    // stage from its own lane quadrant, else rows 32 qd .. of every unit.
+    const int u1 = mix_u1(p);
+    const bool rep4 = mix_rep(p.M);
+    int j = 0;
+    for (int u = mix_u0(p); u < u1; ++j) {
+      const int n = mix_stage_units(p, u, u1), half = j & 1, h = u / kD;
+      if (!bwait(&sh->mixf[half], (j >> 1) & 1, sh)) return;
+      tc_fence_after();
+      const int i = rep4 ? lane : 32 * qd + lane;  // query block of this thread's row
+      for (int k = 0; k < n; ++k) {
+        if (rep4 ? k != qd : 32 * qd >= p.M) continue;
+        float v[64];
+        const uint32_t ta = tmem + (uint32_t)(256 * half + 64 * k) + ((uint32_t)(qd * 32) << 16);
+        tmem_ld16(ta, v);
+        tmem_ld16(ta + 16, v + 16);
+        tmem_ld16(ta + 32, v + 32);
+        tmem_ld16(ta + 48, v + 48);
+        tmem_ld_wait();
+        if (i < p.M) {
+          const int e = u % kD + k;
+          uint8_t* dst = p.smix + ((size_t)h * p.M + i) * kSTile;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(dst + swz128(e, 8 * c)) =
+                make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                           pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->mixe[half]);
+      u += n;
+    }
+    return;
+  }
   {
     for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
       const int a = q % kNA;
@@ -438,7 +588,7 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&p.tm_y, yb, 0, g * kTile + qd * 32);
+          tma_store_2d_hint(&p.tm_y, yb, 0, g * kTile + qd * 32, once);
           tma_store_commit();
         }
         ++nst;
@@ -447,30 +597,106 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
   }
 }
 
-// MIX phase, run by warps 2-15 of every CTA (448 threads) between the SUM and
-// OUT passes.  It starts with a grid barrier on every CTA's SUM partials and
-// ends by arriving at a second one that the producers wait on before loading
-// S~ / z~.  A CTA mixes the contiguous range [blockIdx.x R / G, (blockIdx.x+1)
-// R / G) of the R = heads x 65 summary rows (64 rows of S^T, then z); thread
-// t works on entry t % 64 of row t / 64 of each group of 7 rows: it sums the
-// chunk partials of each block (loads straight from L2) and mixes the block
-// sums for every query block.  Returns false after an abort.
+// SIMT mixing of one summary row for entry c: sums the chunk partials of each
+// block (loads straight from L2) and mixes the block sums with the staged
+// weights wt[b * MAXM + i] = m[i][b]; e = 0..63 is row e of S^T, e = 64 is z.
 template <int MAXM>
-__device__ bool mix_phase(const Params& p, uint8_t* sm, Small* sh, int t) {
-  using L = Layout<MAXM>;
-  constexpr int kRowsPerRound = kMixThreads / kD;  // 7
-  constexpr int kBatch = MAXM <= 32 ? 32 : 16;     // slot values loaded at once
-  const unsigned G = gridDim.x;
-  // grid barrier 1: every CTA's SUM partials are stored
+__device__ void mix_row_simt(const Params& p, const float* wt, int h, int e, int c) {
+  constexpr int kBatch = MAXM <= 32 ? 32 : 16;  // slot values loaded at once
+  const size_t part0 = (size_t)h * p.C;         // first chunk partial of head h
+  float acc[MAXM];
+#pragma unroll
+  for (int i = 0; i < MAXM; ++i) acc[i] = 0.f;
+  float T = 0.f;
+  int xin = 0, b = 0;
+  for (int x0 = 0; x0 < p.C; x0 += kBatch) {
+    const int n = min(kBatch, p.C - x0);
+    float val[kBatch];
+    if (e < kD) {
+      const unsigned short* src = reinterpret_cast<const unsigned short*>(p.ps) + (part0 + x0) * (kD * kD) + e * kD + c;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        val[k] = k < n ? __uint_as_float((uint32_t)__ldcg(src + (size_t)k * (kD * kD)) << 16) : 0.f;
+    } else {
+      const float* src = p.pz + (part0 + x0) * kD + c;
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) val[k] = k < n ? __ldcg(src + (size_t)k * kD) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (k >= n) break;
+      T += val[k];
+      if (++xin == p.cpb) {
+        const float4* w4 = reinterpret_cast<const float4*>(wt + b * MAXM);
+#pragma unroll
+        for (int i = 0; i < MAXM / 4; ++i) {
+          const float4 m4 = w4[i];
+          acc[4 * i] = fmaf(m4.x, T, acc[4 * i]);
+          acc[4 * i + 1] = fmaf(m4.y, T, acc[4 * i + 1]);
+          acc[4 * i + 2] = fmaf(m4.z, T, acc[4 * i + 2]);
+          acc[4 * i + 3] = fmaf(m4.w, T, acc[4 * i + 3]);
+        }
+        T = 0.f;
+        xin = 0;
+        ++b;
+      }
+    }
+  }
+  if (e < kD) {
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i)
+      if (i < p.M)
+        *reinterpret_cast<__nv_bfloat16*>(p.smix + ((size_t)h * p.M + i) * kSTile + swz128(e, c)) =
+            __float2bfloat16_rn(acc[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i)
+      if (i < p.M) p.zmix[((size_t)h * p.M + i) * kD + c] = acc[i];
+  }
+}
+
+// Stages the transposed mixing matrix of head hh (zero-padded to MAXM) for
+// the n threads of named barrier `bar`.
+template <int MAXM>
+__device__ void stage_weights(const Params& p, float* wt, int hh, int t, int n, int bar) {
+  named_bar(bar, n);
+  const float* mw = p.mixing + (size_t)hh * p.M * p.M;
+  for (int j = t; j < MAXM * MAXM; j += n) {
+    const int b = j / MAXM, i = j % MAXM;
+    wt[j] = (b < p.M && i < p.M) ? __ldcg(mw + i * p.M + b) : 0.f;
+  }
+  named_bar(bar, n);
+}
+
+// Start of the MIX phase for warps 2-15 (448 threads): grid barrier 1, on
+// every CTA's SUM partials (and MIX weights).  False after an abort.
+__device__ bool mix_begin(const Params& p, Small* sh, int t) {
   named_bar(kBarMix, kMixThreads);
   bool ok = true;
   if (t == 0) {
     red_release_add(&p.ctr[2], 1u);
-    ok = gwait(&p.ctr[2], G, sh);
+    ok = gwait(&p.ctr[2], gridDim.x, sh);
   }
-  if (!group_and(kBarMix, kMixThreads, ok && !aborted(sh))) return false;
+  return group_and(kBarMix, kMixThreads, ok && !aborted(sh));
+}
 
-  float* wt = reinterpret_cast<float*>(sm + L::kOffY);  // wT[b * MAXM + i] = m[i][b] of head cur_hh
+// End of the MIX phase: this CTA's share of S~ / z~ is stored; arrive at grid
+// barrier 2, which the producers wait on before loading S~ / z~.
+__device__ void mix_end(const Params& p, int t) {
+  named_bar(kBarMix, kMixThreads);
+  if (t == 0) red_release_add(&p.ctr[3], 1u);
+}
+
+// SIMT MIX of all summary rows (when the tensor-core MIX does not apply), by
+// warps 2-15: a CTA takes the contiguous range [blockIdx.x R / G,
+// (blockIdx.x + 1) R / G) of the R = heads x 65 rows; thread t works on entry
+// t % 64 of row t / 64 of each group of 7 rows.
+template <int MAXM>
+__device__ void mix_rows_all(const Params& p, uint8_t* sm, int t) {
+  using L = Layout<MAXM>;
+  constexpr int kRowsPerRound = kMixThreads / kD;  // 7
+  const unsigned G = gridDim.x;
+  float* wt = reinterpret_cast<float*>(sm + L::kOffY);
   const int R = p.heads * kMixRows;
   const int r0 = (int)((long long)blockIdx.x * R / G), r1 = (int)((long long)(blockIdx.x + 1) * R / G);
   const int c = t % kD, rr = t / kD;
@@ -478,80 +704,74 @@ __device__ bool mix_phase(const Params& p, uint8_t* sm, Small* sh, int t) {
   for (int u = r0; u < r1;) {
     const int h = u / kMixRows;
     const int hend = min(r1, (h + 1) * kMixRows);
-    const int hh = h % p.H;
-    if (hh != cur_hh) {
-      named_bar(kBarMix, kMixThreads);
-      const float* mw = p.mixing + (size_t)hh * p.M * p.M;
-      for (int j = t; j < MAXM * MAXM; j += kMixThreads) {
-        const int b = j / MAXM, i = j % MAXM;
-        wt[j] = (b < p.M && i < p.M) ? __ldcg(mw + i * p.M + b) : 0.f;
-      }
-      named_bar(kBarMix, kMixThreads);
-      cur_hh = hh;
+    if (h % p.H != cur_hh) {
+      cur_hh = h % p.H;
+      stage_weights<MAXM>(p, wt, cur_hh, t, kMixThreads, kBarMix);
     }
     for (int base = u; base < hend; base += kRowsPerRound) {
       const int row = base + rr;
-      if (row >= hend) continue;
-      const int e = row - h * kMixRows;  // 0..63: row e of S^T; 64: z
-      const size_t part0 = (size_t)h * p.C;  // first chunk partial of head h
-      float acc[MAXM];
-#pragma unroll
-      for (int i = 0; i < MAXM; ++i) acc[i] = 0.f;
-      float T = 0.f;
-      int xin = 0, b = 0;
-      for (int x0 = 0; x0 < p.C; x0 += kBatch) {
-        const int n = min(kBatch, p.C - x0);
-        float val[kBatch];
-        if (e < kD) {
-          const unsigned short* src =
-              reinterpret_cast<const unsigned short*>(p.ps) + (part0 + x0) * (kD * kD) + e * kD + c;
-#pragma unroll
-          for (int k = 0; k < kBatch; ++k)
-            val[k] = k < n ? __uint_as_float((uint32_t)__ldcg(src + (size_t)k * (kD * kD)) << 16) : 0.f;
-        } else {
-          const float* src = p.pz + (part0 + x0) * kD + c;
-#pragma unroll
-          for (int k = 0; k < kBatch; ++k) val[k] = k < n ? __ldcg(src + (size_t)k * kD) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          if (k >= n) break;
-          T += val[k];
-          if (++xin == p.cpb) {
-            const float4* w4 = reinterpret_cast<const float4*>(wt + b * MAXM);
-#pragma unroll
-            for (int i = 0; i < MAXM / 4; ++i) {
-              const float4 m4 = w4[i];
-              acc[4 * i] = fmaf(m4.x, T, acc[4 * i]);
-              acc[4 * i + 1] = fmaf(m4.y, T, acc[4 * i + 1]);
-              acc[4 * i + 2] = fmaf(m4.z, T, acc[4 * i + 2]);
-              acc[4 * i + 3] = fmaf(m4.w, T, acc[4 * i + 3]);
-            }
-            T = 0.f;
-            xin = 0;
-            ++b;
-          }
-        }
-      }
-      if (e < kD) {
-#pragma unroll
-        for (int i = 0; i < MAXM; ++i)
-          if (i < p.M)
-            *reinterpret_cast<__nv_bfloat16*>(p.smix + ((size_t)h * p.M + i) * kSTile + swz128(e, c)) =
-                __float2bfloat16_rn(acc[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < MAXM; ++i)
-          if (i < p.M) p.zmix[((size_t)h * p.M + i) * kD + c] = acc[i];
-      }
+      if (row < hend) mix_row_simt<MAXM>(p, wt, h, row - h * kMixRows, c);
     }
     u = hend;
   }
-  // grid barrier 2 (arrival only): this CTA's rows are stored; the producers
-  // wait for all CTAs before loading S~ / z~
-  named_bar(kBarMix, kMixThreads);
-  if (t == 0) red_release_add(&p.ctr[3], 1u);
-  return true;
+}
+
+// z rows of the heads h = blockIdx.x + k G, by warps 2-3 (64 threads), while
+// the other warps run the tensor-core MIX units.
+template <int MAXM>
+__device__ void mix_z_rows(const Params& p, uint8_t* sm, int c) {
+  using L = Layout<MAXM>;
+  float* wt = reinterpret_cast<float*>(sm + L::kOffY);
+  int cur_hh = -1;
+  for (int h = blockIdx.x; h < p.heads; h += gridDim.x) {
+    if (h % p.H != cur_hh) {
+      cur_hh = h % p.H;
+      stage_weights<MAXM>(p, wt, cur_hh, c, 64, kBarZ);
+    }
+    mix_row_simt<MAXM>(p, wt, h, kD, c);
+  }
+}
+
+// MIX weights for the tensor-core MIX, built during the SUM pass by warps 2-3:
+// row r, column x of head hh's 128 x 64 tile is m[hh][i][x / cpb] with
+// i = r % 32 (M <= 32) or i = r (M > 32), for i < M and x < C, zero elsewhere
+// (bf16, row-major; TMA swizzles it on the way into shared memory).
+template <class L>
+__device__ void build_mix_weights(const Params& p, uint8_t* sm, int c) {
+  const bool rep4 = mix_rep(p.M);
+  float* ms = reinterpret_cast<float*>(sm + L::kOffY);  // the mixing matrix (Y staging is idle now)
+  const int MM = p.M * p.M;
+  for (int hh = blockIdx.x; hh < p.H; hh += gridDim.x) {
+    const float* src = p.mixing + (size_t)hh * MM;
+    for (int j0 = 0; j0 < MM; j0 += 16 * 64) {  // 16 independent loads per thread in flight
+      float v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int j = j0 + k * 64 + c;
+        v[k] = j < MM ? __ldcg(src + j) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int j = j0 + k * 64 + c;
+        if (j < MM) ms[j] = v[k];
+      }
+    }
+    named_bar(kBarZ, 64);
+    // 128 rows x 64 columns = 1024 pieces of 8 bf16
+    uint4* dst = reinterpret_cast<uint4*>(p.wts + (size_t)hh * kMixWRows * kD);
+    for (int pc = c; pc < kMixWRows * kD / 8; pc += 64) {
+      const int r = pc / 8, x0 = (pc % 8) * 8;
+      const int i = rep4 ? r % 32 : r;
+      float w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int x = x0 + k;
+        w[k] = (i < p.M && x < p.C) ? ms[i * p.M + x / p.cpb] : 0.f;
+      }
+      dst[pc] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
+    }
+    named_bar(kBarZ, 64);
+  }
 }
 
 template <int MAXM>
@@ -571,6 +791,10 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     for (int a = 0; a < kNA; ++a) {
       mbar_init(&sh->acc_full[a], 1);
       mbar_init(&sh->acc_empty[a], 4);
+    }
+    for (int hf = 0; hf < 2; ++hf) {
+      mbar_init(&sh->mixf[hf], 1);
+      mbar_init(&sh->mixe[hf], 4);
     }
     sh->abort = 0;
     sh->prod_q = 0;
@@ -603,11 +827,21 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     __syncwarp();
   } else {
     // warps 2-15: SUM pass (phi and epilogue warps), MIX phase (all), OUT pass
-    int q = 0, nst = 0;
-    if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 0, q);
+    const int t = tid - kWarpMix * 32;
+    int q = 0, qs = 0, nst = 0;
+    if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 0, qs, q);
     else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 0, q, nst);
-    if (mix_phase<MAXM>(p, sm, sh, tid - kWarpMix * 32)) {
-      if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, q);
+    else if (p.tc_mix) build_mix_weights<L>(p, sm, t);
+    if (mix_begin(p, sh, t)) {
+      if (p.tc_mix) {
+        if (warp >= kWarpPhi) phi_passthrough<L>(p, sh, lane, qs, q);
+        else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
+        else mix_z_rows<MAXM>(p, sm, t);
+      } else {
+        mix_rows_all<MAXM>(p, sm, t);
+      }
+      mix_end(p, t);
+      if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, qs, q);
       else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 1, q, nst);
     }
     if (warp >= kWarpEpi && warp < kWarpPhi && lane == 0) tma_store_wait_all0();
@@ -657,12 +891,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// [rows][64] bf16, box 64 x box_rows, 128-byte swizzle.
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// [rows][inner] bf16, box 64 x box_rows, 128-byte swizzle.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, uint64_t inner = kD) {
   auto enc = encoder();
   if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
   cuuint32_t box[2] = {(cuuint32_t)kD, box_rows};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
@@ -672,7 +906,8 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_r
 
 struct TcPlan {
   int C, M, cpb;
-  size_t off_ps, off_pz, off_smix, off_zmix, total;
+  bool tc_mix;  // S^T rows mixed on the tensor cores
+  size_t off_ps, off_pz, off_smix, off_zmix, off_w, total;
 };
 
 inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -688,6 +923,8 @@ TcPlan tc_plan(const MhlaShape& s) {
   p.off_pz = off;   off = a256(off + heads * p.C * (size_t)kD * sizeof(float));
   p.off_smix = off; off = a256(off + heads * p.M * (size_t)kSTile);
   p.off_zmix = off; off = a256(off + heads * p.M * (size_t)kD * sizeof(float));
+  p.tc_mix = p.C % 16 == 0 && p.C <= kD;
+  p.off_w = off;    off = a256(off + (p.tc_mix ? (size_t)s.H * kMixWRows * kD * 2 : 0));
   p.total = off;
   return p;
 }
@@ -744,11 +981,15 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   if (!make_map_2d(&p.tm_q, q, rows, kTile) || !make_map_2d(&p.tm_k, k, rows, kTile) ||
       !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32))
     return cudaErrorInvalidValue;
+  if (pl.tc_mix && (!make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, pl.C, (uint64_t)kD * kD) ||
+                    !make_map_2d(&p.tm_w, w + pl.off_w, (uint64_t)s.H * kMixWRows, kMixWRows)))
+    return cudaErrorInvalidValue;
   p.mixing = mixing;
   p.ps = reinterpret_cast<__nv_bfloat16*>(w + pl.off_ps);
   p.pz = reinterpret_cast<float*>(w + pl.off_pz);
   p.smix = reinterpret_cast<uint8_t*>(w + pl.off_smix);
   p.zmix = reinterpret_cast<float*>(w + pl.off_zmix);
+  p.wts = reinterpret_cast<__nv_bfloat16*>(w + pl.off_w);
   p.den_out = den_out;
   p.ctr = reinterpret_cast<unsigned*>(w + kCounterOffset);
   p.status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
@@ -759,6 +1000,8 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   p.C = pl.C;
   p.cpb = pl.cpb;
   p.TS = s.heads() * pl.C;
+  p.tc_mix = pl.tc_mix ? 1 : 0;
+  p.XS = pl.tc_mix ? s.heads() * kD : 0;
   p.eps = eps;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
