@@ -93,6 +93,7 @@ struct Params {
   CUtensorMap tm_q, tm_k, tm_v;  // [heads*N rows][64] bf16, box 64 x 128, 128-byte swizzle
   CUtensorMap tm_y;              // same tensor shape, box 64 x 32
   CUtensorMap tm_p;              // chunk partials [heads*C rows][4096] bf16, box 64 x C (tensor-core MIX)
+  CUtensorMap tm_ps;             // chunk partials [heads*C*64 rows][64] bf16, box 64 x 32 (SUM stores)
   CUtensorMap tm_w;              // MIX weights [H*128 rows][64] bf16, box 64 x 128 (tensor-core MIX)
   const float* mixing;           // [H][M][M], m[h][i][b]
   __nv_bfloat16* ps;             // chunk partial S^T: [heads * C][64 e][64 c]
@@ -145,6 +146,9 @@ __device__ __forceinline__ void set_abort(Small* sh) { *reinterpret_cast<volatil
 // issues nothing while suspended); false once kWaitLimitNs has passed (and
 // then the CTA aborts) or as soon as another role has aborted.
 __device__ __noinline__ bool bwait(uint64_t* bar, uint32_t parity, Small* sh) {
+  // a short spin first: a suspended thread can take a while to be woken
+  for (int i = 0; i < 256; ++i)
+    if (mbar_test(bar, parity)) return true;
   if (mbar_try_wait_ns(bar, parity, 1000)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
@@ -552,18 +556,31 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
-        if (qd < 2) {
-          // row e = 32 qd + lane of the chunk's S^T: 64 bf16, one 128-byte row
-          uint4* dst = reinterpret_cast<uint4*>(p.ps + ((size_t)g * kD + qd * 32 + lane) * kD);
+        // the chunk's partial goes out through this warp's staging buffer and
+        // a bulk store: rows 32 qd .. 32 qd + 31 of S^T (qd 0, 1; bf16, 128-byte
+        // swizzle for the tensor map), or z (qd 2: rows 64.. all hold it)
+        if (qd < 3) {
+          if (lane == 0 && nst >= 1) tma_store_wait_read0();  // the previous store has read yb
+          __syncwarp();
+          if (qd < 2) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            dst[c] = make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
-                                pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
-        } else if (qd == 2 && lane == 0) {
-          // rows 64..127 all hold z; lane 0 writes it
-          float4* dst = reinterpret_cast<float4*>(p.pz + (size_t)g * kD);
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(yb + swz128(lane, 8 * c)) =
+                  make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                             pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+          } else if (lane == 0) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            for (int c = 0; c < 16; ++c)
+              reinterpret_cast<float4*>(yb)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (qd < 2) tma_store_2d(&p.tm_ps, yb, 0, g * kD + qd * 32);
+            else bulk_store_1d(p.pz + (size_t)g * kD, yb, kD * 4);
+            tma_store_commit();
+          }
+          ++nst;
         }
       } else {
         tmem_ld16(ta, v);
@@ -739,7 +756,9 @@ __device__ void mix_z_rows(const Params& p, uint8_t* sm, int c) {
 template <class L>
 __device__ void build_mix_weights(const Params& p, uint8_t* sm, int c) {
   const bool rep4 = mix_rep(p.M);
-  float* ms = reinterpret_cast<float*>(sm + L::kOffY);  // the mixing matrix (Y staging is idle now)
+  // the mixing matrix, in the upper half of the Y staging area (the epilogue
+  // warps stage their SUM stores in the lower half meanwhile)
+  float* ms = reinterpret_cast<float*>(sm + L::kOffY + 16384);
   const int MM = p.M * p.M;
   for (int hh = blockIdx.x; hh < p.H; hh += gridDim.x) {
     const float* src = p.mixing + (size_t)hh * MM;
@@ -830,8 +849,12 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     const int t = tid - kWarpMix * 32;
     int q = 0, qs = 0, nst = 0;
     if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 0, qs, q);
-    else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 0, q, nst);
-    else if (p.tc_mix) build_mix_weights<L>(p, sm, t);
+    else if (warp >= kWarpEpi) {
+      epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 0, q, nst);
+      // the SUM partials are read after grid barrier 1, some through TMA
+      if (lane == 0) tma_store_wait_all0();
+      fence_proxy_async_global();
+    } else if (p.tc_mix) build_mix_weights<L>(p, sm, t);
     if (mix_begin(p, sh, t)) {
       if (p.tc_mix) {
         if (warp >= kWarpPhi) phi_passthrough<L>(p, sh, lane, qs, q);
@@ -981,6 +1004,7 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   if (!make_map_2d(&p.tm_q, q, rows, kTile) || !make_map_2d(&p.tm_k, k, rows, kTile) ||
       !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32))
     return cudaErrorInvalidValue;
+  if (!make_map_2d(&p.tm_ps, w + pl.off_ps, (uint64_t)s.heads() * pl.C * kD, 32)) return cudaErrorInvalidValue;
   if (pl.tc_mix && (!make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, pl.C, (uint64_t)kD * kD) ||
                     !make_map_2d(&p.tm_w, w + pl.off_w, (uint64_t)s.H * kMixWRows, kMixWRows)))
     return cudaErrorInvalidValue;
