@@ -62,15 +62,20 @@ constexpr int kBarMix = 1;                  // named barrier of the MIX phase (0
 constexpr int kBarZ = 2;                    // named barrier of warps 2-3 (z rows)
 
 constexpr int kMaxNS = 5;
+// The OUT pass re-cuts the input ring into kNSO slots of kOutStage bytes:
+// Q tile (16 KB), S~^T tile (8 KB) and z~ (256 B).
+constexpr int kOutStage = 25 * 1024;
+constexpr int kNSO = 6;
 
 struct Small {
   uint64_t full[kMaxNS], ready[kMaxNS], empty[kMaxNS];
+  uint64_t fullO[kNSO], readyO[kNSO], emptyO[kNSO];  // the OUT pass's ring
   uint64_t acc_full[kNA], acc_empty[kNA];
   uint64_t mixf[2], mixe[2];  // MIX accumulators: TMEM columns [256 j, 256 j + 256)
   uint32_t tbase;
   int abort;
   int last;
-  int prod_q, mma_q;
+  int prod_q, prod_qo, mma_q;
 };
 
 // Dynamic shared memory, from a 1024-byte aligned base: input ring, ones
@@ -86,6 +91,7 @@ struct Layout {
   static constexpr int kOffSmall = kOffDen + kNA * kTile * 4;
   static constexpr size_t kBytes = 1024 + kOffSmall + sizeof(Small);
   static_assert(MAXM * MAXM * 4 <= 32768, "mixing matrix staging");
+  static_assert(kNSO * kOutStage <= NS * kStageBytes, "OUT ring inside the input ring");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -146,13 +152,15 @@ __device__ __forceinline__ void set_abort(Small* sh) { *reinterpret_cast<volatil
 // issues nothing while suspended); false once kWaitLimitNs has passed (and
 // then the CTA aborts) or as soon as another role has aborted.
 __device__ __noinline__ bool bwait(uint64_t* bar, uint32_t parity, Small* sh) {
-  // a short spin first: a suspended thread can take a while to be woken
-  for (int i = 0; i < 256; ++i)
+  // A few polls, then suspended waits with a short limit: a waiter is not
+  // always woken when the phase completes, so the limit bounds the delay,
+  // and suspension keeps waiting warps off the issue slots and the barrier
+  // unit.
+  for (int i = 0; i < 16; ++i)
     if (mbar_test(bar, parity)) return true;
-  if (mbar_try_wait_ns(bar, parity, 1000)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait_ns(bar, parity, 1000)) return true;
+    if (mbar_try_wait_ns(bar, parity, 128)) return true;
     if (aborted(sh)) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
   }
@@ -215,6 +223,24 @@ __device__ __forceinline__ float phi8_dot(uint4& x, const float* z) {
   return a;
 }
 
+// ------------------------------------------------------------------ stores
+// MIX results go out through the load/store units: a warp stages rows of 128
+// bytes in shared memory, then writes them as coalesced 16-byte pieces, four
+// whole rows per instruction.  Staged row r holds its piece c at
+// r * 128 + c * 16; global row r starts at dst + r * stride.
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void warp_store_rows(const uint8_t* yb, uint8_t* dst, int nrows, size_t stride, int lane) {
+  __syncwarp();
+  for (int piece = lane; piece < nrows * 8; piece += 32) {
+    const int r = piece >> 3, c = piece & 7;
+    st_global_v4(dst + r * stride + c * 16, *reinterpret_cast<const uint4*>(yb + r * 128 + c * 16));
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------------ MIX stages
 // The tensor-core MIX units of a CTA are the contiguous range [u0, u1) of the
 // heads x 64 (head, row e of S^T) pairs.  A ring stage carries n <=
@@ -250,14 +276,12 @@ __device__ bool mix_ready(const Params& p, bool& ready) {
   return ready;
 }
 
-template <class L>
-__device__ void issue_mix_loads(const Params& p, uint8_t* sm, Small* sh, int q, int g) {
-  constexpr int kNS = L::NS;
-  const int s = q % kNS;
-  uint8_t* st = sm + s * kStageBytes;
+__device__ void issue_mix_loads(const Params& p, uint8_t* sm, Small* sh, int qo, int g) {
+  const int s = qo % kNSO;
+  uint8_t* st = sm + s * kOutStage;
   const size_t blk = (size_t)(g / p.C) * p.M + (g % p.C) / p.cpb;
-  bulk_load_1d(st + kTileBytes, p.smix + blk * kSTile, kSTile, &sh->full[s]);
-  bulk_load_1d(st + kTileBytes + kSTile, p.zmix + blk * kD, kD * 4, &sh->full[s]);
+  bulk_load_1d(st + kTileBytes, p.smix + blk * kSTile, kSTile, &sh->fullO[s]);
+  bulk_load_1d(st + kTileBytes + kSTile, p.zmix + blk * kD, kD * 4, &sh->fullO[s]);
 }
 
 template <class L>
@@ -272,17 +296,6 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
     mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
     tma_load_2d_hint(st, &p.tm_k, 0, g * kTile, &sh->full[s], once);
     tma_load_2d_hint(st + kTileBytes, &p.tm_v, 0, g * kTile, &sh->full[s], once);
-    // pull the chunk one ring ahead into L2, so its load finds it there
-    const int gp = g + kNS * (int)gridDim.x;
-    if (gp < p.TS) {
-      tma_prefetch_2d(&p.tm_k, 0, gp * kTile);
-      tma_prefetch_2d(&p.tm_v, 0, gp * kTile);
-    }
-  }
-  // and the first OUT chunks' Q tiles, which wait behind the MIX phase
-  for (int k = 0; k < kNS; ++k) {
-    const int gp = blockIdx.x + k * (int)gridDim.x;
-    if (gp < p.TS) tma_prefetch_2d(&p.tm_q, 0, gp * kTile);
   }
   // MIX units (head h, row e of S^T): the chunk partials' row e and the head's
   // weights, once every CTA has stored its partials (grid barrier 1)
@@ -301,49 +314,49 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
       u += n;
     }
   }
-  // OUT pass.  qm = first OUT stage without its S~ / z~ loads.
-  int qm = q;
+  // OUT pass, on the OUT ring over the same memory: every SUM / MIX stage must
+  // have been consumed first.  qm = first OUT stage without its S~ / z~ loads.
+  for (int qq = q > kNS ? q - kNS : 0; qq < q; ++qq)
+    if (!bwait(&sh->empty[qq % kNS], (qq / kNS) & 1, sh)) return q;
+  int qo = 0, qm = 0;
   int gm = blockIdx.x;  // chunk of stage qm
   bool ready = false;
-  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++q) {
-    const int s = q % kNS;
-    if (q >= kNS) {
-      // wait for the stage; until the MIX phase is done, keep checking for it,
+  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qo) {
+    const int s = qo % kNSO;
+    if (qo >= kNSO) {
+      // wait for the slot; until the MIX phase is done, keep checking for it,
       // since the stages ahead cannot drain without their S~ / z~
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait_ns(&sh->empty[s], ((q / kNS) - 1) & 1, 500)) {
+      while (!mbar_try_wait_ns(&sh->emptyO[s], ((qo / kNSO) - 1) & 1, 500)) {
         if (!ready && mix_ready<L>(p, ready)) {
-          for (; qm < q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
+          for (; qm < qo; ++qm, gm += gridDim.x) issue_mix_loads(p, sm, sh, qm, gm);
         }
-        if (aborted(sh)) return q;
+        if (aborted(sh)) break;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
           set_abort(sh);
-          return q;
+          break;
         }
       }
+      if (aborted(sh)) break;
     }
-    uint8_t* st = sm + s * kStageBytes;
-    mbar_arrive_expect_tx(&sh->full[s], kTileBytes + kSTile + kD * 4);
-    tma_load_2d_hint(st, &p.tm_q, 0, g * kTile, &sh->full[s], once);
-    {
-      const int gp = g + kNS * (int)gridDim.x;
-      if (gp < p.TS) tma_prefetch_2d(&p.tm_q, 0, gp * kTile);
-    }
+    uint8_t* st = sm + s * kOutStage;
+    mbar_arrive_expect_tx(&sh->fullO[s], kTileBytes + kSTile + kD * 4);
+    tma_load_2d_hint(st, &p.tm_q, 0, g * kTile, &sh->fullO[s], once);
+    sh->prod_qo = qo + 1;
     if (mix_ready<L>(p, ready)) {
-      for (; qm <= q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
+      for (; qm <= qo; ++qm, gm += gridDim.x) issue_mix_loads(p, sm, sh, qm, gm);
     }
   }
   // every OUT stage still needs its S~ / z~ before the consumers can finish
   const uint64_t t0 = globaltimer_ns();
-  while (qm < q) {
+  while (qm < qo && !aborted(sh)) {
     if (mix_ready<L>(p, ready)) {
-      for (; qm < q; ++qm, gm += gridDim.x) issue_mix_loads<L>(p, sm, sh, qm, gm);
+      for (; qm < qo; ++qm, gm += gridDim.x) issue_mix_loads(p, sm, sh, qm, gm);
       break;
     }
-    if (aborted(sh)) return q;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       set_abort(sh);
-      return q;
+      break;
     }
     __nanosleep(200);
   }
@@ -360,10 +373,16 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
   // physical piece lane&7 is logical piece (lane&7) ^ (row&7) (128-byte swizzle)
   const int r0 = lane >> 3;
   const int g0 = (lane & 7) ^ r0, g1 = (lane & 7) ^ (r0 + 4);
-  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qs, ++qa) {
-    const int s = qs % kNS;
-    if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return;
-    uint8_t* st = sm + s * kStageBytes;
+  // SUM stages come from the input ring (counter qs), OUT stages from the OUT ring
+  int qo = 0;
+  for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qa) {
+    const int s = pass == 0 ? qs % kNS : qo % kNSO;
+    uint64_t* full = pass == 0 ? &sh->full[s] : &sh->fullO[s];
+    uint64_t* ready = pass == 0 ? &sh->ready[s] : &sh->readyO[s];
+    if (!bwait(full, pass == 0 ? (qs / kNS) & 1 : (qo / kNSO) & 1, sh)) return;
+    if (pass == 0) ++qs;
+    else ++qo;
+    uint8_t* st = sm + (pass == 0 ? s * kStageBytes : s * kOutStage);
     uint4* t4 = reinterpret_cast<uint4*>(st) + w * 128 + lane;
     uint4 x[4];
 #pragma unroll
@@ -402,7 +421,7 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
     }
     fence_proxy_async_smem();  // phi tile -> tensor core reads
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sh->ready[s]);
+    if (lane == 0) mbar_arrive(ready);
   }
 }
 
@@ -467,12 +486,18 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
       }
       continue;
     }
-    for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qs, ++qa) {
-      const int s = qs % kNS, a = qa % kNA;
+    int qo = 0;  // OUT stages run on the OUT ring
+    for (int g = blockIdx.x; g < p.TS; g += gridDim.x, ++qa) {
+      const int s = pass == 0 ? qs % kNS : qo % kNSO, a = qa % kNA;
+      uint64_t* ready = pass == 0 ? &sh->ready[s] : &sh->readyO[s];
+      uint64_t* empty = pass == 0 ? &sh->empty[s] : &sh->emptyO[s];
+      const uint32_t parity = pass == 0 ? (qs / kNS) & 1 : (qo / kNSO) & 1;
+      if (pass == 0) ++qs;
+      else ++qo;
       if (qa >= kNA && !bwait(&sh->acc_empty[a], ((qa / kNA) - 1) & 1, sh)) return qa;
-      if (!bwait(&sh->ready[s], (qs / kNS) & 1, sh)) return qa;
+      if (!bwait(ready, parity, sh)) return qa;
       tc_fence_after();
-      const uint32_t st = smem_u32(sm + s * kStageBytes);
+      const uint32_t st = smem_u32(sm + (pass == 0 ? s * kStageBytes : s * kOutStage));
       const uint32_t dst = tmem + (uint32_t)(a * 64);
       // descriptors built once per stage; a K step only moves the start
       // address field (bytes >> 4 in the low bits)
@@ -486,7 +511,7 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
 #pragma unroll
         for (int k = 0; k < kD / 16; ++k) mma_bf16(dst, da + k * (32 >> 4), db + k * (32 >> 4), idesc_out, k > 0);
       }
-      mma_commit(&sh->empty[s]);     // the stage is free once these MMAs have read it
+      mma_commit(empty);             // the stage is free once these MMAs have read it
       mma_commit(&sh->acc_full[a]);  // and the accumulator is ready
     }
   }
@@ -521,8 +546,19 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         tmem_ld16(ta + 32, v + 32);
         tmem_ld16(ta + 48, v + 48);
         tmem_ld_wait();
-        if (i < p.M) {
-          const int e = u % kD + k;
+        const int e = u % kD + k;
+        if (rep4) {
+          // row e of the M tiles S~_i^T: lane i's 128-byte row (pieces already in
+          // the tile's swizzled order) into this warp's staging, then out
+          if (i < p.M) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(yb + i * 128 + (swz128(e, 8 * c) & 127)) =
+                  make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                             pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+          }
+          warp_store_rows(yb, p.smix + (size_t)h * p.M * kSTile + e * 128, p.M, kSTile, lane);
+        } else if (i < p.M) {
           uint8_t* dst = p.smix + ((size_t)h * p.M + i) * kSTile;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
@@ -672,15 +708,63 @@ __device__ void mix_row_simt(const Params& p, const float* wt, int h, int e, int
   }
 }
 
+// z row (e = 64) with a compile-time block length CPB and all C <= 32 chunk
+// partials in registers: block sums first, then independent FMA chains.
+template <int MAXM, int CPB>
+__device__ void mix_z_row_fast(const Params& p, const float* wt, int h, int c) {
+  constexpr int NB = 32 / CPB;
+  const float* src = p.pz + (size_t)h * p.C * kD + c;
+  float val[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) val[k] = k < p.C ? __ldcg(src + (size_t)k * kD) : 0.f;
+  float tb[NB];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    float t = val[b * CPB];
+#pragma unroll
+    for (int k = 1; k < CPB; ++k) t += val[b * CPB + k];
+    tb[b] = t;
+  }
+  float acc[MAXM];
+#pragma unroll
+  for (int i = 0; i < MAXM; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (b >= p.M) break;
+    const float4* w4 = reinterpret_cast<const float4*>(wt + b * MAXM);
+#pragma unroll
+    for (int i = 0; i < MAXM / 4; ++i) {
+      const float4 m4 = w4[i];
+      acc[4 * i] = fmaf(m4.x, tb[b], acc[4 * i]);
+      acc[4 * i + 1] = fmaf(m4.y, tb[b], acc[4 * i + 1]);
+      acc[4 * i + 2] = fmaf(m4.z, tb[b], acc[4 * i + 2]);
+      acc[4 * i + 3] = fmaf(m4.w, tb[b], acc[4 * i + 3]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < MAXM; ++i)
+    if (i < p.M) p.zmix[((size_t)h * p.M + i) * kD + c] = acc[i];
+}
+
 // Stages the transposed mixing matrix of head hh (zero-padded to MAXM) for
 // the n threads of named barrier `bar`.
 template <int MAXM>
 __device__ void stage_weights(const Params& p, float* wt, int hh, int t, int n, int bar) {
   named_bar(bar, n);
   const float* mw = p.mixing + (size_t)hh * p.M * p.M;
-  for (int j = t; j < MAXM * MAXM; j += n) {
-    const int b = j / MAXM, i = j % MAXM;
-    wt[j] = (b < p.M && i < p.M) ? __ldcg(mw + i * p.M + b) : 0.f;
+  for (int j0 = 0; j0 < MAXM * MAXM; j0 += 16 * n) {  // 16 independent loads per thread in flight
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int j = j0 + k * n + t;
+      const int b = j / MAXM, i = j % MAXM;
+      v[k] = (j < MAXM * MAXM && b < p.M && i < p.M) ? __ldcg(mw + i * p.M + b) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int j = j0 + k * n + t;
+      if (j < MAXM * MAXM) wt[j] = v[k];
+    }
   }
   named_bar(bar, n);
 }
@@ -738,12 +822,18 @@ __device__ void mix_rows_all(const Params& p, uint8_t* sm, int t) {
 template <int MAXM>
 __device__ void mix_z_rows(const Params& p, uint8_t* sm, int c) {
   using L = Layout<MAXM>;
-  float* wt = reinterpret_cast<float*>(sm + L::kOffY);
+  float* wt = reinterpret_cast<float*>(sm + L::kOffY + 16384);  // the epilogue warps stage in the lower half
   int cur_hh = -1;
   for (int h = blockIdx.x; h < p.heads; h += gridDim.x) {
     if (h % p.H != cur_hh) {
       cur_hh = h % p.H;
       stage_weights<MAXM>(p, wt, cur_hh, c, 64, kBarZ);
+    }
+    // (with M > 32 there are more than 32 chunks, so the fast rows never apply)
+    if constexpr (MAXM <= 32) {
+      if (p.C <= 32 && p.cpb == 2) { mix_z_row_fast<MAXM, 2>(p, wt, h, c); continue; }
+      if (p.C <= 32 && p.cpb == 1) { mix_z_row_fast<MAXM, 1>(p, wt, h, c); continue; }
+      if (p.C <= 32 && p.cpb == 4) { mix_z_row_fast<MAXM, 4>(p, wt, h, c); continue; }
     }
     mix_row_simt<MAXM>(p, wt, h, kD, c);
   }
@@ -807,6 +897,11 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
       mbar_init(&sh->ready[s], kPhiWarps);
       mbar_init(&sh->empty[s], 1);
     }
+    for (int s = 0; s < kNSO; ++s) {
+      mbar_init(&sh->fullO[s], 1);
+      mbar_init(&sh->readyO[s], kPhiWarps);
+      mbar_init(&sh->emptyO[s], 1);
+    }
     for (int a = 0; a < kNA; ++a) {
       mbar_init(&sh->acc_full[a], 1);
       mbar_init(&sh->acc_empty[a], 4);
@@ -817,6 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     }
     sh->abort = 0;
     sh->prod_q = 0;
+    sh->prod_qo = 0;
     sh->mma_q = 0;
     fence_mbar_init();
   }
@@ -858,7 +954,9 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     if (mix_begin(p, sh, t)) {
       if (p.tc_mix) {
         if (warp >= kWarpPhi) phi_passthrough<L>(p, sh, lane, qs, q);
-        else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
+        else if (warp >= kWarpEpi) {
+          epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
+        }
         else mix_z_rows<MAXM>(p, sm, t);
       } else {
         mix_rows_all<MAXM>(p, sm, t);
@@ -876,6 +974,8 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
   if (tid == 0 && aborted(sh)) {
     const int nq = sh->prod_q;
     for (int q = nq > kNS ? nq - kNS : 0; q < nq; ++q) drain_wait(&sh->full[q % kNS], (q / kNS) & 1);
+    const int no = sh->prod_qo;
+    for (int q = no > kNSO ? no - kNSO : 0; q < no; ++q) drain_wait(&sh->fullO[q % kNSO], (q / kNSO) & 1);
     const int mq = sh->mma_q;
     if (mq > 0) drain_wait(&sh->acc_full[(mq - 1) % kNA], ((mq - 1) / kNA) & 1);
     atomicOr(p.status, 1u);
