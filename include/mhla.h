@@ -160,7 +160,9 @@ mhla_status mhla_forward_noalloc(const void* q, const void* k, const void* v, co
                                  void* y, float* den_out, int B, int H, int N, int d,
                                  int block_size, mhla_dtype dt, float eps, void* stream);
 
-/* Kernel family mhla_forward would use for these arguments (no launch). */
+/* Kernel family mhla_forward would use for these arguments (no launch).
+ * With causal = 1 the answer is for plain causal linear attention (mixing
+ * NULL); causal MHLA with a mixing matrix always runs the SIMT kernels. */
 mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
                             mhla_dtype dt);
 

@@ -250,6 +250,36 @@ def test_causal_small(shape, dtype):
         assert_close_den(den, dbrute, dtype)
 
 
+# bf16, d = 64, N a multiple of 128: the tensor-core causal kernels.  The
+# chunks of all heads are cut into one contiguous segment per CTA, so these
+# shapes put head starts at every position inside a segment and spread heads
+# over several CTAs.
+CAUSAL_TC = [  # B, H, N, chunk
+    (4, 100, 128, 128),   # one chunk per head: several whole heads per CTA
+    (3, 100, 256, 64),    # two chunks per head
+    (1, 5, 10240, 128),   # 80 chunks per head, each head over ~30 CTAs
+    (1, 1, 128, 128),     # a single chunk
+]
+
+
+@pytest.mark.parametrize("shape", CAUSAL_TC, ids=lambda s: "x".join(map(str, s)))
+def test_causal_tcgen05_shapes(shape):
+    B, H, N, chunk = shape
+    assert binding.mhla_forward_path(B, H, N, 64, chunk, 1, torch.bfloat16) == "tcgen05"
+    x = rand_inputs(300 + N + H, (B, H, N, 64), "bf16")
+    y, den = forward_causal(x["q"], x["k"], x["v"], None, chunk)
+    ref, dref = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], 128)
+    assert_close_y(y, ref, "bf16")
+    assert_close_den(den, dref, "bf16")
+
+
+def test_causal_tcgen05_repeat_is_deterministic():
+    x = rand_inputs(41, (2, 3, 1024, 64), "bf16")
+    y1, d1 = forward_causal(x["q"], x["k"], x["v"], None, 128)
+    y2, d2 = forward_causal(x["q"], x["k"], x["v"], None, 128)
+    assert np.array_equal(y1, y2) and np.array_equal(d1, d2)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_causal_mhla_with_mixing(dtype):
     B, H, N, d, chunk = 1, 2, 256, 32, 64

@@ -32,6 +32,12 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
                            const float* mixing, void* y, float* den_out, float eps, MixMode mode,
                            void* ws, cudaStream_t st);
 
+// ---- tcgen05 causal path (bf16, d = 64, plain causal linear attention, N a multiple of 128)
+bool tc_causal_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
+size_t tc_causal_workspace(const MhlaShape& s);
+cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, const void* v, void* y,
+                             float* den_out, float eps, void* ws, cudaStream_t st);
+
 // ---- SIMT path (fp32 mode, and every shape the tensor-core path does not take)
 size_t simt_mhla_workspace(const MhlaShape& s);
 cudaError_t simt_mhla_launch(const MhlaShape& s, mhla_dtype dt, const void* q, const void* k,

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -34,7 +35,8 @@ size_t mhla_ws(int B, int H, int N, int d, int block) {
   MhlaShape s{B, H, N, d, block};
   const size_t a = simt_mhla_workspace(s);
   const size_t b = tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0;
-  return a > b ? a : b;
+  const size_t c = tc_causal_supported(s, MHLA_BF16, MIX_PREFIX) ? tc_causal_workspace(s) : 0;
+  return std::max(a, std::max(b, c));
 }
 
 // Shared validation of the Q/K/V/Y/den/workspace arguments of the MHLA entries.
@@ -82,7 +84,8 @@ mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int caus
       (dt != MHLA_F32 && dt != MHLA_BF16) || (causal != 0 && causal != 1))
     return MHLA_PATH_NONE;
   const MhlaShape s{B, H, N, d, block_size};
-  return tc_mhla_supported(s, dt, causal ? MIX_PREFIX : MIX_FULL) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+  const bool tc = causal ? tc_causal_supported(s, dt, MIX_PREFIX) : tc_mhla_supported(s, dt, MIX_FULL);
+  return tc ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
 
 static mhla_status run_mhla(const void* q, const void* k, const void* v, const float* mixing,
@@ -93,6 +96,8 @@ static mhla_status run_mhla(const void* q, const void* k, const void* v, const f
   if (st != MHLA_OK || (size_t)B * H * N == 0) return st;
   if (mode != MIX_PREFIX && (!mixing || !aligned16(mixing))) return MHLA_ERR_INVALID_ARG;
   MhlaShape s{B, H, N, d, block};
+  if (tc_causal_supported(s, dt, mode))
+    return from_cuda(tc_causal_launch(s, q, k, v, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
   if (tc_mhla_supported(s, dt, mode))
     return from_cuda(tc_mhla_launch(s, q, k, v, mixing, y, den_out, eps, mode, ws,
                                     static_cast<cudaStream_t>(stream)));

@@ -127,23 +127,6 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Every thread of named barrier `id` (n threads) contributes `pred`; all get the AND.
-__device__ __forceinline__ bool group_and(int id, int n, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
 
 __device__ __forceinline__ int aborted(Small* sh) { return *reinterpret_cast<volatile int*>(&sh->abort); }
 __device__ __forceinline__ void set_abort(Small* sh) { *reinterpret_cast<volatile int*>(&sh->abort) = 1; }
@@ -190,19 +173,6 @@ __device__ __noinline__ bool gwait(const unsigned* p, unsigned target, Small* sh
 }
 
 // ------------------------------------------------------------------ phi
-// phi(x) = exp(min(x, 0)) + max(x, 0): x + 1 for x > 0 (exp(0) = 1 exactly),
-// exp(x) otherwise; exp through the hardware base-2 exponential.
-__device__ __forceinline__ float phi_f(float x) {
-  float e;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(x, 0.f) * 1.4426950408889634f));
-  return e + fmaxf(x, 0.f);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
 __device__ __forceinline__ uint32_t phi2(uint32_t w) {
   return pack_bf16(phi_f(__uint_as_float(w << 16)), phi_f(__uint_as_float(w & 0xffff0000u)));
 }
