@@ -31,18 +31,20 @@ size_t elems(int B, int H, int N, int d) { return (size_t)B * H * N * d; }
 
 mhla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MHLA_OK : MHLA_ERR_CUDA; }
 
-size_t mhla_ws(int B, int H, int N, int d, int block) {
+// Workspace of the non-causal (causal = 0) or causal forms: the largest need
+// of the kernel families either form may take for these sizes.
+size_t mhla_ws(int B, int H, int N, int d, int block, int causal) {
   MhlaShape s{B, H, N, d, block};
   const size_t a = simt_mhla_workspace(s);
-  const size_t b = tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0;
-  const size_t c = tc_causal_supported(s, MHLA_BF16, MIX_PREFIX) ? tc_causal_workspace(s) : 0;
-  return std::max(a, std::max(b, c));
+  const size_t b = causal ? (tc_causal_supported(s, MHLA_BF16, MIX_PREFIX) ? tc_causal_workspace(s) : 0)
+                          : (tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0);
+  return std::max(a, b);
 }
 
 // Shared validation of the Q/K/V/Y/den/workspace arguments of the MHLA entries.
 mhla_status check_mhla(const void* q, const void* k, const void* v, const void* y,
                        const float* den_out, int B, int H, int N, int d, int block,
-                       mhla_dtype dt, float eps, const void* ws, size_t ws_bytes) {
+                       mhla_dtype dt, float eps, const void* ws, size_t ws_bytes, int causal) {
   if (!dims_ok(B, H, N) || !valid_d(d)) return MHLA_ERR_INVALID_ARG;
   if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
   if (!std::isfinite(eps) || eps < 0.f) return MHLA_ERR_INVALID_ARG;
@@ -61,7 +63,7 @@ mhla_status check_mhla(const void* q, const void* k, const void* v, const void* 
       return MHLA_ERR_INVALID_ARG;
   }
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MHLA_ERR_INVALID_ARG;
-  if (ws_bytes < mhla_ws(B, H, N, d, block)) return MHLA_ERR_INVALID_ARG;
+  if (ws_bytes < mhla_ws(B, H, N, d, block, causal)) return MHLA_ERR_INVALID_ARG;
   return MHLA_OK;
 }
 
@@ -73,9 +75,8 @@ using namespace mhla;
 extern "C" {
 
 size_t mhla_workspace_bytes(int B, int H, int N, int d, int block_size, int causal) {
-  (void)causal;
   if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0)) return 0;
-  return mhla_ws(B, H, N, d, block_size);
+  return mhla_ws(B, H, N, d, block_size, causal != 0);
 }
 
 mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
@@ -92,7 +93,7 @@ static mhla_status run_mhla(const void* q, const void* k, const void* v, const f
                             void* y, float* den_out, int B, int H, int N, int d, int block,
                             MixMode mode, mhla_dtype dt, float eps, void* ws, size_t ws_bytes,
                             void* stream) {
-  mhla_status st = check_mhla(q, k, v, y, den_out, B, H, N, d, block, dt, eps, ws, ws_bytes);
+  mhla_status st = check_mhla(q, k, v, y, den_out, B, H, N, d, block, dt, eps, ws, ws_bytes, mode != MIX_FULL);
   if (st != MHLA_OK || (size_t)B * H * N == 0) return st;
   if (mode != MIX_PREFIX && (!mixing || !aligned16(mixing))) return MHLA_ERR_INVALID_ARG;
   MhlaShape s{B, H, N, d, block};

@@ -36,6 +36,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -706,9 +707,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
 }
 
 inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
-constexpr size_t kOffAggS = kWorkspacePrefix;
-constexpr size_t kOffAggZ = kOffAggS + (size_t)kMaxCtas * kD * kD * sizeof(float);
-constexpr size_t kCausalWs = kOffAggZ + (size_t)kMaxCtas * kD * sizeof(float);
+// Workspace: the header and counter prefix, then agg_s and agg_z of up to
+// min(T, kMaxCtas) CTAs.
+int max_ctas(const MhlaShape& s) { return (int)std::min<long long>((long long)s.heads() * (s.N / kTile), kMaxCtas); }
+size_t off_agg_z(const MhlaShape& s) { return kWorkspacePrefix + a256((size_t)max_ctas(s) * kD * kD * sizeof(float)); }
 
 int sm_count() {
   int dev = 0, n = 0;
@@ -725,10 +727,7 @@ bool tc_causal_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
   return (long long)s.heads() * s.N < (1ll << 31);
 }
 
-size_t tc_causal_workspace(const MhlaShape& s) {
-  (void)s;
-  return a256(kCausalWs);
-}
+size_t tc_causal_workspace(const MhlaShape& s) { return off_agg_z(s) + a256((size_t)max_ctas(s) * kD * sizeof(float)); }
 
 cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, const void* v, void* y,
                              float* den_out, float eps, void* ws, cudaStream_t st) {
@@ -738,8 +737,8 @@ cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, c
   if (!make_map(&p.tm_q, q, rows, kTile) || !make_map(&p.tm_k, k, rows, kTile) || !make_map(&p.tm_v, v, rows, kTile) ||
       !make_map(&p.tm_y, y, rows, 32))
     return cudaErrorInvalidValue;
-  p.agg_s = reinterpret_cast<float*>(w + kOffAggS);
-  p.agg_z = reinterpret_cast<float*>(w + kOffAggZ);
+  p.agg_s = reinterpret_cast<float*>(w + kWorkspacePrefix);
+  p.agg_z = reinterpret_cast<float*>(w + off_agg_z(s));
   p.den_out = den_out;
   p.status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
   p.T = s.heads() * (s.N / kTile);
@@ -747,7 +746,7 @@ cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, c
   p.eps = eps;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  p.G = std::min(std::min(p.T, sms), kMaxCtas);
+  p.G = std::min(max_ctas(s), sms);
   static bool attr_done = false;
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(causal_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
