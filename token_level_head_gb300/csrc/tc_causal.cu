@@ -24,13 +24,15 @@
 //   warps 8-15  phi in place on the Q and K tiles (16 rows a warp), the fp32
 //               inclusive prefix of phi(K) inside the chunk and from it the
 //               denominator phi(q_t) . (zeta_c + sum_{s <= t} phi(k_s)) + eps
-//   warp 1      MMA issuer: P += phi(K)^T V (M 64, carried in TMEM);
+//   warp 1      MMA issuer: P += phi(K)^T V (carried in TMEM, M 128 with a
+//               ones tile as A rows 0-63, so P lands in lanes 64-127);
 //               scores = phi(Q) phi(K)^T (M 128, N 128); Y~ = phi(Q) P_c;
 //               then Y~ += mask(scores) V once the masked scores are back
-//   warps 4-7   epilogue, one TMEM lane quadrant each: P -> bf16 tile of the
-//               next chunk's P_c; scores -> lower-triangle mask -> bf16 A tile
-//               (written over the stage's Q and K tiles, which are dead by
-//               then); Y = Y~ / den in bf16 through a TMA store
+//   warps 2-3   P -> bf16 tile of the next chunk's P_c
+//   warps 4-7   epilogue, one TMEM lane quadrant each: scores -> lower-
+//               triangle mask -> bf16 A tile (written over the stage's Q and
+//               K tiles, which are dead by then); Y = Y~ / den in bf16
+//               through a TMA store
 // All waits are bounded: on time-out the kernel sets the status word and
 // winds down.
 #include <cuda.h>
@@ -53,21 +55,24 @@ constexpr int kTile = 128;                   // tokens per chunk
 constexpr int kD = 64;                       // head dimension
 constexpr int kTileBytes = kTile * kD * 2;   // 16 KB bf16 tile
 constexpr int kPTile = kD * kD * 2;          // 8 KB bf16 P_c^T tile
-constexpr int kWarpProd = 0, kWarpMma = 1, kWarpEpi = 4, kWarpPhi = 8;
+constexpr int kWarpProd = 0, kWarpMma = 1, kWarpP = 2, kWarpEpi = 4, kWarpPhi = 8;
 constexpr int kPhiWarps = 8;
 constexpr int kBarPhi = 1;                   // named barrier of the phi warps
 constexpr uint64_t kWaitLimitNs = 500000000ull;
 constexpr int kMaxCtas = 256;                // aggregates in the workspace
 
-// causal_out_kernel: TMEM columns of the running P (M 64 layout: row r in
-// lane 32 (r / 16) + r % 16), the two score accumulators and the two Y~.
+// causal_out_kernel: TMEM columns of the running P (rows 64-127), the two
+// score accumulators and the two Y~.
 constexpr uint32_t kOutCols = 512, kColP = 0, kColSc = 128, kColNum = 384;
 constexpr int kNSB = 3;                      // stages: Q, K, V
 constexpr int kStageB = 3 * kTileBytes;
-constexpr int kOffP = kNSB * kStageB;        // 2 P_c^T tiles
+constexpr int kOffOnesB = 0;                 // 16 KB of bf16 ones: A rows 0..63 of the P MMA
+constexpr int kOffStages = kTileBytes;       // the ring (above the ones tile: the MMA's LBO is positive)
+constexpr int kOffP = kOffStages + kNSB * kStageB;  // 2 P_c^T tiles
 constexpr int kOffY = kOffP + 2 * kPTile;    // Y staging, 4 warps x 4 KB
-constexpr int kOffDen = kOffY + 4 * 4096;    // [2][128] fp32
-constexpr int kOffWs = kOffDen + 2 * kTile * 4;  // [2][8 warps][64] fp32 column sums of phi(K)
+constexpr int kNDen = 4;                     // denominator slots
+constexpr int kOffDen = kOffY + 4 * 4096;    // [kNDen][128] fp32
+constexpr int kOffWs = kOffDen + kNDen * kTile * 4;  // [2][8 warps][64] fp32 column sums of phi(K)
 constexpr int kOffZ = kOffWs + 2 * kPhiWarps * kD * 4;  // [2][64] fp32 zeta_c
 constexpr int kOffSmallB = kOffZ + 2 * kD * 4;
 
@@ -81,6 +86,7 @@ constexpr int kOffSmallA = kOffZA + kPhiWarps * kD * 4;
 struct OSmall {
   uint64_t full[kNSB], ready[kNSB], empty[kNSB];
   uint64_t p_full, ptile_full[2], sc_full[2], sc_empty[2], scores_full[2], num_full[2], num_empty[2];
+  uint64_t den_free[kNDen];
   uint64_t fin;
   uint32_t tbase;
   int abort;
@@ -313,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) causal_agg_kernel(const __grid_co
 }
 
 // ================================================================ output
-__device__ int out_producer(const CParams& p, uint8_t* sm, OSmall* sh, int lo, int n) {
+__device__ __noinline__ int out_producer(const CParams& p, uint8_t* sm, OSmall* sh, int lo, int n) {
   const uint64_t once = policy_evict_first();
   int i = 0;
   for (; i < n; ++i) {
     const int s = i % kNSB;
     if (i >= kNSB && !cwait(&sh->empty[s], ((i / kNSB) - 1) & 1, &sh->abort)) break;
-    uint8_t* st = sm + s * kStageB;
+    uint8_t* st = sm + kOffStages + s * kStageB;
     const int row = (lo + i) * kTile;
     mbar_arrive_expect_tx(&sh->full[s], kStageB);
     tma_load_2d_hint(st, &p.tm_q, 0, row, &sh->full[s], once);
@@ -330,7 +336,7 @@ __device__ int out_producer(const CParams& p, uint8_t* sm, OSmall* sh, int lo, i
 }
 
 // phi warp w: phi(K), its in-chunk inclusive prefix, zeta, phi(Q) and den.
-__device__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, int w, int lane, int lo, int n) {
+__device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, int w, int lane, int lo, int n) {
   float* den = reinterpret_cast<float*>(sm + kOffDen);
   float* wsum = reinterpret_cast<float*>(sm + kOffWs);
   float* zb = reinterpret_cast<float*>(sm + kOffZ);
@@ -350,10 +356,11 @@ __device__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, int w, int la
   for (int i = 0; i < n; ++i) {
     const int s = i % kNSB, a = i & 1, c = lo + i;
     bool ok = cwait(&sh->full[s], (i / kNSB) & 1, ab);
-    // den[a] is free once the epilogue of chunk i - 2 has read it
-    if (ok && i >= 2) ok = cwait(&sh->num_empty[a], ((i >> 1) - 1) & 1, ab);
+    // den slot i % kNDen is free once the epilogue of chunk i - kNDen has read it
+    const int dslot = i % kNDen;
+    if (ok && i >= kNDen) ok = cwait(&sh->den_free[dslot], ((i / kNDen) - 1) & 1, ab);
     ok = __all_sync(0xffffffffu, ok);
-    uint8_t* st = sm + s * kStageB;
+    uint8_t* st = sm + kOffStages + s * kStageB;
     float kf[4][8], run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (ok) {
       phi_rows(st + kTileBytes, w, lane, kf);
@@ -408,7 +415,7 @@ __device__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, int w, int la
       d += __shfl_xor_sync(0xffffffffu, d, 1);
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       d += __shfl_xor_sync(0xffffffffu, d, 4);
-      if (j == 0) den[a * kTile + 16 * w + r0 + 4 * i4] = d + p.eps;
+      if (j == 0) den[dslot * kTile + 16 * w + r0 + 4 * i4] = d + p.eps;
     }
     fence_proxy_async_smem();  // phi tiles -> tensor core reads
     __syncwarp();
@@ -416,12 +423,11 @@ __device__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, int w, int la
   }
 }
 
-// The second half of chunk i's MMAs: Y~ += mask(scores) V; frees the stage.
-__device__ bool out_finish(uint8_t* sm, OSmall* sh, uint32_t tmem, int i) {
+// The second half of chunk i's MMAs, once its masked scores are in place:
+// Y~ += mask(scores) V; frees the stage.
+__device__ void out_finish(uint8_t* sm, OSmall* sh, uint32_t tmem, int i) {
   const int a = i & 1, s = i % kNSB;
-  if (!cwait(&sh->scores_full[a], (i >> 1) & 1, &sh->abort)) return false;
-  tc_fence_after();
-  const uint32_t st = smem_u32(sm + s * kStageB);
+  const uint32_t st = smem_u32(sm + kOffStages + s * kStageB);
   // A = masked scores, K-major: s 0..63 over the K tile, s 64..127 over the Q
   // tile; B = V (N = e, K = s: MN-major)
   const uint64_t d0 = smem_desc(st + kTileBytes, 16, 1024), d1 = smem_desc(st, 16, 1024);
@@ -433,52 +439,73 @@ __device__ bool out_finish(uint8_t* sm, OSmall* sh, uint32_t tmem, int i) {
              idesc, true);
   mma_commit(&sh->empty[s]);
   mma_commit(&sh->num_full[a]);
-  return true;
 }
 
-__device__ void out_mma(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem, int lo, int n) {
-  int* ab = &sh->abort;
-  const uint32_t id_p = idesc_bf16_f32(64, 64, 1, 1);
-  const uint32_t id_sc = idesc_bf16_f32(128, 128, 0, 0);
-  const uint32_t id_qp = idesc_bf16_f32(128, 64, 0, 0);
-  const uint32_t ptiles = smem_u32(sm + kOffP);
-  bool ok = true;
-  for (int i = 0; i < n; ++i) {
-    const int a = i & 1, s = i % kNSB, c = lo + i;
-    ok = cwait(&sh->ready[s], (i / kNSB) & 1, ab);
-    if (ok && i >= 2)
-      ok = cwait(&sh->sc_empty[a], ((i >> 1) - 1) & 1, ab) && cwait(&sh->num_empty[a], ((i >> 1) - 1) & 1, ab);
-    // P_c^T is in its tile and the previous P has been read out of TMEM
-    if (ok) ok = cwait(&sh->ptile_full[a], (i >> 1) & 1, ab);
-    if (!ok) break;
-    tc_fence_after();
-    const uint32_t st = smem_u32(sm + s * kStageB);
-    const uint32_t q0 = st, k0 = st + kTileBytes, v0 = st + 2 * kTileBytes;
-    {
-      // P^T[e][c] (+)= sum_t V[t][e] phi(K)[t][c]; a chunk that starts a head starts from zero
-      const uint64_t da = smem_desc(v0, kTileBytes, 1024), db = smem_desc(k0, 8192, 1024);
-      const bool cont = c % p.CH != 0;
+// The first MMAs of chunk i: P += phi(K)^T V, scores, Y~ = phi(Q) P_c.
+__device__ void out_start(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem, int lo, int i) {
+  const int a = i & 1, s = i % kNSB, c = lo + i;
+  const uint32_t ones = smem_u32(sm + kOffOnesB);
+  const uint32_t st = smem_u32(sm + kOffStages + s * kStageB);
+  const uint32_t q0 = st, k0 = st + kTileBytes, v0 = st + 2 * kTileBytes;
+  {
+    // D = [1 ; V^T] phi(K) (M 128, MN-major A: the ones tile, then V, v0 - ones
+    // bytes apart): rows 64 + e hold P^T[e][c] += sum_t V[t][e] phi(K)[t][c];
+    // a chunk that starts a head starts from zero
+    const uint64_t da = smem_desc(ones, v0 - ones, 1024), db = smem_desc(k0, 8192, 1024);
+    const uint32_t idesc = idesc_bf16_f32(128, 64, 1, 1);
+    const bool cont = c % p.CH != 0;
 #pragma unroll
-      for (int k = 0; k < kTile / 16; ++k)
-        mma_bf16(tmem + kColP, da + k * (2048 >> 4), db + k * (2048 >> 4), id_p, cont || k > 0);
-    }
-    mma_commit(&sh->p_full);
-    {
-      const uint64_t da = smem_desc(q0, 16, 1024), db = smem_desc(k0, 16, 1024);
-#pragma unroll
-      for (int k = 0; k < kD / 16; ++k)
-        mma_bf16(tmem + kColSc + 128 * a, da + k * (32 >> 4), db + k * (32 >> 4), id_sc, k > 0);
-    }
-    {
-      const uint64_t da = smem_desc(q0, 16, 1024), db = smem_desc(ptiles + a * kPTile, 16, 1024);
-#pragma unroll
-      for (int k = 0; k < kD / 16; ++k)
-        mma_bf16(tmem + kColNum + 64 * a, da + k * (32 >> 4), db + k * (32 >> 4), id_qp, k > 0);
-    }
-    mma_commit(&sh->sc_full[a]);
-    if (i >= 1 && !(ok = out_finish(sm, sh, tmem, i - 1))) break;
+    for (int k = 0; k < kTile / 16; ++k)
+      mma_bf16(tmem + kColP, da + k * (2048 >> 4), db + k * (2048 >> 4), idesc, cont || k > 0);
   }
-  if (ok && n >= 1) out_finish(sm, sh, tmem, n - 1);
+  mma_commit(&sh->p_full);
+  {
+    const uint64_t da = smem_desc(q0, 16, 1024), db = smem_desc(k0, 16, 1024);
+    const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+    for (int k = 0; k < kD / 16; ++k)
+      mma_bf16(tmem + kColSc + 128 * a, da + k * (32 >> 4), db + k * (32 >> 4), idesc, k > 0);
+  }
+  {
+    const uint64_t da = smem_desc(q0, 16, 1024), db = smem_desc(smem_u32(sm + kOffP) + a * kPTile, 16, 1024);
+    const uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+    for (int k = 0; k < kD / 16; ++k)
+      mma_bf16(tmem + kColNum + 64 * a, da + k * (32 >> 4), db + k * (32 >> 4), idesc, k > 0);
+  }
+  mma_commit(&sh->sc_full[a]);
+}
+
+// MMA issuer: polls the two kinds of work it can do, finishing a chunk whose
+// masked scores are back first (that frees a stage), else starting the next
+// chunk once its phi tiles, its P_c tile and its accumulators are ready.
+__device__ __noinline__ void out_mma(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem, int lo, int n) {
+  int* ab = &sh->abort;
+  int i = 0, f = 0;  // next chunk to start, next chunk to finish
+  uint64_t t0 = globaltimer_ns();
+  while (f < n) {
+    if (f < i && mbar_test(&sh->scores_full[f & 1], (f >> 1) & 1)) {
+      tc_fence_after();
+      out_finish(sm, sh, tmem, f++);
+      t0 = globaltimer_ns();
+      continue;
+    }
+    if (i < n && mbar_test(&sh->ready[i % kNSB], (i / kNSB) & 1) &&
+        mbar_test(&sh->ptile_full[i & 1], (i >> 1) & 1) &&
+        (i < 2 || (mbar_test(&sh->sc_empty[i & 1], ((i >> 1) - 1) & 1) &&
+                   mbar_test(&sh->num_empty[i & 1], ((i >> 1) - 1) & 1)))) {
+      tc_fence_after();
+      out_start(p, sm, sh, tmem, lo, i++);
+      t0 = globaltimer_ns();
+      continue;
+    }
+    if (ab_get(ab)) break;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      ab_set(ab);
+      break;
+    }
+    __nanosleep(32);
+  }
   mma_commit(&sh->fin);
 }
 
@@ -496,10 +523,13 @@ __device__ bool out_store(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
   for (int g = 0; g < 4; ++g) tmem_ld16(ta + 16 * g, v + 16 * g);
   tmem_ld_wait();
   const int t = qd * 32 + lane;
-  const float dn = den[a * kTile + t];
+  const float dn = den[(i % kNDen) * kTile + t];
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(&sh->num_empty[a]);
+  if (lane == 0) {
+    mbar_arrive(&sh->num_empty[a]);
+    mbar_arrive(&sh->den_free[i % kNDen]);
+  }
   const size_t row = (size_t)(lo + i) * kTile + t;
   if (p.den_out != nullptr) p.den_out[row] = dn;
   const float r = 1.f / dn;
@@ -519,86 +549,98 @@ __device__ bool out_store(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
   return true;
 }
 
-__device__ void out_epi(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem, int qd, int lane, int lo, int n) {
+// Warps 2-3 carry P: TMEM lanes 64 + e hold P^T row e (warp 2 rows 0..31,
+// warp 3 rows 32..63).  They seed P with the predecessors' aggregates and,
+// after each chunk's P MMA, write the bf16 P_c^T tile of the next chunk.
+__device__ __noinline__ void out_pchain(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem, int wq, int lane, int lo, int n) {
   int* ab = &sh->abort;
   uint8_t* ptile = sm + kOffP;
-  const uint32_t lq = (uint32_t)(qd * 32) << 16;
-  const int e = 16 * qd + lane;  // P^T row of this lane (lanes 0..15 of the quadrant, M 64 layout)
-  int nst = 0;
+  const uint32_t lq = (uint32_t)(64 + 32 * wq) << 16;
+  const int e = 32 * wq + lane;
   {
-    // P of the first chunk: the predecessors' aggregates in this head, into
-    // TMEM (the MMAs add on) and, in bf16, into the first P_c^T tile
     float v[64];
 #pragma unroll
     for (int x = 0; x < 64; ++x) v[x] = 0.f;
     const int h0 = lo - lo % p.CH;
     if (lo != h0) {
-      if (lane < 16)
-        for (int jj = (int)blockIdx.x - 1; jj >= 0 && seg_lo(p, jj + 1) > h0; --jj) {
-          const float4* src = reinterpret_cast<const float4*>(p.agg_s + ((size_t)jj * kD + e) * kD);
+      for (int jj = (int)blockIdx.x - 1; jj >= 0 && seg_lo(p, jj + 1) > h0; --jj) {
+        const float4* src = reinterpret_cast<const float4*>(p.agg_s + ((size_t)jj * kD + e) * kD);
 #pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const float4 u = __ldcg(src + c4);
-            v[4 * c4] += u.x;
-            v[4 * c4 + 1] += u.y;
-            v[4 * c4 + 2] += u.z;
-            v[4 * c4 + 3] += u.w;
-          }
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 u = __ldcg(src + c4);
+          v[4 * c4] += u.x;
+          v[4 * c4 + 1] += u.y;
+          v[4 * c4 + 2] += u.z;
+          v[4 * c4 + 3] += u.w;
         }
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g) tmem_st16(tmem + kColP + lq + 16 * g, v + 16 * g);
       tmem_st_wait();
     }
-    if (lane < 16)
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) *swz_piece(ptile, e, jj) = pack8(v + 8 * jj);
+    for (int jj = 0; jj < 8; ++jj) *swz_piece(ptile, e, jj) = pack8(v + 8 * jj);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh->ptile_full[0]);
   }
-  for (int i = 0; i < n; ++i) {
-    const int a = i & 1, c = lo + i;
-    // P after chunk i -> the P_c^T tile of chunk i + 1
+  for (int i = 0; i + 1 < n; ++i) {
     if (!cwait(&sh->p_full, i & 1, ab)) return;
     tc_fence_after();
-    if (i + 1 < n) {
-      float v[64];
+    float v[64];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld16(tmem + kColP + lq + 16 * g, v + 16 * g);
-      tmem_ld_wait();
-      tc_fence_before();
-      const bool fresh = (c + 1) % p.CH == 0;
-      if (lane < 16) {
-        uint8_t* dst = ptile + ((i + 1) & 1) * kPTile;
+    for (int g = 0; g < 4; ++g) tmem_ld16(tmem + kColP + lq + 16 * g, v + 16 * g);
+    tmem_ld_wait();
+    tc_fence_before();
+    // the tile of chunk i + 1 was last read by the MMAs of chunk i - 1, which
+    // completed before this chunk's P MMA did
+    uint8_t* dst = ptile + ((i + 1) & 1) * kPTile;
+    const bool fresh = (lo + i + 1) % p.CH == 0;  // chunk i + 1 starts a head
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) *swz_piece(dst, e, jj) = fresh ? make_uint4(0, 0, 0, 0) : pack8(v + 8 * jj);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->ptile_full[(i + 1) & 1]);
-    }
+    for (int jj = 0; jj < 8; ++jj) *swz_piece(dst, e, jj) = fresh ? make_uint4(0, 0, 0, 0) : pack8(v + 8 * jj);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->ptile_full[(i + 1) & 1]);
+  }
+}
+
+// Epilogue warp qd (TMEM lanes 32 qd ..): the Y rows of chunk i - 1, then the
+// masked scores of chunk i.
+__device__ __noinline__ void out_epi(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem, int qd, int lane, int lo, int n) {
+  int* ab = &sh->abort;
+  const uint32_t lq = (uint32_t)(qd * 32) << 16;
+  int nst = 0;
+  for (int i = 0; i < n; ++i) {
+    const int a = i & 1;
+    // Y of chunk i - 1 first: its accumulator is what chunk i + 1 starts on
+    if (i >= 1 && !out_store(p, sm, sh, tmem, qd, lane, lo, i - 1, nst)) return;
     // scores -> mask s <= t -> bf16 A tiles over the stage's K (s < 64) and Q tiles
     if (!cwait(&sh->sc_full[a], (i >> 1) & 1, ab)) return;
     tc_fence_after();
-    uint8_t* st = sm + (i % kNSB) * kStageB;
+    uint8_t* st = sm + kOffStages + (i % kNSB) * kStageB;
     const int t = 32 * qd + lane;
-    const int lim = 32 * qd + 32;  // columns at or beyond lim are zero for this quadrant
+    // 32 columns s0 = 32 qr at a time: below this quadrant's rows they are kept
+    // whole, beyond them they are zero, on the diagonal (qr = qd) masked
+    for (int qr = 0; qr < 4; ++qr) {
+      uint8_t* tile = qr < 2 ? st + kTileBytes : st;
+      const int j0 = 4 * (qr & 1);
+      if (qr > qd) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float v[64];
-#pragma unroll
-      for (int x = 0; x < 64; ++x) v[x] = 0.f;
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-        if (64 * half + 16 * g < lim) tmem_ld16(tmem + kColSc + 128 * a + lq + 64 * half + 16 * g, v + 16 * g);
+        for (int jj = 0; jj < 4; ++jj) *swz_piece(tile, t, j0 + jj) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
+      float v[32];
+      tmem_ld16(tmem + kColSc + 128 * a + lq + 32 * qr, v);
+      tmem_ld16(tmem + kColSc + 128 * a + lq + 32 * qr + 16, v + 16);
       tmem_ld_wait();
+      if (qr == qd) {
 #pragma unroll
-      for (int x = 0; x < 64; ++x)
-        if (64 * half + x > t) v[x] = 0.f;
-      uint8_t* tile = half == 0 ? st + kTileBytes : st;
+        for (int x = 0; x < 32; ++x)
+          if (x > lane) v[x] = 0.f;
+      }
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) *swz_piece(tile, t, jj) = pack8(v + 8 * jj);
+      for (int jj = 0; jj < 4; ++jj) *swz_piece(tile, t, j0 + jj) = pack8(v + 8 * jj);
     }
     tc_fence_before();
     fence_proxy_async_smem();
@@ -607,7 +649,6 @@ __device__ void out_epi(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tmem
       mbar_arrive(&sh->sc_empty[a]);
       mbar_arrive(&sh->scores_full[a]);
     }
-    if (i >= 1 && !out_store(p, sm, sh, tmem, qd, lane, lo, i - 1, nst)) return;
   }
   if (n >= 1) out_store(p, sm, sh, tmem, qd, lane, lo, n - 1, nst);
 }
@@ -627,13 +668,14 @@ __global__ void __launch_bounds__(kThreads, 1) causal_out_kernel(const __grid_co
     mbar_init(&sh->p_full, 1);
     mbar_init(&sh->fin, 1);
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&sh->ptile_full[a], 4);
+      mbar_init(&sh->ptile_full[a], 2);
       mbar_init(&sh->sc_full[a], 1);
       mbar_init(&sh->sc_empty[a], 4);
       mbar_init(&sh->scores_full[a], 4);
       mbar_init(&sh->num_full[a], 1);
       mbar_init(&sh->num_empty[a], 4);
     }
+    for (int d = 0; d < kNDen; ++d) mbar_init(&sh->den_free[d], 4);
     sh->abort = 0;
     sh->prod_q = 0;
     fence_mbar_init();
@@ -648,6 +690,9 @@ __global__ void __launch_bounds__(kThreads, 1) causal_out_kernel(const __grid_co
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_y);
   }
+  for (int i = tid; i < kTileBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sm + kOffOnesB)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -664,6 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1) causal_out_kernel(const __grid_co
   } else if (warp >= kWarpEpi) {
     out_epi(p, sm, sh, tmem, warp - kWarpEpi, lane, lo, n);
     if (lane == 0) tma_store_wait_all0();
+  } else if (warp >= kWarpP) {
+    out_pchain(p, sm, sh, tmem, warp - kWarpP, lane, lo, n);
   }
   __syncthreads();
   if (tid == 0 && ab_get(&sh->abort)) {
