@@ -397,6 +397,34 @@ def test_rala_small(shape, dtype):
     assert_close_y(to_f64(y), ref, dtype)
 
 
+# bf16, d = 32, Cx = 64, H <= 2, N a multiple of 64: the tensor-core RALA
+# kernels (token pairs as 128-byte rows, tiles of 128 pairs).  The offset on
+# Q moves Q_g away from zero, so the logits span tens of units and the
+# softmax depends on its maximum being taken out first.
+RALA_TC = [  # B, H, N, q offset
+    (3, 2, 832, 0.0),     # 416 pairs: three whole tiles and a quarter tile
+    (2, 1, 1024, 0.0),    # one head, whole tiles only
+    (1, 2, 64, 0.0),      # a single quarter-filled tile
+    (2, 2, 448, 1.5),     # peaked softmax
+]
+
+
+@pytest.mark.parametrize("shape", RALA_TC, ids=lambda s: "x".join(map(str, s)))
+def test_rala_tcgen05_shapes(shape):
+    B, H, N, off = shape
+    d, cx = 32, 64
+    q64 = normal(310 + N, 1, (B, H, N, d), d ** -0.5) + off
+    qt, q64 = rounded(q64, "bf16")
+    x = rand_inputs(310 + N, (B, H, N, d), "bf16")
+    xt, x64 = rounded(normal(311, 5, (B, N, cx)), "bf16")
+    wt, w64 = rounded(normal(311, 6, (cx, d), cx ** -0.5), "bf16")
+    y = torch.empty_like(qt)
+    binding.rala_forward(qt, x["k"], x["v"], xt, wt, y)
+    torch.cuda.synchronize()
+    ref = oracle.rala_forward(q64, x["k64"], x["v64"], x64, w64)
+    assert_close_y(to_f64(y), ref, "bf16")
+
+
 def test_rala_full_workload_sampled_batches():
     wl = WORKLOADS["rala"]
     dev = rala_device(wl)

@@ -38,6 +38,12 @@ size_t tc_causal_workspace(const MhlaShape& s);
 cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, const void* v, void* y,
                              float* den_out, float eps, void* ws, cudaStream_t st);
 
+// ---- tcgen05 RALA path (bf16, d = 32, Cx = 64, H <= 2, N a multiple of 64)
+bool tc_rala_supported(int B, int H, int N, int d, int cx, mhla_dtype dt);
+size_t tc_rala_workspace(int B, int H, int N);
+cudaError_t tc_rala_launch(int B, int H, int N, const void* q, const void* k, const void* v, const void* x,
+                           const void* w, void* y, void* ws, cudaStream_t st);
+
 // ---- SIMT path (fp32 mode, and every shape the tensor-core path does not take)
 size_t simt_mhla_workspace(const MhlaShape& s);
 cudaError_t simt_mhla_launch(const MhlaShape& s, mhla_dtype dt, const void* q, const void* k,

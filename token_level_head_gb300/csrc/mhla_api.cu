@@ -152,7 +152,9 @@ mhla_status linattn_decode_step(const void* q, const void* k, const void* v, flo
 
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx) {
   if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256) return 0;
-  return simt_rala_workspace(B, H, N, d, cx);
+  const size_t a = simt_rala_workspace(B, H, N, d, cx);
+  const size_t b = tc_rala_supported(B, H, N, d, cx, MHLA_BF16) ? tc_rala_workspace(B, H, N) : 0;
+  return std::max(a, b);
 }
 
 mhla_status rala_forward(const void* q, const void* k, const void* v, const void* x,
@@ -173,7 +175,9 @@ mhla_status rala_forward(const void* q, const void* k, const void* v, const void
       overlap(y, tb, x, xb) || overlap(y, tb, w, wb))
     return MHLA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHLA_ERR_INVALID_ARG;
-  if (workspace_bytes < simt_rala_workspace(B, H, N, d, cx)) return MHLA_ERR_INVALID_ARG;
+  if (workspace_bytes < rala_workspace_bytes(B, H, N, d, cx)) return MHLA_ERR_INVALID_ARG;
+  if (tc_rala_supported(B, H, N, d, cx, dt))
+    return from_cuda(tc_rala_launch(B, H, N, q, k, v, x, w, y, workspace, static_cast<cudaStream_t>(stream)));
   return from_cuda(simt_rala_launch(B, H, N, d, cx, dt, q, k, v, x, w, y, workspace,
                                     static_cast<cudaStream_t>(stream)));
 }
