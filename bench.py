@@ -394,8 +394,13 @@ def run_ours(args, wl, rank, world, local_rank):
     peak, peak_src = hbm_peak()
     kernel_ms = step_ms if step_ms is not None else elapsed_ms / args.steps
     achieved = alg / (kernel_ms / 1e3) / 1e9
-    path = binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"),
-                                     torch.bfloat16 if wl.dtype == "bf16" else torch.float32)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    if wl.kind == "rala":
+        path = binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
+    elif wl.kind == "decode":
+        path = "simt"
+    else:
+        path = binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
     kernel_name = f"{wl.kind}_{path}"
     value = world * tokens_per_step(wl) * args.steps / (elapsed_ms / 1e3)
     line = {

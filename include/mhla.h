@@ -136,6 +136,11 @@ mhla_status rala_forward(const void* q, const void* k, const void* v, const void
                          const void* w, void* y, int B, int H, int N, int d, int cx,
                          mhla_dtype dt, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Kernel family rala_forward would use for these arguments (no launch):
+ * the tensor-core kernels take bf16 with d = 32, cx = 64, H <= 2 and N a
+ * multiple of 64 (at most 8192); everything else runs the SIMT kernels. */
+mhla_path rala_forward_path(int B, int H, int N, int d, int cx, mhla_dtype dt);
+
 /* Scratch held by mhla_forward_noalloc on every GPU that loads the library. */
 #define MHLA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB */
 

@@ -121,6 +121,13 @@ def test_rala_argument_errors(lib):
 def test_forward_path_query(lib):
     assert binding.PATH_NAMES[lib.mhla_forward_path(1, 1, 256, 16, 64, 0, F32)] == "simt"
     assert binding.PATH_NAMES[lib.mhla_forward_path(1, 1, 256, 48, 64, 0, F32)] == "none"
+    assert binding.PATH_NAMES[lib.mhla_forward_path(4, 16, 8192, 64, 128, 1, BF16)] == "tcgen05"
+    assert binding.PATH_NAMES[lib.mhla_forward_path(4, 16, 8192, 64, 100, 1, BF16)] == "none"
+    assert binding.PATH_NAMES[lib.rala_forward_path(64, 2, 3136, 32, 64, BF16)] == "tcgen05"
+    assert binding.PATH_NAMES[lib.rala_forward_path(64, 2, 3136, 32, 64, F32)] == "simt"
+    assert binding.PATH_NAMES[lib.rala_forward_path(64, 3, 3136, 32, 64, BF16)] == "simt"
+    assert binding.PATH_NAMES[lib.rala_forward_path(64, 2, 3100, 32, 64, BF16)] == "simt"
+    assert binding.PATH_NAMES[lib.rala_forward_path(64, 2, 3136, 32, 60, BF16)] == "none"
 
 
 def test_query_status_rejects_null(lib):

@@ -32,6 +32,7 @@ _SIGNATURES = {
     "rala_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "rala_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "mhla_forward_path": (_i, [_i, _i, _i, _i, _i, _i, _i]),
+    "rala_forward_path": (_i, [_i, _i, _i, _i, _i, _i]),
     "mhla_query_status": (_i, [_vp, _vp]),
     "mhla_status_string": (ctypes.c_char_p, [_i]),
     "mhla_launch_count": (ctypes.c_ulonglong, []),
@@ -109,6 +110,11 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 def mhla_forward_path(B, H, N, d, block_size, causal, dtype) -> str:
     dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
     return PATH_NAMES[int(load().mhla_forward_path(B, H, N, d, block_size, causal, dt))]
+
+
+def rala_forward_path(B, H, N, d, cx, dtype) -> str:
+    dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
+    return PATH_NAMES[int(load().rala_forward_path(B, H, N, d, cx, dt))]
 
 
 def mhla_forward(q, k, v, mixing, y, block_size, *, causal=0, eps=1e-6, den_out=None,

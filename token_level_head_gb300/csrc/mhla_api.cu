@@ -157,6 +157,13 @@ size_t rala_workspace_bytes(int B, int H, int N, int d, int cx) {
   return std::max(a, b);
 }
 
+mhla_path rala_forward_path(int B, int H, int N, int d, int cx, mhla_dtype dt) {
+  if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256 ||
+      (dt != MHLA_F32 && dt != MHLA_BF16))
+    return MHLA_PATH_NONE;
+  return tc_rala_supported(B, H, N, d, cx, dt) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+}
+
 mhla_status rala_forward(const void* q, const void* k, const void* v, const void* x,
                          const void* w, void* y, int B, int H, int N, int d, int cx,
                          mhla_dtype dt, void* workspace, size_t workspace_bytes, void* stream) {
