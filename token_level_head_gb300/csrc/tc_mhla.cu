@@ -100,13 +100,11 @@ struct Params {
   CUtensorMap tm_y;              // same tensor shape, box 64 x 32
   CUtensorMap tm_p;              // chunk partials [heads*C rows][4096] bf16, box 64 x C (tensor-core MIX)
   CUtensorMap tm_ps;             // chunk partials [heads*C*64 rows][64] bf16, box 64 x 32 (SUM stores)
-  CUtensorMap tm_w;              // MIX weights [H*128 rows][64] bf16, box 64 x 128 (tensor-core MIX)
   const float* mixing;           // [H][M][M], m[h][i][b]
   __nv_bfloat16* ps;             // chunk partial S^T: [heads * C][64 e][64 c]
   float* pz;                     // chunk partial z: [heads * C][64]
   uint8_t* smix;                 // S~^T tiles: [heads * M] x 8 KB, K-major, 128-byte swizzle
   float* zmix;                   // z~: [heads * M][64]
-  __nv_bfloat16* wts;            // MIX weight tiles: [H][128 rows][64] bf16 (see build_mix_weights)
   float* den_out;                // [heads * N] or null
   unsigned* ctr;                 // [1] finished CTAs, [2] SUM barrier, [3] MIX barrier
   unsigned* status;
@@ -163,7 +161,7 @@ __device__ __noinline__ bool gwait(const unsigned* p, unsigned target, Small* sh
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    __nanosleep(200);
+    __nanosleep(32);
     if (ld_acquire(p) >= target) return true;
     if (aborted(sh)) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
@@ -215,15 +213,15 @@ __device__ __forceinline__ void warp_store_rows(const uint8_t* yb, uint8_t* dst,
 // The tensor-core MIX units of a CTA are the contiguous range [u0, u1) of the
 // heads x 64 (head, row e of S^T) pairs.  A ring stage carries n <=
 // mix_per_stage(C) consecutive units of one head: their chunk-partial boxes
-// (C slots x 64 entries, C x 128 bytes each) from offset 0 and the head's
-// 128-row weight tile (row i: m[i][x / cpb] over the C slots x) at 16 KB.
+// (C slots x 64 entries, C x 128 bytes each) from offset 0 (TMA) and the
+// head's 128-row weight tile (row i: m[i][x / cpb] over the C slots x) at
+// 16 KB, which the phi warps write from the mixing matrix.
 // MMA: D (128 x 64 n) = W (128 x C) . [boxes] (C x 64 n), fp32 in TMEM.
 // With M <= 32 the weight rows are repeated in every 32-row quarter, so each
 // TMEM lane quadrant holds all M query blocks and epilogue warp k reads unit
 // k's 64 columns from its own quadrant; otherwise rows 0..M-1 hold them once
 // and each unit is its own N = 64 MMA chain.
 constexpr int kMixWOff = 16384;
-constexpr int kMixWRows = 128;
 __device__ __forceinline__ int mix_per_stage(int C) { return min(4, kMixWOff / (C * kD * 2)); }
 __host__ __device__ __forceinline__ bool mix_rep(int M) { return M <= 32; }
 __device__ __forceinline__ int mix_u0(const Params& p) { return (int)((long long)blockIdx.x * p.XS / gridDim.x); }
@@ -267,20 +265,19 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
     tma_load_2d_hint(st, &p.tm_k, 0, g * kTile, &sh->full[s], once);
     tma_load_2d_hint(st + kTileBytes, &p.tm_v, 0, g * kTile, &sh->full[s], once);
   }
-  // MIX units (head h, row e of S^T): the chunk partials' row e and the head's
-  // weights, once every CTA has stored its partials (grid barrier 1)
+  // MIX units (head h, row e of S^T): the chunk partials' row e, once every CTA
+  // has stored its partials (grid barrier 1); the phi warps add the weights
   const int u1 = mix_u1(p);
   if (p.tc_mix && mix_u0(p) < u1) {
     if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
-    fence_proxy_async_global();  // partials and weights were written by generic stores
+    fence_proxy_async_global();  // the partials were written by other CTAs' bulk stores
     for (int u = mix_u0(p); u < u1; ++q) {
       const int s = q % kNS;
       if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
       uint8_t* st = sm + s * kStageBytes;
       const int n = mix_stage_units(p, u, u1), h = u / kD;
-      mbar_arrive_expect_tx(&sh->full[s], n * p.C * kD * 2 + kMixWRows * kD * 2);
+      mbar_arrive_expect_tx(&sh->full[s], n * p.C * kD * 2);
       for (int k = 0; k < n; ++k) tma_load_2d(st + k * p.C * kD * 2, &p.tm_p, (u % kD + k) * kD, h * p.C, &sh->full[s]);
-      tma_load_2d(st + kMixWOff, &p.tm_w, 0, (h % p.H) * kMixWRows, &sh->full[s]);
       u += n;
     }
   }
@@ -395,20 +392,57 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
   }
 }
 
-// phi warps during the MIX units: nothing to transform, the stage is handed on.
+// MIX weight tile of head hh, the A operand of the MIX MMAs (M 128 rows, K = C
+// chunk partials): row r, column x is m[hh][i][x / cpb] with i = r % 32 (M <= 32:
+// the query blocks repeated in the four TMEM lane quadrants) or i = r, for
+// i < M and x < C, zero elsewhere.  Thread t (of 256) holds the bf16 piece
+// (columns 8 (t % 8) ..) of rows t / 8 + 32 kk in v[kk] (v[0] for all kk when
+// M <= 32).
+__device__ __forceinline__ void mix_weight_values(const Params& p, int hh, int t, uint4 (&v)[4]) {
+  const float* m = p.mixing + (size_t)hh * p.M * p.M;
+  const int x0 = 8 * (t & 7);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const int i = (t >> 3) + 32 * kk;
+    float w[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int x = x0 + c;
+      w[c] = (i < p.M && x < p.C) ? __ldg(m + i * p.M + x / p.cpb) : 0.f;
+    }
+    v[kk] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
+    if (mix_rep(p.M)) break;
+  }
+}
+
+// phi warps during the MIX stages: the weight tile of the stage's head, next
+// to the chunk-partial boxes the producer loaded.
 template <class L>
-__device__ void phi_passthrough(const Params& p, Small* sh, int lane, int& qs, int& qa) {
+__device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, int w, int lane, int& qs) {
   constexpr int kNS = L::NS;
+  const int t = w * 32 + lane;  // rows t / 8 + 32 kk, piece t % 8 of the tile
   const int u1 = mix_u1(p);
+  uint4 wv[4];
+  int wh = -1;
   for (int u = mix_u0(p); u < u1; ++qs) {
-    const int n = mix_stage_units(p, u, u1);
+    const int n = mix_stage_units(p, u, u1), hh = (u / kD) % p.H;
+    if (hh != wh) {  // the mixing values of a head are loaded once
+      mix_weight_values(p, hh, t, wv);
+      wh = hh;
+    }
     const int s = qs % kNS;
     if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return;
+    uint8_t* wtile = sm + s * kStageBytes + kMixWOff;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int r = (t >> 3) + 32 * kk;
+      *reinterpret_cast<uint4*>(wtile + r * 128 + (((t & 7) ^ (r & 7)) << 4)) = mix_rep(p.M) ? wv[0] : wv[kk];
+    }
+    fence_proxy_async_smem();  // weight tile -> tensor core reads
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh->ready[s]);
     u += n;
   }
-  (void)qa;
 }
 
 // MMA issuer (one thread).  Returns the number of chunks it issued.
@@ -809,50 +843,6 @@ __device__ void mix_z_rows(const Params& p, uint8_t* sm, int c) {
   }
 }
 
-// MIX weights for the tensor-core MIX, built during the SUM pass by warps 2-3:
-// row r, column x of head hh's 128 x 64 tile is m[hh][i][x / cpb] with
-// i = r % 32 (M <= 32) or i = r (M > 32), for i < M and x < C, zero elsewhere
-// (bf16, row-major; TMA swizzles it on the way into shared memory).
-template <class L>
-__device__ void build_mix_weights(const Params& p, uint8_t* sm, int c) {
-  const bool rep4 = mix_rep(p.M);
-  // the mixing matrix, in the upper half of the Y staging area (the epilogue
-  // warps stage their SUM stores in the lower half meanwhile)
-  float* ms = reinterpret_cast<float*>(sm + L::kOffY + 16384);
-  const int MM = p.M * p.M;
-  for (int hh = blockIdx.x; hh < p.H; hh += gridDim.x) {
-    const float* src = p.mixing + (size_t)hh * MM;
-    for (int j0 = 0; j0 < MM; j0 += 16 * 64) {  // 16 independent loads per thread in flight
-      float v[16];
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int j = j0 + k * 64 + c;
-        v[k] = j < MM ? __ldcg(src + j) : 0.f;
-      }
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int j = j0 + k * 64 + c;
-        if (j < MM) ms[j] = v[k];
-      }
-    }
-    named_bar(kBarZ, 64);
-    // 128 rows x 64 columns = 1024 pieces of 8 bf16
-    uint4* dst = reinterpret_cast<uint4*>(p.wts + (size_t)hh * kMixWRows * kD);
-    for (int pc = c; pc < kMixWRows * kD / 8; pc += 64) {
-      const int r = pc / 8, x0 = (pc % 8) * 8;
-      const int i = rep4 ? r % 32 : r;
-      float w[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int x = x0 + k;
-        w[k] = (i < p.M && x < p.C) ? ms[i * p.M + x / p.cpb] : 0.f;
-      }
-      dst[pc] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
-    }
-    named_bar(kBarZ, 64);
-  }
-}
-
 template <int MAXM>
 __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_constant__ Params p) {
   using L = Layout<MAXM>;
@@ -920,10 +910,10 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
       // the SUM partials are read after grid barrier 1, some through TMA
       if (lane == 0) tma_store_wait_all0();
       fence_proxy_async_global();
-    } else if (p.tc_mix) build_mix_weights<L>(p, sm, t);
+    }
     if (mix_begin(p, sh, t)) {
       if (p.tc_mix) {
-        if (warp >= kWarpPhi) phi_passthrough<L>(p, sh, lane, qs, q);
+        if (warp >= kWarpPhi) phi_mix<L>(p, sm, sh, warp - kWarpPhi, lane, qs);
         else if (warp >= kWarpEpi) {
           epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
         }
@@ -1000,7 +990,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_r
 struct TcPlan {
   int C, M, cpb;
   bool tc_mix;  // S^T rows mixed on the tensor cores
-  size_t off_ps, off_pz, off_smix, off_zmix, off_w, total;
+  size_t off_ps, off_pz, off_smix, off_zmix, total;
 };
 
 inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1017,7 +1007,6 @@ TcPlan tc_plan(const MhlaShape& s) {
   p.off_smix = off; off = a256(off + heads * p.M * (size_t)kSTile);
   p.off_zmix = off; off = a256(off + heads * p.M * (size_t)kD * sizeof(float));
   p.tc_mix = p.C % 16 == 0 && p.C <= kD;
-  p.off_w = off;    off = a256(off + (p.tc_mix ? (size_t)s.H * kMixWRows * kD * 2 : 0));
   p.total = off;
   return p;
 }
@@ -1075,15 +1064,13 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
       !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&p.tm_ps, w + pl.off_ps, (uint64_t)s.heads() * pl.C * kD, 32)) return cudaErrorInvalidValue;
-  if (pl.tc_mix && (!make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, pl.C, (uint64_t)kD * kD) ||
-                    !make_map_2d(&p.tm_w, w + pl.off_w, (uint64_t)s.H * kMixWRows, kMixWRows)))
+  if (pl.tc_mix && !make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, pl.C, (uint64_t)kD * kD))
     return cudaErrorInvalidValue;
   p.mixing = mixing;
   p.ps = reinterpret_cast<__nv_bfloat16*>(w + pl.off_ps);
   p.pz = reinterpret_cast<float*>(w + pl.off_pz);
   p.smix = reinterpret_cast<uint8_t*>(w + pl.off_smix);
   p.zmix = reinterpret_cast<float*>(w + pl.off_zmix);
-  p.wts = reinterpret_cast<__nv_bfloat16*>(w + pl.off_w);
   p.den_out = den_out;
   p.ctr = reinterpret_cast<unsigned*>(w + kCounterOffset);
   p.status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
