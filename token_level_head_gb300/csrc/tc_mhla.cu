@@ -792,32 +792,97 @@ __device__ void mix_end(const Params& p, int t) {
   if (t == 0) red_release_add(&p.ctr[3], 1u);
 }
 
+// Sum of chunk partials x0 .. x1-1 of head h, row e (e < 64: row e of S^T in
+// bf16, e = 64: z in fp32), entry c; up to 16 loads in flight.
+__device__ __forceinline__ float sum_partials(const Params& p, int h, int e, int c, int x0, int x1) {
+  float T = 0.f;
+  for (int xb = x0; xb < x1; xb += 16) {
+    const int n = min(16, x1 - xb);
+    float val[16];
+    if (e < kD) {
+      const unsigned short* src =
+          reinterpret_cast<const unsigned short*>(p.ps) + ((size_t)h * p.C + xb) * (kD * kD) + e * kD + c;
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        val[k] = k < n ? __uint_as_float((uint32_t)__ldcg(src + (size_t)k * (kD * kD)) << 16) : 0.f;
+    } else {
+      const float* src = p.pz + ((size_t)h * p.C + xb) * kD + c;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) val[k] = k < n ? __ldcg(src + (size_t)k * kD) : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) T += val[k];
+  }
+  return T;
+}
+
 // SIMT MIX of all summary rows (when the tensor-core MIX does not apply), by
-// warps 2-15: a CTA takes the contiguous range [blockIdx.x R / G,
-// (blockIdx.x + 1) R / G) of the R = heads x 65 rows; thread t works on entry
-// t % 64 of row t / 64 of each group of 7 rows.
+// warps 2-15 (448 threads = 7 groups of 64, thread c of a group on entry c):
+// the CTA takes rows [blockIdx.x R / G, (blockIdx.x + 1) R / G) of the R =
+// heads x 65 rows, one row at a time.  The mixing is linear, so a row's chunk
+// partials are cut into units - whole blocks (M >= 7) or equal slices of one
+// block (M < 7) - and each group sums the partials of its units and adds
+// m[i][b] x (unit sum) into its accumulator for every query block i; the 7
+// accumulators are then added in shared memory, kRound query blocks at a time.
 template <int MAXM>
 __device__ void mix_rows_all(const Params& p, uint8_t* sm, int t) {
   using L = Layout<MAXM>;
-  constexpr int kRowsPerRound = kMixThreads / kD;  // 7
+  constexpr int kGroups = kMixThreads / kD;  // 7
+  constexpr int kRound = 8;
+  static_assert(MAXM * MAXM * 4 + kGroups * kRound * kD * 4 <= 32768, "MIX staging");
+  float* wt = reinterpret_cast<float*>(sm + L::kOffY);                       // [b][i] = m[i][b]
+  float* red = reinterpret_cast<float*>(sm + L::kOffY + MAXM * MAXM * 4);    // [g][kRound][64]
   const unsigned G = gridDim.x;
-  float* wt = reinterpret_cast<float*>(sm + L::kOffY);
   const int R = p.heads * kMixRows;
   const int r0 = (int)((long long)blockIdx.x * R / G), r1 = (int)((long long)(blockIdx.x + 1) * R / G);
-  const int c = t % kD, rr = t / kD;
+  const int g = t / kD, c = t % kD;
+  const int S = p.M >= kGroups ? 1 : (kGroups + p.M - 1) / p.M;  // slices per block
+  const int units = p.M * S;
   int cur_hh = -1;
-  for (int u = r0; u < r1;) {
-    const int h = u / kMixRows;
-    const int hend = min(r1, (h + 1) * kMixRows);
+  for (int row = r0; row < r1; ++row) {
+    const int h = row / kMixRows, e = row % kMixRows;
     if (h % p.H != cur_hh) {
       cur_hh = h % p.H;
       stage_weights<MAXM>(p, wt, cur_hh, t, kMixThreads, kBarMix);
     }
-    for (int base = u; base < hend; base += kRowsPerRound) {
-      const int row = base + rr;
-      if (row < hend) mix_row_simt<MAXM>(p, wt, h, row - h * kMixRows, c);
+    float acc[MAXM];
+#pragma unroll
+    for (int i = 0; i < MAXM; ++i) acc[i] = 0.f;
+    for (int un = g; un < units; un += kGroups) {
+      const int b = un / S, sl = un % S;
+      const int x0 = b * p.cpb + (sl * p.cpb) / S, x1 = b * p.cpb + ((sl + 1) * p.cpb) / S;
+      const float T = sum_partials(p, h, e, c, x0, x1);
+      const float4* w4 = reinterpret_cast<const float4*>(wt + b * MAXM);
+#pragma unroll
+      for (int i = 0; i < MAXM / 4; ++i) {
+        const float4 m4 = w4[i];
+        acc[4 * i] = fmaf(m4.x, T, acc[4 * i]);
+        acc[4 * i + 1] = fmaf(m4.y, T, acc[4 * i + 1]);
+        acc[4 * i + 2] = fmaf(m4.z, T, acc[4 * i + 2]);
+        acc[4 * i + 3] = fmaf(m4.w, T, acc[4 * i + 3]);
+      }
     }
-    u = hend;
+#pragma unroll
+    for (int i0 = 0; i0 < MAXM; i0 += kRound) {
+      if (i0 >= p.M) break;
+#pragma unroll
+      for (int ii = 0; ii < kRound; ++ii) red[(g * kRound + ii) * kD + c] = acc[i0 + ii];
+      named_bar(kBarMix, kMixThreads);
+      for (int idx = t; idx < kRound * kD; idx += kMixThreads) {
+        const int ii = idx / kD, i = i0 + ii, cc = idx % kD;
+        if (i < p.M) {
+          float v = 0.f;
+#pragma unroll
+          for (int gg = 0; gg < kGroups; ++gg) v += red[(gg * kRound + ii) * kD + cc];
+          if (e < kD)
+            *reinterpret_cast<__nv_bfloat16*>(p.smix + ((size_t)h * p.M + i) * kSTile + swz128(e, cc)) =
+                __float2bfloat16_rn(v);
+          else
+            p.zmix[((size_t)h * p.M + i) * kD + cc] = v;
+        }
+      }
+      named_bar(kBarMix, kMixThreads);
+    }
   }
 }
 
