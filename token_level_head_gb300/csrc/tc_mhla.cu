@@ -109,7 +109,7 @@ struct Params {
   unsigned* ctr;                 // [1] finished CTAs, [2] SUM barrier, [3] MIX barrier
   unsigned* status;
   int heads, H, N, M, C, cpb, TS;  // C = chunks per head, cpb = chunks per block, TS = heads * C
-  int tc_mix;                    // 1: S^T rows mixed on the tensor cores (C % 16 == 0, C <= 64)
+  int tc_mix;                    // 1: S^T rows mixed on the tensor cores (C % 16 == 0, C <= 64 or C % 64 == 0)
   int XS;                        // tensor-core MIX units: heads * 64 (0 without tc_mix)
   float eps;
 };
@@ -222,7 +222,11 @@ __device__ __forceinline__ void warp_store_rows(const uint8_t* yb, uint8_t* dst,
 // k's 64 columns from its own quadrant; otherwise rows 0..M-1 hold them once
 // and each unit is its own N = 64 MMA chain.
 constexpr int kMixWOff = 16384;
-__device__ __forceinline__ int mix_per_stage(int C) { return min(4, kMixWOff / (C * kD * 2)); }
+// With C > 64 partials a head's units go through the MMAs in K chunks of 64
+// partials (one stage each, accumulating in TMEM).
+__host__ __device__ __forceinline__ int mix_kslots(int C) { return C < kD ? C : kD; }
+__host__ __device__ __forceinline__ int mix_nkc(int C) { return C / mix_kslots(C); }
+__device__ __forceinline__ int mix_per_stage(int C) { return min(4, kMixWOff / (mix_kslots(C) * kD * 2)); }
 __host__ __device__ __forceinline__ bool mix_rep(int M) { return M <= 32; }
 __device__ __forceinline__ int mix_u0(const Params& p) { return (int)((long long)blockIdx.x * p.XS / gridDim.x); }
 __device__ __forceinline__ int mix_u1(const Params& p) { return (int)((long long)(blockIdx.x + 1) * p.XS / gridDim.x); }
@@ -271,13 +275,17 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
   if (p.tc_mix && mix_u0(p) < u1) {
     if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
     fence_proxy_async_global();  // the partials were written by other CTAs' bulk stores
-    for (int u = mix_u0(p); u < u1; ++q) {
-      const int s = q % kNS;
-      if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
-      uint8_t* st = sm + s * kStageBytes;
+    const int ks = mix_kslots(p.C), nkc = mix_nkc(p.C);
+    for (int u = mix_u0(p); u < u1;) {
       const int n = mix_stage_units(p, u, u1), h = u / kD;
-      mbar_arrive_expect_tx(&sh->full[s], n * p.C * kD * 2);
-      for (int k = 0; k < n; ++k) tma_load_2d(st + k * p.C * kD * 2, &p.tm_p, (u % kD + k) * kD, h * p.C, &sh->full[s]);
+      for (int kc = 0; kc < nkc; ++kc, ++q) {
+        const int s = q % kNS;
+        if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
+        uint8_t* st = sm + s * kStageBytes;
+        mbar_arrive_expect_tx(&sh->full[s], n * ks * kD * 2);
+        for (int k = 0; k < n; ++k)
+          tma_load_2d(st + k * ks * kD * 2, &p.tm_p, (u % kD + k) * kD, h * p.C + kc * ks, &sh->full[s]);
+      }
       u += n;
     }
   }
@@ -398,17 +406,17 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
 // i < M and x < C, zero elsewhere.  Thread t (of 256) holds the bf16 piece
 // (columns 8 (t % 8) ..) of rows t / 8 + 32 kk in v[kk] (v[0] for all kk when
 // M <= 32).
-__device__ __forceinline__ void mix_weight_values(const Params& p, int hh, int t, uint4 (&v)[4]) {
+__device__ __forceinline__ void mix_weight_values(const Params& p, int hh, int kc, int t, uint4 (&v)[4]) {
   const float* m = p.mixing + (size_t)hh * p.M * p.M;
-  const int x0 = 8 * (t & 7);
+  const int ks = mix_kslots(p.C), x0 = 8 * (t & 7);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
     const int i = (t >> 3) + 32 * kk;
     float w[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const int x = x0 + c;
-      w[c] = (i < p.M && x < p.C) ? __ldg(m + i * p.M + x / p.cpb) : 0.f;
+      const int x = x0 + c;  // column of K chunk kc: partial kc ks + x
+      w[c] = (i < p.M && x < ks) ? __ldg(m + i * p.M + (kc * ks + x) / p.cpb) : 0.f;
     }
     v[kk] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
     if (mix_rep(p.M)) break;
@@ -422,25 +430,28 @@ __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, int w, int lane
   constexpr int kNS = L::NS;
   const int t = w * 32 + lane;  // rows t / 8 + 32 kk, piece t % 8 of the tile
   const int u1 = mix_u1(p);
+  const int nkc = mix_nkc(p.C);
   uint4 wv[4];
-  int wh = -1;
-  for (int u = mix_u0(p); u < u1; ++qs) {
+  int wh = -1;  // (head, K chunk) of the values in wv
+  for (int u = mix_u0(p); u < u1;) {
     const int n = mix_stage_units(p, u, u1), hh = (u / kD) % p.H;
-    if (hh != wh) {  // the mixing values of a head are loaded once
-      mix_weight_values(p, hh, t, wv);
-      wh = hh;
-    }
-    const int s = qs % kNS;
-    if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return;
-    uint8_t* wtile = sm + s * kStageBytes + kMixWOff;
+    for (int kc = 0; kc < nkc; ++kc, ++qs) {
+      if (hh * nkc + kc != wh) {  // the mixing values of a head (chunk) are loaded once
+        mix_weight_values(p, hh, kc, t, wv);
+        wh = hh * nkc + kc;
+      }
+      const int s = qs % kNS;
+      if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return;
+      uint8_t* wtile = sm + s * kStageBytes + kMixWOff;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const int r = (t >> 3) + 32 * kk;
-      *reinterpret_cast<uint4*>(wtile + r * 128 + (((t & 7) ^ (r & 7)) << 4)) = mix_rep(p.M) ? wv[0] : wv[kk];
+      for (int kk = 0; kk < 4; ++kk) {
+        const int r = (t >> 3) + 32 * kk;
+        *reinterpret_cast<uint4*>(wtile + r * 128 + (((t & 7) ^ (r & 7)) << 4)) = mix_rep(p.M) ? wv[0] : wv[kk];
+      }
+      fence_proxy_async_smem();  // weight tile -> tensor core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->ready[s]);
     }
-    fence_proxy_async_smem();  // weight tile -> tensor core reads
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh->ready[s]);
     u += n;
   }
 }
@@ -463,29 +474,33 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
       const int u1 = mix_u1(p);
       const bool rep4 = mix_rep(p.M);
       int j = 0;
-      for (int u = mix_u0(p); u < u1; ++qs, ++j) {
-        const int n = mix_stage_units(p, u, u1);
-        const int s = qs % kNS, half = j & 1;
-        if (!bwait(&sh->ready[s], (qs / kNS) & 1, sh)) return qa;
+      const int ks = mix_kslots(p.C), nkc = mix_nkc(p.C);
+      for (int u = mix_u0(p); u < u1; ++j) {
+        const int n = mix_stage_units(p, u, u1), half = j & 1;
         if (j >= 2 && !bwait(&sh->mixe[half], ((j >> 1) - 1) & 1, sh)) return qa;
-        tc_fence_after();
-        const uint32_t st = smem_u32(sm + s * kStageBytes);
-        const uint64_t da = smem_desc(st + kMixWOff, 16, 1024);
         const uint32_t dst = tmem + (uint32_t)(256 * half);
-        if (rep4) {
-          // one chain, N = 64 n: the boxes are the N chunks, C x 128 bytes apart
-          const uint64_t db = smem_desc(st, p.C * kD * 2, 1024);
-          const uint32_t idesc = idesc_bf16_f32(128, 64 * n, 0, 1);
-          for (int kk = 0; kk < p.C / 16; ++kk) mma_bf16(dst, da + kk * (32 >> 4), db + kk * (2048 >> 4), idesc, kk > 0);
-        } else {
-          for (int k = 0; k < n; ++k) {
-            const uint64_t db = smem_desc(st + k * p.C * kD * 2, 8192, 1024);
-            for (int kk = 0; kk < p.C / 16; ++kk)
-              mma_bf16(dst + 64 * k, da + kk * (32 >> 4), db + kk * (2048 >> 4), idesc_mix, kk > 0);
+        for (int kc = 0; kc < nkc; ++kc, ++qs) {
+          const int s = qs % kNS;
+          if (!bwait(&sh->ready[s], (qs / kNS) & 1, sh)) return qa;
+          tc_fence_after();
+          const uint32_t st = smem_u32(sm + s * kStageBytes);
+          const uint64_t da = smem_desc(st + kMixWOff, 16, 1024);
+          if (rep4) {
+            // one chain, N = 64 n: the boxes are the N units, ks x 128 bytes apart
+            const uint64_t db = smem_desc(st, ks * kD * 2, 1024);
+            const uint32_t idesc = idesc_bf16_f32(128, 64 * n, 0, 1);
+            for (int kk = 0; kk < ks / 16; ++kk)
+              mma_bf16(dst, da + kk * (32 >> 4), db + kk * (2048 >> 4), idesc, kk > 0 || kc > 0);
+          } else {
+            for (int k = 0; k < n; ++k) {
+              const uint64_t db = smem_desc(st + k * ks * kD * 2, 8192, 1024);
+              for (int kk = 0; kk < ks / 16; ++kk)
+                mma_bf16(dst + 64 * k, da + kk * (32 >> 4), db + kk * (2048 >> 4), idesc_mix, kk > 0 || kc > 0);
+            }
           }
+          if (kc == nkc - 1) mma_commit(&sh->mixf[half]);
+          mma_commit(&sh->empty[s]);  // the stage is free once these MMAs have read it
         }
-        mma_commit(&sh->mixf[half]);
-        mma_commit(&sh->empty[s]);  // the stage is free once these MMAs have read it
         u += n;
       }
       continue;
@@ -825,7 +840,7 @@ __device__ __forceinline__ float sum_partials(const Params& p, int h, int e, int
 // m[i][b] x (unit sum) into its accumulator for every query block i; the 7
 // accumulators are then added in shared memory, kRound query blocks at a time.
 template <int MAXM>
-__device__ void mix_rows_all(const Params& p, uint8_t* sm, int t) {
+__device__ void mix_rows_all(const Params& p, uint8_t* sm, int t, bool zonly) {
   using L = Layout<MAXM>;
   constexpr int kGroups = kMixThreads / kD;  // 7
   constexpr int kRound = 8;
@@ -833,14 +848,15 @@ __device__ void mix_rows_all(const Params& p, uint8_t* sm, int t) {
   float* wt = reinterpret_cast<float*>(sm + L::kOffY);                       // [b][i] = m[i][b]
   float* red = reinterpret_cast<float*>(sm + L::kOffY + MAXM * MAXM * 4);    // [g][kRound][64]
   const unsigned G = gridDim.x;
-  const int R = p.heads * kMixRows;
+  const int rows_per_head = zonly ? 1 : kMixRows;  // zonly: the z rows alone
+  const int R = p.heads * rows_per_head;
   const int r0 = (int)((long long)blockIdx.x * R / G), r1 = (int)((long long)(blockIdx.x + 1) * R / G);
   const int g = t / kD, c = t % kD;
   const int S = p.M >= kGroups ? 1 : (kGroups + p.M - 1) / p.M;  // slices per block
   const int units = p.M * S;
   int cur_hh = -1;
   for (int row = r0; row < r1; ++row) {
-    const int h = row / kMixRows, e = row % kMixRows;
+    const int h = row / rows_per_head, e = zonly ? kD : row % kMixRows;
     if (h % p.H != cur_hh) {
       cur_hh = h % p.H;
       stage_weights<MAXM>(p, wt, cur_hh, t, kMixThreads, kBarMix);
@@ -982,9 +998,11 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
         else if (warp >= kWarpEpi) {
           epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
         }
-        else mix_z_rows<MAXM>(p, sm, t);
+        else if (p.C <= kD) mix_z_rows<MAXM>(p, sm, t);
+        // with more than 64 partials the z rows take warps 2-15 after the units
+        if (p.C > kD) mix_rows_all<MAXM>(p, sm, t, true);
       } else {
-        mix_rows_all<MAXM>(p, sm, t);
+        mix_rows_all<MAXM>(p, sm, t, false);
       }
       mix_end(p, t);
       if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, qs, q);
@@ -1071,7 +1089,7 @@ TcPlan tc_plan(const MhlaShape& s) {
   p.off_pz = off;   off = a256(off + heads * p.C * (size_t)kD * sizeof(float));
   p.off_smix = off; off = a256(off + heads * p.M * (size_t)kSTile);
   p.off_zmix = off; off = a256(off + heads * p.M * (size_t)kD * sizeof(float));
-  p.tc_mix = p.C % 16 == 0 && p.C <= kD;
+  p.tc_mix = p.C % 16 == 0 && (p.C <= kD || p.C % kD == 0);
   p.total = off;
   return p;
 }
@@ -1129,7 +1147,7 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
       !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&p.tm_ps, w + pl.off_ps, (uint64_t)s.heads() * pl.C * kD, 32)) return cudaErrorInvalidValue;
-  if (pl.tc_mix && !make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, pl.C, (uint64_t)kD * kD))
+  if (pl.tc_mix && !make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, mix_kslots(pl.C), (uint64_t)kD * kD))
     return cudaErrorInvalidValue;
   p.mixing = mixing;
   p.ps = reinterpret_cast<__nv_bfloat16*>(w + pl.off_ps);
