@@ -408,16 +408,27 @@ __device__ void phi_pass(const Params& p, uint8_t* sm, Small* sh, int w, int lan
 // M <= 32).
 __device__ __forceinline__ void mix_weight_values(const Params& p, int hh, int kc, int t, uint4 (&v)[4]) {
   const float* m = p.mixing + (size_t)hh * p.M * p.M;
-  const int ks = mix_kslots(p.C), x0 = 8 * (t & 7);
+  const int ks = mix_kslots(p.C), x0 = 8 * (t & 7);  // columns x0 .. x0 + 7: partials kc ks + x
+  // block of each of the 8 partials (one division, then a running offset)
+  int bc[8];
+  {
+    const int xg = kc * ks + x0;
+    int b = xg / p.cpb, r = xg - b * p.cpb;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      bc[c] = b;
+      if (++r == p.cpb) {
+        r = 0;
+        ++b;
+      }
+    }
+  }
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
     const int i = (t >> 3) + 32 * kk;
     float w[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int x = x0 + c;  // column of K chunk kc: partial kc ks + x
-      w[c] = (i < p.M && x < ks) ? __ldg(m + i * p.M + (kc * ks + x) / p.cpb) : 0.f;
-    }
+    for (int c = 0; c < 8; ++c) w[c] = (i < p.M && x0 + c < ks) ? __ldg(m + i * p.M + bc[c]) : 0.f;
     v[kk] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
     if (mix_rep(p.M)) break;
   }
