@@ -72,6 +72,7 @@ struct Small {
   uint64_t fullO[kNSO], readyO[kNSO], emptyO[kNSO];  // the OUT pass's ring
   uint64_t acc_full[kNA], acc_empty[kNA];
   uint64_t mixf[2], mixe[2];  // MIX accumulators: TMEM columns [256 j, 256 j + 256)
+  uint64_t fin;               // both MMA issuers' last commits
   uint32_t tbase;
   int abort;
   int last;
@@ -132,7 +133,7 @@ __device__ __forceinline__ void set_abort(Small* sh) { *reinterpret_cast<volatil
 // mbarrier phase wait.  The waiting thread sleeps in the barrier unit (it
 // issues nothing while suspended); false once kWaitLimitNs has passed (and
 // then the CTA aborts) or as soon as another role has aborted.
-__device__ __noinline__ bool bwait(uint64_t* bar, uint32_t parity, Small* sh) {
+__device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, Small* sh) {
   // A few polls, then suspended waits with a short limit: a waiter is not
   // always woken when the phase completes, so the limit bounds the delay,
   // and suspension keeps waiting warps off the issue slots and the barrier
@@ -147,6 +148,11 @@ __device__ __noinline__ bool bwait(uint64_t* bar, uint32_t parity, Small* sh) {
   }
   set_abort(sh);
   return false;
+}
+
+// A phase that has already completed costs one test and no call.
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, Small* sh) {
+  return mbar_test(bar, parity) || bwait_slow(bar, parity, sh);
 }
 
 // Short wait (10 ms at most) used only while winding down after an abort.
@@ -230,6 +236,10 @@ __device__ __forceinline__ int mix_per_stage(int C) { return min(4, kMixWOff / (
 __host__ __device__ __forceinline__ bool mix_rep(int M) { return M <= 32; }
 __device__ __forceinline__ int mix_u0(const Params& p) { return (int)((long long)blockIdx.x * p.XS / gridDim.x); }
 __device__ __forceinline__ int mix_u1(const Params& p) { return (int)((long long)(blockIdx.x + 1) * p.XS / gridDim.x); }
+// SUM chunks of this CTA (the OUT pass's accumulators follow theirs)
+__device__ __forceinline__ int sum_chunks(const Params& p) {
+  return (int)blockIdx.x < p.TS ? (p.TS - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+}
 // units in the stage that starts at unit u
 __device__ __forceinline__ int mix_stage_units(const Params& p, int u, int u1) {
   return min(min(mix_per_stage(p.C), u1 - u), (u / kD + 1) * kD - u);
@@ -469,7 +479,7 @@ __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, int w, int lane
 
 // MMA issuer (one thread).  Returns the number of chunks it issued.
 template <class L>
-__device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem) {
+__device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, int role, int pass_lo, int pass_hi) {
   constexpr int kNS = L::NS;
   const uint32_t ones = smem_u32(sm + L::kOffOnes);
   // SUM: A = V tile (MN-major) with the ones tile as M rows 64..127, B = phi(K)
@@ -478,9 +488,13 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
   const uint32_t idesc_sum = idesc_bf16_f32(128, 64, 1, 1);
   const uint32_t idesc_out = idesc_bf16_f32(128, 64, 0, 0);
   const uint32_t idesc_mix = idesc_bf16_f32(128, 64, 0, 1);
-  int qs = 0, qa = 0;
-  for (int pass = 0; pass < 3; ++pass) {
+  // role 0 issues the even chunks of the SUM and OUT passes and every MIX
+  // stage, role 1 the odd chunks (a single thread spends about as long on one
+  // chunk's waits, MMAs and commits as the chunk takes to stream in)
+  int qs = 0, qa = pass_lo == 2 ? sum_chunks(p) : 0;
+  for (int pass = pass_lo; pass <= pass_hi; ++pass) {
     if (pass == 1) {
+      if (role != 0) continue;
       // MIX stages: TMEM columns [256 (j % 2), +256) for MIX stage j
       const int u1 = mix_u1(p);
       const bool rep4 = mix_rep(p.M);
@@ -524,6 +538,7 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
       const uint32_t parity = pass == 0 ? (qs / kNS) & 1 : (qo / kNSO) & 1;
       if (pass == 0) ++qs;
       else ++qo;
+      if ((qa & 1) != role) continue;
       if (qa >= kNA && !bwait(&sh->acc_empty[a], ((qa / kNA) - 1) & 1, sh)) return qa;
       if (!bwait(ready, parity, sh)) return qa;
       tc_fence_after();
@@ -966,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     sh->prod_q = 0;
     sh->prod_qo = 0;
     sh->mma_q = 0;
+    mbar_init(&sh->fin, 2);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -990,12 +1006,19 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     if (lane == 0) sh->prod_q = producer<L>(p, sm, sh);
     __syncwarp();
   } else if (warp == kWarpMma) {
-    if (lane == 0) sh->mma_q = mma_issuer<L>(p, sm, sh, tmem);
+    if (lane == 0) {
+      mma_issuer<L>(p, sm, sh, tmem, 0, 0, 2);
+      mma_commit(&sh->fin);  // arrives once this thread's MMAs have all completed
+    }
     __syncwarp();
   } else {
     // warps 2-15: SUM pass (phi and epilogue warps), MIX phase (all), OUT pass
     const int t = tid - kWarpMix * 32;
     int q = 0, qs = 0, nst = 0;
+    if (warp == kWarpMix) {  // the second MMA issuer: odd SUM chunks
+      if (lane == 0) mma_issuer<L>(p, sm, sh, tmem, 1, 0, 0);
+      __syncwarp();
+    }
     if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 0, qs, q);
     else if (warp >= kWarpEpi) {
       epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 0, q, nst);
@@ -1018,7 +1041,10 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
       mix_end(p, t);
       if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, qs, q);
       else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 1, q, nst);
+      else if (warp == kWarpMix && lane == 0) mma_issuer<L>(p, sm, sh, tmem, 1, 2, 2);  // odd OUT chunks
     }
+    if (warp == kWarpMix && lane == 0) mma_commit(&sh->fin);
+    __syncwarp();
     if (warp >= kWarpEpi && warp < kWarpPhi && lane == 0) tma_store_wait_all0();
   }
   __syncthreads();
@@ -1030,8 +1056,7 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     for (int q = nq > kNS ? nq - kNS : 0; q < nq; ++q) drain_wait(&sh->full[q % kNS], (q / kNS) & 1);
     const int no = sh->prod_qo;
     for (int q = no > kNSO ? no - kNSO : 0; q < no; ++q) drain_wait(&sh->fullO[q % kNSO], (q / kNSO) & 1);
-    const int mq = sh->mma_q;
-    if (mq > 0) drain_wait(&sh->acc_full[(mq - 1) % kNA], ((mq - 1) / kNA) & 1);
+    drain_wait(&sh->fin, 0);  // every MMA issued has completed
     atomicOr(p.status, 1u);
   }
   tc_fence_before();
