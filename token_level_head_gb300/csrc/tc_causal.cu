@@ -387,23 +387,34 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
       }
     }
     if (!group_and(kBarPhi, kPhiWarps * 32, ok && !ab_get(ab))) return;
-    // zeta_c plus the rows of the warps before this one
-    float off[8];
+    // zeta_c plus the rows of the warps before this one (all warps' totals are
+    // read at once, 16-byte loads; warp 0 also forms zeta of the next chunk)
+    float off[8], tot[8];
+    {
+      const float4* z4 = reinterpret_cast<const float4*>(zb + a * kD + 8 * j);
+      const float4 z0 = z4[0], z1 = z4[1];
+      off[0] = z0.x; off[1] = z0.y; off[2] = z0.z; off[3] = z0.w;
+      off[4] = z1.x; off[5] = z1.y; off[6] = z1.z; off[7] = z1.w;
+    }
 #pragma unroll
-    for (int x = 0; x < 8; ++x) off[x] = zb[a * kD + 8 * j + x];
-    for (int ww = 0; ww < w; ++ww)
+    for (int x = 0; x < 8; ++x) tot[x] = off[x];
 #pragma unroll
-      for (int x = 0; x < 8; ++x) off[x] += wsum[(a * kPhiWarps + ww) * kD + 8 * j + x];
+    for (int ww = 0; ww < kPhiWarps; ++ww) {
+      const float4* w4 = reinterpret_cast<const float4*>(wsum + (a * kPhiWarps + ww) * kD + 8 * j);
+      const float4 u0 = w4[0], u1 = w4[1];
+      const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+      for (int x = 0; x < 8; ++x) {
+        tot[x] += u[x];
+        if (ww < w) off[x] += u[x];
+      }
+    }
     if (w == 0 && r0 == 0 && i + 1 < n) {
       // zeta of the next chunk (zero when it starts a new head)
       const bool fresh = (c + 1) % p.CH == 0;
-#pragma unroll
-      for (int x = 0; x < 8; ++x) {
-        float t = off[x];
-#pragma unroll
-        for (int ww = 0; ww < kPhiWarps; ++ww) t += wsum[(a * kPhiWarps + ww) * kD + 8 * j + x];
-        zb[(a ^ 1) * kD + 8 * j + x] = fresh ? 0.f : t;
-      }
+      float4* zn = reinterpret_cast<float4*>(zb + (a ^ 1) * kD + 8 * j);
+      zn[0] = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(tot[0], tot[1], tot[2], tot[3]);
+      zn[1] = fresh ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(tot[4], tot[5], tot[6], tot[7]);
     }
     float qf[4][8];
     phi_rows(st, w, lane, qf);
