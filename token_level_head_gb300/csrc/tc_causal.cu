@@ -147,16 +147,16 @@ __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // The 16 rows 16 w .. 16 w + 15 of a 128-byte-swizzled bf16 tile with 64
 // columns: lane (r0 = lane / 8, j = lane % 8) takes the logical 16-byte piece
-// j (columns 8 j .. 8 j + 7) of rows 16 w + r0 + 4 i, i = 0..3 (four whole
-// rows per access, no bank conflicts).  Replaces them by phi in bf16 and
-// returns phi in fp32.
+// j (columns 8 j .. 8 j + 7) of the consecutive rows 16 w + 4 r0 + i, i = 0..3
+// (four whole rows per access).  Replaces them by phi in bf16 and returns phi
+// in fp32.
 __device__ __forceinline__ void phi_rows(uint8_t* tile, int w, int lane, float (&f)[4][8]) {
   const int r0 = lane >> 3, j = lane & 7;
   uint4* ptr[4];
   uint4 x[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int t = 16 * w + r0 + 4 * i;
+    const int t = 16 * w + 4 * r0 + i;
     ptr[i] = reinterpret_cast<uint4*>(tile + t * 128 + ((j ^ (t & 7)) << 4));
     x[i] = *ptr[i];
   }
@@ -364,21 +364,22 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
     float kf[4][8], run[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (ok) {
       phi_rows(st + kTileBytes, w, lane, kf);
-      // inclusive prefix over the rows 16 w + 4 i + r0, in that order: over r0
-      // by shuffles (lanes 8 apart), over i by the running sum
+      // inclusive prefix over the rows 16 w + 4 r0 + i: over i inside the lane,
+      // over r0 by shuffles of the lane totals (lanes 8 apart)
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
+      for (int x = 0; x < 8; ++x) {
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          float v = kf[i4][x];
-          float u = __shfl_up_sync(0xffffffffu, v, 8);
-          if (r0 >= 1) v += u;
-          u = __shfl_up_sync(0xffffffffu, v, 16);
-          if (r0 >= 2) v += u;
-          const float tot = __shfl_sync(0xffffffffu, v, 24 + j);
-          kf[i4][x] = run[x] + v;
-          run[x] += tot;
-        }
+        for (int i4 = 1; i4 < 4; ++i4) kf[i4][x] += kf[i4 - 1][x];
+        const float tl = kf[3][x];  // this lane's four rows
+        float v = tl;
+        float u = __shfl_up_sync(0xffffffffu, v, 8);
+        if (r0 >= 1) v += u;
+        u = __shfl_up_sync(0xffffffffu, v, 16);
+        if (r0 >= 2) v += u;
+        run[x] = __shfl_sync(0xffffffffu, v, 24 + j);  // the warp's total
+        const float ex = v - tl;                       // rows of the lanes before
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) kf[i4][x] += ex;
       }
       if (r0 == 0) {
         float4* ws4 = reinterpret_cast<float4*>(wsum + (a * kPhiWarps + w) * kD + 8 * j);
@@ -426,7 +427,7 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
       d += __shfl_xor_sync(0xffffffffu, d, 1);
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       d += __shfl_xor_sync(0xffffffffu, d, 4);
-      if (j == 0) den[dslot * kTile + 16 * w + r0 + 4 * i4] = d + p.eps;
+      if (j == 0) den[dslot * kTile + 16 * w + 4 * r0 + i4] = d + p.eps;
     }
     fence_proxy_async_smem();  // phi tiles -> tensor core reads
     __syncwarp();
