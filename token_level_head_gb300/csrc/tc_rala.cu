@@ -49,6 +49,7 @@ constexpr int kMaxN = 8192;                   // logits kept in shared memory
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpAux = 2, kWarpEpi = 4, kWarpPhi = 8;
 constexpr int kPhiWarps = 8;
 constexpr int kBarPhi = 1;
+constexpr int kBarAux = 3;                    // named barrier of warps 2-3 (output kernel)
 constexpr uint64_t kWaitLimitNs = 500000000ull;
 
 struct RParams {
@@ -543,30 +544,55 @@ __global__ void __launch_bounds__(kThreads, 1) rala_out_kernel(const __grid_cons
     // warps 2-3: the W operand tiles once, then the blockdiag(B_h, B_h) tiles of each stage
     const int t = tid - kWarpAux * 32;  // operand row n = 0..63
     {
-      // W0[n][k] = W[k][n] (n < 32), W1[n][k] = W[k][n - 32] (n >= 32); zero elsewhere
+      // W [64 k][32 e] (4 KB) through the Y staging area (free until the first
+      // tile's MMAs, which wait for these tiles) with 16-byte loads, then
+      // W0[n][k] = W[k][n] (n < 32), W1[n][k] = W[k][n - 32] (n >= 32), zero elsewhere
+      __nv_bfloat16* wst = reinterpret_cast<__nv_bfloat16*>(sm + kOffYO);
+      for (int i = t; i < kCx * kD / 8; i += 64)
+        reinterpret_cast<uint4*>(wst)[i] = __ldg(reinterpret_cast<const uint4*>(p.w) + i);
+      named_bar(kBarAux, 64);
       uint8_t* wt = sm + kOffW + (t < 32 ? 0 : kBdBytes);
       uint8_t* wz = sm + kOffW + (t < 32 ? kBdBytes : 0);
       for (int jj = 0; jj < 8; ++jj) {
         float v[8];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) v[x] = __bfloat162float(p.w[(8 * jj + x) * kD + (t & 31)]);
+        for (int x = 0; x < 8; ++x) v[x] = __bfloat162float(wst[(8 * jj + x) * kD + (t & 31)]);
         *piece_ptr(wt, t, jj) = pack8(v);
         *piece_ptr(wz, t, jj) = make_uint4(0, 0, 0, 0);
       }
     }
+    // row t % 32 of B_h^T for the current batch, kept in registers (a CTA's
+    // tiles are consecutive, so the batch rarely changes)
+    float bv[2][kD];
+    int cur_b = -1;
     for (int i = 0; i < n; ++i) {
       const int s = i % kNSO, g = g0 + i, b = g / p.TPB;
+      if (b != cur_b) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h >= p.H) break;
+          const float4* src = reinterpret_cast<const float4*>(p.bt + ((size_t)(b * p.H + h) * kD + (t & 31)) * kD);
+#pragma unroll
+          for (int c4 = 0; c4 < kD / 4; ++c4) {
+            const float4 u = __ldcg(src + c4);
+            bv[h][4 * c4] = u.x;
+            bv[h][4 * c4 + 1] = u.y;
+            bv[h][4 * c4 + 2] = u.z;
+            bv[h][4 * c4 + 3] = u.w;
+          }
+        }
+        cur_b = b;
+      }
       if (i >= kNSO && !rwait(&sh->empty[s], ((i / kNSO) - 1) & 1, ab)) break;
       uint8_t* st = sm + s * kStageO;
-      for (int h = 0; h < p.H; ++h) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (h >= p.H) break;
         // Bd[n][k] = B^T[n % 32][k % 32] when n and k are in the same half
-        const float4* src = reinterpret_cast<const float4*>(p.bt + ((size_t)(b * p.H + h) * kD + (t & 31)) * kD);
         uint8_t* bd = st + kOffBd + h * kBdBytes;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-          const float4 u0 = __ldcg(src + 2 * jj), u1 = __ldcg(src + 2 * jj + 1);
-          const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-          *piece_ptr(bd, t, (t < 32 ? 0 : 4) + jj) = pack8(v);
+          *piece_ptr(bd, t, (t < 32 ? 0 : 4) + jj) = pack8(&bv[h][8 * jj]);
           *piece_ptr(bd, t, (t < 32 ? 4 : 0) + jj) = make_uint4(0, 0, 0, 0);
         }
       }
