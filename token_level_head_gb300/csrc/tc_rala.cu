@@ -117,11 +117,17 @@ __global__ void __launch_bounds__(256) rala_qsum_kernel(const __nv_bfloat16* __r
   const int p = threadIdx.x & 7, rr = threadIdx.x >> 3;  // 32 rows at a time
   const uint4* src = reinterpret_cast<const uint4*>(q) + ((size_t)u * NP) * 8;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int r = r0 + rr; r < r1; r += 32) {
-    float f[8];
-    unpack8(__ldcs(src + (size_t)r * 8 + p), f);
+  for (int r = r0 + rr; r < r1; r += 4 * 32) {  // four 16-byte loads in flight
+    uint4 u[4];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc[x] += f[x];
+    for (int k = 0; k < 4; ++k) u[k] = r + 32 * k < r1 ? __ldcs(src + (size_t)(r + 32 * k) * 8 + p) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float f[8];
+      unpack8(u[k], f);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) acc[x] += f[x];
+    }
   }
   // lanes p and p ^ 4 hold the same columns (the two tokens of a pair)
 #pragma unroll
