@@ -444,17 +444,73 @@ __device__ __forceinline__ void mix_weight_values(const Params& p, int hh, int k
   }
 }
 
+// One MIX group (n units from unit u, TMEM columns 256 half ..) for the warp
+// on TMEM lane quadrant qd: with M <= 32 the warp takes unit qd from its own
+// quadrant, else rows 32 qd .. of every unit.  S~^T rows go out through the
+// warp's staging buffer yb (whole rows, M <= 32) or straight to the tiles.
+__device__ __forceinline__ void mix_group_rows(const Params& p, uint32_t tmem, int qd, int lane, int u, int n, int half,
+                                               uint8_t* yb) {
+  const bool rep4 = mix_rep(p.M);
+  const int h = u / kD;
+  const int i = rep4 ? lane : 32 * qd + lane;  // query block of this thread's row
+  for (int k = 0; k < n; ++k) {
+    if (rep4 ? k != qd : 32 * qd >= p.M) continue;
+    float v[64];
+    const uint32_t ta = tmem + (uint32_t)(256 * half + 64 * k) + ((uint32_t)(qd * 32) << 16);
+    tmem_ld16(ta, v);
+    tmem_ld16(ta + 16, v + 16);
+    tmem_ld16(ta + 32, v + 32);
+    tmem_ld16(ta + 48, v + 48);
+    tmem_ld_wait();
+    const int e = u % kD + k;
+    if (rep4 && yb != nullptr) {
+      // row e of the M tiles S~_i^T: lane i's 128-byte row (pieces already in
+      // the tile's swizzled order) into this warp's staging, then out
+      if (i < p.M) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(yb + i * 128 + (swz128(e, 8 * c) & 127)) =
+              make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                         pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+      }
+      warp_store_rows(yb, p.smix + (size_t)h * p.M * kSTile + e * 128, p.M, kSTile, lane);
+    } else if (i < p.M) {
+      uint8_t* dst = p.smix + ((size_t)h * p.M + i) * kSTile;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(dst + swz128(e, 8 * c)) =
+            make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                       pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+    }
+  }
+}
+
 // phi warps during the MIX stages: the weight tile of the stage's head, next
-// to the chunk-partial boxes the producer loaded.
+// to the chunk-partial boxes the producer loaded; warps 8-11 (TMEM lane
+// quadrants 0-3) also take the rows of the odd MIX groups out of TMEM, after
+// writing the next group's weights.
+// An odd MIX group j (TMEM columns 256..511) for phi warp qd = 0..3.
+__device__ __forceinline__ bool mix_odd_group(const Params& p, Small* sh, uint32_t tmem, int qd, int lane, int j, int u,
+                                              int n) {
+  if (!bwait(&sh->mixf[1], (j >> 1) & 1, sh)) return false;
+  tc_fence_after();
+  mix_group_rows(p, tmem, qd, lane, u, n, 1, nullptr);
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sh->mixe[1]);
+  return true;
+}
+
 template <class L>
-__device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, int w, int lane, int& qs) {
+__device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, int w, int lane, int& qs) {
   constexpr int kNS = L::NS;
   const int t = w * 32 + lane;  // rows t / 8 + 32 kk, piece t % 8 of the tile
   const int u1 = mix_u1(p);
   const int nkc = mix_nkc(p.C);
   uint4 wv[4];
   int wh = -1;  // (head, K chunk) of the values in wv
-  for (int u = mix_u0(p); u < u1;) {
+  int j = 0, up = 0, np = 0;  // group index; the previous group's units
+  for (int u = mix_u0(p); u < u1; ++j) {
     const int n = mix_stage_units(p, u, u1), hh = (u / kD) % p.H;
     for (int kc = 0; kc < nkc; ++kc, ++qs) {
       if (hh * nkc + kc != wh) {  // the mixing values of a head (chunk) are loaded once
@@ -473,8 +529,12 @@ __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, int w, int lane
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->ready[s]);
     }
+    if (w < 4 && j >= 1 && ((j - 1) & 1) && !mix_odd_group(p, sh, tmem, w, lane, j - 1, up, np)) return;
+    up = u;
+    np = n;
     u += n;
   }
+  if (w < 4 && j >= 1 && ((j - 1) & 1)) mix_odd_group(p, sh, tmem, w, lane, j - 1, up, np);
 }
 
 // MMA issuer (one thread).  Returns the number of chunks it issued.
@@ -572,46 +632,19 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
   uint8_t* yb = sm + L::kOffY + qd * 4096;
   const uint64_t once = policy_evict_first();  // Y is written once
   if (pass == 2) {
-    // MIX stages (see the MMA issuer): with M <= 32 warp qd takes unit qd of the
-    // stage from its own lane quadrant, else rows 32 qd .. of every unit.
+    // MIX groups (see the MMA issuer): the even ones (TMEM columns 0..255);
+    // phi warps 8-11 take the odd ones
     const int u1 = mix_u1(p);
-    const bool rep4 = mix_rep(p.M);
     int j = 0;
     for (int u = mix_u0(p); u < u1; ++j) {
-      const int n = mix_stage_units(p, u, u1), half = j & 1, h = u / kD;
+      const int n = mix_stage_units(p, u, u1), half = j & 1;
+      if (half) {
+        u += n;
+        continue;
+      }
       if (!bwait(&sh->mixf[half], (j >> 1) & 1, sh)) return;
       tc_fence_after();
-      const int i = rep4 ? lane : 32 * qd + lane;  // query block of this thread's row
-      for (int k = 0; k < n; ++k) {
-        if (rep4 ? k != qd : 32 * qd >= p.M) continue;
-        float v[64];
-        const uint32_t ta = tmem + (uint32_t)(256 * half + 64 * k) + ((uint32_t)(qd * 32) << 16);
-        tmem_ld16(ta, v);
-        tmem_ld16(ta + 16, v + 16);
-        tmem_ld16(ta + 32, v + 32);
-        tmem_ld16(ta + 48, v + 48);
-        tmem_ld_wait();
-        const int e = u % kD + k;
-        if (rep4) {
-          // row e of the M tiles S~_i^T: lane i's 128-byte row (pieces already in
-          // the tile's swizzled order) into this warp's staging, then out
-          if (i < p.M) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(yb + i * 128 + (swz128(e, 8 * c) & 127)) =
-                  make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
-                             pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
-          }
-          warp_store_rows(yb, p.smix + (size_t)h * p.M * kSTile + e * 128, p.M, kSTile, lane);
-        } else if (i < p.M) {
-          uint8_t* dst = p.smix + ((size_t)h * p.M + i) * kSTile;
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(dst + swz128(e, 8 * c)) =
-                make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
-                           pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
-        }
-      }
+      mix_group_rows(p, tmem, qd, lane, u, n, half, yb);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->mixe[half]);
@@ -1028,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     }
     if (mix_begin(p, sh, t)) {
       if (p.tc_mix) {
-        if (warp >= kWarpPhi) phi_mix<L>(p, sm, sh, warp - kWarpPhi, lane, qs);
+        if (warp >= kWarpPhi) phi_mix<L>(p, sm, sh, tmem, warp - kWarpPhi, lane, qs);
         else if (warp >= kWarpEpi) {
           epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
         }
