@@ -77,7 +77,7 @@ constexpr int kOffZ = kOffWs + 2 * kPhiWarps * kD * 4;  // [2][64] fp32 zeta_c
 constexpr int kOffSmallB = kOffZ + 2 * kD * 4;
 
 // causal_agg_kernel: a K, V ring and the warps' phi(K) column sums.
-constexpr uint32_t kAggCols = 64;
+constexpr uint32_t kAggCols = 128;           // two accumulators, one per MMA issuer
 constexpr int kNSA = 6;
 constexpr int kStageA = 2 * kTileBytes;
 constexpr int kOffZA = kNSA * kStageA;       // [8 warps][64] fp32
@@ -125,7 +125,7 @@ __device__ __forceinline__ void ab_set(int* ab) { *reinterpret_cast<volatile int
 // Bounded mbarrier phase wait (polls, then suspended waits with a short
 // limit); false after kWaitLimitNs (the CTA then aborts) or once another role
 // has aborted.
-__device__ __noinline__ bool cwait(uint64_t* bar, uint32_t parity, int* ab) {
+__device__ __noinline__ bool cwait_slow(uint64_t* bar, uint32_t parity, int* ab) {
   for (int i = 0; i < 16; ++i)
     if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -136,6 +136,11 @@ __device__ __noinline__ bool cwait(uint64_t* bar, uint32_t parity, int* ab) {
   }
   ab_set(ab);
   return false;
+}
+
+// A phase that has already completed costs one test and no call.
+__device__ __forceinline__ bool cwait(uint64_t* bar, uint32_t parity, int* ab) {
+  return mbar_test(bar, parity) || cwait_slow(bar, parity, ab);
 }
 
 // Short wait (10 ms at most), only while winding down after an abort.
@@ -197,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1) causal_agg_kernel(const __grid_co
       mbar_init(&sh->ready[s], kPhiWarps);
       mbar_init(&sh->empty[s], 1);
     }
-    mbar_init(&sh->done, 1);
-    mbar_init(&sh->fin, 1);
+    mbar_init(&sh->done, 2);
+    mbar_init(&sh->fin, 2);
     sh->abort = 0;
     sh->prod_q = 0;
     fence_mbar_init();
@@ -233,12 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1) causal_agg_kernel(const __grid_co
       sh->prod_q = i;
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+    // two MMA issuers (one thread alone spends about a chunk's streaming time
+    // on its waits and MMAs): issuer r takes chunks i with i % 2 = r into
+    // accumulator r (TMEM columns 64 r ..)
     if (lane == 0) {
+      const int r = warp - kWarpMma;
       // D[e][c] += sum_t V[t][e] phi(K)[t][c]: A = V (MN-major, M 64), B = phi(K) (MN-major)
       const uint32_t idesc = idesc_bf16_f32(64, 64, 1, 1);
       bool ok = true;
-      for (int i = 0; i < n && ok; ++i) {
+      for (int i = r; i < n && ok; i += 2) {
         const int s = i % kNSA;
         ok = cwait(&sh->ready[s], (i / kNSA) & 1, ab);
         if (!ok) break;
@@ -247,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) causal_agg_kernel(const __grid_co
         const uint64_t da = smem_desc(st + kTileBytes, kTileBytes, 1024), db = smem_desc(st, 8192, 1024);
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
-          mma_bf16(tmem, da + k * (2048 >> 4), db + k * (2048 >> 4), idesc, i > 0 || k > 0);
+          mma_bf16(tmem + 64 * r, da + k * (2048 >> 4), db + k * (2048 >> 4), idesc, i > r || k > 0);
         mma_commit(&sh->empty[s]);
       }
       if (ok) mma_commit(&sh->done);
@@ -293,15 +302,28 @@ __global__ void __launch_bounds__(kThreads, 1) causal_agg_kernel(const __grid_co
     const int qd = warp - kWarpEpi;
     if (cwait(&sh->done, 0, ab)) {
       tc_fence_after();
-      float v[64];
       const uint32_t ta = tmem + ((uint32_t)(qd * 32) << 16);
+      const bool two = n > 1;  // the second accumulator holds the odd chunks
+      float4* dst = reinterpret_cast<float4*>(p.agg_s + ((size_t)blockIdx.x * kD + 16 * qd + lane) * kD);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld16(ta + 16 * g, v + 16 * g);
-      tmem_ld_wait();
-      if (lane < 16) {
-        float4* dst = reinterpret_cast<float4*>(p.agg_s + ((size_t)blockIdx.x * kD + 16 * qd + lane) * kD);
+      for (int h = 0; h < 2; ++h) {
+        float v[32], v2[32];
+        tmem_ld16(ta + 32 * h, v);
+        tmem_ld16(ta + 32 * h + 16, v + 16);
+        if (two) {
+          tmem_ld16(ta + 64 + 32 * h, v2);
+          tmem_ld16(ta + 64 + 32 * h + 16, v2 + 16);
+        }
+        tmem_ld_wait();
+        if (two) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) dst[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+          for (int x = 0; x < 32; ++x) v[x] += v2[x];
+        }
+        if (lane < 16) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            dst[8 * h + c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        }
       }
     }
   }
