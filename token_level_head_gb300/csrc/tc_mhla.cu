@@ -72,6 +72,8 @@ struct Small {
   uint64_t fullO[kNSO], readyO[kNSO], emptyO[kNSO];  // the OUT pass's ring
   uint64_t acc_full[kNA], acc_empty[kNA];
   uint64_t mixf[2], mixe[2];  // MIX accumulators: TMEM columns [256 j, 256 j + 256)
+  uint64_t mixs[kMaxNS];      // transposed MIX: the MMAs of MIX stage j have completed
+  uint64_t wready;            // transposed MIX: the weight tiles are in place
   uint64_t fin;               // both MMA issuers' last commits
   uint32_t tbase;
   int abort;
@@ -85,6 +87,7 @@ struct Small {
 // and the barriers.
 template <int MAXM>
 struct Layout {
+  static constexpr int kMaxM = MAXM;
   static constexpr int NS = 5;                            // stages of the input ring
   static constexpr int kOffOnes = NS * kStageBytes;       // 16 KB of bf16 ones (A rows 64..127 of SUM)
   static constexpr int kOffY = kOffOnes + kTileBytes;     // Y staging / mixing matrix
@@ -101,6 +104,7 @@ struct Params {
   CUtensorMap tm_y;              // same tensor shape, box 64 x 32
   CUtensorMap tm_p;              // chunk partials [heads*C rows][4096] bf16, box 64 x C (tensor-core MIX)
   CUtensorMap tm_ps;             // chunk partials [heads*C*64 rows][64] bf16, box 64 x 32 (SUM stores)
+  CUtensorMap tm_pp;             // chunk partials as (c 64, x heads*C, e 64), box 64 x C x 2 (transposed MIX)
   const float* mixing;           // [H][M][M], m[h][i][b]
   __nv_bfloat16* ps;             // chunk partial S^T: [heads * C][64 e][64 c]
   float* pz;                     // chunk partial z: [heads * C][64]
@@ -112,6 +116,8 @@ struct Params {
   int heads, H, N, M, C, cpb, TS;  // C = chunks per head, cpb = chunks per block, TS = heads * C
   int tc_mix;                    // 1: S^T rows mixed on the tensor cores (C % 16 == 0, C <= 64 or C % 64 == 0)
   int XS;                        // tensor-core MIX units: heads * 64 (0 without tc_mix)
+  int mix_t;                     // 1: transposed tensor-core MIX (C <= 64; see the MIX stages)
+  int mix_n;                     // transposed MIX: N of its MMAs, M rounded up to 16
   float eps;
 };
 
@@ -245,6 +251,17 @@ __device__ __forceinline__ int mix_stage_units(const Params& p, int u, int u1) {
   return min(min(mix_per_stage(p.C), u1 - u), (u / kD + 1) * kD - u);
 }
 
+// Transposed MIX (C <= 64).  The MMA computes D^T = P^T W^T: A = the
+// chunk-partial boxes of a PAIR of units of one head (MN-major, M 128: unit k's
+// 64 entries c are rows 64 k + c), B = the head's weight tile (K-major, row i =
+// query block, column x = m[i][x / cpb]; N = M rounded up to 16), K = C.  TMEM
+// lane 64 k + c, column i then holds S~_i^T[e_k][c].  A pair needs only N TMEM
+// columns, so every pair of the CTA gets its own accumulator and no MMA waits
+// for an epilogue; 128 / C pairs share a ring stage, and the weight tiles of
+// the CTA's heads sit in the Y staging area (which the MIX phase does not use).
+__device__ __forceinline__ int mix_pair_units(int u, int u1) { return min(2, min(u1 - u, (u / kD + 1) * kD - u)); }
+__device__ __forceinline__ int mix_t_pps(const Params& p) { return 128 / p.C; }
+
 // ------------------------------------------------------------------ roles
 // Producer (one thread).  Returns the number of stages it filled.  The OUT
 // stages' Q tiles are loaded as soon as a stage is free; their S~ / z~ loads
@@ -282,7 +299,25 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
   // MIX units (head h, row e of S^T): the chunk partials' row e, once every CTA
   // has stored its partials (grid barrier 1); the phi warps add the weights
   const int u1 = mix_u1(p);
-  if (p.tc_mix && mix_u0(p) < u1) {
+  if (p.mix_t && mix_u0(p) < u1) {
+    if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
+    fence_proxy_async_global();  // the partials were written by other CTAs' bulk stores
+    const int pps = mix_t_pps(p), box = p.C * kD * 2;
+    for (int u = mix_u0(p); u < u1; ++q) {
+      const int s = q % kNS;
+      if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
+      int np = 0;
+      for (int uu = u; np < pps && uu < u1; ++np) uu += mix_pair_units(uu, u1);
+      uint8_t* st = sm + s * kStageBytes;
+      // one box per pair: rows e, e + 1 of its head's partials (past e = 63 the
+      // box reads zeros; past the CTA's range, rows it does not use)
+      mbar_arrive_expect_tx(&sh->full[s], np * 2 * box);
+      for (int k = 0; k < pps && u < u1; ++k) {
+        tma_load_3d(st + 2 * k * box, &p.tm_pp, 0, (u / kD) * p.C, u % kD, &sh->full[s]);
+        u += mix_pair_units(u, u1);
+      }
+    }
+  } else if (p.tc_mix && mix_u0(p) < u1) {
     if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
     fence_proxy_async_global();  // the partials were written by other CTAs' bulk stores
     const int ks = mix_kslots(p.C), nkc = mix_nkc(p.C);
@@ -537,6 +572,86 @@ __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, 
   if (w < 4 && j >= 1 && ((j - 1) & 1)) mix_odd_group(p, sh, tmem, w, lane, j - 1, up, np);
 }
 
+// Transposed MIX, phi warps: the weight tiles of the heads of the CTA's units
+// (head h0 + l at l N 128 bytes of the Y staging area; row i, piece pc holds
+// m[h][i][x / cpb] for x = 8 pc .. 8 pc + 7, zero past M or C).  Thread t
+// holds pieces t + 256 k (at most four: the tiles fit 16 KB); the values are
+// read before grid barrier 1 and written once the staging area is free.
+__device__ __forceinline__ void mix_t_weights_load(const Params& p, int w, int lane, uint4 (&pk)[4]) {
+  const int u0 = mix_u0(p), u1 = mix_u1(p), N = p.mix_n;
+  const int h0 = u0 / kD, nh = u0 < u1 ? (u1 - 1) / kD - h0 + 1 : 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int idx = w * 32 + lane + k * kPhiWarps * 32;
+    if (idx >= nh * N * 8) break;
+    const int pc = idx & 7, r = idx >> 3, i = r % N, l = r / N;
+    const float* m = p.mixing + ((size_t)((h0 + l) % p.H) * p.M + i) * p.M;
+    float v[8];
+    int b = (8 * pc) / p.cpb, rr = 8 * pc - b * p.cpb;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      v[c] = (i < p.M && 8 * pc + c < p.C) ? __ldg(m + b) : 0.f;
+      if (++rr == p.cpb) {
+        rr = 0;
+        ++b;
+      }
+    }
+    pk[k] = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+  }
+}
+
+template <class L>
+__device__ void mix_t_weights_store(const Params& p, uint8_t* sm, Small* sh, int w, int lane, const uint4 (&pk)[4]) {
+  const int u0 = mix_u0(p), u1 = mix_u1(p), N = p.mix_n;
+  const int h0 = u0 / kD, nh = u0 < u1 ? (u1 - 1) / kD - h0 + 1 : 0;
+  uint8_t* wt = sm + L::kOffY;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int idx = w * 32 + lane + k * kPhiWarps * 32;
+    if (idx >= nh * N * 8) break;
+    const int pc = idx & 7, r = idx >> 3, i = r % N;
+    *reinterpret_cast<uint4*>(wt + r * 128 + ((pc ^ (i & 7)) << 4)) = pk[k];
+  }
+  fence_proxy_async_smem();  // weight tiles -> tensor core reads
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sh->wready);
+}
+
+// Transposed MIX, warps 4-15 in three groups of four: group g takes the pairs
+// j = g mod 3, and the warp on TMEM lane quadrant qd reads unit qd / 2 of the
+// pair, entries c = 32 (qd % 2) + lane: S~_i^T[e][c] for the M query blocks i,
+// in bf16, straight into the S~^T tiles.
+template <class L>
+__device__ bool mix_t_epi(const Params& p, Small* sh, uint32_t tmem, int g, int qd, int lane) {
+  constexpr int MAXM = L::kMaxM;
+  const int u1 = mix_u1(p), pps = mix_t_pps(p), N = p.mix_n;
+  const int kq = qd >> 1, c = 32 * (qd & 1) + lane;
+  int j = 0;
+  for (int u = mix_u0(p); u < u1; ++j) {
+    const int n = mix_pair_units(u, u1);
+    if (j % 3 == g) {
+      if (!bwait(&sh->mixs[j / pps], 0, sh)) return false;
+      tc_fence_after();
+      float v[MAXM];
+      const uint32_t ta = tmem + (uint32_t)(j * N) + ((uint32_t)(qd * 32) << 16);
+#pragma unroll
+      for (int cc = 0; cc < MAXM / 16; ++cc)
+        if (16 * cc < N) tmem_ld16(ta + 16 * cc, v + 16 * cc);
+      tmem_ld_wait();
+      if (kq < n) {
+        const int uu = u + kq;
+        uint8_t* dst = p.smix + (size_t)(uu / kD) * p.M * kSTile + swz128(uu % kD, c);
+#pragma unroll
+        for (int i = 0; i < MAXM; ++i)
+          if (i < p.M) *reinterpret_cast<__nv_bfloat16*>(dst + (size_t)i * kSTile) = __float2bfloat16_rn(v[i]);
+      }
+    }
+    u += n;
+  }
+  tc_fence_before();
+  return true;
+}
+
 // MMA issuer (one thread).  Returns the number of chunks it issued.
 template <class L>
 __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, int role, int pass_lo, int pass_hi) {
@@ -553,6 +668,33 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
   // chunk's waits, MMAs and commits as the chunk takes to stream in)
   int qs = 0, qa = pass_lo == 2 ? sum_chunks(p) : 0;
   for (int pass = pass_lo; pass <= pass_hi; ++pass) {
+    if (pass == 1 && p.mix_t) {
+      if (role != 0 || mix_u0(p) >= mix_u1(p)) continue;
+      if (!bwait(&sh->wready, 0, sh)) return qa;
+      tc_fence_after();
+      const int u1 = mix_u1(p), pps = mix_t_pps(p), box = p.C * kD * 2, h0 = mix_u0(p) / kD;
+      const uint32_t idesc = idesc_bf16_f32(128, p.mix_n, 1, 0);
+      const uint32_t wt = smem_u32(sm + L::kOffY);
+      int j = 0;
+      for (int u = mix_u0(p), sg = 0; u < u1; ++sg, ++qs) {
+        const int s = qs % kNS;
+        if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return qa;
+        tc_fence_after();
+        const uint32_t st = smem_u32(sm + s * kStageBytes);
+        for (int k = 0; k < pps && u < u1; ++k, ++j) {
+          // A: the pair's two boxes, one 64-entry atom each (box bytes apart);
+          // B: the weight tile of the pair's head
+          const uint64_t da = smem_desc(st + 2 * k * box, box, 1024);
+          const uint64_t db = smem_desc(wt + (uint32_t)((u / kD - h0) * p.mix_n * 128), 16, 1024);
+          for (int kk = 0; kk < p.C / 16; ++kk)
+            mma_bf16(tmem + (uint32_t)(j * p.mix_n), da + kk * (2048 >> 4), db + kk * (32 >> 4), idesc, kk > 0);
+          u += mix_pair_units(u, u1);
+        }
+        mma_commit(&sh->mixs[sg]);
+        mma_commit(&sh->empty[s]);  // the stage is free once these MMAs have read it
+      }
+      continue;
+    }
     if (pass == 1) {
       if (role != 0) continue;
       // MIX stages: TMEM columns [256 (j % 2), +256) for MIX stage j
@@ -1015,6 +1157,8 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     sh->prod_qo = 0;
     sh->mma_q = 0;
     mbar_init(&sh->fin, 2);
+    for (int j = 0; j < kMaxNS; ++j) mbar_init(&sh->mixs[j], 1);
+    mbar_init(&sh->wready, kPhiWarps);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -1026,6 +1170,8 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     prefetch_tmap(&p.tm_k);
     prefetch_tmap(&p.tm_v);
     prefetch_tmap(&p.tm_y);
+    if (p.mix_t) prefetch_tmap(&p.tm_pp);
+    else if (p.tc_mix) prefetch_tmap(&p.tm_p);
   }
   for (int i = tid; i < kTileBytes / 16; i += kThreads)
     reinterpret_cast<uint4*>(sm + L::kOffOnes)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
@@ -1059,8 +1205,14 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
       if (lane == 0) tma_store_wait_all0();
       fence_proxy_async_global();
     }
+    uint4 wpk[4];
+    if (p.mix_t && warp >= kWarpPhi) mix_t_weights_load(p, warp - kWarpPhi, lane, wpk);
     if (mix_begin(p, sh, t)) {
-      if (p.tc_mix) {
+      if (p.mix_t) {
+        if (warp >= kWarpPhi) mix_t_weights_store<L>(p, sm, sh, warp - kWarpPhi, lane, wpk);
+        if (warp >= kWarpEpi) mix_t_epi<L>(p, sh, tmem, (warp - kWarpEpi) >> 2, warp & 3, lane);
+        else mix_z_rows<MAXM>(p, sm, t);
+      } else if (p.tc_mix) {
         if (warp >= kWarpPhi) phi_mix<L>(p, sm, sh, tmem, warp - kWarpPhi, lane, qs);
         else if (warp >= kWarpEpi) {
           epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 2, q, nst);
@@ -1139,6 +1291,21 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The chunk partials [heads * C][64 e][64 c] bf16 as a 3-D tensor (c, x =
+// head * C + chunk, e), box 64 x C x 2: the two units of a transposed-MIX pair,
+// each a C x 128-byte box with the 128-byte swizzle.
+bool make_map_pairs(CUtensorMap* m, const void* base, int heads, int C) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads * C, (cuuint64_t)kD};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * kD * 2, (cuuint64_t)kD * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kD, (cuuint32_t)C, 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct TcPlan {
   int C, M, cpb;
   bool tc_mix;  // S^T rows mixed on the tensor cores
@@ -1161,6 +1328,19 @@ TcPlan tc_plan(const MhlaShape& s) {
   p.tc_mix = p.C % 16 == 0 && (p.C <= kD || p.C % kD == 0);
   p.total = off;
   return p;
+}
+
+// Whether the transposed MIX applies with this grid: C <= 64, and every CTA's
+// pairs fit the TMEM columns, its weight tiles the 16 KB below the z weights,
+// and its MIX stages the input ring once.
+bool mix_t_fits(const TcPlan& pl, int heads, int grid) {
+  if (!pl.tc_mix || pl.C > kD || grid <= 0) return false;
+  const int N = (pl.M + 15) / 16 * 16;
+  const long long upc = ((long long)heads * kD + grid - 1) / grid;  // units of a CTA, at most
+  const long long hs = (upc - 1) / kD + 2;                          // heads they can touch
+  const long long pairs = (upc + 1) / 2 + hs;                       // a head boundary splits a pair
+  const long long pps = 128 / pl.C;
+  return hs * N * 128 <= 16384 && pairs * N <= (long long)kTmemCols && (pairs + pps - 1) / pps <= kMaxNS;
 }
 
 int sm_count() {
@@ -1218,6 +1398,11 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   if (!make_map_2d(&p.tm_ps, w + pl.off_ps, (uint64_t)s.heads() * pl.C * kD, 32)) return cudaErrorInvalidValue;
   if (pl.tc_mix && !make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, mix_kslots(pl.C), (uint64_t)kD * kD))
     return cudaErrorInvalidValue;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = s.heads() * pl.C < sms ? s.heads() * pl.C : sms;
+  p.mix_t = mix_t_fits(pl, s.heads(), grid) && make_map_pairs(&p.tm_pp, w + pl.off_ps, s.heads(), pl.C) ? 1 : 0;
+  p.mix_n = (pl.M + 15) / 16 * 16;
   p.mixing = mixing;
   p.ps = reinterpret_cast<__nv_bfloat16*>(w + pl.off_ps);
   p.pz = reinterpret_cast<float*>(w + pl.off_pz);
@@ -1236,9 +1421,6 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   p.tc_mix = pl.tc_mix ? 1 : 0;
   p.XS = pl.tc_mix ? s.heads() * kD : 0;
   p.eps = eps;
-  const int sms = sm_count();
-  if (sms <= 0) return cudaErrorInvalidDevice;
-  const int grid = p.TS < sms ? p.TS : sms;
   cudaError_t e;
   if (p.M <= 16)
     e = launch_t<16>(p, grid, st);
