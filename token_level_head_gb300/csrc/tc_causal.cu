@@ -69,9 +69,9 @@ constexpr int kStageB = 3 * kTileBytes;
 constexpr int kOffOnesB = 0;                 // 16 KB of bf16 ones: A rows 0..63 of the P MMA
 constexpr int kOffStages = kTileBytes;       // the ring (above the ones tile: the MMA's LBO is positive)
 constexpr int kOffP = kOffStages + kNSB * kStageB;  // 2 P_c^T tiles
-constexpr int kOffY = kOffP + 2 * kPTile;    // Y staging, 4 warps x 4 KB
+constexpr int kOffY = kOffP + 2 * kPTile;    // Y staging, 4 warps x 2 x 4 KB
 constexpr int kNDen = 4;                     // denominator slots
-constexpr int kOffDen = kOffY + 4 * 4096;    // [kNDen][128] fp32
+constexpr int kOffDen = kOffY + 4 * 8192;    // [kNDen][128] fp32
 constexpr int kOffWs = kOffDen + kNDen * kTile * 4;  // [2][8 warps][64] fp32 column sums of phi(K)
 constexpr int kOffZ = kOffWs + 2 * kPhiWarps * kD * 4;  // [2][64] fp32 zeta_c
 constexpr int kOffSmallB = kOffZ + 2 * kD * 4;
@@ -550,7 +550,7 @@ __device__ bool out_store(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
   if (!cwait(&sh->num_full[a], (i >> 1) & 1, &sh->abort)) return false;
   tc_fence_after();
   const float* den = reinterpret_cast<const float*>(sm + kOffDen);
-  uint8_t* yb = sm + kOffY + qd * 4096;
+  uint8_t* yb = sm + kOffY + qd * 8192 + (nst & 1) * 4096;  // two buffers a warp
   float v[64];
   const uint32_t ta = tmem + kColNum + 64 * a + ((uint32_t)(qd * 32) << 16);
 #pragma unroll
@@ -569,7 +569,7 @@ __device__ bool out_store(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
   const float r = 1.f / dn;
 #pragma unroll
   for (int x = 0; x < 64; ++x) v[x] *= r;
-  if (lane == 0 && nst >= 1) tma_store_wait_read0();  // the previous store has read yb
+  if (lane == 0 && nst >= 1) tma_store_wait_read1();  // the store of two chunks ago has read yb
   __syncwarp();
 #pragma unroll
   for (int jj = 0; jj < 8; ++jj) *swz_piece(yb, lane, jj) = pack8(v + 8 * jj);

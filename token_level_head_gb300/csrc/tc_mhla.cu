@@ -816,24 +816,26 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         // a bulk store: rows 32 qd .. 32 qd + 31 of S^T (qd 0, 1; bf16, 128-byte
         // swizzle for the tensor map), or z (qd 2: rows 64.. all hold it)
         if (qd < 3) {
-          if (lane == 0 && nst >= 1) tma_store_wait_read0();  // the previous store has read yb
+          // two staging buffers per warp, as in the OUT pass
+          uint8_t* yo = sm + L::kOffY + qd * 8192 + (nst & 1) * 4096;
+          if (lane == 0 && nst >= 1) tma_store_wait_read1();  // the store of two chunks ago has read yo
           __syncwarp();
           if (qd < 2) {
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-              *reinterpret_cast<uint4*>(yb + swz128(lane, 8 * c)) =
+              *reinterpret_cast<uint4*>(yo + swz128(lane, 8 * c)) =
                   make_uint4(pack_bf16(v[8 * c], v[8 * c + 1]), pack_bf16(v[8 * c + 2], v[8 * c + 3]),
                              pack_bf16(v[8 * c + 4], v[8 * c + 5]), pack_bf16(v[8 * c + 6], v[8 * c + 7]));
           } else if (lane == 0) {
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              reinterpret_cast<float4*>(yb)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+              reinterpret_cast<float4*>(yo)[c] = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (qd < 2) tma_store_2d(&p.tm_ps, yb, 0, g * kD + qd * 32);
-            else bulk_store_1d(p.pz + (size_t)g * kD, yb, kD * 4);
+            if (qd < 2) tma_store_2d(&p.tm_ps, yo, 0, g * kD + qd * 32);
+            else bulk_store_1d(p.pz + (size_t)g * kD, yo, kD * 4);
             tma_store_commit();
           }
           ++nst;
@@ -851,17 +853,20 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
         if (p.den_out != nullptr) p.den_out[(size_t)g * kTile + row] = dn;
         const float r = 1.f / dn;
-        if (lane == 0 && nst >= 1) tma_store_wait_read0();  // the previous store has read yb
+        // Y staging: two 4 KB buffers per warp (the whole 32 KB area is free
+        // after the MIX phase); the store of two chunks ago has read this one
+        uint8_t* yo = sm + L::kOffY + qd * 8192 + (nst & 1) * 4096;
+        if (lane == 0 && nst >= 1) tma_store_wait_read1();
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<uint4*>(yb + swz128(lane, 8 * c)) =
+          *reinterpret_cast<uint4*>(yo + swz128(lane, 8 * c)) =
               make_uint4(pack_bf16(v[8 * c] * r, v[8 * c + 1] * r), pack_bf16(v[8 * c + 2] * r, v[8 * c + 3] * r),
                          pack_bf16(v[8 * c + 4] * r, v[8 * c + 5] * r), pack_bf16(v[8 * c + 6] * r, v[8 * c + 7] * r));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d_hint(&p.tm_y, yb, 0, g * kTile + qd * 32, once);
+          tma_store_2d_hint(&p.tm_y, yo, 0, g * kTile + qd * 32, once);
           tma_store_commit();
         }
         ++nst;
