@@ -118,6 +118,9 @@ TC_SHAPES = [  # bf16, d = 64, blocks of whole 128-token tiles: the tcgen05 kern
     (1, 1, 8192, 64, 128),    # M = 64, one chunk per block
     (3, 5, 640, 64, 128),     # odd head count, M = 5
     (2, 1, 1536, 64, 512),    # 4 chunks per block
+    (2, 2, 6144, 64, 128),    # C = 48 partials (three K steps, two pairs a stage), M = 48
+    (1, 3, 6144, 64, 256),    # M = 24: query blocks 24..31 of the mixing MMA are padding
+    (1, 3, 4096, 64, 128),    # M = 32, C = 32
 ]
 
 
