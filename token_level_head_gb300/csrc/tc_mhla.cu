@@ -118,6 +118,7 @@ struct Params {
   int XS;                        // tensor-core MIX units: heads * 64 (0 without tc_mix)
   int mix_t;                     // 1: transposed tensor-core MIX (C <= 64; see the MIX stages)
   int mix_n;                     // transposed MIX: N of its MMAs, M rounded up to 16
+  int zx;                        // 1: the CTAs with a z row take no MIX units (C > 64, heads <= grid / 4)
   float eps;
 };
 
@@ -240,8 +241,26 @@ __host__ __device__ __forceinline__ int mix_kslots(int C) { return C < kD ? C : 
 __host__ __device__ __forceinline__ int mix_nkc(int C) { return C / mix_kslots(C); }
 __device__ __forceinline__ int mix_per_stage(int C) { return min(4, kMixWOff / (mix_kslots(C) * kD * 2)); }
 __host__ __device__ __forceinline__ bool mix_rep(int M) { return M <= 32; }
-__device__ __forceinline__ int mix_u0(const Params& p) { return (int)((long long)blockIdx.x * p.XS / gridDim.x); }
-__device__ __forceinline__ int mix_u1(const Params& p) { return (int)((long long)(blockIdx.x + 1) * p.XS / gridDim.x); }
+// With zx set (C > 64 and few heads; only kernels with M > 32) the CTAs that
+// mix a z row (heads rows over the grid, see mix_rows_all) take no units: the
+// z rows then run beside the units instead of after them.  CTA b is then unit
+// CTA b - (z rows before b).  The kernels with M <= 32 keep the plain split
+// (their code stays as compact as before).
+template <class L>
+__device__ __forceinline__ int mix_ubound(const Params& p, int k) {
+  if constexpr (L::kMaxM > 32) {
+    if (p.zx) {
+      const long long b = blockIdx.x, G = gridDim.x;
+      if ((b + 1) * p.heads / G > b * p.heads / G) return 0;  // a z-row CTA: no units
+      return (int)((b - b * p.heads / G + k) * p.XS / (G - p.heads));
+    }
+  }
+  return (int)(((long long)blockIdx.x + k) * p.XS / gridDim.x);
+}
+template <class L>
+__device__ __forceinline__ int mix_u0(const Params& p) { return mix_ubound<L>(p, 0); }
+template <class L>
+__device__ __forceinline__ int mix_u1(const Params& p) { return mix_ubound<L>(p, 1); }
 // SUM chunks of this CTA (the OUT pass's accumulators follow theirs)
 __device__ __forceinline__ int sum_chunks(const Params& p) {
   return (int)blockIdx.x < p.TS ? (p.TS - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -298,12 +317,12 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
   }
   // MIX units (head h, row e of S^T): the chunk partials' row e, once every CTA
   // has stored its partials (grid barrier 1); the phi warps add the weights
-  const int u1 = mix_u1(p);
-  if (p.mix_t && mix_u0(p) < u1) {
+  const int u1 = mix_u1<L>(p);
+  if (p.mix_t && mix_u0<L>(p) < u1) {
     if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
     fence_proxy_async_global();  // the partials were written by other CTAs' bulk stores
     const int pps = mix_t_pps(p), box = p.C * kD * 2;
-    for (int u = mix_u0(p); u < u1; ++q) {
+    for (int u = mix_u0<L>(p); u < u1; ++q) {
       const int s = q % kNS;
       if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
       int np = 0;
@@ -317,11 +336,11 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
         u += mix_pair_units(u, u1);
       }
     }
-  } else if (p.tc_mix && mix_u0(p) < u1) {
+  } else if (p.tc_mix && mix_u0<L>(p) < u1) {
     if (!gwait(&p.ctr[2], gridDim.x, sh)) return q;
     fence_proxy_async_global();  // the partials were written by other CTAs' bulk stores
     const int ks = mix_kslots(p.C), nkc = mix_nkc(p.C);
-    for (int u = mix_u0(p); u < u1;) {
+    for (int u = mix_u0<L>(p); u < u1;) {
       const int n = mix_stage_units(p, u, u1), h = u / kD;
       for (int kc = 0; kc < nkc; ++kc, ++q) {
         const int s = q % kNS;
@@ -540,15 +559,22 @@ template <class L>
 __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, int w, int lane, int& qs) {
   constexpr int kNS = L::NS;
   const int t = w * 32 + lane;  // rows t / 8 + 32 kk, piece t % 8 of the tile
-  const int u1 = mix_u1(p);
+  const int u1 = mix_u1<L>(p);
   const int nkc = mix_nkc(p.C);
+  // kernels with M > 32 (long K chunks of partials) load the next stage's
+  // mixing values one stage ahead; the others just before the stage
+  constexpr bool kAhead = L::kMaxM > 32;
   uint4 wv[4];
   int wh = -1;  // (head, K chunk) of the values in wv
+  if (kAhead && mix_u0<L>(p) < u1) {
+    wh = ((mix_u0<L>(p) / kD) % p.H) * nkc;
+    mix_weight_values(p, wh / nkc, 0, t, wv);
+  }
   int j = 0, up = 0, np = 0;  // group index; the previous group's units
-  for (int u = mix_u0(p); u < u1; ++j) {
+  for (int u = mix_u0<L>(p); u < u1; ++j) {
     const int n = mix_stage_units(p, u, u1), hh = (u / kD) % p.H;
     for (int kc = 0; kc < nkc; ++kc, ++qs) {
-      if (hh * nkc + kc != wh) {  // the mixing values of a head (chunk) are loaded once
+      if (!kAhead && hh * nkc + kc != wh) {  // the mixing values of a head (chunk) are loaded once
         mix_weight_values(p, hh, kc, t, wv);
         wh = hh * nkc + kc;
       }
@@ -563,6 +589,17 @@ __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, 
       fence_proxy_async_smem();  // weight tile -> tensor core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->ready[s]);
+      // the next stage's values (its head, its K chunk): their loads run while
+      // this stage's MMAs do and while the next stage's boxes arrive
+      int nh = hh, nk = kc + 1;
+      if (nk == nkc) {
+        nk = 0;
+        nh = u + n < u1 ? ((u + n) / kD) % p.H : -1;
+      }
+      if (kAhead && nh >= 0 && nh * nkc + nk != wh) {
+        mix_weight_values(p, nh, nk, t, wv);
+        wh = nh * nkc + nk;
+      }
     }
     if (w < 4 && j >= 1 && ((j - 1) & 1) && !mix_odd_group(p, sh, tmem, w, lane, j - 1, up, np)) return;
     up = u;
@@ -577,8 +614,9 @@ __device__ void phi_mix(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem, 
 // m[h][i][x / cpb] for x = 8 pc .. 8 pc + 7, zero past M or C).  Thread t
 // holds pieces t + 256 k (at most four: the tiles fit 16 KB); the values are
 // read before grid barrier 1 and written once the staging area is free.
+template <class L>
 __device__ __forceinline__ void mix_t_weights_load(const Params& p, int w, int lane, uint4 (&pk)[4]) {
-  const int u0 = mix_u0(p), u1 = mix_u1(p), N = p.mix_n;
+  const int u0 = mix_u0<L>(p), u1 = mix_u1<L>(p), N = p.mix_n;
   const int h0 = u0 / kD, nh = u0 < u1 ? (u1 - 1) / kD - h0 + 1 : 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -602,7 +640,7 @@ __device__ __forceinline__ void mix_t_weights_load(const Params& p, int w, int l
 
 template <class L>
 __device__ void mix_t_weights_store(const Params& p, uint8_t* sm, Small* sh, int w, int lane, const uint4 (&pk)[4]) {
-  const int u0 = mix_u0(p), u1 = mix_u1(p), N = p.mix_n;
+  const int u0 = mix_u0<L>(p), u1 = mix_u1<L>(p), N = p.mix_n;
   const int h0 = u0 / kD, nh = u0 < u1 ? (u1 - 1) / kD - h0 + 1 : 0;
   uint8_t* wt = sm + L::kOffY;
 #pragma unroll
@@ -624,10 +662,10 @@ __device__ void mix_t_weights_store(const Params& p, uint8_t* sm, Small* sh, int
 template <class L>
 __device__ bool mix_t_epi(const Params& p, Small* sh, uint32_t tmem, int g, int qd, int lane) {
   constexpr int MAXM = L::kMaxM;
-  const int u1 = mix_u1(p), pps = mix_t_pps(p), N = p.mix_n;
+  const int u1 = mix_u1<L>(p), pps = mix_t_pps(p), N = p.mix_n;
   const int kq = qd >> 1, c = 32 * (qd & 1) + lane;
   int j = 0;
-  for (int u = mix_u0(p); u < u1; ++j) {
+  for (int u = mix_u0<L>(p); u < u1; ++j) {
     const int n = mix_pair_units(u, u1);
     if (j % 3 == g) {
       if (!bwait(&sh->mixs[j / pps], 0, sh)) return false;
@@ -669,14 +707,14 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
   int qs = 0, qa = pass_lo == 2 ? sum_chunks(p) : 0;
   for (int pass = pass_lo; pass <= pass_hi; ++pass) {
     if (pass == 1 && p.mix_t) {
-      if (role != 0 || mix_u0(p) >= mix_u1(p)) continue;
+      if (role != 0 || mix_u0<L>(p) >= mix_u1<L>(p)) continue;
       if (!bwait(&sh->wready, 0, sh)) return qa;
       tc_fence_after();
-      const int u1 = mix_u1(p), pps = mix_t_pps(p), box = p.C * kD * 2, h0 = mix_u0(p) / kD;
+      const int u1 = mix_u1<L>(p), pps = mix_t_pps(p), box = p.C * kD * 2, h0 = mix_u0<L>(p) / kD;
       const uint32_t idesc = idesc_bf16_f32(128, p.mix_n, 1, 0);
       const uint32_t wt = smem_u32(sm + L::kOffY);
       int j = 0;
-      for (int u = mix_u0(p), sg = 0; u < u1; ++sg, ++qs) {
+      for (int u = mix_u0<L>(p), sg = 0; u < u1; ++sg, ++qs) {
         const int s = qs % kNS;
         if (!bwait(&sh->full[s], (qs / kNS) & 1, sh)) return qa;
         tc_fence_after();
@@ -698,11 +736,11 @@ __device__ int mma_issuer(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem
     if (pass == 1) {
       if (role != 0) continue;
       // MIX stages: TMEM columns [256 (j % 2), +256) for MIX stage j
-      const int u1 = mix_u1(p);
+      const int u1 = mix_u1<L>(p);
       const bool rep4 = mix_rep(p.M);
       int j = 0;
       const int ks = mix_kslots(p.C), nkc = mix_nkc(p.C);
-      for (int u = mix_u0(p); u < u1; ++j) {
+      for (int u = mix_u0<L>(p); u < u1; ++j) {
         const int n = mix_stage_units(p, u, u1), half = j & 1;
         if (j >= 2 && !bwait(&sh->mixe[half], ((j >> 1) - 1) & 1, sh)) return qa;
         const uint32_t dst = tmem + (uint32_t)(256 * half);
@@ -776,9 +814,9 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
   if (pass == 2) {
     // MIX groups (see the MMA issuer): the even ones (TMEM columns 0..255);
     // phi warps 8-11 take the odd ones
-    const int u1 = mix_u1(p);
+    const int u1 = mix_u1<L>(p);
     int j = 0;
-    for (int u = mix_u0(p); u < u1; ++j) {
+    for (int u = mix_u0<L>(p); u < u1; ++j) {
       const int n = mix_stage_units(p, u, u1), half = j & 1;
       if (half) {
         u += n;
@@ -1211,7 +1249,7 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
       fence_proxy_async_global();
     }
     uint4 wpk[4];
-    if (p.mix_t && warp >= kWarpPhi) mix_t_weights_load(p, warp - kWarpPhi, lane, wpk);
+    if (p.mix_t && warp >= kWarpPhi) mix_t_weights_load<L>(p, warp - kWarpPhi, lane, wpk);
     if (mix_begin(p, sh, t)) {
       if (p.mix_t) {
         if (warp >= kWarpPhi) mix_t_weights_store<L>(p, sm, sh, warp - kWarpPhi, lane, wpk);
@@ -1408,6 +1446,7 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   const int grid = s.heads() * pl.C < sms ? s.heads() * pl.C : sms;
   p.mix_t = mix_t_fits(pl, s.heads(), grid) && make_map_pairs(&p.tm_pp, w + pl.off_ps, s.heads(), pl.C) ? 1 : 0;
   p.mix_n = (pl.M + 15) / 16 * 16;
+  p.zx = pl.tc_mix && pl.C > kD && 4 * s.heads() <= grid ? 1 : 0;
   p.mixing = mixing;
   p.ps = reinterpret_cast<__nv_bfloat16*>(w + pl.off_ps);
   p.pz = reinterpret_cast<float*>(w + pl.off_pz);
