@@ -77,6 +77,23 @@ def tokens_per_step(wl):
     return wl.B * wl.H if wl.kind == "decode" else wl.B * wl.H * wl.N
 
 
+def max_over_ranks(ms, world, device=None):
+    """The job's time: the largest of the ranks' times (an all-reduce MAX over
+    the default process group when there is more than one rank)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank_step, steps, world, ms):
+    """Whole-job throughput: every rank's units over the job's time (weak scaling)."""
+    return world * tokens_per_rank_step * steps / (ms / 1e3)
+
+
 def describe(wl):
     s = f"{wl.name}: B{wl.B} H{wl.H} N{wl.N} d{wl.d} {wl.dtype}"
     if wl.kind == "mhla":
@@ -408,10 +425,7 @@ def run_ours(args, wl, rank, world, local_rank):
         durs = [events[i].elapsed_time(events[i + 1]) for i in range(chunk)]
         step_ms = sum(durs) / len(durs)
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, device)
 
     # end to end through host buffers
     e2e = None
@@ -423,12 +437,9 @@ def run_ours(args, wl, rank, world, local_rank):
         if world > 1:
             dist.barrier()
         e_ms = runner.e2e_run(k_e2e)
-        if world > 1:
-            t = torch.tensor([e_ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, world, device)
         h2d, d2h = runner.e2e_bytes()
-        e2e = {"value": world * tokens_per_step(wl) * k_e2e / (e_ms / 1e3), "unit": "tokens/s",
+        e2e = {"value": job_value(tokens_per_step(wl), k_e2e, world, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e,
                "ms_per_step": e_ms / k_e2e,
                "pipelining": "host->device copies (one stream per input), calls and device->host "
@@ -448,7 +459,7 @@ def run_ours(args, wl, rank, world, local_rank):
     else:
         path = binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
     kernel_name = f"{wl.kind}_{path}"
-    value = world * tokens_per_step(wl) * args.steps / (elapsed_ms / 1e3)
+    value = job_value(tokens_per_step(wl), args.steps, world, elapsed_ms)
     line = {
         "metric": METRIC if wl.name == "dit" else f"{wl.name} tokens/s",
         "value": value,
