@@ -183,6 +183,15 @@ const char* mhla_status_string(mhla_status s);
  * this process since it was loaded; a diagnostic counter. */
 unsigned long long mhla_launch_count(void);
 
+/* Diagnostic: sets the limit, in nanoseconds, of every bounded device-side
+ * wait of the bf16 tensor-core forward for calls launched after it (process
+ * wide; 0 restores the default of 0.5 s).  With a limit too short for the
+ * work in flight a call gives up: its output is incomplete, the kernel lets
+ * its copies and MMAs in flight finish, leaves the workspace counters at
+ * zero, and mhla_query_status() then reports MHLA_ERR_TIMEOUT.  The pages
+ * describe no such control; it exists to exercise that failure path. */
+void mhla_debug_set_wait_limit_ns(unsigned long long ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -111,16 +111,23 @@ def test_small_shapes(shape, dtype):
     assert_close_den(den, dref, dtype)
 
 
-TC_SHAPES = [  # bf16, d = 64, blocks of whole 128-token tiles: the tcgen05 kernel
-    (1, 1, 128, 64, 128),     # one chunk, M = 1
+TC_SHAPES = [  # bf16, d = 64, blocks of whole 128-token tiles: the tcgen05 kernels
+    # C = N / 128 a multiple of 16: the three-pass kernel
     (2, 3, 2048, 64, 128),    # M = 16, one chunk per block
     (1, 2, 4096, 64, 4096),   # M = 1 with 32 chunks (split block sums)
     (1, 1, 8192, 64, 128),    # M = 64, one chunk per block
-    (3, 5, 640, 64, 128),     # odd head count, M = 5
-    (2, 1, 1536, 64, 512),    # 4 chunks per block
     (2, 2, 6144, 64, 128),    # C = 48 partials (three K steps, two pairs a stage), M = 48
     (1, 3, 6144, 64, 256),    # M = 24: query blocks 24..31 of the mixing MMA are padding
     (1, 3, 4096, 64, 128),    # M = 32, C = 32
+    (1, 2, 16384, 64, 2048),  # C = 128 > 64: the MIX MMAs in K chunks of 64 partials, M = 8
+    (1, 1, 32768, 64, 32768), # M = 1 over C = 256 partials (z rows on CTAs of their own)
+    # C not a multiple of 16: the stream kernel (partials zero-filled to 16)
+    (1, 1, 128, 64, 128),     # one chunk, M = 1
+    (3, 5, 640, 64, 128),     # odd head count, M = 5
+    (2, 1, 1536, 64, 512),    # 4 chunks per block, C = 12
+    (2, 3, 1152, 64, 384),    # 3 chunks per block, C = 9
+    (4, 6, 1024, 64, 256),    # DiT-like blocks of 256 over 1024 tokens, 24 heads
+    (1, 2, 8064, 64, 128),    # C = 63, M = 63: one tile per MIX item, 32 items a head
 ]
 
 
@@ -171,6 +178,110 @@ def test_extreme_values_fp32():
     assert_close_den(den, dref, "f32")
 
 
+# Edge cases on the bf16 tensor-core paths (both non-causal kernels): inputs far
+# from zero (both branches of phi, exp of large negative values), eps = 0,
+# identity mixing (per-block global linear attention, a closed form the
+# oracle computes separately) and mixing with exact zeros.
+TC_EDGE = [(2, 3, 2048, 64, 256), (2, 3, 1152, 64, 128)]  # three-pass kernel, stream kernel
+
+
+@pytest.mark.parametrize("shape", TC_EDGE, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("scale", [4.0, 6.0])
+def test_tcgen05_large_inputs_eps0(shape, scale):
+    B, H, N, d, block = shape
+    x = rand_inputs(600 + N, (B, H, N, d), "bf16", scale=scale)
+    mix_t, mix64 = rand_mixing(17, H, N // block)
+    y, den = forward(x["q"], x["k"], x["v"], mix_t, block, eps=0.0)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block, eps=0.0)
+    assert_close_y(y, ref, "bf16")
+    assert_close_den(den, dref, "bf16")
+
+
+@pytest.mark.parametrize("shape", TC_EDGE, ids=lambda s: "x".join(map(str, s)))
+def test_tcgen05_identity_mixing_is_blockwise_linear_attention(shape):
+    B, H, N, d, block = shape
+    M = N // block
+    x = rand_inputs(610 + N, (B, H, N, d), "bf16")
+    eye = np.broadcast_to(np.eye(M), (H, M, M)).astype(np.float32)
+    y, den = forward(x["q"], x["k"], x["v"], torch.from_numpy(np.ascontiguousarray(eye)).cuda(), block)
+    split = lambda a: a.reshape(B, H, M, block, d).transpose(0, 2, 1, 3, 4).reshape(B * M, H, block, d)  # noqa: E731
+    ref, dref = oracle.global_linear_attention(split(x["q64"]), split(x["k64"]), split(x["v64"]))
+    ref = ref.reshape(B, M, H, block, d).transpose(0, 2, 1, 3, 4).reshape(B, H, N, d)
+    dref = dref.reshape(B, M, H, block).transpose(0, 2, 1, 3).reshape(B, H, N)
+    assert_close_y(y, ref, "bf16")
+    assert_close_den(den, dref, "bf16")
+
+
+@pytest.mark.parametrize("shape", TC_EDGE, ids=lambda s: "x".join(map(str, s)))
+def test_tcgen05_mixing_with_exact_zeros(shape):
+    B, H, N, d, block = shape
+    M = N // block
+    x = rand_inputs(620 + N, (B, H, N, d), "bf16")
+    u = uniform(21, 9, (H, M, M)) + 0.05
+    u[uniform(21, 10, (H, M, M)) < 0.5] = 0.0
+    u[np.arange(H)[:, None], np.arange(M)[None, :], np.arange(M)[None, :]] += 0.5  # no all-zero row
+    mix = (u / u.sum(axis=-1, keepdims=True)).astype(np.float32)
+    y, den = forward(x["q"], x["k"], x["v"], torch.from_numpy(mix).cuda(), block)
+    ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix.astype(np.float64), block)
+    assert_close_y(y, ref, "bf16")
+    assert_close_den(den, dref, "bf16")
+
+
+@pytest.mark.parametrize("shape", [(2, 3, 2048, 64, 256), (2, 3, 1152, 64, 128)], ids=lambda s: "x".join(map(str, s)))
+def test_tcgen05_without_den_out(shape):
+    """The bench's call form: no den_out, a workspace reused by repeated calls."""
+    B, H, N, d, block = shape
+    x = rand_inputs(630 + N, (B, H, N, d), "bf16")
+    mix_t, mix64 = rand_mixing(23, H, N // block)
+    ws = binding.new_workspace(binding.mhla_workspace_bytes(B, H, N, d, block), "cuda")
+    y = torch.empty_like(x["q"])
+    for _ in range(3):
+        binding.mhla_forward(x["q"], x["k"], x["v"], mix_t, y, block, workspace=ws)
+    assert binding.mhla_query_status(ws) == 0
+    ref, _ = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block)
+    assert_close_y(to_f64(y), ref, "bf16")
+
+
+def test_canary_regions_untouched():
+    """Y, den_out and the workspace sit inside larger buffers filled with a pattern; nothing
+    outside the regions the call owns may change (both tensor-core kernels and a SIMT shape)."""
+    pad = 4096
+    for shape in [(2, 3, 2048, 64, 256), (2, 3, 1152, 64, 128), (1, 2, 256, 32, 64)]:
+        B, H, N, d, block = shape
+        x = rand_inputs(640 + N, (B, H, N, d), "bf16")
+        mix_t, mix64 = rand_mixing(29, H, N // block)
+        n_y, n_d = B * H * N * d, B * H * N
+        ybuf = torch.full((n_y + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+        dbuf = torch.full((n_d + 2 * pad,), -7.5, dtype=torch.float32, device="cuda")
+        nws = binding.mhla_workspace_bytes(B, H, N, d, block)
+        wbuf = torch.full((nws + 2 * pad,), 0xA5, dtype=torch.uint8, device="cuda")
+        ws = wbuf[pad:pad + nws]
+        ws.zero_()
+        y = ybuf[pad:pad + n_y].view(torch.bfloat16).view(B, H, N, d)
+        den = dbuf[pad:pad + n_d].view(B, H, N)
+        binding.mhla_forward(x["q"], x["k"], x["v"], mix_t, y, block, den_out=den, workspace=ws)
+        torch.cuda.synchronize()
+        assert binding.mhla_query_status(ws) == 0
+        for buf, fill in ((ybuf, 12345), (dbuf, -7.5), (wbuf, 0xA5)):
+            assert bool((buf[:pad] == fill).all()) and bool((buf[-pad:] == fill).all()), f"canary {shape}"
+        ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block)
+        assert_close_y(to_f64(y), ref, "bf16")
+        assert_close_den(to_f64(den), dref, "bf16")
+
+
+def test_device_generator_matches_host_generator():
+    """The full-size tests generate Q, K, V on the device and the oracle's slices on the host:
+    both must be the same bf16 values, bit for bit."""
+    from workloads import normal_device
+    shape = (2, 3, 1000, 64)
+    for tid in (1, 2, 3):
+        dev = normal_device(20261204, tid, shape, 0.125, device="cuda", dtype=torch.bfloat16)
+        host = bf16_bits(normal(20261204, tid, shape, 0.125))
+        assert np.array_equal(dev.view(torch.int16).cpu().numpy().view(np.uint16), host)
+    devf = normal_device(20261205, 4, (7, 33), 1.0, device="cuda", dtype=torch.float32).cpu().numpy()
+    assert np.array_equal(devf, normal(20261205, 4, (7, 33), 1.0).astype(np.float32))
+
+
 @pytest.mark.parametrize("name", ["dit"])
 def test_full_workload_all_heads(name):
     wl = WORKLOADS[name]
@@ -183,12 +294,12 @@ def test_full_workload_all_heads(name):
 
 
 @pytest.mark.parametrize("name", ["hires", "hires_m1"])
-def test_full_workload_sampled_heads(name):
+def test_full_workload_every_head(name):
     wl = WORKLOADS[name]
     dev = mhla_device(wl)
     y, den = forward(dev["q"], dev["k"], dev["v"], dev["mixing"], wl.block)
     assert np.all(np.isfinite(y)) and np.all(den > 0)
-    heads = [(0, 1), (0, 4)]
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
     x = mhla_host(wl, heads=heads)
     ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
     for i, (b, h) in enumerate(heads):
@@ -297,12 +408,12 @@ def test_causal_mhla_with_mixing(dtype):
     assert np.array_equal(y2, y) and np.array_equal(den2, den)
 
 
-def test_causal_full_workload_sampled_heads():
+def test_causal_full_workload_every_head():
     wl = WORKLOADS["causal"]
     dev = mhla_device(wl)
     y, den = forward_causal(dev["q"], dev["k"], dev["v"], None, wl.block)
     assert np.all(np.isfinite(y)) and np.all(den > 0)
-    heads = [(0, 0), (2, 9), (3, 15)]
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
     x = mhla_host(wl, heads=heads)
     ref, dref = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)
     for i, (b, h) in enumerate(heads):
@@ -352,7 +463,7 @@ def test_decode_full_workload_sampled_units():
     kf = torch.where(dev["prefix_k"].float() > 0, dev["prefix_k"].float() + 1, torch.exp(dev["prefix_k"].float()))
     S = torch.einsum("pbhc,pbhe->bhce", kf, dev["prefix_v"].float()).contiguous()
     z = kf.sum(dim=0).contiguous()
-    units = [0, 1234, B * H - 1]
+    units = list(range(0, B * H, 64)) + [B * H - 1]  # every 64th unit and the last: 65 units
     host = decode_host(wl, units)
     s0 = np.einsum("puc,pue->uce", oracle.phi(host["prefix_k64"]), host["prefix_v64"]).astype(np.float32)
     z0 = oracle.phi(host["prefix_k64"]).sum(axis=0).astype(np.float32)
@@ -428,7 +539,7 @@ def test_rala_tcgen05_shapes(shape):
     assert_close_y(to_f64(y), ref, "bf16")
 
 
-def test_rala_full_workload_sampled_batches():
+def test_rala_full_workload_every_batch():
     wl = WORKLOADS["rala"]
     dev = rala_device(wl)
     y = torch.empty_like(dev["q"])
@@ -436,7 +547,7 @@ def test_rala_full_workload_sampled_batches():
     torch.cuda.synchronize()
     y = to_f64(y)
     assert np.all(np.isfinite(y))
-    batches = [0, 33, 63]
+    batches = list(range(wl.B))
     host = rala_host(wl, batches)
     ref = oracle.rala_forward(host["q64"], host["k64"], host["v64"], host["x64"], host["w64"])
     assert_close_y(y[batches], ref, wl.dtype)

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "mhla_status_string": (ctypes.c_char_p, [_i]),
     "mhla_launch_count": (ctypes.c_ulonglong, []),
     "mhla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
+    "mhla_debug_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -189,3 +190,8 @@ def mhla_query_status(workspace, stream=None) -> int:
 
 def mhla_launch_count() -> int:
     return int(load().mhla_launch_count())
+
+
+def mhla_debug_set_wait_limit_ns(ns: int) -> None:
+    """Diagnostic: limit of the device-side waits of the bf16 tensor-core forward (0 = default)."""
+    load().mhla_debug_set_wait_limit_ns(int(ns))

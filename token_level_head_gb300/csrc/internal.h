@@ -32,6 +32,16 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
                            const float* mixing, void* y, float* den_out, float eps, MixMode mode,
                            void* ws, cudaStream_t st);
 
+// ---- tcgen05 stream path (bf16, d = 64, blocks of whole 128-token tiles, at most 64 tiles a head):
+// summaries, mixing and output as one ordered list of items with per-head readiness counters
+bool tc_stream_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
+size_t tc_stream_workspace(const MhlaShape& s);
+cudaError_t tc_stream_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
+                             const float* mixing, void* y, float* den_out, float eps, void* ws,
+                             cudaStream_t st);
+// Limit of every bounded device-side wait of the stream kernel (0 restores the default 0.5 s).
+void tc_stream_set_wait_limit(unsigned long long ns);
+
 // ---- tcgen05 causal path (bf16, d = 64, plain causal linear attention, N a multiple of 128)
 bool tc_causal_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
 size_t tc_causal_workspace(const MhlaShape& s);

@@ -38,7 +38,8 @@ size_t mhla_ws(int B, int H, int N, int d, int block, int causal) {
   const size_t a = simt_mhla_workspace(s);
   const size_t b = causal ? (tc_causal_supported(s, MHLA_BF16, MIX_PREFIX) ? tc_causal_workspace(s) : 0)
                           : (tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0);
-  return std::max(a, b);
+  const size_t c = !causal && tc_stream_supported(s, MHLA_BF16, MIX_FULL) ? tc_stream_workspace(s) : 0;
+  return std::max(a, std::max(b, c));
 }
 
 // Shared validation of the Q/K/V/Y/den/workspace arguments of the MHLA entries.
@@ -85,7 +86,8 @@ mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int caus
       (dt != MHLA_F32 && dt != MHLA_BF16) || (causal != 0 && causal != 1))
     return MHLA_PATH_NONE;
   const MhlaShape s{B, H, N, d, block_size};
-  const bool tc = causal ? tc_causal_supported(s, dt, MIX_PREFIX) : tc_mhla_supported(s, dt, MIX_FULL);
+  const bool tc = causal ? tc_causal_supported(s, dt, MIX_PREFIX)
+                         : (tc_stream_supported(s, dt, MIX_FULL) || tc_mhla_supported(s, dt, MIX_FULL));
   return tc ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
 
@@ -99,6 +101,8 @@ static mhla_status run_mhla(const void* q, const void* k, const void* v, const f
   MhlaShape s{B, H, N, d, block};
   if (tc_causal_supported(s, dt, mode))
     return from_cuda(tc_causal_launch(s, q, k, v, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
+  if (tc_stream_supported(s, dt, mode))
+    return from_cuda(tc_stream_launch(s, q, k, v, mixing, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
   if (tc_mhla_supported(s, dt, mode))
     return from_cuda(tc_mhla_launch(s, q, k, v, mixing, y, den_out, eps, mode, ws,
                                     static_cast<cudaStream_t>(stream)));
@@ -216,5 +220,7 @@ const char* mhla_status_string(mhla_status s) {
 }
 
 unsigned long long mhla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+void mhla_debug_set_wait_limit_ns(unsigned long long ns) { tc_stream_set_wait_limit(ns); }
 
 }  // extern "C"
