@@ -107,25 +107,44 @@ def describe(wl):
     return s
 
 
-def parse_traffic(kernel_name):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel source is unchanged since."""
+# The sources whose code a kernel family's DRAM traffic depends on: a traffic
+# record in profiles/ counts only while their digest is unchanged.
+KERNEL_SOURCES = {
+    "mhla_tcgen05": ["tc_mhla.cu"],
+    "mhla_tcgen05_stream": ["tc_stream.cu", "stream_sched.h"],
+    "causal_tcgen05": ["tc_causal.cu"],
+    "rala_tcgen05": ["tc_rala.cu"],
+}
+SHARED_SOURCES = ["tc_common.cuh", "common.cuh"]
+
+
+def parse_traffic(kernel_name, workload_name):
+    """DRAM bytes per call recorded from an ncu capture of this kernel family on this workload,
+    if the family's sources are unchanged since (else None)."""
     import glob
-    src = source_digest()
+    src = source_digest(kernel_name)
     for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
         text = open(path).read()
         m_k = re.search(r"^bench_kernel:\s*(\S+)", text, re.M)
+        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
         m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
         m_s = re.search(r"^source_sha256:\s*([0-9a-f]+)", text, re.M)
-        if m_k and m_t and m_s and m_k.group(1) == kernel_name and m_s.group(1) == src:
+        if (m_k and m_w and m_t and m_s and m_k.group(1) == kernel_name and m_w.group(1) == workload_name
+                and m_s.group(1) == src):
             return float(m_t.group(1))
     return None
 
 
-def source_digest():
+def source_digest(kernel_name):
+    """sha256 (16 hex digits) of the sources of one kernel family (unknown families: all of csrc)."""
     import glob
+    csrc = os.path.join(ROOT, "token_level_head_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel_name)
+    files = ([os.path.join(csrc, n) for n in names + SHARED_SOURCES] if names is not None
+             else sorted(glob.glob(os.path.join(csrc, "*"))))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "token_level_head_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for path in files:
+        with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -361,6 +380,127 @@ def capture(torch, runner, steps, first, with_events):
 
 
 # ------------------------------------------------------------ our arm
+def kernel_path(binding, wl):
+    import torch
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    if wl.kind == "rala":
+        return binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
+    if wl.kind == "decode":
+        return "simt"
+    return binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
+
+
+def time_steps(torch, binding, runner, steps, warmup, world=1, sampler=None):
+    """W eager + graph warm-up steps, then `steps` timed steps (CUDA graphs, events on the
+    launching stream).  Returns (elapsed ms of the timed region, mean per-step ms from events
+    inside the graph or None, kernels per step, wall-clock window)."""
+    import torch.distributed as dist
+    for i in range(max(1, warmup)):
+        runner.step(i)
+    torch.cuda.synchronize()
+    launches0 = binding.mhla_launch_count()
+    chunk = min(steps, 64 * runner.R)
+    chunk -= chunk % runner.R if chunk >= runner.R else 0
+    chunk = max(chunk, 1)
+    g, events = capture(torch, runner, chunk, 0, True)
+    per_step_kernels = (binding.mhla_launch_count() - launches0) / chunk
+    rem = steps % chunk
+    g_rem = capture(torch, runner, rem, 0, False)[0] if rem else None
+    n_chunks = steps // chunk
+    g_warm = capture(torch, runner, max(warmup, 1), 0, False)[0]
+    torch.cuda.synchronize()
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record()
+    for _ in range(n_chunks):
+        g.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    if sampler is not None:
+        time.sleep(0.2)
+        sampler.stop()
+    step_ms = None
+    if events:
+        durs = [events[i].elapsed_time(events[i + 1]) for i in range(chunk)]
+        step_ms = sum(durs) / len(durs)
+    return start.elapsed_time(end), step_ms, per_step_kernels, (t0, t1)
+
+
+def parity_of_timed_output(runner, n_slices=4):
+    """The timed output of one rotating set (after the graph replays: no den_out, the shared
+    workspace) against the float64 oracle on sampled slices: max slice-relative error."""
+    import numpy as np
+    import oracle
+    import workloads
+    wl = runner.wl
+    s = runner.sets[min(1, runner.R - 1)]
+    if wl.kind in ("mhla", "causal"):
+        units = wl.B * wl.H
+        pick = sorted({0, units - 1} | {(units * i) // n_slices for i in range(n_slices)})[:n_slices]
+        heads = [(u // wl.H, u % wl.H) for u in pick]
+        x = workloads.mhla_host(wl, heads=heads)
+        if wl.kind == "mhla":
+            ref, _ = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
+        else:
+            ref, _ = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)
+        got = np.stack([s["y"][b, h].float().cpu().numpy() for b, h in heads]).astype(np.float64)
+        ref = ref[0]
+        desc = f"{len(heads)} of {units} (batch, head) slices"
+    elif wl.kind == "rala":
+        batches = [0, wl.B - 1][:n_slices]
+        host = workloads.rala_host(wl, batches)
+        ref = oracle.rala_forward(host["q64"], host["k64"], host["v64"], host["x64"], host["w64"])
+        got = s["y"][batches].float().cpu().numpy().astype(np.float64)
+        ref = ref.reshape(len(batches) * wl.H, wl.N, wl.d)
+        got = got.reshape(len(batches) * wl.H, wl.N, wl.d)
+        desc = f"{len(batches)} of {wl.B} samples"
+    else:
+        return None
+    err = np.abs(got - ref).reshape(len(got), -1).max(1) / np.abs(ref).reshape(len(ref), -1).max(1)
+    tol = 2e-2 if wl.dtype == "bf16" else 1e-4
+    return {"max_slice_rel_err": float(err.max()), "tol": tol, "ok": bool(err.max() <= tol),
+            "sample": f"{desc}, timed output (no den_out, reused workspace, graph replay)"}
+
+
+def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
+    """value, launch time and roofline of one more workload (one GPU, no e2e or CPU baseline)."""
+    runner = Runner(wl, device, l2, sets)
+    elapsed_ms, step_ms, kernels, _ = time_steps(torch, binding, runner, steps, warmup)
+    alg = workload_bytes(wl)
+    peak, _ = hbm_peak()
+    kernel_ms = step_ms if step_ms is not None else elapsed_ms / steps
+    achieved = alg / (kernel_ms / 1e3) / 1e9
+    path = kernel_path(binding, wl)
+    kname = f"{wl.kind}_{path}"
+    out = {"workload": describe(wl), "value": tokens_per_step(wl) * steps / (elapsed_ms / 1e3),
+           "unit": "tokens/s" if wl.kind != "decode" else "units/s", "steps": steps,
+           "ms_per_step": elapsed_ms / steps, "launch_ms": kernel_ms, "kernels_per_step": kernels,
+           "path": path, "alg_bytes": alg, "achieved_GBps": achieved, "roofline_frac": achieved / peak,
+           "traffic": parse_traffic(kname, wl.name), "kernel": kname}
+    if wl.kind == "decode":
+        out["note"] = ("effective bandwidth: the 68 MB recurrent state may stay in L2 from one step to "
+                       "the next, so this is not a DRAM figure")
+    else:
+        out["parity"] = parity_of_timed_output(runner, n_slices=2)
+    del runner
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -378,54 +518,11 @@ def run_ours(args, wl, rank, world, local_rank):
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     runner = Runner(wl, device, l2, args.sets)
 
-    # eager warm-up (lazy initialisation), then capture
-    for i in range(max(1, args.warmup)):
-        runner.step(i)
-    torch.cuda.synchronize()
-    launches0 = binding.mhla_launch_count()
-    chunk = min(args.steps, 64 * runner.R)
-    chunk -= chunk % runner.R if chunk >= runner.R else 0
-    chunk = max(chunk, 1)
-    g, events = capture(torch, runner, chunk, 0, True)
-    per_step_kernels = (binding.mhla_launch_count() - launches0) / chunk
-    rem = args.steps % chunk
-    g_rem = capture(torch, runner, rem, 0, False)[0] if rem else None
-    n_chunks = args.steps // chunk
-    g_warm = capture(torch, runner, max(args.warmup, 1), 0, False)[0]
-    torch.cuda.synchronize()
-
-    g_warm.replay()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank)
-    if rank == 0:
-        sampler.start()
-        time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    start.record()
-    for _ in range(n_chunks):
-        g.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    end.record()
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if rank == 0:
-        time.sleep(0.2)
-        sampler.stop()
-    step_ms = None
-    if events:
-        durs = [events[i].elapsed_time(events[i + 1]) for i in range(chunk)]
-        step_ms = sum(durs) / len(durs)
-
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    elapsed_ms, step_ms, per_step_kernels, (t_wall0, t_wall1) = time_steps(
+        torch, binding, runner, args.steps, args.warmup, world, sampler)
     elapsed_ms = max_over_ranks(elapsed_ms, world, device)
+    parity = parity_of_timed_output(runner) if rank == 0 else None
 
     # end to end through host buffers
     e2e = None
@@ -451,13 +548,7 @@ def run_ours(args, wl, rank, world, local_rank):
     peak, peak_src = hbm_peak()
     kernel_ms = step_ms if step_ms is not None else elapsed_ms / args.steps
     achieved = alg / (kernel_ms / 1e3) / 1e9
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-    if wl.kind == "rala":
-        path = binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
-    elif wl.kind == "decode":
-        path = "simt"
-    else:
-        path = binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
+    path = kernel_path(binding, wl)
     kernel_name = f"{wl.kind}_{path}"
     value = job_value(tokens_per_step(wl), args.steps, world, elapsed_ms)
     line = {
@@ -480,18 +571,38 @@ def run_ours(args, wl, rank, world, local_rank):
                    "timing": "CUDA graphs, CUDA events on the launching stream",
                    "path": path},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": parse_traffic(kernel_name),
+                     "frac": achieved / peak, "traffic": parse_traffic(kernel_name, wl.name),
                      "kernel": kernel_name, "kernels_per_step": per_step_kernels,
                      "alg_bytes_per_launch": alg, "launch_ms": kernel_ms, "peak_source": peak_src,
                      "frac_of_nominal_8TBps": achieved / 8000.0},
         "gpu_launches": int(round(per_step_kernels * args.steps)),
         "clocks": sampler.summary(t_wall0, t_wall1),
+        "parity": parity,
     }
     if e2e is not None:
         line["e2e"] = e2e
+    # the other workloads of the pages (one GPU): rooflines and launch times beside the metric's
+    if world == 1 and not args.no_workloads:
+        del runner
+        torch.cuda.empty_cache()
+        extra = {}
+        for name in ("hires", "hires_m1", "causal", "rala", "decode"):
+            if name == wl.name:
+                continue
+            try:
+                extra[name] = workload_line(torch, binding, workloads_mod().WORKLOADS[name], device, l2,
+                                            min(args.steps, 200), args.warmup)
+            except Exception as e:  # report, do not lose the metric line
+                extra[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+        line["workloads"] = extra
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     return line
+
+
+def workloads_mod():
+    import workloads
+    return workloads
 
 
 # ------------------------------------------------------ oracle (CPU) arm
@@ -527,30 +638,69 @@ def _default_sample_units(wl):
     return {"mhla": max(1, min(wl.B * wl.H, 8)), "causal": 2, "decode": 256, "rala": 2}[wl.kind]
 
 
+def _cpu_work(args):
+    """One CPU-baseline worker: runs the oracle sample repeatedly for `seconds`."""
+    name, n_units, seconds = args
+    import workloads
+    wl = workloads.WORKLOADS[name]
+    fn, tokens, desc = _oracle_sample(wl, n_units)
+    fn()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        fn()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            break
+    return n * tokens, dt, desc
+
+
+_CPU_WORKER = r"""
+import json, sys
+sys.path.insert(0, %(root)r)
+from bench import _cpu_work
+
+if __name__ == "__main__":
+    import multiprocessing as mp
+    name, n_units, seconds, procs = sys.argv[1], int(sys.argv[2]), float(sys.argv[3]), int(sys.argv[4])
+    if procs == 1:
+        res = [_cpu_work((name, n_units, seconds))]
+    else:
+        with mp.get_context("spawn").Pool(procs) as pool:
+            res = pool.map(_cpu_work, [(name, n_units, seconds)] * procs)
+    tokens = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    print(json.dumps({"value": tokens / wall, "seconds": wall, "procs": procs, "desc": res[0][2]}))
+"""
+
+
 def cpu_baseline(wl, budget_s=10.0, n_units=None):
-    """The oracle as it stands, single-threaded, on a bounded sample, repeated for ~budget_s seconds."""
-    code = (
-        "import json, sys, time; sys.path.insert(0, %r)\n"
-        "import bench, workloads\n"
-        "wl = workloads.WORKLOADS[%r]\n"
-        "fn, tokens, desc = bench._oracle_sample(wl, %d)\n"
-        "fn()\n"
-        "t0 = time.perf_counter(); n = 0\n"
-        "while True:\n"
-        "    fn(); n += 1\n"
-        "    if time.perf_counter() - t0 >= %f: break\n"
-        "dt = time.perf_counter() - t0\n"
-        "print(json.dumps({'value': n * tokens / dt, 'reps': n, 'seconds': dt, 'desc': desc}))\n"
-    ) % (ROOT, wl.name, n_units or _default_sample_units(wl), budget_s)
+    """The oracle as it stands, on a bounded sample of the workload, timed on this host's cores:
+    one spawned process per core (one BLAS thread each) running the sample side by side over
+    independent slices, and one thread alone.  ``cores`` = the processes of the first figure."""
+    cores = os.cpu_count() or 1
+    n_units = n_units or _default_sample_units(wl)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
-    if res.returncode != 0:
-        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                "sample": f"failed: {res.stderr.strip()[-300:]}"}
-    r = json.loads(res.stdout.strip().splitlines()[-1])
-    return {"value": r["value"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{r['desc']}; float64 numpy oracle, 1 thread, {r['reps']} reps in {r['seconds']:.1f} s"}
+    code = _CPU_WORKER % {"root": ROOT}
+    out = {}
+    for procs in (cores, 1):
+        res = subprocess.run([sys.executable, "-c", code, wl.name, str(n_units), str(budget_s / 2), str(procs)],
+                             capture_output=True, text=True, env=env, timeout=300)
+        if res.returncode != 0:
+            out[procs] = {"error": res.stderr.strip()[-300:]}
+        else:
+            out[procs] = json.loads(res.stdout.strip().splitlines()[-1])
+    allc, one = out[cores], out[1]
+    if "error" in allc:
+        return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"failed: {allc['error']}"}
+    return {"value": allc["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{allc['desc']}, per process; float64 numpy oracle, {cores} processes x 1 thread, "
+                      f"{allc['seconds']:.1f} s",
+            "host_cpus": cores,
+            "single_thread": {"value": one.get("value"), "cores": 1}}
 
 
 def run_reference(args, wl, rank):
@@ -601,6 +751,8 @@ def main(argv=None):
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other workloads' roofline lines (the metric line only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--sets", type=int, default=0,
                    help="rotating input sets (default: enough to exceed 3x L2); 1 for small profiler captures")

@@ -23,10 +23,12 @@
  *     in/out, fp32 accumulation; summaries, normalisers and decode state are
  *     fp32).  Outputs have the input dtype.
  *   - Every pointer is a DEVICE pointer unless stated otherwise, 16-byte
- *     aligned; the caller owns all memory, including the workspace.  The
- *     library allocates nothing and keeps no per-call state outside the
- *     workspace; calls are asynchronous on `stream` (a cudaStream_t, 0 = the
- *     legacy default stream) and do not synchronise the host.
+ *     aligned; the caller owns all memory, including the workspace.  No call
+ *     allocates memory (the one device-resident buffer of the library is the
+ *     fixed scratch array of mhla_forward_noalloc, below) and no call keeps
+ *     per-call state outside the workspace; calls are asynchronous on `stream`
+ *     (a cudaStream_t, 0 = the legacy default stream) and do not synchronise
+ *     the host.
  *   - Argument errors are detected on the host before any launch and return
  *     MHLA_ERR_INVALID_ARG (or MHLA_ERR_UNSUPPORTED for valid but
  *     unimplemented combinations) without touching device memory.  Launch
@@ -61,8 +63,17 @@ typedef enum {
 
 typedef enum { MHLA_F32 = 0, MHLA_BF16 = 1 } mhla_dtype;
 
-/* Which kernel family mhla_forward / mhla_forward_causal would run. */
-typedef enum { MHLA_PATH_NONE = 0, MHLA_PATH_SIMT = 1, MHLA_PATH_TCGEN05 = 2 } mhla_path;
+/* Which kernel family mhla_forward / mhla_forward_causal would run:
+ * TCGEN05 the three-pass tensor-core kernel (summaries, grid-wide mixing,
+ * output), TCGEN05_STREAM the tensor-core kernel that runs them as one stream
+ * of work items with per-head readiness (bf16, d = 64, N / 128 not a multiple
+ * of 16). */
+typedef enum {
+  MHLA_PATH_NONE = 0,
+  MHLA_PATH_SIMT = 1,
+  MHLA_PATH_TCGEN05 = 2,
+  MHLA_PATH_TCGEN05_STREAM = 3
+} mhla_path;
 
 /* Workspace bytes for mhla_forward (causal = 0) or mhla_forward_causal
  * (causal = 1, block_size = chunk) with these sizes; 0 if the sizes are
@@ -151,7 +162,12 @@ mhla_path rala_forward_path(int B, int H, int N, int d, int cx, mhla_dtype dt);
  * fixed memory pool).  The result is that of mhla_forward(..., causal = 0,
  * ...) computed by the SIMT kernels; all arguments mean the same.
  *   Scratch: a file-scope device array of MHLA_NOALLOC_SCRATCH_BYTES per GPU,
- *   reserved when the library is loaded and held until the process exits.
+ *   held until the process exits.  The CUDA runtime reserves it when it loads
+ *   the library's device code on that GPU: with the default lazy module
+ *   loading (CUDA_MODULE_LOADING=LAZY) that is the first call of this entry
+ *   point on the device, which can therefore still fail for lack of device
+ *   memory; make one warm-up call at start-up, while memory is known to be
+ *   free (with CUDA_MODULE_LOADING=EAGER it happens at context creation).
  *   Sizes whose scratch need exceeds it return MHLA_ERR_UNSUPPORTED before
  *   any launch (the DiT-like B8 H6 N4096 d64 M16 case needs 25.2 MB).
  *   Set-up: the first call on each device looks up the array's device address

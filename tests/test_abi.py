@@ -136,3 +136,32 @@ def test_query_status_rejects_null(lib):
 
 def test_launch_counter_starts_readable(lib):
     assert isinstance(binding.mhla_launch_count(), int)
+
+
+def test_binding_rejects_mismatched_tensors():
+    """Shape and dtype checks of the Python wrappers run before any device use (CPU tensors here)."""
+    import torch
+    q = torch.zeros(1, 2, 256, 64, dtype=torch.bfloat16)
+    ok_mix = torch.ones(2, 4, 4)
+    cases = [
+        dict(k=q[:, :1], msg="k: shape"),
+        dict(v=q.float(), msg="v: dtype"),
+        dict(y=torch.zeros(1, 2, 128, 64, dtype=torch.bfloat16), msg="y: shape"),
+        dict(mixing=torch.ones(2, 4, 4, dtype=torch.bfloat16), msg="mixing: dtype"),
+        dict(mixing=torch.ones(2, 2, 2), msg="mixing: shape"),
+        dict(den_out=torch.zeros(1, 2, 256, dtype=torch.float64), msg="den_out: dtype"),
+    ]
+    for c in cases:
+        args = dict(k=q, v=q, y=q.clone(), mixing=ok_mix, den_out=None)
+        msg = c.pop("msg")
+        args.update(c)
+        with pytest.raises(ValueError, match=msg):
+            binding.mhla_forward(q, args["k"], args["v"], args["mixing"], args["y"], 64, den_out=args["den_out"])
+    with pytest.raises(ValueError, match="CUDA"):  # consistent shapes, but not on a GPU
+        binding.mhla_forward(q, q, q, ok_mix, q.clone(), 64)
+    q3 = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="S: shape"):
+        binding.linattn_decode_step(q3, q3, q3, torch.zeros(2, 64, 64), torch.zeros(1, 2, 64), q3.clone())
+    with pytest.raises(ValueError, match="w: shape"):
+        binding.rala_forward(q, q, q, torch.zeros(1, 256, 64, dtype=torch.bfloat16),
+                             torch.zeros(64, 32, dtype=torch.bfloat16), q.clone())

@@ -31,27 +31,25 @@ def test_algorithmic_bytes_of_the_workloads():
 
 
 def test_traffic_record_needs_matching_sources(monkeypatch):
-    names = []
-    for path in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
-        text = open(os.path.join(ROOT, "profiles", path)).read()
-        for line in text.splitlines():
-            if line.startswith("bench_kernel:"):
-                names.append(line.split()[1])
-    assert names, "no profile names a bench kernel"
-    monkeypatch.setattr(bench, "source_digest", lambda: "0" * 16)
-    for n in names:
-        assert bench.parse_traffic(n) is None  # counters of other sources are not reported
-    real = {}
+    records = []
     for path in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
         text = open(os.path.join(ROOT, "profiles", path)).read()
         fields = dict(l.split(":", 1) for l in text.splitlines() if ":" in l and l.split(":")[0] in
-                      ("bench_kernel", "traffic_bytes_per_launch", "source_sha256"))
+                      ("bench_kernel", "workload", "traffic_bytes_per_launch", "source_sha256"))
         if "bench_kernel" in fields:
-            real[fields["bench_kernel"].strip()] = (float(fields["traffic_bytes_per_launch"]),
-                                                    fields["source_sha256"].strip())
-    for n, (traffic, digest) in real.items():
-        monkeypatch.setattr(bench, "source_digest", lambda d=digest: d)
-        assert bench.parse_traffic(n) == traffic
+            records.append((fields["bench_kernel"].strip(), fields["workload"].strip(),
+                            float(fields["traffic_bytes_per_launch"]), fields["source_sha256"].strip()))
+    assert records, "no profile names a bench kernel"
+    monkeypatch.setattr(bench, "source_digest", lambda *a: "0" * 16)
+    for kname, wname, _, _ in records:
+        assert bench.parse_traffic(kname, wname) is None  # counters of other sources are not reported
+    for kname, wname, traffic, digest in records:
+        monkeypatch.setattr(bench, "source_digest", lambda *a, d=digest: d)
+        assert bench.parse_traffic(kname, wname) == traffic
+        assert bench.parse_traffic(kname, "no-such-workload") is None
+    # each record is keyed on its own family's sources
+    monkeypatch.undo()
+    assert bench.source_digest("mhla_tcgen05") != bench.source_digest("causal_tcgen05")
 
 
 def test_hbm_peak_is_positive():

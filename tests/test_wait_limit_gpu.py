@@ -31,7 +31,7 @@ def lib():
 
 def test_wait_limit_gives_up_then_next_call_is_correct():
     B, H, N, d, block = 2, 3, 1152, 64, 128  # C = 9 chunks a head: the stream kernel
-    assert binding.mhla_forward_path(B, H, N, d, block, 0, torch.bfloat16) == "tcgen05"
+    assert binding.mhla_forward_path(B, H, N, d, block, 0, torch.bfloat16) == "tcgen05_stream"
     x = rand_inputs(700, (B, H, N, d), "bf16")
     mix_t, mix64 = rand_mixing(31, H, N // block)
     ws = binding.new_workspace(binding.mhla_workspace_bytes(B, H, N, d, block), "cuda")

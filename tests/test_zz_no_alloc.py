@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_util import TOL_DEN, TOL_Y, rel, slice_rel, to_f64
 from token_level_head_gb300 import binding
 from token_level_head_gb300.build import build_library
@@ -65,8 +66,27 @@ def test_noalloc_matches_mhla_forward_twice_in_a_row():
         assert np.all(np.isfinite(y))
         assert slice_rel(y, y_ref) <= TOL_Y["bf16"]
         assert rel(den, d_ref) <= TOL_DEN["bf16"]
+    # fp32: mhla_forward runs the same kernels here, so the oracle checks it directly
     small = _inputs(7, (2, 3, 192, 16), torch.float32, 64)
+    ref, dref = oracle.mhla_block_form(*(to_f64(small[n]) for n in ("q", "k", "v", "mixing")), 64)
     for _ in range(2):
         y, den, y_ref, d_ref = _both(small, 64)
         assert slice_rel(y, y_ref) <= TOL_Y["f32"]
         assert rel(den, d_ref) <= TOL_DEN["f32"]
+        assert slice_rel(y, ref) <= TOL_Y["f32"]
+        assert rel(den, dref) <= TOL_DEN["f32"]
+
+
+@pytest.mark.gpu
+def test_noalloc_small_call_after_large_call_sees_no_leftovers():
+    """The scratch keeps the last call's contents; a smaller call after a larger one must not read them."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build_library()
+    big = _inputs(11, (4, 6, 2048, 64), torch.bfloat16, 128)
+    _both(big, 128)
+    small = _inputs(12, (1, 2, 512, 64), torch.bfloat16, 256)
+    y, den, _, _ = _both(small, 256)
+    ref, dref = oracle.mhla_block_form(*(to_f64(small[n]) for n in ("q", "k", "v", "mixing")), 256)
+    assert slice_rel(y, ref) <= TOL_Y["bf16"]
+    assert rel(den, dref) <= TOL_DEN["bf16"]

@@ -18,7 +18,7 @@ from .build import LIB_PATH
 
 MHLA_OK, MHLA_ERR_INVALID_ARG, MHLA_ERR_UNSUPPORTED, MHLA_ERR_CUDA, MHLA_ERR_TIMEOUT = range(5)
 MHLA_F32, MHLA_BF16 = 0, 1
-PATH_NAMES = {0: "none", 1: "simt", 2: "tcgen05"}
+PATH_NAMES = {0: "none", 1: "simt", 2: "tcgen05", 3: "tcgen05_stream"}
 
 _lib = None
 
@@ -84,8 +84,8 @@ def _dtype(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream, device=None):
+    s = torch.cuda.current_stream(device) if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -93,6 +93,40 @@ def _need_cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _expect(t, name, shape, dtype):
+    """Raises ValueError unless tensor ``t`` has this shape and dtype (checked before any device use)."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+
+
+def _same_device(q, *ts):
+    """All tensors contiguous on q's CUDA device; returns that device."""
+    _need_cuda(q, *ts)
+    for t in ts:
+        if t is not None and t.device != q.device:
+            raise ValueError(f"tensor on {t.device}, expected {q.device} (the device of q)")
+    return q.device
+
+
+def _mhla_args(q, k, v, mixing, y, den_out, block, mixing_required=True):
+    if q.dim() != 4:
+        raise ValueError(f"q: expected [B, H, N, d], got shape {tuple(q.shape)}")
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("y", y)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(den_out, "den_out", (B, H, N), torch.float32)
+    if mixing is None:
+        if mixing_required:
+            raise ValueError("mixing: required")
+    elif block > 0 and N % block == 0:
+        _expect(mixing, "mixing", (H, N // block, N // block), torch.float32)
+    return B, H, N, d
 
 
 def mhla_workspace_bytes(B: int, H: int, N: int, d: int, block_size: int, causal: int = 0) -> int:
@@ -118,16 +152,21 @@ def rala_forward_path(B, H, N, d, cx, dtype) -> str:
     return PATH_NAMES[int(load().rala_forward_path(B, H, N, d, cx, dt))]
 
 
+# Every wrapper checks shapes and dtypes against q, then that every tensor is a
+# contiguous CUDA tensor on q's device, and runs the call with q's device
+# current (the library takes its device from the current device).
+
 def mhla_forward(q, k, v, mixing, y, block_size, *, causal=0, eps=1e-6, den_out=None,
                  workspace=None, stream=None):
     """Non-causal (or, with causal=1, causal) MHLA forward; q/k/v/y [B, H, N, d], mixing [H, M, M] fp32."""
-    _need_cuda(q, k, v, mixing, y, den_out, workspace)
-    B, H, N, d = q.shape
-    if workspace is None:
-        workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, block_size, causal), q.device)
-    st = load().mhla_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
-                             B, H, N, d, block_size, causal, _dtype(q), eps, _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream(stream))
+    B, H, N, d = _mhla_args(q, k, v, mixing, y, den_out, block_size, mixing_required=not causal)
+    dev = _same_device(q, k, v, mixing, y, den_out, workspace)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, block_size, causal), dev)
+        st = load().mhla_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                 B, H, N, d, block_size, causal, _dtype(q), eps, _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward", st)
     return y
 
@@ -135,37 +174,53 @@ def mhla_forward(q, k, v, mixing, y, block_size, *, causal=0, eps=1e-6, den_out=
 def mhla_forward_causal(q, k, v, mixing, y, chunk, *, eps=1e-6, den_out=None, workspace=None,
                         stream=None):
     """Causal chunked forward; mixing None = plain causal linear attention."""
-    _need_cuda(q, k, v, mixing, y, den_out, workspace)
-    B, H, N, d = q.shape
-    if workspace is None:
-        workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, chunk, 1), q.device)
-    st = load().mhla_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
-                                    B, H, N, d, chunk, _dtype(q), eps, _ptr(workspace),
-                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    B, H, N, d = _mhla_args(q, k, v, mixing, y, den_out, chunk, mixing_required=False)
+    dev = _same_device(q, k, v, mixing, y, den_out, workspace)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, chunk, 1), dev)
+        st = load().mhla_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                        B, H, N, d, chunk, _dtype(q), eps, _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward_causal", st)
     return y
 
 
 def linattn_decode_step(q, k, v, S, z, out, *, eps=1e-6, den_out=None, stream=None):
     """One recurrent decode step; q/k/v/out [B, H, d], S [B, H, d, d] fp32, z [B, H, d] fp32 (updated)."""
-    _need_cuda(q, k, v, S, z, out, den_out)
+    if q.dim() != 3:
+        raise ValueError(f"q: expected [B, H, d], got shape {tuple(q.shape)}")
     B, H, d = q.shape
-    st = load().linattn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out),
-                                    _ptr(den_out), B, H, d, _dtype(q), eps, _stream(stream))
+    for name, t in (("k", k), ("v", v), ("out", out)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(S, "S", (B, H, d, d), torch.float32)
+    _expect(z, "z", (B, H, d), torch.float32)
+    _expect(den_out, "den_out", (B, H), torch.float32)
+    dev = _same_device(q, k, v, S, z, out, den_out)
+    with torch.cuda.device(dev):
+        st = load().linattn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out),
+                                        _ptr(den_out), B, H, d, _dtype(q), eps, _stream(stream, dev))
     _check("linattn_decode_step", st)
     return out
 
 
 def rala_forward(q, k, v, x, w, y, *, workspace=None, stream=None):
     """Rank-augmented linear attention; q/k/v/y [B, H, N, d], x [B, N, cx], w [cx, d]."""
-    _need_cuda(q, k, v, x, w, y, workspace)
+    if q.dim() != 4 or x.dim() != 3:
+        raise ValueError("q: expected [B, H, N, d]; x: expected [B, N, cx]")
     B, H, N, d = q.shape
     cx = x.shape[-1]
-    if workspace is None:
-        workspace = new_workspace(rala_workspace_bytes(B, H, N, d, cx), q.device)
-    st = load().rala_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(x), _ptr(w), _ptr(y), B, H, N, d, cx,
-                             _dtype(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                             _stream(stream))
+    for name, t in (("k", k), ("v", v), ("y", y)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(x, "x", (B, N, cx), q.dtype)
+    _expect(w, "w", (cx, d), q.dtype)
+    dev = _same_device(q, k, v, x, w, y, workspace)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(rala_workspace_bytes(B, H, N, d, cx), dev)
+        st = load().rala_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(x), _ptr(w), _ptr(y), B, H, N, d, cx,
+                                 _dtype(q), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream, dev))
     _check("rala_forward", st)
     return y
 
@@ -176,16 +231,18 @@ def mhla_forward_noalloc(q, k, v, mixing, y, block_size, *, eps=1e-6, den_out=No
     The library keeps a fixed 32 MiB scratch array per GPU for it; calls that
     overlap on the GPU share that array and must not run concurrently.
     """
-    _need_cuda(q, k, v, mixing, y, den_out)
-    B, H, N, d = q.shape
-    st = load().mhla_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
-                                     B, H, N, d, block_size, _dtype(q), eps, _stream(stream))
+    B, H, N, d = _mhla_args(q, k, v, mixing, y, den_out, block_size)
+    dev = _same_device(q, k, v, mixing, y, den_out)
+    with torch.cuda.device(dev):
+        st = load().mhla_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                         B, H, N, d, block_size, _dtype(q), eps, _stream(stream, dev))
     _check("mhla_forward_noalloc", st)
     return y
 
 
 def mhla_query_status(workspace, stream=None) -> int:
-    return int(load().mhla_query_status(_ptr(workspace), _stream(stream)))
+    with torch.cuda.device(workspace.device):
+        return int(load().mhla_query_status(_ptr(workspace), _stream(stream, workspace.device)))
 
 
 def mhla_launch_count() -> int:

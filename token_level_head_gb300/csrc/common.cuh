@@ -5,9 +5,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "mhla.h"
 
 namespace mhla {
+
+// The opt-in dynamic shared memory size of a kernel, set on each device the
+// first time the kernel is launched there (cudaFuncSetAttribute is per device;
+// the first call of a process may run on any device and from any host thread).
+class SmemOptIn {
+ public:
+  cudaError_t ensure(const void* fn, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu_);
+    if (dev < 64 && ((done_ >> dev) & 1ull)) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev < 64) done_ |= 1ull << dev;
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  unsigned long long done_ = 0;  // a bit per device
+};
 
 // phi(x) = ELU(x) + 1: x + 1 for x > 0, exp(x) otherwise
 // ("Linear Attention notes" §二, first kernel choice).

@@ -86,9 +86,9 @@ mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int caus
       (dt != MHLA_F32 && dt != MHLA_BF16) || (causal != 0 && causal != 1))
     return MHLA_PATH_NONE;
   const MhlaShape s{B, H, N, d, block_size};
-  const bool tc = causal ? tc_causal_supported(s, dt, MIX_PREFIX)
-                         : (tc_stream_supported(s, dt, MIX_FULL) || tc_mhla_supported(s, dt, MIX_FULL));
-  return tc ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+  if (causal) return tc_causal_supported(s, dt, MIX_PREFIX) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+  if (tc_stream_supported(s, dt, MIX_FULL)) return MHLA_PATH_TCGEN05_STREAM;
+  return tc_mhla_supported(s, dt, MIX_FULL) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
 
 static mhla_status run_mhla(const void* q, const void* k, const void* v, const float* mixing,

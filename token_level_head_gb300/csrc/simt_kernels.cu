@@ -259,13 +259,9 @@ cudaError_t mhla_launch_t(const MhlaShape& s, const SimtPlan& pl, const void* q,
   note_launch();
   const int tile = divisor_at_most(s.block, kOutTile);
   const size_t smem = out_smem_bytes(D);
-  static bool attr_done = false;  // set once (outside any graph capture: the first call is eager)
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(simt_out_kernel<T, D>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    attr_done = true;
-  }
+  static SmemOptIn opt_in;  // the first call on a device is eager (outside any graph capture)
+  if (cudaError_t err = opt_in.ensure((const void*)simt_out_kernel<T, D>, (int)smem); err != cudaSuccess)
+    return err;
   const int intra = mode == MIX_FULL ? 0 : (mode == MIX_STRICT_LOWER ? 1 : 2);
   simt_out_kernel<T, D><<<dim3(s.N / tile, heads), kThreads, smem, st>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), s_mix, z_mix,
@@ -521,14 +517,10 @@ cudaError_t rala_t(int B, int H, int N, int cx, const void* q, const void* k, co
       bpart, mpart, spart, bkv, pl.ntiles, D);
   note_launch();
   const size_t smem = sizeof(float) * ((size_t)cx * D + (size_t)D * D);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t err = cudaFuncSetAttribute(rala_out_kernel<T, D>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)(sizeof(float) * (256 * D + D * D)));
-    if (err != cudaSuccess) return err;
-    attr_done = true;
-  }
+  static SmemOptIn opt_in;
+  if (cudaError_t err = opt_in.ensure((const void*)rala_out_kernel<T, D>, (int)(sizeof(float) * (256 * D + D * D)));
+      err != cudaSuccess)
+    return err;
   rala_out_kernel<T, D><<<dim3((N + kTokTile - 1) / kTokTile, heads), kThreads, smem, st>>>(
       static_cast<const T*>(q), static_cast<const T*>(x), static_cast<const T*>(w), bkv,
       static_cast<T*>(y), H, N, cx);

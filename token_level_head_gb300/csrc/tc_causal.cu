@@ -828,14 +828,10 @@ cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, c
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   p.G = std::min(max_ctas(s), sms);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(causal_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(causal_agg_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAggSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static SmemOptIn opt_out, opt_agg;
+  cudaError_t e = opt_out.ensure((const void*)causal_out_kernel, (int)kOutSmem);
+  if (e == cudaSuccess) e = opt_agg.ensure((const void*)causal_agg_kernel, (int)kAggSmem);
+  if (e != cudaSuccess) return e;
   if (p.CH > 1) {  // with one chunk per head no segment starts inside a head
     causal_agg_kernel<<<p.G, kThreads, kAggSmem, st>>>(p);
     note_launch();

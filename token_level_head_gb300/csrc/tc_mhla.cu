@@ -1395,13 +1395,9 @@ int sm_count() {
 
 template <int MAXM>
 cudaError_t launch_t(const Params& p, int grid, cudaStream_t st) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(mhla_tc_kernel<MAXM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Layout<MAXM>::kBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static SmemOptIn opt_in;
+  if (cudaError_t e = opt_in.ensure((const void*)mhla_tc_kernel<MAXM>, (int)Layout<MAXM>::kBytes); e != cudaSuccess)
+    return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);

@@ -693,14 +693,10 @@ cudaError_t tc_rala_launch(int B, int H, int N, const void* q, const void* k, co
   p.tiles = B * p.TPB;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(rala_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(rala_out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOSmem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static SmemOptIn opt_b, opt_out;
+  cudaError_t e = opt_b.ensure((const void*)rala_b_kernel, (int)kBSmem);
+  if (e == cudaSuccess) e = opt_out.ensure((const void*)rala_out_kernel, (int)kOSmem);
+  if (e != cudaSuccess) return e;
   rala_qsum_kernel<<<dim3(kSlices, U), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(q), p.qpart, NP);
   rala_b_kernel<<<U, kThreads, kBSmem, st>>>(p);
   rala_out_kernel<<<std::min(p.tiles, sms), kThreads, kOSmem, st>>>(p);

@@ -834,20 +834,8 @@ cudaError_t tc_stream_launch(const MhlaShape& s, const void* q, const void* k, c
   p.wait_ns = g_wait_ns;
   p.eps = eps;
 
-  // the opt-in shared memory size, once per device
-  static std::mutex mu;
-  static unsigned long long attr_set = 0;  // bit per device
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    if (dev < 64 && !(attr_set >> dev & 1ull)) {
-      e = cudaFuncSetAttribute(mhla_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-      if (e != cudaSuccess) return e;
-      attr_set |= 1ull << dev;
-    } else if (dev >= 64) {
-      e = cudaFuncSetAttribute(mhla_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-      if (e != cudaSuccess) return e;
-    }
-  }
+  static SmemOptIn opt_in;
+  if ((e = opt_in.ensure((const void*)mhla_stream_kernel, kSmemLimit)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
