@@ -37,6 +37,13 @@ from .mhla_oracle import (  # noqa: F401
     causal_mhla_chunked,
     causal_mhla_bruteforce,
     decode_steps,
+    decayed_causal_bruteforce,
+    mhla_block_form_unnormalized,
+    grid_block_ids,
+    mhla_block_form_ids,
+    mhla_token_expansion_ids,
+    locality_mixing_init,
+    causal_mhla_stream,
     rala_forward,
     rala_bruteforce,
     numerical_rank,

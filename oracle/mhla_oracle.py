@@ -39,7 +39,17 @@ PIN_STATUS = {
     "causal_bruteforce": "hand-derived golden fixture; last row equals non-causal global LA",
     "causal_mhla_chunked": "equals its masked brute force; all-ones mixing equals causal LA",
     "causal_mhla_bruteforce": "all-ones mixing equals causal_bruteforce; golden fixture",
-    "decode_steps": "equals rows of the causal forward on prefix+steps; final state = sum phi(k) v^T",
+    "decode_steps": "equals rows of the causal forward on prefix+steps; final state = sum phi(k) v^T; "
+                    "with decay: equals decayed_causal_bruteforce",
+    "decayed_causal_bruteforce": "gamma = 1 equals causal_bruteforce; gamma = 0 keeps only the token itself "
+                                 "(out = v); hand-computed two-token value",
+    "mhla_block_form_unnormalized": "equals the brute-force sum without the division; Y * den of the block form",
+    "grid_block_ids": "hand-listed ids of a 4 x 4 grid in 2 x 2 tiles",
+    "mhla_block_form_ids": "equals its token expansion; contiguous ids equal mhla_block_form; "
+                           "equals the block form of the tile-permuted tokens",
+    "mhla_token_expansion_ids": "equals mhla_token_expansion for contiguous ids",
+    "locality_mixing_init": "hand-computed 1 x 3 and 2 x 2 grids; rows sum to 1, diagonal largest",
+    "causal_mhla_stream": "equals causal_mhla_bruteforce; all-ones mixing equals causal linear attention",
     "rala_forward": "brute form; closed forms at Q=0 and K=0; softmax weights sum to 1",
     "rala_bruteforce": "closed forms at Q=0 and K=0; hand-derived golden fixture",
     "numerical_rank": "diagonal matrices of known rank",
@@ -287,14 +297,16 @@ def causal_mhla_bruteforce(q, k, v, mixing, block_size, eps=1e-6):
     return y, den
 
 
-def decode_steps(s0, z0, qs, ks, vs, eps=1e-6):
+def decode_steps(s0, z0, qs, ks, vs, eps=1e-6, gamma=1.0):
     """Recurrent decode: T single-token steps from state (S, z).
 
     Linear Attention notes §四 (and §八: the state is a fixed-size d x d
     "KV cache"): per step S <- S + phi(k) v^T, z <- z + phi(k), then
-    out = phi(q)^T S / (phi(q)^T z + eps).  ``s0``: [..., d, d] with
-    S[c, e] = sum phi(k)_c v_e; ``z0``: [..., d]; ``qs, ks, vs``: [T, ..., d].
-    Returns ``(outs [T, ..., d], dens [T, ...], S_T, z_T)``.
+    out = phi(q)^T S / (phi(q)^T z + eps).  With ``gamma`` the RetNet decay of
+    the notes' §七, S <- gamma S + phi(k) v^T; the normaliser z decays the same
+    way (the notes write only S; the reading keeps out a weighted mean).
+    ``s0``: [..., d, d] with S[c, e] = sum phi(k)_c v_e; ``z0``: [..., d];
+    ``qs, ks, vs``: [T, ..., d].  Returns ``(outs [T, ..., d], dens [T, ...], S_T, z_T)``.
     """
     s, z = _f64(s0).copy(), _f64(z0).copy()
     qs, ks, vs = _f64(qs), _f64(ks), _f64(vs)
@@ -302,12 +314,37 @@ def decode_steps(s0, z0, qs, ks, vs, eps=1e-6):
     dens = np.empty(vs.shape[:-1])
     for t in range(qs.shape[0]):
         qt, kt = phi(qs[t]), phi(ks[t])
-        s = s + kt[..., :, None] * vs[t][..., None, :]
-        z = z + kt
+        s = gamma * s + kt[..., :, None] * vs[t][..., None, :]
+        z = gamma * z + kt
         dn = np.einsum("...c,...c->...", qt, z) + eps
         outs[t] = np.einsum("...c,...ce->...e", qt, s) / dn[..., None]
         dens[t] = dn
     return outs, dens, s, z
+
+
+def decayed_causal_bruteforce(q, k, v, gamma, eps=1e-6, s0=None, z0=None):
+    """Causal linear attention with RetNet decay from its explicit weights.  Returns ``(Y, den)``.
+
+    Linear Attention notes §七: unrolling S_t = gamma S_{t-1} + phi(k_t) v_t^T
+    from an initial state S_{-1} = s0 gives S_t = gamma^(t+1) s0 +
+    sum_{s<=t} gamma^(t-s) phi(k_s) v_s^T (z likewise); out_t = phi(q_t)^T S_t
+    / (phi(q_t)^T z_t + eps).  The score of query t on key s is
+    gamma^(t-s) phi(q_t)^T phi(k_s) for s <= t.  ``q, k, v``: [..., N, d];
+    ``s0, z0`` default to zero.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    *lead, n, d = q.shape
+    t = np.arange(n)
+    w = np.where(t[:, None] >= t[None, :], float(gamma) ** np.maximum(t[:, None] - t[None, :], 0), 0.0)
+    qf = phi(q)
+    a = np.einsum("...tc,...sc->...ts", qf, phi(k)) * w
+    num = np.einsum("...ts,...se->...te", a, v)
+    dn = a.sum(axis=-1) + eps
+    if s0 is not None:
+        g = float(gamma) ** (t + 1)
+        num = num + g[:, None] * np.einsum("...tc,...ce->...te", qf, _f64(s0))
+        dn = dn + g * np.einsum("...tc,...c->...t", qf, _f64(z0))
+    return num / dn[..., None], dn
 
 
 def _rala_weights(q1, k1):
@@ -362,6 +399,121 @@ def rala_bruteforce(q, k, v, x, w):
             scores = (phi(q[b, h]) @ phi(k[b, h]).T) * alpha[None, :]
             y[b, h] = gate * (scores @ v[b, h])
     return y
+
+
+def mhla_block_form_unnormalized(q, k, v, mixing, block_size):
+    """MHLA forward without the normaliser: Y_t = phi(q_t)^T S~_{b(t)}.
+
+    MHLA paper §4.1 ("the normalisation term can be omitted" for long
+    sequences in language and video models): the block form's numerator.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    m, mix = _check_blocks(n, block_size, mixing)
+    kb = phi(k).reshape(bsz, nh, m, block_size, d)
+    vb = v.reshape(bsz, nh, m, block_size, d)
+    s = np.einsum("bhmjc,bhmje->bhmce", kb, vb)
+    s_mix = np.einsum("hib,zhbce->zhice", mix, s)
+    qb = phi(q).reshape(bsz, nh, m, block_size, d)
+    return np.einsum("bhitc,bhice->bhite", qb, s_mix).reshape(bsz, nh, n, d)
+
+
+def grid_block_ids(grid_h, grid_w, tile_h, tile_w):
+    """b(t) for tokens on a grid_h x grid_w grid in row-major order, blocks the tile_h x
+    tile_w tiles, numbered row-major over the (grid_h / tile_h) x (grid_w / tile_w) tile grid.
+
+    MHLA paper §4.1: in vision models the blocks lie on 2-D (or 3-D) grids;
+    Fig. 4b shows M = 25 blocks as a 5 x 5 grid.
+    """
+    if grid_h % tile_h or grid_w % tile_w:
+        raise ValueError("the tiles must cover the grid")
+    r, c = np.divmod(np.arange(grid_h * grid_w), grid_w)
+    return (r // tile_h) * (grid_w // tile_w) + (c // tile_w)
+
+
+def mhla_block_form_ids(q, k, v, mixing, block_ids, eps=1e-6):
+    """MHLA forward with blocks given token by token (``block_ids[t]`` = b(t)).  Returns ``(Y, den)``.
+
+    MHLA paper §4.1 with blocks that need not be contiguous token ranges:
+    S_b = sum_{t: b(t)=b} phi(K_t) V_t^T, z_b = sum_{t: b(t)=b} phi(K_t),
+    S~_i = sum_b m_ib S_b, Y_t = phi(q_t)^T S~_{b(t)} / (phi(q_t)^T z~_{b(t)} + eps).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    ids = np.asarray(block_ids)
+    m = int(ids.max()) + 1
+    mix = _f64(mixing)
+    if mix.shape[-2:] != (m, m):
+        raise ValueError(f"mixing must be [H, {m}, {m}]")
+    onehot = (ids[None, :] == np.arange(m)[:, None]).astype(np.float64)  # [M, N]
+    kf = phi(k)
+    s = np.einsum("bt,zhtc,zhte->zhbce", onehot, kf, v)
+    z = np.einsum("bt,zhtc->zhbc", onehot, kf)
+    s_mix = np.einsum("hib,zhbce->zhice", mix, s)
+    z_mix = np.einsum("hib,zhbc->zhic", mix, z)
+    qf = phi(q)
+    num = np.einsum("zhtc,zhtce->zhte", qf, s_mix[:, :, ids])
+    den = np.einsum("zhtc,zhtc->zht", qf, z_mix[:, :, ids]) + eps
+    return num / den[..., None], den
+
+
+def mhla_token_expansion_ids(q, k, v, mixing, block_ids, eps=1e-6):
+    """Brute force of :func:`mhla_block_form_ids`: the N x N scores m_{b(t), b(s)}
+    phi(q_t)^T phi(k_s) (MHLA paper §4.2 eq. 5), Y_t = sum_s A_ts v_s / (sum_s A_ts + eps)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    ids = np.asarray(block_ids)
+    mix = _f64(mixing)
+    a = np.einsum("zhtc,zhsc->zhts", phi(q), phi(k)) * mix[:, ids[:, None], ids[None, :]][None]
+    den = a.sum(axis=-1) + eps
+    return np.einsum("zhts,zhse->zhte", a, v) / den[..., None], den
+
+
+def locality_mixing_init(blocks_h, blocks_w):
+    """Locality-based initial mixing matrix for blocks on a blocks_h x blocks_w grid.  [M, M].
+
+    MHLA paper §4.2: m^(0)_{i,j} proportional to 1 - dist(i, j) / max_k dist(i, k),
+    dist the Euclidean distance between the blocks' grid positions, each row
+    then normalised to sum to 1.  With a single block the row is [1].
+    """
+    r, c = np.divmod(np.arange(blocks_h * blocks_w), blocks_w)
+    dist = np.sqrt((r[:, None] - r[None, :]) ** 2.0 + (c[:, None] - c[None, :]) ** 2.0)
+    far = dist.max(axis=1, keepdims=True)
+    m0 = np.where(far > 0, 1.0 - dist / np.where(far > 0, far, 1.0), 1.0)
+    return m0 / m0.sum(axis=1, keepdims=True)
+
+
+def causal_mhla_stream(q, k, v, mixing, block_size, eps=1e-6):
+    """Causal MHLA inference, one token at a time.  Returns ``(Y, den)``.
+
+    MHLA paper App. C ("因果推理"): the summaries of finished blocks are frozen;
+    for a token of block i the running summary of block i takes the token
+    (S_i <- S_i + phi(k) v^T, z_i <- z_i + phi(k)) and the output reads the
+    mixture sum_{b<i} m_{i,b} S_b + m_{i,i} S_i (z likewise), then divides
+    as everywhere else (the reading of :func:`causal_mhla_chunked`).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    m, mix = _check_blocks(n, block_size, mixing)
+    frozen_s = np.zeros((bsz, nh, m, d, d))
+    frozen_z = np.zeros((bsz, nh, m, d))
+    y = np.empty_like(v)
+    den = np.empty((bsz, nh, n))
+    for t in range(n):
+        i = t // block_size
+        if t % block_size == 0:
+            s_cur = np.zeros((bsz, nh, d, d))
+            z_cur = np.zeros((bsz, nh, d))
+        qt, kt = phi(q[:, :, t]), phi(k[:, :, t])
+        s_cur = s_cur + kt[..., :, None] * v[:, :, t][..., None, :]
+        z_cur = z_cur + kt
+        s_mix = np.einsum("hb,zhbce->zhce", mix[:, i, :i], frozen_s[:, :, :i]) + mix[:, i, i][None, :, None, None] * s_cur
+        z_mix = np.einsum("hb,zhbc->zhc", mix[:, i, :i], frozen_z[:, :, :i]) + mix[:, i, i][None, :, None] * z_cur
+        dn = np.einsum("zhc,zhc->zh", qt, z_mix) + eps
+        y[:, :, t] = np.einsum("zhc,zhce->zhe", qt, s_mix) / dn[..., None]
+        den[:, :, t] = dn
+        if t % block_size == block_size - 1:
+            frozen_s[:, :, i] = s_cur
+            frozen_z[:, :, i] = z_cur
+    return y, den
 
 
 def numerical_rank(a, rtol=None):

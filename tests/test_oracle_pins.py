@@ -310,3 +310,123 @@ def test_rala_one_dominant_key(rala_small):
     expect = np.einsum("bnc,cd->bnd", x, w)[:, None] * (2.0 * d * 31.0 * v[..., 7, :])[:, :, None, :]
     for fn in (oracle.rala_forward, oracle.rala_bruteforce):
         assert close(fn(q, k, v, x, w), expect, 1e-12), fn
+
+
+# --------------------------------------------------- decay (RetNet) pins
+def test_decayed_bruteforce_special_cases(causal_small):
+    q, k, v = causal_small
+    ref, dref = oracle.causal_bruteforce(q, k, v, 1e-6)
+    y1, d1 = oracle.decayed_causal_bruteforce(q, k, v, 1.0, 1e-6)
+    assert close(y1, ref, 1e-12) and close(d1, dref, 1e-12)
+    # gamma = 0: every token sees only itself, so out_t = v_t (eps negligible)
+    y0, d0 = oracle.decayed_causal_bruteforce(q, k, v, 0.0, 0.0)
+    assert close(y0, v, 1e-12)
+    assert close(d0, np.einsum("...tc,...tc->...t", oracle.phi(q), oracle.phi(k)), 1e-12)
+
+
+def test_decayed_bruteforce_two_tokens_by_hand():
+    """d = 1, tokens x = [0, ln 2]: phi = [1, 3];  gamma = 1/2, v = [2, 5], q = [0, 0] (phi 1):
+    out_0 = 1*2 / 1 = 2;  out_1 = (0.5 * 1 * 2 + 1 * 3 * 5) / (0.5 * 1 + 3) = 16 / 3.5."""
+    q = np.zeros((1, 1, 2, 1))
+    k = np.array([0.0, math.log(2.0)]).reshape(1, 1, 2, 1)
+    k[0, 0, 1, 0] = 2.0  # phi(2) = 3
+    v = np.array([2.0, 5.0]).reshape(1, 1, 2, 1)
+    y, den = oracle.decayed_causal_bruteforce(q, k, v, 0.5, 0.0)
+    assert close(y.ravel(), [2.0, 16.0 / 3.5], 1e-14) and close(den.ravel(), [1.0, 3.5], 1e-14)
+
+
+def test_decode_with_decay_equals_decayed_bruteforce(causal_small):
+    q, k, v = causal_small
+    s0 = normal(12, 1, (2, 2, 8, 8))
+    z0 = np.abs(normal(12, 2, (2, 2, 8))) + 1.0
+    steps = lambda x: np.moveaxis(x, 2, 0)  # noqa: E731  [T, B, H, d]
+    for gamma in (0.9, 0.5):
+        outs, dens, s_t, z_t = oracle.decode_steps(s0, z0, steps(q), steps(k), steps(v), 1e-6, gamma=gamma)
+        ref, dref = oracle.decayed_causal_bruteforce(q, k, v, gamma, 1e-6, s0=s0, z0=z0)
+        assert close(np.moveaxis(outs, 0, 2), ref, 1e-10) and close(np.moveaxis(dens, 0, 2), dref, 1e-10)
+        n = q.shape[2]
+        w = gamma ** np.arange(n - 1, -1, -1)
+        s_ref = gamma ** n * s0 + np.einsum("t,bhtc,bhte->bhce", w, oracle.phi(k), v)
+        assert close(s_t, s_ref, 1e-10)
+
+
+# ------------------------------------------------- normaliser-free pins
+def test_unnormalized_equals_bruteforce_sum(tiny):
+    wl, x = tiny
+    mix, block = x["mixing64"], wl.block
+    num = oracle.mhla_block_form_unnormalized(x["q64"], x["k64"], x["v64"], mix, block)
+    a = oracle.mhla_attention_matrix(x["q64"][0, 0], x["k64"][0, 0], mix[0], block)
+    assert close(num[0, 0], a @ x["v64"][0, 0], 1e-11)
+    y, den = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix, block, 1e-6)
+    assert close(num, y * den[..., None], 1e-11)
+
+
+# ---------------------------------------------------- 2-D block pins
+def test_grid_block_ids_by_hand():
+    ids = oracle.grid_block_ids(4, 4, 2, 2)
+    assert ids.tolist() == [0, 0, 1, 1, 0, 0, 1, 1, 2, 2, 3, 3, 2, 2, 3, 3]
+    assert oracle.grid_block_ids(2, 6, 1, 6).tolist() == [0] * 6 + [1] * 6
+
+
+@pytest.fixture(scope="module")
+def grid_small():
+    q = normal(21, 1, (1, 2, 64, 4), 0.5)   # an 8 x 8 token grid
+    k = normal(21, 2, (1, 2, 64, 4), 0.5)
+    v = normal(21, 3, (1, 2, 64, 4))
+    u = uniform(21, 4, (2, 4, 4)) + 0.05
+    return q, k, v, u / u.sum(axis=-1, keepdims=True)
+
+
+def test_grid_blocks_equal_token_expansion(grid_small):
+    q, k, v, mix = grid_small
+    ids = oracle.grid_block_ids(8, 8, 4, 4)
+    y1, d1 = oracle.mhla_block_form_ids(q, k, v, mix, ids, 1e-6)
+    y2, d2 = oracle.mhla_token_expansion_ids(q, k, v, mix, ids, 1e-6)
+    assert close(y1, y2, 1e-11) and close(d1, d2, 1e-11)
+
+
+def test_contiguous_ids_equal_the_1d_block_form(grid_small):
+    q, k, v, mix = grid_small
+    ids = oracle.block_of(64, 16)
+    y1, d1 = oracle.mhla_block_form_ids(q, k, v, mix, ids, 1e-6)
+    y2, d2 = oracle.mhla_block_form(q, k, v, mix, 16, 1e-6)
+    assert close(y1, y2, 1e-12) and close(d1, d2, 1e-12)
+    y3, d3 = oracle.mhla_token_expansion_ids(q, k, v, mix, ids, 1e-6)
+    y4, d4 = oracle.mhla_token_expansion(q, k, v, mix, 16, 1e-6)
+    assert close(y3, y4, 1e-12) and close(d3, d4, 1e-12)
+    # rows of the grid as tiles (tile_h = 1... here 2 rows of 8 = 16 tokens) are contiguous blocks
+    assert oracle.grid_block_ids(8, 8, 2, 8).tolist() == ids.tolist()
+
+
+def test_grid_blocks_are_1d_blocks_of_the_tile_ordered_tokens(grid_small):
+    q, k, v, mix = grid_small
+    ids = oracle.grid_block_ids(8, 8, 4, 4)
+    order = np.argsort(ids, kind="stable")   # tokens of tile 0, then tile 1, ...
+    y1, d1 = oracle.mhla_block_form_ids(q, k, v, mix, ids, 1e-6)
+    y2, d2 = oracle.mhla_block_form(q[:, :, order], k[:, :, order], v[:, :, order], mix, 16, 1e-6)
+    assert close(y1[:, :, order], y2, 1e-12) and close(d1[:, :, order], d2, 1e-12)
+
+
+def test_locality_init_by_hand():
+    m = oracle.locality_mixing_init(1, 3)
+    assert close(m, [[2 / 3, 1 / 3, 0], [0, 1, 0], [0, 1 / 3, 2 / 3]], 1e-15)
+    m = oracle.locality_mixing_init(2, 2)
+    a = 1 - 1 / math.sqrt(2)
+    row0 = np.array([1, a, a, 0]) / (1 + 2 * a)
+    assert close(m[0], row0, 1e-15) and close(m[3], row0[::-1], 1e-15)
+    assert close(oracle.locality_mixing_init(1, 1), [[1.0]], 0)
+    m = oracle.locality_mixing_init(5, 5)       # Fig. 4b's M = 25
+    assert close(m.sum(axis=1), np.ones(25), 1e-14) and np.all(m >= 0)
+    assert np.all(np.argmax(m, axis=1) == np.arange(25))
+
+
+# ------------------------------------------- streaming causal MHLA pins
+def test_causal_mhla_stream_equals_bruteforce(causal_small):
+    q, k, v = causal_small
+    mix = np.tril(uniform(5, 4, (2, 4, 4)) + 0.05)
+    y1, d1 = oracle.causal_mhla_stream(q, k, v, mix, 24, 1e-6)
+    y2, d2 = oracle.causal_mhla_bruteforce(q, k, v, mix, 24, 1e-6)
+    assert close(y1, y2, 1e-11) and close(d1, d2, 1e-11)
+    y3, d3 = oracle.causal_mhla_stream(q, k, v, np.ones((2, 4, 4)), 24, 1e-6)
+    ref, dref = oracle.causal_recurrent(q, k, v, 1e-6)
+    assert close(y3, ref, 1e-11) and close(d3, dref, 1e-11)
