@@ -67,6 +67,9 @@ def workload_bytes(wl):
     if wl.kind == "decode":
         units = wl.B * wl.H
         return units * (2 * (wl.d * wl.d + wl.d) * 4 + 4 * wl.d * eb)
+    if wl.kind == "decode_steps":  # the state once in and out, each step's q, k, v, out, den
+        units = wl.B * wl.H
+        return units * (2 * (wl.d * wl.d + wl.d) * 4 + wl.N * (4 * wl.d * eb + 4))
     if wl.kind == "rala":
         cx = wl.extra["cx"]
         return 4 * t + wl.B * wl.N * cx * eb + cx * wl.d * eb
@@ -75,6 +78,18 @@ def workload_bytes(wl):
 
 def tokens_per_step(wl):
     return wl.B * wl.H if wl.kind == "decode" else wl.B * wl.H * wl.N
+
+
+def workload_flops(wl):
+    """fp32 operations of one fused decode call (an FMA counts 2): per unit and step the state
+    update and the output read 2 d^2 FMAs, the denominator d FMAs, z d adds."""
+    assert wl.kind == "decode_steps"
+    return wl.B * wl.H * wl.N * (4 * wl.d * wl.d + 3 * wl.d)
+
+
+def fp32_peak_tflops(sm_count, sm_mhz=2070.0):
+    """FP32 FMA peak: 128 FP32 lanes per SM, 2 operations per FMA, at the given SM clock."""
+    return sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
 
 
 def max_over_ranks(ms, world, device=None):
@@ -102,6 +117,9 @@ def describe(wl):
         s += f" causal chunk {wl.block}"
     elif wl.kind == "decode":
         s = f"{wl.name}: {wl.B}x{wl.H} units d{wl.d} {wl.dtype}, one recurrent step, fp32 state"
+    elif wl.kind == "decode_steps":
+        s = (f"{wl.name}: {wl.B}x{wl.H} units d{wl.d} {wl.dtype}, {wl.N} recurrent steps in one call, "
+             f"fp32 state")
     elif wl.kind == "rala":
         s += f" cx{wl.extra['cx']}"
     return s
@@ -114,6 +132,7 @@ KERNEL_SOURCES = {
     "mhla_tcgen05_stream": ["tc_stream.cu", "stream_sched.h"],
     "causal_tcgen05": ["tc_causal.cu"],
     "rala_tcgen05": ["tc_rala.cu"],
+    "decode_steps_simt": ["decode_steps.cu"],
 }
 SHARED_SOURCES = ["tc_common.cuh", "common.cuh"]
 
@@ -222,7 +241,7 @@ class Runner:
         self.device = device
         step_bytes = workload_bytes(wl)
         self.R = sets if sets > 0 else max(1, min(16, math.ceil(3 * l2_bytes / step_bytes)))
-        if wl.kind == "decode":
+        if wl.kind in ("decode", "decode_steps"):
             self.R = 1  # the recurrent state is carried from one step to the next
         self.sets = []
         if wl.kind in ("mhla", "causal"):
@@ -251,6 +270,17 @@ class Runner:
             self.sets.append({"steps": dev, "S": S, "z": z,
                               "out": torch.empty(wl.B, wl.H, wl.d, dtype=dev["step_q"].dtype, device=device)})
             self.ws = None
+        elif wl.kind == "decode_steps":
+            dev = workloads.decode_device(wl, device)
+            kf = dev["prefix_k"].float()
+            kf = torch.where(kf > 0, kf + 1, torch.exp(kf))
+            S = torch.einsum("pbhc,pbhe->bhce", kf, dev["prefix_v"].float()).contiguous()
+            z = kf.sum(dim=0).contiguous()
+            del dev["prefix_k"], dev["prefix_v"], kf
+            self.sets.append({"steps": dev, "S": S, "z": z, "out": torch.empty_like(dev["step_q"]),
+                              "den": torch.empty(dev["step_q"].shape[:-1], dtype=torch.float32,
+                                                 device=device)})
+            self.ws = None
         self.step_index = 0
 
     def step(self, i):
@@ -268,6 +298,10 @@ class Runner:
             st = s["steps"]
             t = i % st["step_q"].shape[0]
             b.linattn_decode_step(st["step_q"][t], st["step_k"][t], st["step_v"][t], s["S"], s["z"], s["out"])
+        elif wl.kind == "decode_steps":
+            st = s["steps"]
+            b.linattn_decode_steps(st["step_q"], st["step_k"], st["step_v"], s["S"], s["z"], s["out"],
+                                   den_out=s["den"])
 
     # ---- end to end: host inputs -> device -> forward -> host output
     def e2e_setup(self):
@@ -276,6 +310,11 @@ class Runner:
         if self.wl.kind == "decode":
             st = s["steps"]
             self.h_in = {k: st[k][:8].cpu().pin_memory() for k in ("step_q", "step_k", "step_v")}
+            self.h_out = torch.empty_like(s["out"], device="cpu").pin_memory()
+            return
+        if self.wl.kind == "decode_steps":
+            st = s["steps"]
+            self.h_in = {k: st[k].cpu().pin_memory() for k in ("step_q", "step_k", "step_v")}
             self.h_out = torch.empty_like(s["out"], device="cpu").pin_memory()
             return
         names = ["q", "k", "v"] + (["x"] if self.wl.kind == "rala" else [])
@@ -298,6 +337,13 @@ class Runner:
             self.binding.linattn_decode_step(st["step_q"][t], st["step_k"][t], st["step_v"][t], s["S"], s["z"], s["out"])
             self.h_out.copy_(s["out"], non_blocking=True)
             return
+        if wl.kind == "decode_steps":
+            st = s["steps"]
+            for n in ("step_q", "step_k", "step_v"):
+                st[n].copy_(self.h_in[n], non_blocking=True)
+            self._call(s, i)
+            self.h_out.copy_(s["out"], non_blocking=True)
+            return
         for n, h in self.h_in.items():
             s[n].copy_(h, non_blocking=True)
         self._call(s, i)
@@ -309,7 +355,7 @@ class Runner:
         output comes down (second copy stream); every step still moves its own
         inputs and output.  Returns the elapsed ms (first copy to last copy)."""
         torch = self.torch
-        if self.wl.kind == "decode":
+        if self.wl.kind in ("decode", "decode_steps"):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -387,6 +433,8 @@ def kernel_path(binding, wl):
         return binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
     if wl.kind == "decode":
         return "simt"
+    if wl.kind == "decode_steps":
+        return "simt"
     return binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
 
 
@@ -460,6 +508,8 @@ def parity_of_timed_output(runner, n_slices=4):
         got = np.stack([s["y"][b, h].float().cpu().numpy() for b, h in heads]).astype(np.float64)
         ref = ref[0]
         desc = f"{len(heads)} of {units} (batch, head) slices"
+    elif wl.kind == "decode_steps":
+        return parity_of_decode_steps(runner)
     elif wl.kind == "rala":
         batches = [0, wl.B - 1][:n_slices]
         host = workloads.rala_host(wl, batches)
@@ -474,6 +524,53 @@ def parity_of_timed_output(runner, n_slices=4):
     tol = 2e-2 if wl.dtype == "bf16" else 1e-4
     return {"max_slice_rel_err": float(err.max()), "tol": tol, "ok": bool(err.max() <= tol),
             "sample": f"{desc}, timed output (no den_out, reused workspace, graph replay)"}
+
+
+def parity_of_decode_steps(runner):
+    """One more fused decode call in the timed configuration, with the state of two units (the
+    first and the last) set to the oracle's prefix summary: those units' outputs and final state
+    against the float64 oracle's recurrence."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    wl, s = runner.wl, runner.sets[0]
+    U, d, T = wl.B * wl.H, wl.d, wl.N
+    units = [0, U - 1]
+    host = workloads.decode_host(wl, units)
+    kf = oracle.phi(host["prefix_k64"])
+    s0 = np.einsum("puc,pue->uce", kf, host["prefix_v64"]).astype(np.float32)
+    z0 = kf.sum(axis=0).astype(np.float32)
+    Sf, zf = s["S"].view(U, d, d), s["z"].view(U, d)
+    for i, u in enumerate(units):
+        Sf[u] = torch.from_numpy(s0[i]).to(Sf.device)
+        zf[u] = torch.from_numpy(z0[i]).to(zf.device)
+    runner.step(0)
+    torch.cuda.synchronize()
+    sel = torch.tensor(units, device=Sf.device)
+    got = s["out"].view(T, U, d)[:, sel].float().cpu().numpy().astype(np.float64).transpose(1, 0, 2)
+    s_got = Sf[sel].cpu().numpy().astype(np.float64)
+    ref, _, s_t, _ = oracle.decode_steps(s0, z0, host["step_q64"], host["step_k64"], host["step_v64"])
+    ref = ref.transpose(1, 0, 2)
+    err = np.abs(got - ref).reshape(len(units), -1).max(1) / np.abs(ref).reshape(len(units), -1).max(1)
+    s_err = float((np.abs(s_got - s_t).reshape(len(units), -1).max(1)
+                   / np.abs(s_t).reshape(len(units), -1).max(1)).max())
+    tol = 2e-2 if wl.dtype == "bf16" else 1e-4
+    return {"max_slice_rel_err": float(err.max()), "state_rel_err": s_err, "tol": tol,
+            "ok": bool(err.max() <= tol and s_err <= 1e-4),
+            "sample": f"2 of {U} units, all {T} steps of one timed-configuration call, state set to the "
+                      f"oracle's {wl.extra['prefix']}-token prefix summary"}
+
+
+def alu_roofline(torch, wl, device, launch_ms):
+    """The fused decode's roofline: fp32 FMA issue (its loop is bound by it), against the FP32
+    peak at the maximum SM clock (152 SMs x 128 lanes x 2 x 2070 MHz on GB300)."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peak = fp32_peak_tflops(sms)
+    achieved = workload_flops(wl) / (launch_ms / 1e3) / 1e12
+    return {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "peak_source": f"derived: {sms} SMs x 128 FP32 lanes x 2 flops x 2070 MHz",
+            "alg_flops_per_launch": workload_flops(wl)}
 
 
 def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
@@ -494,6 +591,10 @@ def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
     if wl.kind == "decode":
         out["note"] = ("effective bandwidth: the 68 MB recurrent state may stay in L2 from one step to "
                        "the next, so this is not a DRAM figure")
+    elif wl.kind == "decode_steps":
+        out["unit"] = "unit-steps/s"
+        out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
+        out["parity"] = parity_of_timed_output(runner)
     else:
         out["parity"] = parity_of_timed_output(runner, n_slices=2)
     del runner
@@ -579,6 +680,10 @@ def run_ours(args, wl, rank, world, local_rank):
         "clocks": sampler.summary(t_wall0, t_wall1),
         "parity": parity,
     }
+    if wl.kind == "decode_steps":  # bound by fp32 FMA issue, not by HBM
+        line["roofline"] = dict(alu_roofline(torch, wl, device, kernel_ms), kernel=kernel_name,
+                                traffic=line["roofline"]["traffic"], kernels_per_step=per_step_kernels,
+                                launch_ms=kernel_ms, effective_GBps=achieved)
     if e2e is not None:
         line["e2e"] = e2e
     # the other workloads of the pages (one GPU): rooflines and launch times beside the metric's
@@ -586,12 +691,13 @@ def run_ours(args, wl, rank, world, local_rank):
         del runner
         torch.cuda.empty_cache()
         extra = {}
-        for name in ("hires", "hires_m1", "causal", "rala", "decode"):
+        for name in ("hires", "hires_m1", "causal", "rala", "decode", "decode_fused"):
             if name == wl.name:
                 continue
             try:
-                extra[name] = workload_line(torch, binding, workloads_mod().WORKLOADS[name], device, l2,
-                                            min(args.steps, 200), args.warmup)
+                wl_x = workloads_mod().WORKLOADS[name]
+                n_x = min(args.steps, 20 if wl_x.kind == "decode_steps" else 200)
+                extra[name] = workload_line(torch, binding, wl_x, device, l2, n_x, args.warmup)
             except Exception as e:  # report, do not lose the metric line
                 extra[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
         line["workloads"] = extra
@@ -627,6 +733,13 @@ def _oracle_sample(wl, n_units):
         z0 = np.zeros((n_units, wl.d))
         fn = lambda: oracle.decode_steps(s0, z0, host["step_q64"], host["step_k64"], host["step_v64"])  # noqa: E731
         return fn, n_units, f"{n_units} of {wl.B * wl.H} units, one step"
+    if wl.kind == "decode_steps":
+        units = list(range(n_units))
+        host = workloads.decode_host(wl, units)
+        s0 = np.zeros((n_units, wl.d, wl.d))
+        z0 = np.zeros((n_units, wl.d))
+        fn = lambda: oracle.decode_steps(s0, z0, host["step_q64"], host["step_k64"], host["step_v64"])  # noqa: E731
+        return fn, n_units * wl.N, f"{n_units} of {wl.B * wl.H} units, all {wl.N} steps"
     if wl.kind == "rala":
         host = workloads.rala_host(wl, list(range(n_units)))
         fn = lambda: oracle.rala_forward(host["q64"], host["k64"], host["v64"], host["x64"], host["w64"])  # noqa: E731
@@ -635,7 +748,8 @@ def _oracle_sample(wl, n_units):
 
 
 def _default_sample_units(wl):
-    return {"mhla": max(1, min(wl.B * wl.H, 8)), "causal": 2, "decode": 256, "rala": 2}[wl.kind]
+    return {"mhla": max(1, min(wl.B * wl.H, 8)), "causal": 2, "decode": 256, "decode_steps": 4,
+            "rala": 2}[wl.kind]
 
 
 def _cpu_work(args):

@@ -8,7 +8,8 @@
  *           output), §4.2 (token-level form, chunkwise-parallel causal form),
  *           App. C (causal chunked linear attention and causal inference).
  *   [LA]    "Linear Attention（线性注意力）笔记" — §二 (phi = ELU + 1),
- *           §四 (recurrent form, eps in the denominator), §五 (parallel form).
+ *           §四 (recurrent form, eps in the denominator), §五 (parallel form),
+ *           §七 (RetNet decay), §八 (the constant-size state).
  *   [MASK]  "4. Attention" tutorial — "Mask": the causal mask removes only
  *           the future (strict upper triangle).
  *   [RALA]  "Breaking the Low-Rank Dilemma of Linear Attention" notes — key
@@ -130,6 +131,26 @@ mhla_status mhla_forward_causal(const void* q, const void* k, const void* v, con
 mhla_status linattn_decode_step(const void* q, const void* k, const void* v, float* S, float* z,
                                 void* out, float* den_out, int B, int H, int d, mhla_dtype dt,
                                 float eps, void* stream);
+
+/* T consecutive recurrent decode steps in one call, for B*H independent
+ * (batch, head) states ([LA] §四 recurrence; [LA] §七 RetNet decay; the
+ * fixed-size state of [LA] §八).
+ *   q, k, v : [T, B, H, d] (dtype dt)    — step t's tokens at [t]
+ *   S       : [B, H, d, d] fp32, in/out — as in linattn_decode_step
+ *   z       : [B, H, d] fp32, in/out
+ *   out     : [T, B, H, d] (dtype dt)    — must not overlap the inputs or the state
+ *   den_out : [T, B, H] fp32 or NULL     — each step's phi(q) . z + eps
+ *   gamma   : decay in [0, 1]; 1 gives exactly the steps of linattn_decode_step.
+ *   Per step: S <- gamma S + phi(k) v^T; z <- gamma z + phi(k);
+ *   out = phi(q) S / (phi(q) . z + eps).  (The notes decay S; z decays with
+ *   it so that the output stays a weighted mean of the values.)
+ *   Equal, up to fp32 rounding, to T calls of linattn_decode_step when
+ *   gamma = 1; the state is read once and written once per call.
+ *   T = 0 or B*H = 0 returns MHLA_OK without a launch.  B*H above 2^29
+ *   returns MHLA_ERR_UNSUPPORTED.  No workspace. */
+mhla_status linattn_decode_steps(const void* q, const void* k, const void* v, float* S, float* z,
+                                 void* out, float* den_out, int T, int B, int H, int d, mhla_dtype dt,
+                                 float eps, float gamma, void* stream);
 
 /* Workspace bytes for rala_forward; 0 if the sizes are invalid. */
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx);

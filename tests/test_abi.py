@@ -107,6 +107,28 @@ def test_decode_argument_errors(lib):
     assert dec(q=P + 2) == INVALID
 
 
+def test_decode_steps_argument_errors(lib):
+    def dec(q=P, k=2 * P, v=3 * P, S=4 * P, z=6 * P, out=7 * P, den=None, T=3, B=2, H=2, d=64, dt=BF16,
+            eps=1e-6, gamma=1.0):
+        return lib.linattn_decode_steps(q, k, v, S, z, out, den, T, B, H, d, dt, eps, gamma, None)
+    assert dec(d=24) == INVALID
+    assert dec(T=-1) == INVALID
+    assert dec(S=None) == INVALID
+    assert dec(z=4 * P + 64) == INVALID                    # z inside S
+    assert dec(out=P) == INVALID                           # out aliases q
+    assert dec(out=P + 2 * 2 * 64 * 2) == INVALID          # out overlaps step 1 of q
+    assert dec(den=P) == INVALID                           # den_out aliases q
+    assert dec(eps=-0.5) == INVALID
+    assert dec(gamma=1.5) == INVALID
+    assert dec(gamma=-0.1) == INVALID
+    assert dec(gamma=float("nan")) == INVALID
+    assert dec(q=P + 2) == INVALID
+    assert dec(B=1 << 15, H=1 << 15) == UNSUPPORTED
+    # empty: no steps, or no units
+    assert dec(T=0, q=None, k=None, v=None, out=None) == OK
+    assert dec(B=0, q=None, k=None, v=None, out=None, S=None, z=None) == OK
+
+
 def test_rala_argument_errors(lib):
     def rala(cx=64, d=32, ws=8 * P, wsb=1 << 30, y=6 * P, x=4 * P):
         return lib.rala_forward(P, 2 * P, 3 * P, x, 5 * P, y, 2, 2, 3136, d, cx, BF16, ws, wsb, None)
@@ -162,6 +184,12 @@ def test_binding_rejects_mismatched_tensors():
     q3 = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="S: shape"):
         binding.linattn_decode_step(q3, q3, q3, torch.zeros(2, 64, 64), torch.zeros(1, 2, 64), q3.clone())
+    q4 = torch.zeros(3, 1, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="den_out: shape"):
+        binding.linattn_decode_steps(q4, q4, q4, torch.zeros(1, 2, 64, 64), torch.zeros(1, 2, 64), q4.clone(),
+                                     den_out=torch.zeros(1, 2))
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.linattn_decode_steps(q4, q4, q4, torch.zeros(1, 2, 64, 64), torch.zeros(1, 2, 64), q4.clone())
     with pytest.raises(ValueError, match="w: shape"):
         binding.rala_forward(q, q, q, torch.zeros(1, 256, 64, dtype=torch.bfloat16),
                              torch.zeros(64, 32, dtype=torch.bfloat16), q.clone())

@@ -28,6 +28,12 @@ def test_algorithmic_bytes_of_the_workloads():
     dec = W["decode"]
     assert bench.tokens_per_step(dec) == 256 * 16
     assert bench.workload_bytes(dec) == 4096 * (2 * (64 * 64 + 64) * 4 + 4 * 64 * 2)
+    # fused decode: the state once in and out, 1024 steps of q, k, v, out (bf16) and den (fp32)
+    fused = W["decode_fused"]
+    assert bench.tokens_per_step(fused) == 4096 * 1024
+    assert bench.workload_bytes(fused) == 4096 * (2 * (64 * 64 + 64) * 4 + 1024 * (4 * 64 * 2 + 4))
+    assert bench.workload_flops(fused) == 4096 * 1024 * (4 * 64 * 64 + 3 * 64)
+    assert abs(bench.fp32_peak_tflops(152) - 80.548) < 0.001
 
 
 def test_traffic_record_needs_matching_sources(monkeypatch):

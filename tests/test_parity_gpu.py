@@ -490,6 +490,105 @@ def test_decode_full_workload_sampled_units():
     assert_close_y(to_f64(Sf[sel])[:, None], s_t[:, None], "f32", what="state S")
 
 
+# ------------------------------------------------------------ fused decode
+def decode_state(seed, P, B, H, d):
+    """fp32 state (S, z) summarising a P-token random prefix, and its float64 values."""
+    pk = normal(seed, 1, (P, B, H, d), d ** -0.5)
+    pv = normal(seed, 2, (P, B, H, d), d ** -0.5)
+    kf = oracle.phi(pk)
+    s0 = np.einsum("pbhc,pbhe->bhce", kf, pv).astype(np.float32)
+    z0 = kf.sum(axis=0).astype(np.float32)
+    return s0, z0
+
+
+def decode_steps_run(S, z, q, k, v, gamma=1.0, eps=1e-6):
+    out = torch.empty_like(q)
+    den = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    binding.linattn_decode_steps(q, k, v, S, z, out, eps=eps, gamma=gamma, den_out=den)
+    torch.cuda.synchronize()
+    return to_f64(out), to_f64(den)
+
+
+@pytest.mark.parametrize("gamma", [1.0, 0.9])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+def test_decode_steps_small(d, dtype, gamma):
+    """T steps in one call against the oracle's recurrence (B*H = 15 units: a
+    ragged last CTA; T = 13 > the cp.async ring depth)."""
+    B, H, T, P = 3, 5, 13, 40
+    s0, z0 = decode_state(11 + d, P, B, H, d)
+    steps = {n: rounded(normal(12 + d, 3 + i, (T, B, H, d), d ** -0.5), dtype) for i, n in enumerate("qkv")}
+    S, z = torch.from_numpy(s0).cuda(), torch.from_numpy(z0).cuda()
+    outs, dens = decode_steps_run(S, z, steps["q"][0], steps["k"][0], steps["v"][0], gamma)
+    ref, dref, s_t, z_t = oracle.decode_steps(s0, z0, steps["q"][1], steps["k"][1], steps["v"][1], 1e-6,
+                                              gamma=gamma)
+    assert_close_y(outs.reshape(T * B, H, d)[:, :, None], ref.reshape(T * B, H, d)[:, :, None], dtype)
+    assert_close_den(dens, dref, dtype)
+    assert_close_y(to_f64(S), s_t, "f32", what="state S")
+    assert rel(to_f64(z), z_t) < 1e-5
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_decode_steps_equal_single_steps(d):
+    """gamma = 1: one fused call gives the outputs and state of T single-step calls, up to fp32
+    rounding (the fused kernel's exp is the hardware base-2 exponential, about 2^-22 relative)."""
+    B, H, T = 2, 7, 9
+    s0, z0 = decode_state(31, 20, B, H, d)
+    steps = {n: rounded(normal(32, 3 + i, (T, B, H, d), d ** -0.5), "f32")[0] for i, n in enumerate("qkv")}
+    S1, z1 = torch.from_numpy(s0).cuda(), torch.from_numpy(z0).cuda()
+    S2, z2 = S1.clone(), z1.clone()
+    outs, dens = decode_steps_run(S1, z1, steps["q"], steps["k"], steps["v"])
+    outs1, dens1 = decode_run(S2, z2, steps["q"], steps["k"], steps["v"])
+    assert slice_rel(outs.reshape(T * B, H, d), outs1.reshape(T * B, H, d)) < 1e-5
+    assert rel(dens, dens1) < 1e-5
+    assert rel(to_f64(z1), to_f64(z2)) < 1e-5
+    assert slice_rel(to_f64(S1), to_f64(S2)) < 1e-5
+
+
+def test_decode_steps_zero_steps_keep_the_state():
+    S = torch.randn(2, 3, 64, 64, device="cuda")
+    z = torch.rand(2, 3, 64, device="cuda")
+    S0, z0 = S.clone(), z.clone()
+    q = torch.empty(0, 2, 3, 64, dtype=torch.bfloat16, device="cuda")
+    binding.linattn_decode_steps(q, q, q, S, z, q.clone())
+    torch.cuda.synchronize()
+    assert torch.equal(S, S0) and torch.equal(z, z0)
+
+
+def test_decode_steps_full_workload_sampled_units():
+    """The decode workload's 1024 steps for all 4096 units in one call, checked
+    on 65 units against the oracle; every output finite, every denominator > eps."""
+    wl = WORKLOADS["decode"]
+    B, H, d = wl.B, wl.H, wl.d
+    dev = decode_device(wl)
+    kf = torch.where(dev["prefix_k"].float() > 0, dev["prefix_k"].float() + 1, torch.exp(dev["prefix_k"].float()))
+    S = torch.einsum("pbhc,pbhe->bhce", kf, dev["prefix_v"].float()).contiguous()
+    z = kf.sum(dim=0).contiguous()
+    units = list(range(0, B * H, 64)) + [B * H - 1]
+    host = decode_host(wl, units)
+    s0 = np.einsum("puc,pue->uce", oracle.phi(host["prefix_k64"]), host["prefix_v64"]).astype(np.float32)
+    z0 = oracle.phi(host["prefix_k64"]).sum(axis=0).astype(np.float32)
+    Sf, zf = S.view(B * H, d, d), z.view(B * H, d)
+    for i, u in enumerate(units):
+        Sf[u] = torch.from_numpy(s0[i]).cuda()
+        zf[u] = torch.from_numpy(z0[i]).cuda()
+    out = torch.empty_like(dev["step_q"])
+    den = torch.empty(out.shape[:-1], dtype=torch.float32, device="cuda")
+    binding.linattn_decode_steps(dev["step_q"], dev["step_k"], dev["step_v"], S, z, out, den_out=den)
+    torch.cuda.synchronize()
+    assert bool(torch.isfinite(out.float()).all())
+    assert bool((den > 1e-6).all())
+    T = wl.N
+    sel = torch.tensor(units, device="cuda")
+    outs = out.view(T, B * H, d)[:, sel]
+    dens = den.view(T, B * H)[:, sel]
+    ref, dref, s_t, z_t = oracle.decode_steps(s0, z0, host["step_q64"], host["step_k64"], host["step_v64"])
+    assert_close_y(to_f64(outs).transpose(1, 0, 2)[:, None], ref.transpose(1, 0, 2)[:, None], "bf16")
+    assert_close_den(to_f64(dens), dref, "bf16")
+    assert_close_y(to_f64(Sf[sel])[:, None], s_t[:, None], "f32", what="state S")
+    assert rel(to_f64(zf[sel]), z_t) < 1e-5
+
+
 # ----------------------------------------------------------------------- RALA
 RALA = [  # B, H, N, d, cx
     (2, 2, 200, 16, 32),

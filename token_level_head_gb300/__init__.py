@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     EXPORTED,
     MhlaError,
     linattn_decode_step,
+    linattn_decode_steps,
     load,
     mhla_forward,
     mhla_forward_causal,

@@ -29,6 +29,7 @@ _SIGNATURES = {
     "mhla_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "mhla_forward_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "linattn_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "linattn_decode_steps": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp]),
     "rala_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "rala_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "mhla_forward_path": (_i, [_i, _i, _i, _i, _i, _i, _i]),
@@ -201,6 +202,26 @@ def linattn_decode_step(q, k, v, S, z, out, *, eps=1e-6, den_out=None, stream=No
         st = load().linattn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out),
                                         _ptr(den_out), B, H, d, _dtype(q), eps, _stream(stream, dev))
     _check("linattn_decode_step", st)
+    return out
+
+
+def linattn_decode_steps(q, k, v, S, z, out, *, eps=1e-6, gamma=1.0, den_out=None, stream=None):
+    """T recurrent decode steps in one call; q/k/v/out [T, B, H, d], S [B, H, d, d] fp32,
+    z [B, H, d] fp32 (updated), den_out [T, B, H] fp32; ``gamma`` the decay in [0, 1]."""
+    if q.dim() != 4:
+        raise ValueError(f"q: expected [T, B, H, d], got shape {tuple(q.shape)}")
+    T, B, H, d = q.shape
+    for name, t in (("k", k), ("v", v), ("out", out)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(S, "S", (B, H, d, d), torch.float32)
+    _expect(z, "z", (B, H, d), torch.float32)
+    _expect(den_out, "den_out", (T, B, H), torch.float32)
+    dev = _same_device(q, k, v, S, z, out, den_out)
+    with torch.cuda.device(dev):
+        st = load().linattn_decode_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(S), _ptr(z), _ptr(out),
+                                         _ptr(den_out), T, B, H, d, _dtype(q), eps, gamma,
+                                         _stream(stream, dev))
+    _check("linattn_decode_steps", st)
     return out
 
 

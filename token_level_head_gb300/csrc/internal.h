@@ -62,6 +62,10 @@ cudaError_t simt_mhla_launch(const MhlaShape& s, mhla_dtype dt, const void* q, c
 cudaError_t simt_decode_launch(int units, int d, mhla_dtype dt, const void* q, const void* k,
                                const void* v, float* S, float* z, void* out, float* den_out,
                                float eps, cudaStream_t st);
+// ---- fused multi-step decode: T recurrent steps per launch, the state held on chip
+cudaError_t decode_steps_launch(int T_steps, int units, int d, mhla_dtype dt, const void* q, const void* k,
+                                const void* v, float* S, float* z, void* out, float* den_out, float eps,
+                                float gamma, cudaStream_t st);
 size_t simt_rala_workspace(int B, int H, int N, int d, int cx);
 cudaError_t simt_rala_launch(int B, int H, int N, int d, int cx, mhla_dtype dt, const void* q,
                              const void* k, const void* v, const void* x, const void* w, void* y,

@@ -154,6 +154,38 @@ mhla_status linattn_decode_step(const void* q, const void* k, const void* v, flo
                                       static_cast<cudaStream_t>(stream)));
 }
 
+mhla_status linattn_decode_steps(const void* q, const void* k, const void* v, float* S, float* z,
+                                 void* out, float* den_out, int T, int B, int H, int d, mhla_dtype dt,
+                                 float eps, float gamma, void* stream) {
+  if (T < 0 || B < 0 || H < 0 || !valid_d(d)) return MHLA_ERR_INVALID_ARG;
+  if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return MHLA_ERR_INVALID_ARG;
+  if (!std::isfinite(gamma) || gamma < 0.f || gamma > 1.f) return MHLA_ERR_INVALID_ARG;
+  const size_t units = (size_t)B * H;
+  if (units == 0) return MHLA_OK;
+  if (!S || !z) return MHLA_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !out)) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(S) || !aligned16(z) ||
+      !aligned16(out) || (den_out && !aligned16(den_out)))
+    return MHLA_ERR_INVALID_ARG;
+  if (units > 0x7fffffffu / 4) return MHLA_ERR_UNSUPPORTED;
+  const size_t vb = (size_t)T * units * d * dtype_bytes(dt), sb = units * d * d * sizeof(float),
+               zb = units * d * sizeof(float), db = (size_t)T * units * sizeof(float);
+  if (T > 0 && (overlap(out, vb, q, vb) || overlap(out, vb, k, vb) || overlap(out, vb, v, vb) ||
+                overlap(out, vb, S, sb) || overlap(out, vb, z, zb) || overlap(S, sb, q, vb) ||
+                overlap(S, sb, k, vb) || overlap(S, sb, v, vb) || overlap(z, zb, q, vb) ||
+                overlap(z, zb, k, vb) || overlap(z, zb, v, vb)))
+    return MHLA_ERR_INVALID_ARG;
+  if (overlap(S, sb, z, zb)) return MHLA_ERR_INVALID_ARG;
+  if (den_out && T > 0 &&
+      (overlap(den_out, db, q, vb) || overlap(den_out, db, k, vb) || overlap(den_out, db, v, vb) ||
+       overlap(den_out, db, out, vb) || overlap(den_out, db, S, sb) || overlap(den_out, db, z, zb)))
+    return MHLA_ERR_INVALID_ARG;
+  if (T == 0) return MHLA_OK;
+  return from_cuda(decode_steps_launch(T, (int)units, d, dt, q, k, v, S, z, out, den_out, eps, gamma,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx) {
   if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256) return 0;
   const size_t a = simt_rala_workspace(B, H, N, d, cx);

@@ -48,7 +48,8 @@ __device__ __forceinline__ bool group_and(int id, int n, bool pred) {
 
 // ---------------------------------------------------------------- values
 // phi(x) = exp(min(x, 0)) + max(x, 0): x + 1 for x > 0 (exp(0) = 1 exactly),
-// exp(x) otherwise; exp through the hardware base-2 exponential.
+// exp(x) otherwise.  exp(x) = 2^(x log2 e), taken with the hardware base-2
+// exponential (ex2.approx) of x * log2 e, log2 e = 1.4426950408889634.
 __device__ __forceinline__ float phi_f(float x) {
   float e;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(fminf(x, 0.f) * 1.4426950408889634f));

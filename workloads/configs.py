@@ -26,7 +26,7 @@ from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, normal, normal_at
 class Workload:
     name: str
     index: int              # seed = SEED_BASE + index
-    kind: str               # "mhla" | "causal" | "decode" | "rala"
+    kind: str               # "mhla" | "causal" | "decode" | "decode_steps" | "rala"
     B: int
     H: int
     N: int                  # tokens (decode: number of steps)
@@ -63,6 +63,9 @@ WORKLOADS = {
     # recurrent decode: batch 256 x 16 heads, 1024 steps after a 2048-token prefix
     "decode": Workload("decode", 4, "decode", 256, 16, 1024, 64, 0, "bf16", 0.125,
                        extra={"prefix": 2048}),
+    # the same decode workload with all 1024 steps in one fused call (state held on chip)
+    "decode_fused": Workload("decode_fused", 4, "decode_steps", 256, 16, 1024, 64, 0, "bf16", 0.125,
+                             extra={"prefix": 2048}),
     # rank-augmented variant: 56x56 tokens, X [B, N, 64], W [64, 32]
     "rala": Workload("rala", 5, "rala", 64, 2, 3136, 32, 0, "bf16", 32 ** -0.5,
                      extra={"cx": 64}),
