@@ -111,7 +111,10 @@ def job_value(tokens_per_rank_step, steps, world, ms):
 
 def describe(wl):
     s = f"{wl.name}: B{wl.B} H{wl.H} N{wl.N} d{wl.d} {wl.dtype}"
-    if wl.kind == "mhla":
+    if wl.kind == "mhla" and "grid" in wl.extra:
+        gh, gw, th, tw = wl.extra["grid"]
+        s += f" M{wl.M} (2-D blocks: {gh}x{gw} grid, {th}x{tw} tiles)"
+    elif wl.kind == "mhla":
         s += f" M{wl.M} (blocks of {wl.block})"
     elif wl.kind == "causal":
         s += f" causal chunk {wl.block}"
@@ -288,7 +291,10 @@ class Runner:
 
     def _call(self, s, i):
         wl, b = self.wl, self.binding
-        if wl.kind == "mhla":
+        if wl.kind == "mhla" and "grid" in wl.extra:
+            gh, gw, th, tw = wl.extra["grid"]
+            b.mhla_forward_grid(s["q"], s["k"], s["v"], s["mixing"], s["y"], (gh, gw), (th, tw), workspace=self.ws)
+        elif wl.kind == "mhla":
             b.mhla_forward(s["q"], s["k"], s["v"], s["mixing"], s["y"], wl.block, workspace=self.ws)
         elif wl.kind == "causal":
             b.mhla_forward_causal(s["q"], s["k"], s["v"], None, s["y"], wl.block, workspace=self.ws)
@@ -435,6 +441,8 @@ def kernel_path(binding, wl):
         return "simt"
     if wl.kind == "decode_steps":
         return "simt"
+    if "grid" in wl.extra:
+        return binding.mhla_forward_grid_path(wl.B, wl.H, *wl.extra["grid"], wl.d, tdt)
     return binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
 
 
@@ -501,7 +509,10 @@ def parity_of_timed_output(runner, n_slices=4):
         pick = sorted({0, units - 1} | {(units * i) // n_slices for i in range(n_slices)})[:n_slices]
         heads = [(u // wl.H, u % wl.H) for u in pick]
         x = workloads.mhla_host(wl, heads=heads)
-        if wl.kind == "mhla":
+        if wl.kind == "mhla" and "grid" in wl.extra:
+            ids = oracle.grid_block_ids(*wl.extra["grid"])
+            ref, _ = oracle.mhla_block_form_ids(x["q64"], x["k64"], x["v64"], x["mixing64"], ids)
+        elif wl.kind == "mhla":
             ref, _ = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
         else:
             ref, _ = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)
@@ -691,7 +702,7 @@ def run_ours(args, wl, rank, world, local_rank):
         del runner
         torch.cuda.empty_cache()
         extra = {}
-        for name in ("hires", "hires_m1", "causal", "rala", "decode", "decode_fused"):
+        for name in ("dit_grid", "hires", "hires_m1", "causal", "rala", "decode", "decode_fused"):
             if name == wl.name:
                 continue
             try:
@@ -721,7 +732,10 @@ def _oracle_sample(wl, n_units):
     if wl.kind in ("mhla", "causal"):
         heads = [(i // wl.H % wl.B, i % wl.H) for i in range(n_units)]
         x = workloads.mhla_host(wl, heads=heads)
-        if wl.kind == "mhla":
+        if wl.kind == "mhla" and "grid" in wl.extra:
+            ids = oracle.grid_block_ids(*wl.extra["grid"])
+            fn = lambda: oracle.mhla_block_form_ids(x["q64"], x["k64"], x["v64"], x["mixing64"], ids)  # noqa: E731
+        elif wl.kind == "mhla":
             fn = lambda: oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)  # noqa: E731
         else:
             fn = lambda: oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)  # noqa: E731

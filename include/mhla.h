@@ -119,6 +119,41 @@ mhla_status mhla_forward_causal(const void* q, const void* k, const void* v, con
                                 mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* Non-causal MHLA with 2-D blocks ([MHLA] §4.1: for images the blocks lie on
+ * a 2-D grid, Fig. 4b).  The N = grid_h * grid_w tokens of each (b, h) slice
+ * are a grid_h x grid_w grid in row-major order (token t = row * grid_w + col,
+ * the layout of the [B, H, N, d] tensors is unchanged); the blocks are the
+ * tile_h x tile_w tiles of the grid, numbered row-major over the
+ * (grid_h / tile_h) x (grid_w / tile_w) tile grid, M = their count; b(t) is
+ * the tile holding token t.  Then, as in mhla_forward:
+ *   S_b = sum_{t: b(t)=b} phi(K_t) V_t^T,  z_b likewise,
+ *   S~_i = sum_b m[h][i][b] S_b,  Y_t = phi(Q_t) S~_{b(t)} / (phi(Q_t) . z~_{b(t)} + eps).
+ *   mixing : [H, M, M] fp32 (mhla_locality_mixing gives the paper's initial value).
+ *   tile_h must divide grid_h and tile_w grid_w, else MHLA_ERR_INVALID_ARG.
+ *   workspace: mhla_workspace_bytes(B, H, grid_h * grid_w, d, tile_h * tile_w, 0).
+ *   On a one-row grid (grid_h = tile_h = 1) the blocks are contiguous ranges
+ *   of tile_w tokens and the result is that of mhla_forward.
+ *   Other arguments as in mhla_forward. */
+mhla_status mhla_forward_grid(const void* q, const void* k, const void* v, const float* mixing,
+                              void* y, float* den_out, int B, int H, int grid_h, int grid_w,
+                              int tile_h, int tile_w, int d, mhla_dtype dt, float eps,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* Kernel family mhla_forward_grid would use (no launch): the tensor-core
+ * kernels take bf16, d = 64, tiles of a multiple of 128 tokens with tile_w
+ * dividing 128 or a multiple of 128, M <= 64; else the SIMT kernels. */
+mhla_path mhla_forward_grid_path(int B, int H, int grid_h, int grid_w, int tile_h, int tile_w, int d,
+                                 mhla_dtype dt);
+
+/* The locality-based initial mixing matrix of [MHLA] §4.2 for blocks on a
+ * blocks_h x blocks_w grid (M = blocks_h * blocks_w, numbered row-major):
+ * m[i][j] proportional to 1 - dist(i, j) / max_k dist(i, k), dist the
+ * Euclidean distance between the blocks' grid positions, each row normalised
+ * to sum to 1 (a single block: [[1]]).  `m` is a HOST array [M][M] fp32 that
+ * the caller owns; computed on the host (a one-off initialisation, not part
+ * of the forward).  M above 65536 returns MHLA_ERR_INVALID_ARG. */
+mhla_status mhla_locality_mixing(float* m, int blocks_h, int blocks_w);
+
 /* One recurrent decode step for B*H independent (batch, head) states
  * ([LA] §四; the fixed-size state of [LA] §八; [MHLA] App. C inference).
  *   q, k, v : [B, H, d] (dtype dt)       — this step's token

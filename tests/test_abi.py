@@ -129,6 +129,39 @@ def test_decode_steps_argument_errors(lib):
     assert dec(B=0, q=None, k=None, v=None, out=None, S=None, z=None) == OK
 
 
+def test_grid_argument_errors_and_paths(lib):
+    def grid(gh=64, gw=64, th=16, tw=16, d=64, dt=BF16, ws=8 * P, wsb=1 << 30, mix=4 * P, y=5 * P):
+        return lib.mhla_forward_grid(P, 2 * P, 3 * P, mix, y, None, 2, 6, gh, gw, th, tw, d, dt, 1e-6,
+                                     ws, wsb, None)
+    assert grid(th=12) == INVALID                          # tiles do not cover the grid
+    assert grid(tw=0) == INVALID
+    assert grid(gw=0) == INVALID
+    assert grid(d=40) == INVALID
+    assert grid(mix=None) == INVALID
+    assert grid(y=P) == INVALID                            # y aliases q
+    assert grid(wsb=64) == INVALID                         # workspace too small
+    assert grid(gh=0) == OK                                # no tokens
+    path = lambda *a: binding.PATH_NAMES[lib.mhla_forward_grid_path(8, 6, *a)]  # noqa: E731
+    assert path(64, 64, 16, 16, 64, BF16) == "tcgen05"
+    assert path(16, 256, 1, 128, 64, BF16) == "tcgen05"    # 128-token rows of a tile
+    assert path(8, 512, 2, 256, 64, BF16) == "tcgen05"
+    assert path(64, 64, 16, 16, 64, F32) == "simt"
+    assert path(64, 60, 16, 12, 64, BF16) == "simt"         # tile width neither divides nor is a multiple of 128
+    assert path(64, 64, 4, 4, 64, BF16) == "simt"           # 16-token tiles
+    assert path(64, 64, 12, 16, 64, BF16) == "none"
+
+
+def test_locality_mixing_matches_the_oracle(lib):
+    import numpy as np
+    import oracle
+    for bh, bw in [(1, 1), (1, 6), (4, 4), (3, 5), (8, 8)]:
+        got = binding.locality_mixing(bh, bw).numpy()
+        assert np.abs(got - oracle.locality_mixing_init(bh, bw)).max() < 1e-7
+    assert lib.mhla_locality_mixing(None, 2, 2) == INVALID
+    with pytest.raises(binding.MhlaError):
+        binding.locality_mixing(0, 3)
+
+
 def test_rala_argument_errors(lib):
     def rala(cx=64, d=32, ws=8 * P, wsb=1 << 30, y=6 * P, x=4 * P):
         return lib.rala_forward(P, 2 * P, 3 * P, x, 5 * P, y, 2, 2, 3136, d, cx, BF16, ws, wsb, None)

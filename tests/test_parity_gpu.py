@@ -294,6 +294,24 @@ def test_full_workload_all_heads(name):
     assert_close_den(den, dref, wl.dtype)
 
 
+def test_dit_grid_full_workload_all_heads():
+    """The DiT-like workload with 2-D 16 x 16 blocks, in the bench's launch configuration, all
+    48 heads against the oracle (blocks given token by token)."""
+    wl = WORKLOADS["dit_grid"]
+    gh, gw, th, tw = wl.extra["grid"]
+    assert binding.mhla_forward_grid_path(wl.B, wl.H, gh, gw, th, tw, wl.d, torch.bfloat16) == "tcgen05"
+    dev = mhla_device(wl)
+    y = torch.empty_like(dev["q"])
+    den = torch.empty(dev["q"].shape[:3], dtype=torch.float32, device="cuda")
+    binding.mhla_forward_grid(dev["q"], dev["k"], dev["v"], dev["mixing"], y, (gh, gw), (th, tw), den_out=den)
+    torch.cuda.synchronize()
+    x = mhla_host(wl)
+    ref, dref = oracle.mhla_block_form_ids(x["q64"], x["k64"], x["v64"], x["mixing64"],
+                                           oracle.grid_block_ids(gh, gw, th, tw))
+    assert_close_y(to_f64(y), ref, wl.dtype)
+    assert_close_den(to_f64(den), dref, wl.dtype)
+
+
 @pytest.mark.parametrize("name", ["hires", "hires_m1"])
 def test_full_workload_every_head(name):
     wl = WORKLOADS[name]
@@ -488,6 +506,78 @@ def test_decode_full_workload_sampled_units():
     assert_close_y(to_f64(outs).transpose(1, 0, 2)[:, None], ref.transpose(1, 0, 2)[:, None], "bf16")
     assert_close_den(to_f64(dens), dref, "bf16")
     assert_close_y(to_f64(Sf[sel])[:, None], s_t[:, None], "f32", what="state S")
+
+
+# ----------------------------------------------------------- 2-D grid blocks
+GRID = [  # B, H, grid_h, grid_w, tile_h, tile_w, d, dtype, mixing, path
+    (2, 3, 12, 20, 3, 5, 16, "f32", "random", "simt"),
+    (1, 2, 16, 16, 4, 8, 32, "bf16", "locality", "simt"),
+    (1, 1, 8, 24, 8, 3, 64, "bf16", "random", "simt"),
+    (2, 3, 64, 64, 16, 16, 64, "bf16", "locality", "tcgen05"),     # the DiT latent grid, 4 x 4 tiles
+    (1, 2, 32, 64, 8, 16, 64, "bf16", "random", "tcgen05"),
+    (1, 2, 16, 256, 1, 128, 64, "bf16", "random", "tcgen05"),     # one-row tiles of 128
+    (1, 1, 8, 512, 2, 256, 64, "bf16", "locality", "tcgen05"),    # 128-token pieces of tile rows
+    (1, 2, 128, 8, 16, 8, 64, "bf16", "random", "tcgen05"),       # 16-row boxes
+    (1, 1, 256, 2, 128, 1, 64, "bf16", "random", "tcgen05"),      # one-column tiles
+    (3, 2, 48, 32, 16, 16, 64, "f32", "locality", "simt"),
+]
+
+
+def grid_mixing(kind, H, bh, bw, seed):
+    M = bh * bw
+    if kind == "locality":
+        m = binding.locality_mixing(bh, bw).numpy()
+        mix = np.broadcast_to(m, (H, M, M)).copy()
+    else:
+        u = uniform(seed, 9, (H, M, M)) + 0.05
+        mix = (u / u.sum(axis=-1, keepdims=True)).astype(np.float32)
+    return torch.from_numpy(mix).cuda(), mix.astype(np.float64)
+
+
+@pytest.mark.parametrize("shape", GRID, ids=lambda s: "x".join(map(str, s[:7])) + f"-{s[7]}-{s[8]}")
+def test_grid_blocks(shape):
+    B, H, gh, gw, th, tw, d, dtype, mk, path = shape
+    assert binding.mhla_forward_grid_path(B, H, gh, gw, th, tw, d, torch_dtype(dtype)) == path
+    N = gh * gw
+    x = rand_inputs(300 + gh + gw + d, (B, H, N, d), dtype)
+    mix_t, mix64 = grid_mixing(mk, H, gh // th, gw // tw, 31 + th)
+    y = torch.empty_like(x["q"])
+    den = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    binding.mhla_forward_grid(x["q"], x["k"], x["v"], mix_t, y, (gh, gw), (th, tw), den_out=den)
+    torch.cuda.synchronize()
+    ids = oracle.grid_block_ids(gh, gw, th, tw)
+    ref, dref = oracle.mhla_block_form_ids(x["q64"], x["k64"], x["v64"], mix64, ids)
+    assert_close_y(to_f64(y), ref, dtype)
+    assert_close_den(to_f64(den), dref, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_grid_of_one_row_equals_contiguous_blocks(dtype):
+    """grid_h = tile_h = 1: the tiles are contiguous token ranges, the call is mhla_forward's
+    (same kernel family, same arithmetic: equal bit for bit)."""
+    B, H, N, d, block = 2, 3, 2048, 64, 256
+    path = binding.mhla_forward_path(B, H, N, d, block, 0, torch_dtype(dtype))
+    assert path == binding.mhla_forward_grid_path(B, H, 1, N, 1, block, d, torch_dtype(dtype))
+    x = rand_inputs(77, (B, H, N, d), dtype)
+    mix_t, _ = rand_mixing(78, H, N // block)
+    y1, y2 = torch.empty_like(x["q"]), torch.empty_like(x["q"])
+    binding.mhla_forward(x["q"], x["k"], x["v"], mix_t, y1, block)
+    binding.mhla_forward_grid(x["q"], x["k"], x["v"], mix_t, y2, (1, N), (1, block))
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_grid_tiny_brute_force():
+    """A 6 x 8 grid of 2 x 4 tiles against the N x N token expansion of eq. 5."""
+    B, H, gh, gw, th, tw, d = 1, 2, 6, 8, 2, 4, 16
+    x = rand_inputs(91, (B, H, gh * gw, d), "f32")
+    mix_t, mix64 = grid_mixing("random", H, gh // th, gw // tw, 92)
+    y = torch.empty_like(x["q"])
+    binding.mhla_forward_grid(x["q"], x["k"], x["v"], mix_t, y, (gh, gw), (th, tw))
+    torch.cuda.synchronize()
+    ref, _ = oracle.mhla_token_expansion_ids(x["q64"], x["k64"], x["v64"], mix64,
+                                             oracle.grid_block_ids(gh, gw, th, tw))
+    assert_close_y(to_f64(y), ref, "f32")
 
 
 # ------------------------------------------------------------ fused decode

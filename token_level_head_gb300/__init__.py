@@ -11,8 +11,11 @@ from .binding import (  # noqa: F401
     linattn_decode_step,
     linattn_decode_steps,
     load,
+    locality_mixing,
     mhla_forward,
     mhla_forward_causal,
+    mhla_forward_grid,
+    mhla_forward_grid_path,
     mhla_forward_noalloc,
     mhla_forward_path,
     mhla_launch_count,

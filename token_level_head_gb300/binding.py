@@ -30,6 +30,9 @@ _SIGNATURES = {
     "mhla_forward_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "linattn_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "linattn_decode_steps": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp]),
+    "mhla_forward_grid": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "mhla_forward_grid_path": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
+    "mhla_locality_mixing": (_i, [_vp, _i, _i]),
     "rala_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "rala_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp]),
     "mhla_forward_path": (_i, [_i, _i, _i, _i, _i, _i, _i]),
@@ -148,6 +151,19 @@ def mhla_forward_path(B, H, N, d, block_size, causal, dtype) -> str:
     return PATH_NAMES[int(load().mhla_forward_path(B, H, N, d, block_size, causal, dt))]
 
 
+def mhla_forward_grid_path(B, H, grid_h, grid_w, tile_h, tile_w, d, dtype) -> str:
+    dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
+    return PATH_NAMES[int(load().mhla_forward_grid_path(B, H, grid_h, grid_w, tile_h, tile_w, d, dt))]
+
+
+def locality_mixing(blocks_h, blocks_w) -> torch.Tensor:
+    """The locality-based initial mixing matrix [M, M] (fp32, CPU) for blocks on a grid."""
+    M = blocks_h * blocks_w
+    m = torch.empty(max(M, 0), max(M, 0), dtype=torch.float32)
+    _check("mhla_locality_mixing", load().mhla_locality_mixing(_ptr(m), blocks_h, blocks_w))
+    return m
+
+
 def rala_forward_path(B, H, N, d, cx, dtype) -> str:
     dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
     return PATH_NAMES[int(load().rala_forward_path(B, H, N, d, cx, dt))]
@@ -169,6 +185,34 @@ def mhla_forward(q, k, v, mixing, y, block_size, *, causal=0, eps=1e-6, den_out=
                                  B, H, N, d, block_size, causal, _dtype(q), eps, _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward", st)
+    return y
+
+
+def mhla_forward_grid(q, k, v, mixing, y, grid_hw, tile_hw, *, eps=1e-6, den_out=None, workspace=None,
+                      stream=None):
+    """Non-causal MHLA with 2-D blocks: the N tokens are a grid_hw = (grid_h, grid_w) grid in
+    row-major order, the blocks its tile_hw = (tile_h, tile_w) tiles; mixing [H, M, M] fp32."""
+    (gh, gw), (th, tw) = grid_hw, tile_hw
+    if q.dim() != 4:
+        raise ValueError(f"q: expected [B, H, N, d], got shape {tuple(q.shape)}")
+    if q.shape[2] != gh * gw:
+        raise ValueError(f"q: N = {q.shape[2]}, expected grid_h * grid_w = {gh * gw}")
+    if th <= 0 or tw <= 0 or gh % th or gw % tw:
+        raise ValueError(f"tiles {tile_hw} do not cover the grid {grid_hw}")
+    B, H, N, d = q.shape
+    for name, t in (("k", k), ("v", v), ("y", y)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(den_out, "den_out", (B, H, N), torch.float32)
+    M = (gh // th) * (gw // tw)
+    _expect(mixing, "mixing", (H, M, M), torch.float32)
+    dev = _same_device(q, k, v, mixing, y, den_out, workspace)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, th * tw, 0), dev)
+        st = load().mhla_forward_grid(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                      B, H, gh, gw, th, tw, d, _dtype(q), eps, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    _check("mhla_forward_grid", st)
     return y
 
 

@@ -14,8 +14,13 @@ void note_launch(int n = 1);
 // How the non-causal / causal MHLA work is split into summary partials.
 struct MhlaShape {
   int B, H, N, d, block;  // block = block_size (non-causal) or chunk (causal)
+  // 2-D blocks (non-causal only): tokens on a gh x gw grid in row-major order, blocks the
+  // th x tw tiles numbered row-major; gw == 0 means contiguous blocks of `block` tokens.
+  // With a grid, N = gh * gw and block = th * tw.
+  int gh = 0, gw = 0, th = 0, tw = 0;
   int heads() const { return B * H; }
   int M() const { return N / block; }
+  bool grid() const { return gw > 0; }
 };
 
 // Mixing modes of the summary-mixing stage.

@@ -91,14 +91,26 @@ mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int caus
   return tc_mhla_supported(s, dt, MIX_FULL) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
 
+// 2-D block geometry: tokens on a gh x gw grid, blocks th x tw tiles covering it.
+static bool grid_ok(int gh, int gw, int th, int tw) {
+  return gh >= 0 && gw > 0 && th > 0 && tw > 0 && gh % th == 0 && gw % tw == 0 &&
+         (long long)gh * gw <= 0x7fffffffLL && (long long)th * tw <= 0x7fffffffLL;
+}
+
 static mhla_status run_mhla(const void* q, const void* k, const void* v, const float* mixing,
                             void* y, float* den_out, int B, int H, int N, int d, int block,
                             MixMode mode, mhla_dtype dt, float eps, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            void* stream, const int* grid = nullptr) {
   mhla_status st = check_mhla(q, k, v, y, den_out, B, H, N, d, block, dt, eps, ws, ws_bytes, mode != MIX_FULL);
   if (st != MHLA_OK || (size_t)B * H * N == 0) return st;
   if (mode != MIX_PREFIX && (!mixing || !aligned16(mixing))) return MHLA_ERR_INVALID_ARG;
   MhlaShape s{B, H, N, d, block};
+  if (grid != nullptr) {  // {gh, gw, th, tw}, validated by the caller
+    s.gh = grid[0];
+    s.gw = grid[1];
+    s.th = grid[2];
+    s.tw = grid[3];
+  }
   if (tc_causal_supported(s, dt, mode))
     return from_cuda(tc_causal_launch(s, q, k, v, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
   if (tc_stream_supported(s, dt, mode))
@@ -120,6 +132,48 @@ mhla_status mhla_forward(const void* q, const void* k, const void* v, const floa
                                workspace, workspace_bytes, stream);
   return run_mhla(q, k, v, mixing, y, den_out, B, H, N, d, block_size, MIX_FULL, dt, eps,
                   workspace, workspace_bytes, stream);
+}
+
+mhla_status mhla_forward_grid(const void* q, const void* k, const void* v, const float* mixing,
+                              void* y, float* den_out, int B, int H, int grid_h, int grid_w,
+                              int tile_h, int tile_w, int d, mhla_dtype dt, float eps,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  if (!grid_ok(grid_h, grid_w, tile_h, tile_w)) return MHLA_ERR_INVALID_ARG;
+  const int g[4] = {grid_h, grid_w, tile_h, tile_w};
+  return run_mhla(q, k, v, mixing, y, den_out, B, H, grid_h * grid_w, d, tile_h * tile_w, MIX_FULL, dt,
+                  eps, workspace, workspace_bytes, stream, g);
+}
+
+mhla_path mhla_forward_grid_path(int B, int H, int grid_h, int grid_w, int tile_h, int tile_w, int d,
+                                 mhla_dtype dt) {
+  if (!dims_ok(B, H, 0) || !valid_d(d) || !grid_ok(grid_h, grid_w, tile_h, tile_w) ||
+      (dt != MHLA_F32 && dt != MHLA_BF16))
+    return MHLA_PATH_NONE;
+  MhlaShape s{B, H, grid_h * grid_w, d, tile_h * tile_w};
+  s.gh = grid_h;
+  s.gw = grid_w;
+  s.th = tile_h;
+  s.tw = tile_w;
+  return tc_mhla_supported(s, dt, MIX_FULL) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+}
+
+mhla_status mhla_locality_mixing(float* m, int blocks_h, int blocks_w) {
+  if (!m || blocks_h <= 0 || blocks_w <= 0 || (long long)blocks_h * blocks_w > 65536) return MHLA_ERR_INVALID_ARG;
+  const int M = blocks_h * blocks_w;
+  for (int i = 0; i < M; ++i) {
+    const int ri = i / blocks_w, ci = i % blocks_w;
+    double far = 0.0;  // distance from block i to the farthest block
+    for (int j = 0; j < M; ++j)
+      far = std::max(far, std::hypot((double)(j / blocks_w - ri), (double)(j % blocks_w - ci)));
+    // weight 1 - dist / far (a lone block: 1), each row normalised to sum to 1
+    auto weight = [&](int j) {
+      return far > 0.0 ? 1.0 - std::hypot((double)(j / blocks_w - ri), (double)(j % blocks_w - ci)) / far : 1.0;
+    };
+    double sum = 0.0;
+    for (int j = 0; j < M; ++j) sum += weight(j);
+    for (int j = 0; j < M; ++j) m[(size_t)i * M + j] = (float)(weight(j) / sum);
+  }
+  return MHLA_OK;
 }
 
 mhla_status mhla_forward_causal(const void* q, const void* k, const void* v, const float* mixing,

@@ -31,18 +31,37 @@ inline int divisor_at_most(int n, int cap) {
   return 1;
 }
 
+// Token of the j-th position of block b: blocks are the th x tw tiles, numbered row-major, of
+// a grid of rows gw tokens wide (MHLA paper §4.1: blocks on a 2-D grid for images).
+// Contiguous blocks of `block` tokens are the 1 x block tiles of a 1 x N grid.
+struct TokMap {
+  int gw, tw, th, bpr;  // grid width, tile width and height, tiles per grid row
+  __device__ __forceinline__ int tok(int b, int j) const {
+    const int lr = j / tw, lc = j - lr * tw;
+    const int br = b / bpr, bc = b - br * bpr;
+    return (br * th + lr) * gw + bc * tw + lc;
+  }
+};
+
+TokMap tok_map(const MhlaShape& s) {
+  if (s.grid()) return TokMap{s.gw, s.tw, s.th, s.gw / s.tw};
+  return TokMap{s.N, s.block, 1, s.N / s.block};
+}
+
 // ---------------------------------------------------------------- summaries
 // S_part[head][p] = sum_{t in chunk p} phi(K_t) V_t^T ; z_part[head][p] = sum phi(K_t)
-// (MHLA paper §4.1, local KV summary; chunks subdivide the blocks).
+// (MHLA paper §4.1, local KV summary; chunks subdivide the blocks; chunk p holds positions
+// [(p % P) chunk, (p % P + 1) chunk) of block p / P).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 simt_summary_kernel(const T* __restrict__ K, const T* __restrict__ V, float* __restrict__ s_part,
-                    float* __restrict__ z_part, int N, int chunk) {
+                    float* __restrict__ z_part, int N, int chunk, int P, TokMap map) {
   constexpr int E = (D * D + kThreads - 1) / kThreads;
   __shared__ float sk[kTokTile][D];
   __shared__ float sv[kTokTile][D];
   const int head = blockIdx.y, part = blockIdx.x;
-  const size_t base = ((size_t)head * N + (size_t)part * chunk) * D;
+  const int blk = part / P, j0 = (part - blk * P) * chunk;
+  const size_t hbase = (size_t)head * N * D;
   float acc[E];
 #pragma unroll
   for (int j = 0; j < E; ++j) acc[j] = 0.f;
@@ -50,8 +69,9 @@ simt_summary_kernel(const T* __restrict__ K, const T* __restrict__ V, float* __r
   for (int t0 = 0; t0 < chunk; t0 += kTokTile) {
     const int nt = min(kTokTile, chunk - t0);
     for (int i = threadIdx.x; i < nt * D; i += kThreads) {
-      sk[i / D][i % D] = phi(to_f(K[base + (size_t)t0 * D + i]));
-      sv[i / D][i % D] = to_f(V[base + (size_t)t0 * D + i]);
+      const size_t at = hbase + (size_t)map.tok(blk, j0 + t0 + i / D) * D + i % D;
+      sk[i / D][i % D] = phi(to_f(K[at]));
+      sv[i / D][i % D] = to_f(V[at]);
     }
     __syncthreads();
 #pragma unroll
@@ -137,13 +157,15 @@ simt_mix_kernel(const float* __restrict__ s_part, const float* __restrict__ z_pa
 //     / [phi(Q_t).z~_i + w_ii * sum_{s in block i, s<=t} phi(Q_t).phi(K_s) + eps]
 // The intra-block terms are present only for the causal forms (intra_mode 1:
 // w_ii = m_ii of the mixing, intra_mode 2: w_ii = 1); MHLA paper §4.1 output,
-// App. C chunk form with the lower triangle including the diagonal.
+// App. C chunk form with the lower triangle including the diagonal.  A CTA takes
+// positions t0 .. t0 + tile - 1 of block t0 / block (tokens by `map`; the causal
+// forms have contiguous blocks, so there position and token coincide).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                 const float* __restrict__ s_mix, const float* __restrict__ z_mix,
                 const float* __restrict__ mixing, T* __restrict__ Y, float* __restrict__ den_out,
-                int H, int N, int block, int tile, float eps, int intra_mode) {
+                int H, int N, int block, int tile, float eps, int intra_mode, TokMap map) {
   constexpr int ROWS = kThreads / D;
   constexpr int PASSES = (kOutTile + ROWS - 1) / ROWS;
   extern __shared__ float smem[];
@@ -160,7 +182,9 @@ simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
   const size_t hbase = (size_t)head * N * D;
   for (int i = threadIdx.x; i < D * D; i += kThreads) sS[i] = s_mix[((size_t)head * M + blk) * D * D + i];
   for (int i = threadIdx.x; i < D; i += kThreads) sz[i] = z_mix[((size_t)head * M + blk) * D + i];
-  for (int i = threadIdx.x; i < tile * D; i += kThreads) sq[i] = phi(to_f(Q[hbase + (size_t)t0 * D + i]));
+  const int j0 = t0 - blk * block;
+  for (int i = threadIdx.x; i < tile * D; i += kThreads)
+    sq[i] = phi(to_f(Q[hbase + (size_t)map.tok(blk, j0 + i / D) * D + i % D]));
   __syncthreads();
   const int e = threadIdx.x % D, r = threadIdx.x / D;
   float num[PASSES], nin[PASSES], rs[PASSES];
@@ -210,8 +234,9 @@ simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
       for (int c = 0; c < D; ++c) den = fmaf(sq[t * D + c], sz[c], den);
       den = den + w_ii * rs[p] + eps;
       const float y = (num[p] + w_ii * nin[p]) / den;
-      Y[hbase + (size_t)(t0 + t) * D + e] = from_f<T>(y);
-      if (den_out != nullptr && e == 0) den_out[(size_t)head * N + t0 + t] = den;
+      const int tok = map.tok(blk, j0 + t);
+      Y[hbase + (size_t)tok * D + e] = from_f<T>(y);
+      if (den_out != nullptr && e == 0) den_out[(size_t)head * N + tok] = den;
     }
   }
 }
@@ -250,8 +275,9 @@ cudaError_t mhla_launch_t(const MhlaShape& s, const SimtPlan& pl, const void* q,
   float* s_mix = reinterpret_cast<float*>(ws + pl.off_smix);
   float* z_mix = reinterpret_cast<float*>(ws + pl.off_zmix);
   const int heads = s.heads(), M = s.M();
+  const TokMap map = tok_map(s);
   simt_summary_kernel<T, D><<<dim3(pl.parts, heads), kThreads, 0, st>>>(
-      static_cast<const T*>(k), static_cast<const T*>(v), s_part, z_part, s.N, pl.chunk);
+      static_cast<const T*>(k), static_cast<const T*>(v), s_part, z_part, s.N, pl.chunk, pl.P, map);
   note_launch();
   const int ents = D * D + D;
   simt_mix_kernel<<<dim3((ents + kThreads - 1) / kThreads, heads), kThreads, 0, st>>>(
@@ -265,7 +291,7 @@ cudaError_t mhla_launch_t(const MhlaShape& s, const SimtPlan& pl, const void* q,
   const int intra = mode == MIX_FULL ? 0 : (mode == MIX_STRICT_LOWER ? 1 : 2);
   simt_out_kernel<T, D><<<dim3(s.N / tile, heads), kThreads, smem, st>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), s_mix, z_mix,
-      mixing, static_cast<T*>(y), den_out, s.H, s.N, s.block, tile, eps, intra);
+      mixing, static_cast<T*>(y), den_out, s.H, s.N, s.block, tile, eps, intra, map);
   note_launch();
   return cudaGetLastError();
 }

@@ -102,6 +102,7 @@ struct Layout {
 struct Params {
   CUtensorMap tm_q, tm_k, tm_v;  // [heads*N rows][64] bf16, box 64 x 128, 128-byte swizzle
   CUtensorMap tm_y;              // same tensor shape, box 64 x 32
+                                 // (2-D blocks: (64, gw, heads*gh) boxes of 128 / 32 tokens of a tile)
   CUtensorMap tm_p;              // chunk partials [heads*C rows][4096] bf16, box 64 x C (tensor-core MIX)
   CUtensorMap tm_ps;             // chunk partials [heads*C*64 rows][64] bf16, box 64 x 32 (SUM stores)
   CUtensorMap tm_pp;             // chunk partials as (c 64, x heads*C, e 64), box 64 x C x 2 (transposed MIX)
@@ -119,8 +120,43 @@ struct Params {
   int mix_t;                     // 1: transposed tensor-core MIX (C <= 64; see the MIX stages)
   int mix_n;                     // transposed MIX: N of its MMAs, M rounded up to 16
   int zx;                        // 1: the CTAs with a z row take no MIX units (C > 64, heads <= grid / 4)
+  int grid2d;                    // 1: 2-D blocks (tokens on a gw-wide grid, blocks th x tw tiles)
+  int gw, gh, tw, th, bpr;       // grid width / height, tile width / height, tiles per grid row
   float eps;
 };
+
+// 2-D blocks: grid position (x = column, y = head * gh + row) of the token at offset `off`
+// of chunk g, a chunk being 128 consecutive tokens of its block in the tile's row-major order.
+struct GridPos {
+  int x, y;
+};
+__device__ __forceinline__ GridPos grid_pos(const Params& p, int g, int off) {
+  const int hd = g / p.C, gi = g - hd * p.C;
+  const int b = gi / p.cpb;
+  const int lo = (gi - b * p.cpb) * kTile + off;
+  const int lr = lo / p.tw, lc = lo - lr * p.tw;
+  const int br = b / p.bpr, bc = b - br * p.bpr;
+  return {bc * p.tw + lc, hd * p.gh + br * p.th + lr};
+}
+
+// Q / K / V tile of chunk g: 128 rows of 64 (contiguous blocks: rows g * 128 ..; 2-D blocks:
+// a box of whole tile rows, or 128 tokens of one tile row), the same 128-byte-swizzled image.
+__device__ __forceinline__ void load_chunk(void* dst, const CUtensorMap* m, const Params& p, int g, uint64_t* bar,
+                                           uint64_t pol) {
+  if (p.grid2d) {
+    const GridPos t = grid_pos(p, g, 0);
+    tma_load_3d_hint(dst, m, 0, t.x, t.y, bar, pol);
+  } else {
+    tma_load_2d_hint(dst, m, 0, g * kTile, bar, pol);
+  }
+}
+
+// Token index (head * N + t) of row `row` of chunk g.
+__device__ __forceinline__ size_t chunk_token(const Params& p, int g, int row) {
+  if (!p.grid2d) return (size_t)g * kTile + row;
+  const GridPos t = grid_pos(p, g, row);
+  return (size_t)t.y * p.gw + t.x;
+}
 
 // ------------------------------------------------------------------ waits
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -312,8 +348,8 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
     if (q >= kNS && !bwait(&sh->empty[s], ((q / kNS) - 1) & 1, sh)) return q;
     uint8_t* st = sm + s * kStageBytes;
     mbar_arrive_expect_tx(&sh->full[s], kStageBytes);
-    tma_load_2d_hint(st, &p.tm_k, 0, g * kTile, &sh->full[s], once);
-    tma_load_2d_hint(st + kTileBytes, &p.tm_v, 0, g * kTile, &sh->full[s], once);
+    load_chunk(st, &p.tm_k, p, g, &sh->full[s], once);
+    load_chunk(st + kTileBytes, &p.tm_v, p, g, &sh->full[s], once);
   }
   // MIX units (head h, row e of S^T): the chunk partials' row e, once every CTA
   // has stored its partials (grid barrier 1); the phi warps add the weights
@@ -380,7 +416,7 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
     }
     uint8_t* st = sm + s * kOutStage;
     mbar_arrive_expect_tx(&sh->fullO[s], kTileBytes + kSTile + kD * 4);
-    tma_load_2d_hint(st, &p.tm_q, 0, g * kTile, &sh->fullO[s], once);
+    load_chunk(st, &p.tm_q, p, g, &sh->fullO[s], once);
     sh->prod_qo = qo + 1;
     if (mix_ready<L>(p, ready)) {
       for (; qm <= qo; ++qm, gm += gridDim.x) issue_mix_loads(p, sm, sh, qm, gm);
@@ -889,7 +925,7 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
-        if (p.den_out != nullptr) p.den_out[(size_t)g * kTile + row] = dn;
+        if (p.den_out != nullptr) p.den_out[chunk_token(p, g, row)] = dn;
         const float r = 1.f / dn;
         // Y staging: two 4 KB buffers per warp (the whole 32 KB area is free
         // after the MIX phase); the store of two chunks ago has read this one
@@ -904,7 +940,12 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d_hint(&p.tm_y, yo, 0, g * kTile + qd * 32, once);
+          if (p.grid2d) {
+            const GridPos t = grid_pos(p, g, qd * 32);
+            tma_store_3d_hint(&p.tm_y, yo, 0, t.x, t.y, once);
+          } else {
+            tma_store_2d_hint(&p.tm_y, yo, 0, g * kTile + qd * 32, once);
+          }
           tma_store_commit();
         }
         ++nst;
@@ -1334,6 +1375,19 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q / K / V / Y of 2-D blocks: (64, gw, rows = heads * gh) bf16, box 64 x bw x bh, 128-byte swizzle.
+bool make_map_grid(CUtensorMap* m, const void* base, uint64_t gw, uint64_t rows, uint32_t bw, uint32_t bh) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)gw, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)gw * kD * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kD, bw, bh};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The chunk partials [heads * C][64 e][64 c] bf16 as a 3-D tensor (c, x =
 // head * C + chunk, e), box 64 x C x 2: the two units of a transposed-MIX pair,
 // each a C x 128-byte box with the 128-byte swizzle.
@@ -1416,6 +1470,9 @@ cudaError_t launch_t(const Params& p, int grid, cudaStream_t st) {
 bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
   if (dt != MHLA_BF16 || s.d != kD || mode != MIX_FULL) return false;
   if (s.block % kTile != 0 || s.N % kTile != 0) return false;
+  // 2-D blocks: a 128-token chunk is whole tile rows (tw divides 128) or part of one
+  // (128 divides tw); so is a 32-token piece of Y (tw divides 32, or 32 divides tw)
+  if (s.grid() && !(kTile % s.tw == 0 || s.tw % kTile == 0)) return false;
   if ((long long)s.heads() * s.N >= (1ll << 31)) return false;
   if (s.heads() > kMaxCounterHeads) return false;
   return s.M() <= 64;
@@ -1431,9 +1488,24 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   char* w = static_cast<char*>(ws);
   Params p;
   const uint64_t rows = (uint64_t)s.heads() * s.N;
-  if (!make_map_2d(&p.tm_q, q, rows, kTile) || !make_map_2d(&p.tm_k, k, rows, kTile) ||
-      !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32))
+  if (s.grid()) {
+    const uint64_t grows = (uint64_t)s.heads() * s.gh;
+    const uint32_t bw = s.tw < kTile ? s.tw : kTile, yw = s.tw < 32 ? s.tw : 32;
+    if (!make_map_grid(&p.tm_q, q, s.gw, grows, bw, kTile / bw) ||
+        !make_map_grid(&p.tm_k, k, s.gw, grows, bw, kTile / bw) ||
+        !make_map_grid(&p.tm_v, v, s.gw, grows, bw, kTile / bw) ||
+        !make_map_grid(&p.tm_y, y, s.gw, grows, yw, 32 / yw))
+      return cudaErrorInvalidValue;
+  } else if (!make_map_2d(&p.tm_q, q, rows, kTile) || !make_map_2d(&p.tm_k, k, rows, kTile) ||
+             !make_map_2d(&p.tm_v, v, rows, kTile) || !make_map_2d(&p.tm_y, y, rows, 32)) {
     return cudaErrorInvalidValue;
+  }
+  p.grid2d = s.grid() ? 1 : 0;
+  p.gw = s.gw;
+  p.gh = s.gh;
+  p.tw = s.grid() ? s.tw : 1;
+  p.th = s.th;
+  p.bpr = s.grid() ? s.gw / s.tw : 1;
   if (!make_map_2d(&p.tm_ps, w + pl.off_ps, (uint64_t)s.heads() * pl.C * kD, 32)) return cudaErrorInvalidValue;
   if (pl.tc_mix && !make_map_2d(&p.tm_p, w + pl.off_ps, (uint64_t)s.heads() * pl.C, mix_kslots(pl.C), (uint64_t)kD * kD))
     return cudaErrorInvalidValue;

@@ -770,6 +770,7 @@ void tc_stream_set_wait_limit(unsigned long long ns) { g_wait_ns = ns == 0 ? kDe
 // the three-pass kernel is faster (DiT-like B8 H6 N4096: 32 us against 57 us,
 // L2-warm) and keeps those shapes.
 bool tc_stream_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
+  if (s.grid()) return false;  // contiguous blocks only
   if (dt != MHLA_BF16 || s.d != kD || mode != MIX_FULL) return false;
   if (s.block % kTile != 0 || s.N % kTile != 0 || s.N / kTile > 64 || (s.N / kTile) % 16 == 0) return false;
   if (s.heads() > kMaxCounterHeads || (long long)s.heads() * s.N >= (1ll << 31)) return false;

@@ -55,6 +55,9 @@ WORKLOADS = {
     "tiny": Workload("tiny", 1, "mhla", 1, 1, 256, 16, 64, "f32", 1.0, "uniform_rows"),
     # DiT-S/2-like: 64x64 latent patch grid, row-major, M = 16 blocks of 256
     "dit": Workload("dit", 2, "mhla", 8, 6, 4096, 64, 256, "bf16", 0.125, "softmax_diag2"),
+    # the same DiT-S/2-like inputs with 2-D blocks: the 64x64 grid cut into 4 x 4 tiles of 16x16
+    "dit_grid": Workload("dit_grid", 2, "mhla", 8, 6, 4096, 64, 256, "bf16", 0.125, "softmax_diag2",
+                         extra={"grid": (64, 64, 16, 16)}),
     # 256x256 token grid, M = 64 blocks of 1024, and the same inputs with M = 1
     "hires": Workload("hires", 3, "mhla", 1, 6, 65536, 64, 1024, "bf16", 0.125, "softmax"),
     "hires_m1": Workload("hires_m1", 3, "mhla", 1, 6, 65536, 64, 65536, "bf16", 0.125, "ones"),
