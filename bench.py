@@ -70,6 +70,14 @@ def workload_bytes(wl):
     if wl.kind == "decode_steps":  # the state once in and out, each step's q, k, v, out, den
         units = wl.B * wl.H
         return units * (2 * (wl.d * wl.d + wl.d) * 4 + wl.N * (4 * wl.d * eb + 4))
+    if wl.kind == "stream":
+        # each token's q, k, v, out, den; at each block start the frozen summaries of the
+        # blocks before it (to mix them); each block's summary written once
+        units, P, blk = wl.B * wl.H, wl.extra["prefix"], wl.block
+        first, last = P // blk, (P + wl.N - 1) // blk
+        slot = (wl.d * wl.d + wl.d) * 4
+        reads = sum(range(first, last + 1)) * slot + (slot if P % blk else 0)
+        return units * (wl.N * (4 * wl.d * eb + 4) + reads + (last - first + 1) * slot)
     if wl.kind == "rala":
         cx = wl.extra["cx"]
         return 4 * t + wl.B * wl.N * cx * eb + cx * wl.d * eb
@@ -77,7 +85,7 @@ def workload_bytes(wl):
 
 
 def tokens_per_step(wl):
-    return wl.B * wl.H if wl.kind == "decode" else wl.B * wl.H * wl.N
+    return wl.B * wl.H if wl.kind == "decode" else wl.B * wl.H * wl.N  # stream: N tokens a unit
 
 
 def workload_flops(wl):
@@ -123,6 +131,9 @@ def describe(wl):
     elif wl.kind == "decode_steps":
         s = (f"{wl.name}: {wl.B}x{wl.H} units d{wl.d} {wl.dtype}, {wl.N} recurrent steps in one call, "
              f"fp32 state")
+    elif wl.kind == "stream":
+        s = (f"{wl.name}: {wl.B}x{wl.H} units d{wl.d} {wl.dtype}, causal MHLA inference of {wl.N} tokens "
+             f"after a {wl.extra['prefix']}-token prefix, blocks of {wl.block}, M{wl.M}")
     elif wl.kind == "rala":
         s += f" cx{wl.extra['cx']}"
     return s
@@ -244,7 +255,7 @@ class Runner:
         self.device = device
         step_bytes = workload_bytes(wl)
         self.R = sets if sets > 0 else max(1, min(16, math.ceil(3 * l2_bytes / step_bytes)))
-        if wl.kind in ("decode", "decode_steps"):
+        if wl.kind in ("decode", "decode_steps", "stream"):
             self.R = 1  # the recurrent state is carried from one step to the next
         self.sets = []
         if wl.kind in ("mhla", "causal"):
@@ -272,6 +283,22 @@ class Runner:
             z = kf.sum(dim=0).contiguous()
             self.sets.append({"steps": dev, "S": S, "z": z,
                               "out": torch.empty(wl.B, wl.H, wl.d, dtype=dev["step_q"].dtype, device=device)})
+            self.ws = None
+        elif wl.kind == "stream":
+            dev = workloads.decode_device(wl, device)
+            P, blk, M = wl.extra["prefix"], wl.block, wl.M
+            kf = dev["prefix_k"].float()
+            kf = torch.where(kf > 0, kf + 1, torch.exp(kf))
+            S = torch.zeros(wl.B, wl.H, M, wl.d, wl.d, device=device)
+            z = torch.zeros(wl.B, wl.H, M, wl.d, device=device)
+            nb = P // blk
+            kb = kf.view(nb, blk, wl.B, wl.H, wl.d)
+            S[:, :, :nb] = torch.einsum("nsbhc,nsbhe->bhnce", kb, dev["prefix_v"].float().view(nb, blk, wl.B, wl.H, wl.d))
+            z[:, :, :nb] = kb.sum(dim=1).permute(1, 2, 0, 3)
+            del dev["prefix_k"], dev["prefix_v"], kf, kb
+            mix = torch.from_numpy(workloads.make_mixing(wl).astype("float32")).to(device)
+            self.sets.append({"steps": dev, "S": S, "z": z, "mixing": mix, "out": torch.empty_like(dev["step_q"]),
+                              "den": torch.empty(dev["step_q"].shape[:-1], dtype=torch.float32, device=device)})
             self.ws = None
         elif wl.kind == "decode_steps":
             dev = workloads.decode_device(wl, device)
@@ -308,6 +335,10 @@ class Runner:
             st = s["steps"]
             b.linattn_decode_steps(st["step_q"], st["step_k"], st["step_v"], s["S"], s["z"], s["out"],
                                    den_out=s["den"])
+        elif wl.kind == "stream":
+            st = s["steps"]
+            b.mhla_causal_stream(st["step_q"], st["step_k"], st["step_v"], s["mixing"], s["S"], s["z"], s["out"],
+                                 wl.extra["prefix"], wl.block, den_out=s["den"])
 
     # ---- end to end: host inputs -> device -> forward -> host output
     def e2e_setup(self):
@@ -439,7 +470,7 @@ def kernel_path(binding, wl):
         return binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
     if wl.kind == "decode":
         return "simt"
-    if wl.kind == "decode_steps":
+    if wl.kind in ("decode_steps", "stream"):
         return "simt"
     if "grid" in wl.extra:
         return binding.mhla_forward_grid_path(wl.B, wl.H, *wl.extra["grid"], wl.d, tdt)
@@ -521,6 +552,8 @@ def parity_of_timed_output(runner, n_slices=4):
         desc = f"{len(heads)} of {units} (batch, head) slices"
     elif wl.kind == "decode_steps":
         return parity_of_decode_steps(runner)
+    elif wl.kind == "stream":
+        return parity_of_stream(runner)
     elif wl.kind == "rala":
         batches = [0, wl.B - 1][:n_slices]
         host = workloads.rala_host(wl, batches)
@@ -571,6 +604,29 @@ def parity_of_decode_steps(runner):
             "ok": bool(err.max() <= tol and s_err <= 1e-4),
             "sample": f"2 of {U} units, all {T} steps of one timed-configuration call, state set to the "
                       f"oracle's {wl.extra['prefix']}-token prefix summary"}
+
+
+def parity_of_stream(runner):
+    """Two units (the first and the last) of the timed stream call against the oracle's token-by-token
+    causal MHLA over the prefix and the streamed tokens (the prefix's own outputs are not compared)."""
+    import numpy as np
+    import oracle
+    import workloads
+    wl, s = runner.wl, runner.sets[0]
+    U, d, T, P = wl.B * wl.H, wl.d, wl.N, wl.extra["prefix"]
+    units = [0, U - 1]
+    host = workloads.decode_host(wl, units)
+    k64 = np.concatenate([host["prefix_k64"], host["step_k64"]]).transpose(1, 0, 2)[None]
+    v64 = np.concatenate([host["prefix_v64"], host["step_v64"]]).transpose(1, 0, 2)[None]
+    q64 = np.concatenate([np.zeros_like(host["prefix_k64"]), host["step_q64"]]).transpose(1, 0, 2)[None]
+    mix = workloads.make_mixing(wl)[[u % wl.H for u in units]]
+    ref, _ = oracle.causal_mhla_stream(q64, k64, v64, mix, wl.block)
+    ref = ref[0, :, P:]
+    got = s["out"].view(T, U, d)[:, units].float().cpu().numpy().astype(np.float64).transpose(1, 0, 2)
+    err = np.abs(got - ref).reshape(len(units), -1).max(1) / np.abs(ref).reshape(len(units), -1).max(1)
+    tol = 2e-2 if wl.dtype == "bf16" else 1e-4
+    return {"max_slice_rel_err": float(err.max()), "tol": tol, "ok": bool(err.max() <= tol),
+            "sample": f"2 of {U} units, all {T} tokens of the timed call (graph replay)"}
 
 
 def alu_roofline(torch, wl, device, launch_ms):
@@ -702,12 +758,12 @@ def run_ours(args, wl, rank, world, local_rank):
         del runner
         torch.cuda.empty_cache()
         extra = {}
-        for name in ("dit_grid", "hires", "hires_m1", "causal", "rala", "decode", "decode_fused"):
+        for name in ("dit_grid", "hires", "hires_m1", "causal", "rala", "decode", "decode_fused", "stream"):
             if name == wl.name:
                 continue
             try:
                 wl_x = workloads_mod().WORKLOADS[name]
-                n_x = min(args.steps, 20 if wl_x.kind == "decode_steps" else 200)
+                n_x = min(args.steps, 20 if wl_x.kind in ("decode_steps", "stream") else 200)
                 extra[name] = workload_line(torch, binding, wl_x, device, l2, n_x, args.warmup)
             except Exception as e:  # report, do not lose the metric line
                 extra[name] = {"error": f"{type(e).__name__}: {e}"[:300]}

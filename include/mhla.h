@@ -187,6 +187,29 @@ mhla_status linattn_decode_steps(const void* q, const void* k, const void* v, fl
                                  void* out, float* den_out, int T, int B, int H, int d, mhla_dtype dt,
                                  float eps, float gamma, void* stream);
 
+/* Causal MHLA inference, token by token ([MHLA] App. C, causal inference):
+ * tokens t0 .. t0 + T - 1 of each (b, h) sequence, whose blocks are the
+ * contiguous ranges of `block` tokens (block i holds tokens i*block ..).
+ *   q, k, v : [T, B, H, d] (dtype dt) — token t0 + n at [n]
+ *   mixing  : [H, M, M] fp32, read at and below the diagonal (m[h][i][b], b <= i)
+ *   S       : [B, H, M, d, d] fp32, in/out — slot b: the summary sum phi(k) v^T of
+ *             block b (S[c][e] = sum phi(k)_c v_e); slots of finished blocks are
+ *             frozen, the slot of the block holding token t0 holds its running
+ *             summary of the tokens before t0 (ignored, taken as zero, when t0
+ *             starts the block)
+ *   z       : [B, H, M, d] fp32, in/out — the same for sum phi(k)
+ *   out     : [T, B, H, d] (dtype dt);  den_out : [T, B, H] fp32 or NULL
+ *   Per token t in block i: S_i += phi(k) v^T; z_i += phi(k);
+ *     out = phi(q) (sum_{b<i} m_ib S_b + m_ii S_i)
+ *         / (phi(q) . (sum_{b<i} m_ib z_b + m_ii z_i) + eps);
+ *   on return the slots of the blocks the call touched hold their summaries
+ *   (running for the last one).  Token by token this equals
+ *   mhla_forward_causal with this mixing and chunk = block.
+ *   t0 + T must not pass M * block (MHLA_ERR_INVALID_ARG).  No workspace. */
+mhla_status mhla_causal_stream(const void* q, const void* k, const void* v, const float* mixing, float* S,
+                               float* z, void* out, float* den_out, int t0, int T, int B, int H, int d,
+                               int block, int M, mhla_dtype dt, float eps, void* stream);
+
 /* Workspace bytes for rala_forward; 0 if the sizes are invalid. */
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx);
 

@@ -162,6 +162,24 @@ def test_locality_mixing_matches_the_oracle(lib):
         binding.locality_mixing(0, 3)
 
 
+def test_causal_stream_argument_errors(lib):
+    def cs(q=P, S=4 * P, z=6 * P, out=7 * P, mix=8 * P, t0=0, T=5, B=2, H=2, d=64, block=64, M=4, eps=1e-6):
+        return lib.mhla_causal_stream(q, 2 * P, 3 * P, mix, S, z, out, None, t0, T, B, H, d, block, M, BF16,
+                                      eps, None)
+    assert cs(d=48) == INVALID
+    assert cs(t0=-1) == INVALID
+    assert cs(t0=250, T=7) == INVALID                      # past the last block (4 x 64 tokens)
+    assert cs(block=0) == INVALID
+    assert cs(M=0) == INVALID
+    assert cs(mix=None) == INVALID
+    assert cs(out=P) == INVALID                            # out aliases q
+    assert cs(z=4 * P + 64) == INVALID                     # z inside S
+    assert cs(eps=float("inf")) == INVALID
+    assert cs(T=0, q=None, out=None) == OK
+    assert lib.mhla_causal_stream(None, None, None, None, None, None, None, None, 0, 4, 0, 2, 64, 64, 4, BF16,
+                                  1e-6, None) == OK        # no units
+
+
 def test_rala_argument_errors(lib):
     def rala(cx=64, d=32, ws=8 * P, wsb=1 << 30, y=6 * P, x=4 * P):
         return lib.rala_forward(P, 2 * P, 3 * P, x, 5 * P, y, 2, 2, 3136, d, cx, BF16, ws, wsb, None)

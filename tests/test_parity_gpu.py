@@ -580,6 +580,118 @@ def test_grid_tiny_brute_force():
     assert_close_y(to_f64(y), ref, "f32")
 
 
+# ------------------------------------------------- causal MHLA inference (stream)
+def lower_mixing(seed, H, M):
+    """Row-normalised weights at and below the diagonal (above it: values the kernels must not read
+    into the result, here large)."""
+    u = np.tril(uniform(seed, 9, (H, M, M)) + 0.05)
+    mix = u / u.sum(axis=-1, keepdims=True) + np.triu(np.full((M, M), 7.0), 1)
+    mix = mix.astype(np.float32)
+    return torch.from_numpy(mix).cuda(), np.tril(mix.astype(np.float64))
+
+
+def stream_run(x, mix_t, S, z, block, t0, T, dtype):
+    """Tokens t0 .. t0 + T - 1 of the [B, H, N, d] inputs through mhla_causal_stream."""
+    sl = {n: x[n][:, :, t0:t0 + T].permute(2, 0, 1, 3).contiguous() for n in "qkv"}
+    out = torch.empty_like(sl["q"])
+    den = torch.empty(sl["q"].shape[:3], dtype=torch.float32, device="cuda")
+    binding.mhla_causal_stream(sl["q"], sl["k"], sl["v"], mix_t, S, z, out, t0, block, den_out=den)
+    return out, den
+
+
+STREAM = [  # B, H, N, d, block, dtype
+    (2, 3, 96, 16, 32, "f32"),
+    (1, 2, 256, 64, 64, "bf16"),
+    (1, 2, 256, 64, 64, "f32"),
+    (1, 2, 128, 128, 32, "bf16"),
+    (2, 1, 200, 32, 40, "f32"),
+]
+
+
+@pytest.mark.parametrize("shape", STREAM, ids=lambda s: "x".join(map(str, s)))
+def test_causal_stream_against_the_oracle(shape):
+    """Whole sequences token by token, in three calls cut inside blocks."""
+    B, H, N, d, block, dtype = shape
+    M = N // block
+    x = rand_inputs(600 + N + d, (B, H, N, d), dtype)
+    mix_t, mix64 = lower_mixing(601 + d, H, M)
+    S = torch.full((B, H, M, d, d), float("nan"), device="cuda")  # every slot is written before it is read
+    z = torch.full((B, H, M, d), float("nan"), device="cuda")
+    cuts = [0, block // 2 + 1, N - block - 3, N]
+    outs, dens = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        o, dn = stream_run(x, mix_t, S, z, block, a, b - a, dtype)
+        outs.append(o)
+        dens.append(dn)
+    torch.cuda.synchronize()
+    y = to_f64(torch.cat(outs).permute(1, 2, 0, 3))
+    den = to_f64(torch.cat(dens).permute(1, 2, 0))
+    ref, dref = oracle.causal_mhla_stream(x["q64"], x["k64"], x["v64"], mix64, block)
+    assert_close_y(y, ref, dtype)
+    assert_close_den(den, dref, dtype)
+    # the slots hold the blocks' summaries
+    kf = oracle.phi(x["k64"]).reshape(B, H, M, block, d)
+    s_ref = np.einsum("bhmtc,bhmte->bhmce", kf, x["v64"].reshape(B, H, M, block, d))
+    assert_close_y(to_f64(S).reshape(B * H * M, 1, d, d), s_ref.reshape(B * H * M, 1, d, d), "f32",
+                   what="block summaries")
+
+
+def test_causal_stream_equals_the_chunk_form():
+    """Token by token equals mhla_forward_causal with the same mixing and chunk = block."""
+    B, H, N, d, block = 2, 2, 512, 64, 128
+    M = N // block
+    x = rand_inputs(640, (B, H, N, d), "bf16")
+    mix_t, _ = lower_mixing(641, H, M)
+    S = torch.zeros(B, H, M, d, d, device="cuda")
+    z = torch.zeros(B, H, M, d, device="cuda")
+    o, dn = stream_run(x, mix_t, S, z, block, 0, N, "bf16")
+    yc, denc = forward_causal(x["q"], x["k"], x["v"], mix_t, block)
+    torch.cuda.synchronize()
+    assert slice_rel(to_f64(o.permute(1, 2, 0, 3)), yc) < 2e-2
+    assert rel(to_f64(dn.permute(1, 2, 0)), denc) < 1e-4
+
+
+def test_causal_stream_resumes_from_a_prefix_state():
+    """The slots filled from a P-token prefix by the oracle; the next tokens give rows P.. of the
+    oracle's stream over the whole sequence."""
+    B, H, N, d, block, P = 1, 3, 320, 32, 64, 150
+    M = N // block
+    x = rand_inputs(650, (B, H, N, d), "f32")
+    mix_t, mix64 = lower_mixing(651, H, M)
+    kf = oracle.phi(x["k64"][:, :, :P])
+    vp = x["v64"][:, :, :P]
+    S0 = np.zeros((B, H, M, d, d))
+    z0 = np.zeros((B, H, M, d))
+    for b in range((P + block - 1) // block):
+        sl = slice(b * block, min(P, (b + 1) * block))
+        S0[:, :, b] = np.einsum("bhtc,bhte->bhce", kf[:, :, sl], vp[:, :, sl])
+        z0[:, :, b] = kf[:, :, sl].sum(axis=2)
+    S = torch.from_numpy(S0.astype(np.float32)).cuda()
+    z = torch.from_numpy(z0.astype(np.float32)).cuda()
+    o, dn = stream_run(x, mix_t, S, z, block, P, N - P, "f32")
+    torch.cuda.synchronize()
+    ref, dref = oracle.causal_mhla_stream(x["q64"], x["k64"], x["v64"], mix64, block)
+    assert_close_y(to_f64(o.permute(1, 2, 0, 3)), ref[:, :, P:], "f32")
+    assert_close_den(to_f64(dn.permute(1, 2, 0)), dref[:, :, P:], "f32")
+
+
+def test_stream_full_workload_sampled_units():
+    """The stream workload in the bench's launch configuration (4096 units, 1024 tokens after a
+    2048-token prefix, M = 24): two units against the oracle over all 3072 tokens, and every
+    output finite."""
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    runner = bench.Runner(WORKLOADS["stream"], torch.device("cuda"), 126 << 20)
+    runner.step(0)
+    torch.cuda.synchronize()
+    s = runner.sets[0]
+    assert bool(torch.isfinite(s["out"].float()).all()) and bool((s["den"] > 1e-6).all())
+    res = bench.parity_of_stream(runner)
+    assert res["ok"], res
+
+
 # ------------------------------------------------------------ fused decode
 def decode_state(seed, P, B, H, d):
     """fp32 state (S, z) summarising a P-token random prefix, and its float64 values."""

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     linattn_decode_steps,
     load,
     locality_mixing,
+    mhla_causal_stream,
     mhla_forward,
     mhla_forward_causal,
     mhla_forward_grid,

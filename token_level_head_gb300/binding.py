@@ -30,6 +30,7 @@ _SIGNATURES = {
     "mhla_forward_causal": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "linattn_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "linattn_decode_steps": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp]),
+    "mhla_causal_stream": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "mhla_forward_grid": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "mhla_forward_grid_path": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "mhla_locality_mixing": (_i, [_vp, _i, _i]),
@@ -214,6 +215,28 @@ def mhla_forward_grid(q, k, v, mixing, y, grid_hw, tile_hw, *, eps=1e-6, den_out
                                       workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward_grid", st)
     return y
+
+
+def mhla_causal_stream(q, k, v, mixing, S, z, out, t0, block, *, eps=1e-6, den_out=None, stream=None):
+    """Causal MHLA inference for tokens t0 .. t0 + T - 1: q/k/v/out [T, B, H, d], mixing [H, M, M]
+    fp32, S [B, H, M, d, d] and z [B, H, M, d] fp32 block summaries (updated)."""
+    if q.dim() != 4 or S.dim() != 5:
+        raise ValueError("q: expected [T, B, H, d]; S: expected [B, H, M, d, d]")
+    T, B, H, d = q.shape
+    M = S.shape[2]
+    for name, t in (("k", k), ("v", v), ("out", out)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(mixing, "mixing", (H, M, M), torch.float32)
+    _expect(S, "S", (B, H, M, d, d), torch.float32)
+    _expect(z, "z", (B, H, M, d), torch.float32)
+    _expect(den_out, "den_out", (T, B, H), torch.float32)
+    dev = _same_device(q, k, v, mixing, S, z, out, den_out)
+    with torch.cuda.device(dev):
+        st = load().mhla_causal_stream(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(S), _ptr(z), _ptr(out),
+                                       _ptr(den_out), t0, T, B, H, d, block, M, _dtype(q), eps,
+                                       _stream(stream, dev))
+    _check("mhla_causal_stream", st)
+    return out
 
 
 def mhla_forward_causal(q, k, v, mixing, y, chunk, *, eps=1e-6, den_out=None, workspace=None,

@@ -71,6 +71,10 @@ cudaError_t simt_decode_launch(int units, int d, mhla_dtype dt, const void* q, c
 cudaError_t decode_steps_launch(int T_steps, int units, int d, mhla_dtype dt, const void* q, const void* k,
                                 const void* v, float* S, float* z, void* out, float* den_out, float eps,
                                 float gamma, cudaStream_t st);
+// ---- causal MHLA inference, token by token: one CTA per unit, running and mixed state in registers
+cudaError_t causal_stream_launch(int t0, int T_steps, int units, int H, int d, int block, int M, mhla_dtype dt,
+                                 const void* q, const void* k, const void* v, const float* mixing, float* S,
+                                 float* z, void* out, float* den_out, float eps, cudaStream_t st);
 size_t simt_rala_workspace(int B, int H, int N, int d, int cx);
 cudaError_t simt_rala_launch(int B, int H, int N, int d, int cx, mhla_dtype dt, const void* q,
                              const void* k, const void* v, const void* x, const void* w, void* y,

@@ -240,6 +240,36 @@ mhla_status linattn_decode_steps(const void* q, const void* k, const void* v, fl
                                        static_cast<cudaStream_t>(stream)));
 }
 
+mhla_status mhla_causal_stream(const void* q, const void* k, const void* v, const float* mixing, float* S,
+                               float* z, void* out, float* den_out, int t0, int T, int B, int H, int d,
+                               int block, int M, mhla_dtype dt, float eps, void* stream) {
+  if (T < 0 || B < 0 || H < 0 || t0 < 0 || block <= 0 || M <= 0 || !valid_d(d)) return MHLA_ERR_INVALID_ARG;
+  if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return MHLA_ERR_INVALID_ARG;
+  if ((long long)t0 + T > (long long)M * block) return MHLA_ERR_INVALID_ARG;  // past the last block
+  const size_t units = (size_t)B * H;
+  if (units == 0 || T == 0) return MHLA_OK;
+  if (!q || !k || !v || !mixing || !S || !z || !out) return MHLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(mixing) || !aligned16(S) ||
+      !aligned16(z) || !aligned16(out) || (den_out && !aligned16(den_out)))
+    return MHLA_ERR_INVALID_ARG;
+  if (units > 0x7fffffffu) return MHLA_ERR_UNSUPPORTED;
+  const size_t vb = (size_t)T * units * d * dtype_bytes(dt), sb = units * M * (size_t)d * d * sizeof(float),
+               zb = units * M * (size_t)d * sizeof(float), db = (size_t)T * units * sizeof(float),
+               mb = (size_t)H * M * M * sizeof(float);
+  const void* ins[] = {q, k, v, mixing};
+  const size_t inb[] = {vb, vb, vb, mb};
+  for (int i = 0; i < 4; ++i)
+    if (overlap(out, vb, ins[i], inb[i]) || overlap(S, sb, ins[i], inb[i]) || overlap(z, zb, ins[i], inb[i]) ||
+        (den_out && overlap(den_out, db, ins[i], inb[i])))
+      return MHLA_ERR_INVALID_ARG;
+  if (overlap(out, vb, S, sb) || overlap(out, vb, z, zb) || overlap(S, sb, z, zb) ||
+      (den_out && (overlap(den_out, db, out, vb) || overlap(den_out, db, S, sb) || overlap(den_out, db, z, zb))))
+    return MHLA_ERR_INVALID_ARG;
+  return from_cuda(causal_stream_launch(t0, T, (int)units, H, d, block, M, dt, q, k, v, mixing, S, z, out, den_out,
+                                        eps, static_cast<cudaStream_t>(stream)));
+}
+
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx) {
   if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256) return 0;
   const size_t a = simt_rala_workspace(B, H, N, d, cx);

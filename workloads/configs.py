@@ -18,7 +18,7 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, normal, normal_at,
+from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, lower_row_normalised_mixing, normal, normal_at,
                   normal_device, row_softmax_mixing, uniform_row_normalised_mixing)
 
 
@@ -26,7 +26,7 @@ from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, normal, normal_at
 class Workload:
     name: str
     index: int              # seed = SEED_BASE + index
-    kind: str               # "mhla" | "causal" | "decode" | "decode_steps" | "rala"
+    kind: str               # "mhla" | "causal" | "decode" | "decode_steps" | "stream" | "rala"
     B: int
     H: int
     N: int                  # tokens (decode: number of steps)
@@ -43,6 +43,8 @@ class Workload:
 
     @property
     def M(self) -> int:
+        if "M" in self.extra:
+            return self.extra["M"]
         return self.N // self.block if self.block else 0
 
     @property
@@ -69,6 +71,10 @@ WORKLOADS = {
     # the same decode workload with all 1024 steps in one fused call (state held on chip)
     "decode_fused": Workload("decode_fused", 4, "decode_steps", 256, 16, 1024, 64, 0, "bf16", 0.125,
                              extra={"prefix": 2048}),
+    # causal MHLA inference on the decode shape: 1024 tokens after a 2048-token prefix, blocks of
+    # 128 (M = 24 for the 3072 tokens), a causal mixing matrix; N counts the streamed tokens
+    "stream": Workload("stream", 4, "stream", 256, 16, 1024, 64, 128, "bf16", 0.125, "lower_uniform_rows",
+                       extra={"prefix": 2048, "M": 24}),
     # rank-augmented variant: 56x56 tokens, X [B, N, 64], W [64, 32]
     "rala": Workload("rala", 5, "rala", 64, 2, 3136, 32, 0, "bf16", 32 ** -0.5,
                      extra={"cx": 64}),
@@ -97,6 +103,8 @@ def make_mixing(wl: Workload) -> np.ndarray:
         m = row_softmax_mixing(wl.seed, wl.H, wl.M, diag_boost=2.0)
     elif wl.mixing == "softmax":
         m = row_softmax_mixing(wl.seed, wl.H, wl.M)
+    elif wl.mixing == "lower_uniform_rows":
+        m = lower_row_normalised_mixing(wl.seed, wl.H, wl.M)
     elif wl.mixing == "ones":
         m = np.ones((wl.H, wl.M, wl.M))
     else:

@@ -133,6 +133,13 @@ def row_softmax_mixing(seed: int, h: int, m: int, diag_boost: float = 0.0) -> np
     return e / e.sum(axis=-1, keepdims=True)
 
 
+def lower_row_normalised_mixing(seed: int, h: int, m: int) -> np.ndarray:
+    """[h, m, m] causal mixing: U(0,1) + 0.05 entries at and below the diagonal, zero above,
+    each row divided by its sum."""
+    u = np.tril(uniform(seed, TID["mix"], (h, m, m)) + 0.05)
+    return u / u.sum(axis=-1, keepdims=True)
+
+
 # ------------------------------------------------------------------- torch
 def _signed(x: int) -> int:
     x &= _M64
