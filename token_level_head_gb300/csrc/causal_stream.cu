@@ -56,7 +56,7 @@ causal_stream_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   __shared__ __align__(16) T ring[kPipe][3][D];
   __shared__ float sq[2][D], sk[2][D], sv[2][D];  // phi(q), phi(k), v of a token, by parity
   __shared__ float red[G][D];
-  __shared__ float sden[D];
+  __shared__ float sden[(D + 31) / 32];  // per-warp sums of the denominator terms
   if (T_steps <= 0) return;
   const int u = blockIdx.x, tid = threadIdx.x;
   const int e = tid % D, g = tid / D;
@@ -101,18 +101,24 @@ causal_stream_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
       // first token, else the slot's), and P_bi from the frozen summaries
       const bool fresh = t % block == 0;
       mii = mh[(size_t)bi * M + bi];
+      float p[RPT];
+#pragma unroll
+      for (int j = 0; j < RPT; ++j) p[j] = 0.f;
+      float pz = 0.f;
+      for (int b = 0; b < bi; ++b) {  // the RPT loads of a block are independent
+        const float w = mh[(size_t)bi * M + b];
+        const float* sb = Su + (size_t)b * D * D + e;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) p[j] = fmaf(w, sb[(size_t)(g + G * j) * D], p[j]);
+        if (tid < D) pz = fmaf(w, zu[(size_t)b * D + tid], pz);
+      }
 #pragma unroll
       for (int j = 0; j < RPT; ++j) {
-        const int c = g + G * j;
-        float p = 0.f;
-        for (int b = 0; b < bi; ++b) p = fmaf(mh[(size_t)bi * M + b], Su[((size_t)b * D + c) * D + e], p);
-        sc[j] = fresh ? 0.f : Su[((size_t)bi * D + c) * D + e];
-        r[j] = fmaf(mii, sc[j], p);
+        sc[j] = fresh ? 0.f : Su[((size_t)bi * D + g + G * j) * D + e];
+        r[j] = fmaf(mii, sc[j], p[j]);
       }
       if (tid < D) {
-        float p = 0.f;
-        for (int b = 0; b < bi; ++b) p = fmaf(mh[(size_t)bi * M + b], zu[(size_t)b * D + tid], p);
-        zeta = p;
+        zeta = pz;
         zc = fresh ? 0.f : zu[(size_t)bi * D + tid];
       }
       cur = bi;
@@ -134,14 +140,21 @@ causal_stream_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
       part = fmaf(pq[c], r[j], part);
     }
     red[g][e] = part;
-    if (tid < D) {
-      zc += pk[tid];
-      sden[tid] = pq[tid] * fmaf(mii, zc, zeta);
+    if (tid < ((D + 31) & ~31)) {  // the warps holding z rows: warp sums of phi(q)_c (zeta_c + m_ii z_c)
+      float dp = 0.f;
+      if (tid < D) {
+        zc += pk[tid];
+        dp = pq[tid] * fmaf(mii, zc, zeta);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dp += __shfl_xor_sync(0xffffffffu, dp, o);
+      if ((tid & 31) == 0) sden[tid >> 5] = dp;
     }
     __syncthreads();
     if (tid < D) {
       float den = 0.f;
-      for (int c = 0; c < D; ++c) den += sden[c];
+#pragma unroll
+      for (int w = 0; w < (D + 31) / 32; ++w) den += sden[w];
       den += eps;
       float num = 0.f;
 #pragma unroll
