@@ -38,6 +38,13 @@ from .mhla_oracle import (  # noqa: F401
     causal_mhla_bruteforce,
     decode_steps,
     decayed_causal_bruteforce,
+    phi_relu,
+    phi_exp,
+    FEATURE_MAPS,
+    mhla_block_form_feature,
+    mhla_token_expansion_feature,
+    causal_variant_recurrent,
+    causal_variant_bruteforce,
     mhla_block_form_unnormalized,
     grid_block_ids,
     mhla_block_form_ids,

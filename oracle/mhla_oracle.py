@@ -50,6 +50,16 @@ PIN_STATUS = {
     "mhla_token_expansion_ids": "equals mhla_token_expansion for contiguous ids",
     "locality_mixing_init": "hand-computed 1 x 3 and 2 x 2 grids; rows sum to 1, diagonal largest",
     "causal_mhla_stream": "equals causal_mhla_bruteforce; all-ones mixing equals causal linear attention",
+    "phi_relu": "closed-form values at -1, 0, 2",
+    "phi_exp": "closed-form values at 0, ln 2",
+    "mhla_block_form_feature": "equals its token expansion for each feature map and with / without the "
+                               "normaliser; ReLU with Q <= 0 gives Y = 0, den = eps; hand-derived d = 1 "
+                               "exp example; elu1 equals mhla_block_form",
+    "mhla_token_expansion_feature": "hand-derived d = 1 exp example; ReLU with Q <= 0 gives Y = 0",
+    "causal_variant_recurrent": "equals its brute force for every feature and decay; gamma = 1, elu1 equals "
+                                "causal_bruteforce; gamma = 0 keeps only the token itself",
+    "causal_variant_bruteforce": "gamma = 1, elu1 equals causal_bruteforce; decayed elu1 equals "
+                                 "decayed_causal_bruteforce; gamma = 0 closed form",
     "rala_forward": "brute form; closed forms at Q=0 and K=0; softmax weights sum to 1",
     "rala_bruteforce": "closed forms at Q=0 and K=0; hand-derived golden fixture",
     "numerical_rank": "diagonal matrices of known rank",
@@ -345,6 +355,100 @@ def decayed_causal_bruteforce(q, k, v, gamma, eps=1e-6, s0=None, z0=None):
         num = num + g[:, None] * np.einsum("...tc,...ce->...te", qf, _f64(s0))
         dn = dn + g * np.einsum("...tc,...c->...t", qf, _f64(z0))
     return num / dn[..., None], dn
+
+
+def phi_relu(x):
+    """Feature map phi(x) = ReLU(x) = max(x, 0): Linear Attention notes §二 (third listed choice)."""
+    return np.maximum(_f64(x), 0.0)
+
+
+def phi_exp(x):
+    """Feature map phi(x) = exp(x): Linear Attention notes §二 (second listed choice)."""
+    return np.exp(_f64(x))
+
+
+# Linear Attention notes §二's kernel choices by name.
+FEATURE_MAPS = {"elu1": phi, "relu": phi_relu, "exp": phi_exp}
+
+
+def mhla_block_form_feature(q, k, v, mixing, block_size, feature="elu1", eps=1e-6, normalise=True):
+    """MHLA block form with the feature map of the Linear Attention notes §二 named by
+    ``feature``, and with the normaliser left out when ``normalise`` is false (MHLA paper §4.1:
+    it may be omitted; then Y is the numerator alone).  Returns ``(Y, den)``; ``den`` is the
+    denominator phi(q)^T z~ + eps either way.
+
+    S_b = sum_{t in b} phi(k_t) v_t^T, z_b = sum_{t in b} phi(k_t); S~_i = sum_b m_ib S_b;
+    Y_t = phi(q_t)^T S~_{b(t)} [/ (phi(q_t)^T z~_{b(t)} + eps)].
+    """
+    f = FEATURE_MAPS[feature]
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bsz, nh, n, d = q.shape
+    m, mix = _check_blocks(n, block_size, mixing)
+    kb = f(k).reshape(bsz, nh, m, block_size, d)
+    vb = v.reshape(bsz, nh, m, block_size, d)
+    s_b = np.einsum("bhmjc,bhmje->bhmce", kb, vb)
+    z_b = kb.sum(axis=3)
+    s_mix = np.einsum("hib,zhbce->zhice", mix, s_b)
+    z_mix = np.einsum("hib,zhbc->zhic", mix, z_b)
+    qb = f(q).reshape(bsz, nh, m, block_size, d)
+    num = np.einsum("bhitc,bhice->bhite", qb, s_mix).reshape(bsz, nh, n, d)
+    den = np.einsum("bhitc,bhic->bhit", qb, z_mix).reshape(bsz, nh, n) + eps
+    return (num / den[..., None] if normalise else num), den
+
+
+def mhla_token_expansion_feature(q, k, v, mixing, block_size, feature="elu1", eps=1e-6, normalise=True):
+    """Brute force of :func:`mhla_block_form_feature`: scores A_ts = m_{b(t),b(s)}
+    phi(q_t)^T phi(k_s) (MHLA paper §4.2 eq. 5 with the notes' §二 feature map),
+    Y_t = sum_s A_ts v_s [/ (sum_s A_ts + eps)].  Returns ``(Y, den)``."""
+    f = FEATURE_MAPS[feature]
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n = q.shape[-2]
+    _, mix = _check_blocks(n, block_size, mixing)
+    b = block_of(n, block_size)
+    a = np.einsum("zhtc,zhsc->zhts", f(q), f(k)) * mix[:, b[:, None], b[None, :]][None]
+    den = a.sum(axis=-1) + eps
+    num = np.einsum("zhts,zhse->zhte", a, v)
+    return (num / den[..., None] if normalise else num), den
+
+
+def causal_variant_recurrent(q, k, v, feature="elu1", gamma=1.0, eps=1e-6, normalise=True):
+    """Causal linear attention by its recurrence with the notes' variants.  Returns ``(Y, den)``.
+
+    Linear Attention notes §四 recurrence, §七 RetNet decay (S_t = gamma S_{t-1} + phi(k_t)
+    v_t^T; z decays the same way) and §二 feature map; MHLA paper §4.1: without the
+    normaliser Y_t = phi(q_t)^T S_t.  ``q, k, v``: [..., N, d].
+    """
+    f = FEATURE_MAPS[feature]
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    *lead, n, d = q.shape
+    s = np.zeros((*lead, d, d))
+    z = np.zeros((*lead, d))
+    y = np.empty_like(v)
+    den = np.empty((*lead, n))
+    for t in range(n):
+        qt, kt = f(q[..., t, :]), f(k[..., t, :])
+        s = gamma * s + kt[..., :, None] * v[..., t, None, :]
+        z = gamma * z + kt
+        dn = np.einsum("...c,...c->...", qt, z) + eps
+        num = np.einsum("...c,...ce->...e", qt, s)
+        y[..., t, :] = num / dn[..., None] if normalise else num
+        den[..., t] = dn
+    return y, den
+
+
+def causal_variant_bruteforce(q, k, v, feature="elu1", gamma=1.0, eps=1e-6, normalise=True):
+    """Causal linear attention with the notes' variants from the explicit weights
+    gamma^(t-s) phi(q_t)^T phi(k_s), s <= t (Linear Attention notes §七 unrolled, §二 feature
+    map; MHLA paper §4.1 for the optional normaliser).  Returns ``(Y, den)``."""
+    f = FEATURE_MAPS[feature]
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    n = q.shape[-2]
+    t = np.arange(n)
+    w = np.where(t[:, None] >= t[None, :], float(gamma) ** np.maximum(t[:, None] - t[None, :], 0), 0.0)
+    a = np.einsum("...tc,...sc->...ts", f(q), f(k)) * w
+    num = np.einsum("...ts,...se->...te", a, v)
+    dn = a.sum(axis=-1) + eps
+    return (num / dn[..., None] if normalise else num), dn
 
 
 def _rala_weights(q1, k1):

@@ -430,3 +430,72 @@ def test_causal_mhla_stream_equals_bruteforce(causal_small):
     y3, d3 = oracle.causal_mhla_stream(q, k, v, np.ones((2, 4, 4)), 24, 1e-6)
     ref, dref = oracle.causal_recurrent(q, k, v, 1e-6)
     assert close(y3, ref, 1e-11) and close(d3, dref, 1e-11)
+
+
+# ------------------------------------------- feature maps, normaliser, decay
+def test_other_feature_maps_closed_forms():
+    assert oracle.phi_relu(-1.0) == 0.0 and oracle.phi_relu(0.0) == 0.0 and oracle.phi_relu(2.0) == 2.0
+    assert oracle.phi_exp(0.0) == 1.0
+    assert math.isclose(oracle.phi_exp(math.log(2.0)), 2.0, rel_tol=1e-15)
+
+
+@pytest.mark.parametrize("feature", ["elu1", "relu", "exp"])
+@pytest.mark.parametrize("normalise", [True, False])
+def test_feature_block_form_equals_token_expansion(feature, normalise):
+    q = normal(31, 1, (2, 2, 48, 6), 0.6)
+    k = normal(31, 2, (2, 2, 48, 6), 0.6)
+    v = normal(31, 3, (2, 2, 48, 6))
+    u = uniform(31, 4, (2, 4, 4)) + 0.05
+    mix = u / u.sum(axis=-1, keepdims=True)
+    y1, d1 = oracle.mhla_block_form_feature(q, k, v, mix, 12, feature, 1e-6, normalise)
+    y2, d2 = oracle.mhla_token_expansion_feature(q, k, v, mix, 12, feature, 1e-6, normalise)
+    assert close(y1, y2, 1e-11) and close(d1, d2, 1e-11)
+    if feature == "elu1":  # the default map is the block form's own
+        ref, dref = oracle.mhla_block_form(q, k, v, mix, 12, 1e-6)
+        assert close(d1, dref, 1e-11)
+        assert close(y1, ref if normalise else ref * dref[..., None], 1e-11)
+
+
+def test_relu_features_of_nonpositive_queries_give_zero():
+    q = -np.abs(normal(32, 1, (1, 2, 16, 4)))
+    k = normal(32, 2, (1, 2, 16, 4))
+    v = normal(32, 3, (1, 2, 16, 4))
+    mix = np.ones((2, 2, 2))
+    for fn in (oracle.mhla_block_form_feature, oracle.mhla_token_expansion_feature):
+        y, den = fn(q, k, v, mix, 8, "relu", 1e-6)
+        assert np.all(y == 0.0) and np.all(den == 1e-6)
+
+
+def test_exp_feature_by_hand():
+    # d = 1, one block: phi(q) = 1, phi(k) = (1, 2), v = (1, 3):
+    # Y = (1*1*1 + 1*2*3) / (1 + 2 + eps) for both queries, which share phi(q) = 1
+    q = as4([[0.0], [0.0]])
+    k = as4([[0.0], [math.log(2.0)]])
+    v = as4([[1.0], [3.0]])
+    for fn in (oracle.mhla_block_form_feature, oracle.mhla_token_expansion_feature):
+        y, den = fn(q, k, v, np.ones((1, 1, 1)), 2, "exp", 0.0)
+        assert close(y[0, 0, :, 0], [7.0 / 3.0, 7.0 / 3.0], 1e-14) and close(den[0, 0], [3.0, 3.0], 1e-14)
+
+
+@pytest.mark.parametrize("feature", ["elu1", "relu", "exp"])
+@pytest.mark.parametrize("gamma", [1.0, 0.9, 0.5])
+def test_causal_variant_recurrence_equals_bruteforce(causal_small, feature, gamma):
+    q, k, v = causal_small
+    for normalise in (True, False):
+        y1, d1 = oracle.causal_variant_recurrent(q, k, v, feature, gamma, 1e-6, normalise)
+        y2, d2 = oracle.causal_variant_bruteforce(q, k, v, feature, gamma, 1e-6, normalise)
+        assert close(y1, y2, 1e-10) and close(d1, d2, 1e-10)
+
+
+def test_causal_variants_reduce_to_the_pinned_forms(causal_small):
+    q, k, v = causal_small
+    y, d = oracle.causal_variant_bruteforce(q, k, v)
+    ref, dref = oracle.causal_bruteforce(q, k, v, 1e-6)
+    assert close(y, ref, 1e-11) and close(d, dref, 1e-11)
+    y, d = oracle.causal_variant_bruteforce(q, k, v, "elu1", 0.8)
+    ref, dref = oracle.decayed_causal_bruteforce(q, k, v, 0.8, 1e-6)
+    assert close(y, ref, 1e-11) and close(d, dref, 1e-11)
+    # gamma = 0: every token attends to itself alone, Y_t = a_tt v_t / (a_tt + eps)
+    y, d = oracle.causal_variant_recurrent(q, k, v, "elu1", 0.0)
+    a = np.einsum("bhtc,bhtc->bht", oracle.phi(q), oracle.phi(k))
+    assert close(y, a[..., None] * v / (a + 1e-6)[..., None], 1e-12)
