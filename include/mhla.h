@@ -119,6 +119,41 @@ mhla_status mhla_forward_causal(const void* q, const void* k, const void* v, con
                                 mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes,
                                 void* stream);
 
+/* Variants of the forward (mhla_forward_ex). */
+typedef enum {
+  MHLA_PHI_ELU1 = 0, /* phi(x) = ELU(x) + 1 (the default everywhere)   [LA §二] */
+  MHLA_PHI_RELU = 1, /* phi(x) = max(x, 0)                              [LA §二] */
+  MHLA_PHI_EXP = 2   /* phi(x) = exp(x)                                 [LA §二] */
+} mhla_feature;
+
+typedef struct {
+  int feature;   /* an mhla_feature */
+  int normalise; /* 1: Y = numerator / (phi(q) . z~ + eps) (default);
+                    0: Y = numerator alone ([MHLA] §4.1: the normalisation may be
+                    omitted for long sequences); den_out, if given, still receives
+                    the denominator */
+  float gamma;   /* RetNet decay of plain causal linear attention ([LA] §七), in
+                    [0, 1]; 1 = none.  Y_t = sum_{s<=t} gamma^(t-s) (phi(q_t).phi(k_s)) v_s
+                    / (sum_{s<=t} gamma^(t-s) phi(q_t).phi(k_s) + eps) */
+} mhla_options;
+
+/* mhla_forward with variants (opt NULL = the defaults {ELU1, 1, 1.0}, exactly
+ * mhla_forward).  gamma != 1 needs causal = 1 and mixing = NULL (plain causal
+ * linear attention), else MHLA_ERR_INVALID_ARG; a feature outside the enum,
+ * normalise not 0 / 1 or gamma outside [0, 1] are MHLA_ERR_INVALID_ARG.  The
+ * tensor-core kernels take ELU + 1 without decay (normalise 0 or 1); the other
+ * variants run on the SIMT kernels.  Same workspace as mhla_forward. */
+mhla_status mhla_forward_ex(const void* q, const void* k, const void* v, const float* mixing,
+                            void* y, float* den_out, int B, int H, int N, int d, int block_size,
+                            int causal, mhla_dtype dt, float eps, const mhla_options* opt,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Kernel family mhla_forward_ex would use for these arguments (no launch);
+ * `with_mixing` says whether a mixing matrix is passed (it selects causal MHLA
+ * or plain causal linear attention when causal = 1). */
+mhla_path mhla_forward_ex_path(int B, int H, int N, int d, int block_size, int causal, int with_mixing,
+                               mhla_dtype dt, const mhla_options* opt);
+
 /* Non-causal MHLA with 2-D blocks ([MHLA] §4.1: for images the blocks lie on
  * a 2-D grid, Fig. 4b).  The N = grid_h * grid_w tokens of each (b, h) slice
  * are a grid_h x grid_w grid in row-major order (token t = row * grid_w + col,

@@ -180,6 +180,33 @@ def test_causal_stream_argument_errors(lib):
                                   1e-6, None) == OK        # no units
 
 
+def test_options_argument_errors(lib):
+    import ctypes
+    def ex(feature=0, normalise=1, gamma=1.0, causal=0, mix=4 * P, B=2):
+        opt = binding.MhlaOptions(feature, normalise, gamma)
+        return lib.mhla_forward_ex(P, 2 * P, 3 * P, mix, 5 * P, None, B, 2, 256, 64, 64, causal, BF16, 1e-6,
+                                   ctypes.byref(opt), 8 * P, 1 << 30, None)
+    assert ex(feature=3) == INVALID
+    assert ex(normalise=2) == INVALID
+    assert ex(gamma=1.5) == INVALID
+    assert ex(gamma=0.9) == INVALID                        # decay outside plain causal linear attention
+    assert ex(gamma=0.9, causal=1) == INVALID              # causal MHLA (mixing given) has no decay
+    assert ex(gamma=0.9, causal=1, mix=None, B=0) == OK    # plain causal, no units
+    assert ex(feature=2, B=0) == OK
+    path = lambda **kw: binding.mhla_forward_ex_path(8, 6, 4096, 64, 256, 0, 1, torch_bf16(), **kw)  # noqa: E731
+    assert path() == "tcgen05" and path(normalise=False) == "tcgen05"
+    assert path(feature="relu") == "simt" and path(feature="exp") == "simt"
+    assert binding.mhla_forward_ex_path(4, 16, 8192, 64, 128, 1, 0, torch_bf16(), gamma=0.9) == "simt"
+    assert binding.mhla_forward_ex_path(4, 16, 8192, 64, 128, 0, 1, torch_bf16(), gamma=0.9) == "none"
+    with pytest.raises(ValueError, match="feature"):
+        binding.mhla_forward_ex_path(1, 1, 256, 64, 64, 0, 1, torch_bf16(), feature="tanh")
+
+
+def torch_bf16():
+    import torch
+    return torch.bfloat16
+
+
 def test_rala_argument_errors(lib):
     def rala(cx=64, d=32, ws=8 * P, wsb=1 << 30, y=6 * P, x=4 * P):
         return lib.rala_forward(P, 2 * P, 3 * P, x, 5 * P, y, 2, 2, 3136, d, cx, BF16, ws, wsb, None)

@@ -508,6 +508,92 @@ def test_decode_full_workload_sampled_units():
     assert_close_y(to_f64(Sf[sel])[:, None], s_t[:, None], "f32", what="state S")
 
 
+# ------------------------------------------ variants: phi, normaliser, decay
+VARIANT_SHAPES = [  # B, H, N, d, block, dtype
+    (2, 3, 192, 16, 64, "f32"),
+    (1, 2, 512, 64, 128, "bf16"),
+    (2, 2, 256, 32, 256, "f32"),
+]
+
+
+@pytest.mark.parametrize("feature", ["relu", "exp"])
+@pytest.mark.parametrize("normalise", [True, False])
+@pytest.mark.parametrize("shape", VARIANT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_feature_variants_noncausal(shape, feature, normalise):
+    B, H, N, d, block, dtype = shape
+    assert binding.mhla_forward_ex_path(B, H, N, d, block, 0, 1, torch_dtype(dtype), feature=feature) == "simt"
+    x = rand_inputs(700 + N + d, (B, H, N, d), dtype)
+    mix_t, mix64 = rand_mixing(701, H, N // block)
+    y = torch.empty_like(x["q"])
+    den = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    binding.mhla_forward_ex(x["q"], x["k"], x["v"], mix_t, y, block, feature=feature, normalise=normalise,
+                            den_out=den)
+    torch.cuda.synchronize()
+    ref, dref = oracle.mhla_block_form_feature(x["q64"], x["k64"], x["v64"], mix64, block, feature, 1e-6,
+                                               normalise)
+    assert_close_y(to_f64(y), ref, dtype)
+    assert_close_den(to_f64(den), dref, dtype)
+
+
+# normaliser-free output on every kernel family: SIMT, tcgen05, tcgen05 stream, causal tcgen05
+UNNORM = [  # B, H, N, d, block, causal, dtype, path
+    (2, 3, 256, 32, 64, 0, "f32", "simt"),
+    (2, 6, 4096, 64, 256, 0, "bf16", "tcgen05"),
+    (2, 3, 1152, 64, 384, 0, "bf16", "tcgen05_stream"),
+    (2, 4, 2048, 64, 128, 1, "bf16", "tcgen05"),
+    (1, 2, 384, 32, 64, 1, "f32", "simt"),
+]
+
+
+@pytest.mark.parametrize("shape", UNNORM, ids=lambda s: "x".join(map(str, s[:6])) + f"-{s[6]}")
+def test_normaliser_free_output(shape):
+    B, H, N, d, block, causal, dtype, path = shape
+    assert binding.mhla_forward_ex_path(B, H, N, d, block, causal, 0 if causal else 1, torch_dtype(dtype),
+                                        normalise=False) == path
+    x = rand_inputs(720 + N + d, (B, H, N, d), dtype)
+    mix_t, mix64 = (None, None) if causal else rand_mixing(721, H, N // block)
+    y = torch.empty_like(x["q"])
+    den = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    binding.mhla_forward_ex(x["q"], x["k"], x["v"], mix_t, y, block, causal=causal, normalise=False, den_out=den)
+    torch.cuda.synchronize()
+    if causal:
+        ref, dref = oracle.causal_variant_bruteforce(x["q64"], x["k64"], x["v64"], "elu1", 1.0, 1e-6, False)
+    else:
+        ref, dref = oracle.mhla_block_form_feature(x["q64"], x["k64"], x["v64"], mix64, block, "elu1", 1e-6,
+                                                   False)
+    assert_close_y(to_f64(y), ref, dtype)
+    assert_close_den(to_f64(den), dref, dtype)
+
+
+@pytest.mark.parametrize("gamma", [0.9, 0.99, 0.0])
+@pytest.mark.parametrize("shape", [(2, 2, 320, 32, 64, "f32"), (1, 3, 512, 64, 128, "bf16"),
+                                   (1, 2, 300, 16, 60, "f32")], ids=lambda s: "x".join(map(str, s)))
+def test_causal_decay(shape, gamma):
+    """Plain causal linear attention with RetNet decay, chunked on the SIMT kernels, against the
+    explicit decayed weights; the result must not depend on the chunk."""
+    B, H, N, d, chunk, dtype = shape
+    assert binding.mhla_forward_ex_path(B, H, N, d, chunk, 1, 0, torch_dtype(dtype), gamma=gamma) == "simt"
+    x = rand_inputs(740 + N + d, (B, H, N, d), dtype)
+    y = torch.empty_like(x["q"])
+    den = torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    binding.mhla_forward_ex(x["q"], x["k"], x["v"], None, y, chunk, causal=1, gamma=gamma, den_out=den)
+    torch.cuda.synchronize()
+    ref, dref = oracle.causal_variant_bruteforce(x["q64"], x["k64"], x["v64"], "elu1", gamma)
+    assert_close_y(to_f64(y), ref, dtype)
+    assert_close_den(to_f64(den), dref, dtype)
+
+
+def test_causal_decay_with_relu_and_no_normaliser():
+    B, H, N, d, chunk = 1, 2, 256, 32, 64
+    x = rand_inputs(760, (B, H, N, d), "f32")
+    y = torch.empty_like(x["q"])
+    binding.mhla_forward_ex(x["q"], x["k"], x["v"], None, y, chunk, causal=1, gamma=0.95, feature="relu",
+                            normalise=False)
+    torch.cuda.synchronize()
+    ref, _ = oracle.causal_variant_recurrent(x["q64"], x["k64"], x["v64"], "relu", 0.95, 1e-6, False)
+    assert_close_y(to_f64(y), ref, "f32")
+
+
 # ----------------------------------------------------------- 2-D grid blocks
 GRID = [  # B, H, grid_h, grid_w, tile_h, tile_w, d, dtype, mixing, path
     (2, 3, 12, 20, 3, 5, 16, "f32", "random", "simt"),

@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     mhla_causal_stream,
     mhla_forward,
     mhla_forward_causal,
+    mhla_forward_ex,
+    mhla_forward_ex_path,
     mhla_forward_grid,
     mhla_forward_grid_path,
     mhla_forward_noalloc,

@@ -31,6 +31,8 @@ _SIGNATURES = {
     "linattn_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "linattn_decode_steps": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _vp]),
     "mhla_causal_stream": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp]),
+    "mhla_forward_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp]),
+    "mhla_forward_ex_path": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "mhla_forward_grid": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "mhla_forward_grid_path": (_i, [_i, _i, _i, _i, _i, _i, _i, _i]),
     "mhla_locality_mixing": (_i, [_vp, _i, _i]),
@@ -186,6 +188,46 @@ def mhla_forward(q, k, v, mixing, y, block_size, *, causal=0, eps=1e-6, den_out=
                                  B, H, N, d, block_size, causal, _dtype(q), eps, _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward", st)
+    return y
+
+
+FEATURES = {"elu1": 0, "relu": 1, "exp": 2}
+
+
+class MhlaOptions(ctypes.Structure):
+    """The C struct mhla_options: feature map, normaliser on / off, causal decay."""
+    _fields_ = [("feature", ctypes.c_int), ("normalise", ctypes.c_int), ("gamma", ctypes.c_float)]
+
+
+def _options(feature, normalise, gamma):
+    if feature not in FEATURES:
+        raise ValueError(f"feature: one of {sorted(FEATURES)}, got {feature!r}")
+    return MhlaOptions(FEATURES[feature], 1 if normalise else 0, float(gamma))
+
+
+def mhla_forward_ex_path(B, H, N, d, block_size, causal, with_mixing, dtype, *, feature="elu1", normalise=True,
+                         gamma=1.0) -> str:
+    dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
+    opt = _options(feature, normalise, gamma)
+    return PATH_NAMES[int(load().mhla_forward_ex_path(B, H, N, d, block_size, causal, int(bool(with_mixing)), dt,
+                                                      ctypes.byref(opt)))]
+
+
+def mhla_forward_ex(q, k, v, mixing, y, block_size, *, causal=0, feature="elu1", normalise=True, gamma=1.0,
+                    eps=1e-6, den_out=None, workspace=None, stream=None):
+    """mhla_forward with variants: feature map ("elu1", "relu", "exp"), normalise (False: the
+    numerator alone), gamma (decay; plain causal linear attention, mixing None, only)."""
+    opt = _options(feature, normalise, gamma)
+    B, H, N, d = _mhla_args(q, k, v, mixing, y, den_out, block_size, mixing_required=not causal)
+    dev = _same_device(q, k, v, mixing, y, den_out, workspace)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(mhla_workspace_bytes(B, H, N, d, block_size, causal), dev)
+        st = load().mhla_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(y), _ptr(den_out),
+                                    B, H, N, d, block_size, causal, _dtype(q), eps, ctypes.byref(opt),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream, dev))
+    _check("mhla_forward_ex", st)
     return y
 
 

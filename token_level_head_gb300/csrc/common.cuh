@@ -36,6 +36,11 @@ class SmemOptIn {
 // ("Linear Attention notes" §二, first kernel choice).
 __device__ __forceinline__ float phi(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
+// The feature maps of "Linear Attention notes" §二: 0 = ELU + 1, 1 = ReLU, 2 = exp.
+__device__ __forceinline__ float phi_k(float x, int kind) {
+  return kind == 0 ? phi(x) : kind == 1 ? fmaxf(x, 0.f) : expf(x);
+}
+
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 

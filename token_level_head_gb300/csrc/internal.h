@@ -18,7 +18,13 @@ struct MhlaShape {
   // th x tw tiles numbered row-major; gw == 0 means contiguous blocks of `block` tokens.
   // With a grid, N = gh * gw and block = th * tw.
   int gh = 0, gw = 0, th = 0, tw = 0;
+  // Variants: feature map (0 ELU + 1, 1 ReLU, 2 exp), whether Y is divided by the
+  // denominator, and the decay gamma of plain causal linear attention (1 = none).
+  int phi_kind = 0;
+  bool normalise = true;
+  float gamma = 1.f;
   int heads() const { return B * H; }
+  bool plain_phi() const { return phi_kind == 0 && gamma == 1.f; }
   int M() const { return N / block; }
   bool grid() const { return gw > 0; }
 };

@@ -97,14 +97,28 @@ static bool grid_ok(int gh, int gw, int th, int tw) {
          (long long)gh * gw <= 0x7fffffffLL && (long long)th * tw <= 0x7fffffffLL;
 }
 
+// Options valid for this form (mode)?  Fills the variant fields of s.
+static bool apply_options(MhlaShape& s, const mhla_options* opt, MixMode mode) {
+  if (opt == nullptr) return true;
+  if (opt->feature < MHLA_PHI_ELU1 || opt->feature > MHLA_PHI_EXP) return false;
+  if (opt->normalise != 0 && opt->normalise != 1) return false;
+  if (!std::isfinite(opt->gamma) || opt->gamma < 0.f || opt->gamma > 1.f) return false;
+  if (opt->gamma != 1.f && mode != MIX_PREFIX) return false;  // decay: plain causal linear attention only
+  s.phi_kind = opt->feature;
+  s.normalise = opt->normalise != 0;
+  s.gamma = opt->gamma;
+  return true;
+}
+
 static mhla_status run_mhla(const void* q, const void* k, const void* v, const float* mixing,
                             void* y, float* den_out, int B, int H, int N, int d, int block,
                             MixMode mode, mhla_dtype dt, float eps, void* ws, size_t ws_bytes,
-                            void* stream, const int* grid = nullptr) {
+                            void* stream, const int* grid = nullptr, const mhla_options* opt = nullptr) {
   mhla_status st = check_mhla(q, k, v, y, den_out, B, H, N, d, block, dt, eps, ws, ws_bytes, mode != MIX_FULL);
   if (st != MHLA_OK || (size_t)B * H * N == 0) return st;
   if (mode != MIX_PREFIX && (!mixing || !aligned16(mixing))) return MHLA_ERR_INVALID_ARG;
   MhlaShape s{B, H, N, d, block};
+  if (!apply_options(s, opt, mode)) return MHLA_ERR_INVALID_ARG;
   if (grid != nullptr) {  // {gh, gw, th, tw}, validated by the caller
     s.gh = grid[0];
     s.gw = grid[1];
@@ -132,6 +146,31 @@ mhla_status mhla_forward(const void* q, const void* k, const void* v, const floa
                                workspace, workspace_bytes, stream);
   return run_mhla(q, k, v, mixing, y, den_out, B, H, N, d, block_size, MIX_FULL, dt, eps,
                   workspace, workspace_bytes, stream);
+}
+
+mhla_status mhla_forward_ex(const void* q, const void* k, const void* v, const float* mixing,
+                            void* y, float* den_out, int B, int H, int N, int d, int block_size,
+                            int causal, mhla_dtype dt, float eps, const mhla_options* opt,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (causal != 0 && causal != 1) return MHLA_ERR_INVALID_ARG;
+  const MixMode mode = !causal ? MIX_FULL : mixing ? MIX_STRICT_LOWER : MIX_PREFIX;
+  MhlaShape probe{B, H, N, d, block_size};
+  if (!apply_options(probe, opt, mode)) return MHLA_ERR_INVALID_ARG;  // before the no-op exits
+  return run_mhla(q, k, v, mixing, y, den_out, B, H, N, d, block_size, mode, dt, eps, workspace,
+                  workspace_bytes, stream, nullptr, opt);
+}
+
+mhla_path mhla_forward_ex_path(int B, int H, int N, int d, int block_size, int causal, int with_mixing,
+                               mhla_dtype dt, const mhla_options* opt) {
+  if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0) ||
+      (dt != MHLA_F32 && dt != MHLA_BF16) || (causal != 0 && causal != 1))
+    return MHLA_PATH_NONE;
+  const MixMode mode = !causal ? MIX_FULL : with_mixing ? MIX_STRICT_LOWER : MIX_PREFIX;
+  MhlaShape s{B, H, N, d, block_size};
+  if (!apply_options(s, opt, mode)) return MHLA_PATH_NONE;
+  if (tc_causal_supported(s, dt, mode)) return MHLA_PATH_TCGEN05;  // the order of run_mhla
+  if (tc_stream_supported(s, dt, mode)) return MHLA_PATH_TCGEN05_STREAM;
+  return tc_mhla_supported(s, dt, mode) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
 
 mhla_status mhla_forward_grid(const void* q, const void* k, const void* v, const float* mixing,

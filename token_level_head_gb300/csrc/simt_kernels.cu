@@ -11,6 +11,7 @@
 // kernels follow "Breaking the Low-Rank Dilemma of Linear Attention", key
 // designs 1 and 2.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 #include "internal.h"
@@ -51,11 +52,14 @@ TokMap tok_map(const MhlaShape& s) {
 // ---------------------------------------------------------------- summaries
 // S_part[head][p] = sum_{t in chunk p} phi(K_t) V_t^T ; z_part[head][p] = sum phi(K_t)
 // (MHLA paper §4.1, local KV summary; chunks subdivide the blocks; chunk p holds positions
-// [(p % P) chunk, (p % P + 1) chunk) of block p / P).
+// [(p % P) chunk, (p % P + 1) chunk) of block p / P).  With a decay gamma != 1 (plain causal
+// linear attention, "Linear Attention notes" §七) each token is weighted gamma^(block - 1 - j),
+// j its position in the block: the block's summary decayed to its last token.
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 simt_summary_kernel(const T* __restrict__ K, const T* __restrict__ V, float* __restrict__ s_part,
-                    float* __restrict__ z_part, int N, int chunk, int P, TokMap map) {
+                    float* __restrict__ z_part, int N, int chunk, int P, TokMap map, int phi_kind,
+                    float gamma, int block) {
   constexpr int E = (D * D + kThreads - 1) / kThreads;
   __shared__ float sk[kTokTile][D];
   __shared__ float sv[kTokTile][D];
@@ -69,8 +73,10 @@ simt_summary_kernel(const T* __restrict__ K, const T* __restrict__ V, float* __r
   for (int t0 = 0; t0 < chunk; t0 += kTokTile) {
     const int nt = min(kTokTile, chunk - t0);
     for (int i = threadIdx.x; i < nt * D; i += kThreads) {
-      const size_t at = hbase + (size_t)map.tok(blk, j0 + t0 + i / D) * D + i % D;
-      sk[i / D][i % D] = phi(to_f(K[at]));
+      const int j = j0 + t0 + i / D;
+      const size_t at = hbase + (size_t)map.tok(blk, j) * D + i % D;
+      const float w = gamma == 1.f ? 1.f : powf(gamma, (float)(block - 1 - j));
+      sk[i / D][i % D] = w * phi_k(to_f(K[at]), phi_kind);
       sv[i / D][i % D] = to_f(V[at]);
     }
     __syncthreads();
@@ -102,13 +108,14 @@ simt_summary_kernel(const T* __restrict__ K, const T* __restrict__ V, float* __r
 // causal variants of §4.2 / App. C):
 //   MIX_FULL:         S~_i = sum_j m_ij S_j
 //   MIX_STRICT_LOWER: S~_i = sum_{j<i} m_ij S_j
-//   MIX_PREFIX:       S~_i = sum_{j<i} S_j
+//   MIX_PREFIX:       S~_i = sum_{j<i} S_j   (with decay: S~_i = gamma^block S~_{i-1} + S_{i-1},
+//                     the state after block i - 1's last token)
 // where S_j = sum of the P partials of block j.  Same for z.  One thread per
 // entry of the (d*d + d) summary.
 __global__ void __launch_bounds__(kThreads)
 simt_mix_kernel(const float* __restrict__ s_part, const float* __restrict__ z_part,
                 const float* __restrict__ mixing, float* __restrict__ s_mix,
-                float* __restrict__ z_mix, int H, int M, int P, int D, int mode) {
+                float* __restrict__ z_mix, int H, int M, int P, int D, int mode, float decay_block) {
   const int head = blockIdx.y;
   const int dd = D * D;
   const int ent = blockIdx.x * blockDim.x + threadIdx.x;
@@ -124,7 +131,7 @@ simt_mix_kernel(const float* __restrict__ s_part, const float* __restrict__ z_pa
       dst[(size_t)b * stride] = run;
       float tsum = 0.f;
       for (int p = 0; p < P; ++p) tsum += src[(size_t)(b * P + p) * stride];
-      run += tsum;
+      run = fmaf(run, decay_block, tsum);
     }
     return;
   }
@@ -160,12 +167,17 @@ simt_mix_kernel(const float* __restrict__ s_part, const float* __restrict__ z_pa
 // App. C chunk form with the lower triangle including the diagonal.  A CTA takes
 // positions t0 .. t0 + tile - 1 of block t0 / block (tokens by `map`; the causal
 // forms have contiguous blocks, so there position and token coincide).
+// Variants: the feature map phi_kind; normalise = 0 writes the numerator alone
+// (MHLA paper §4.1: the normaliser may be left out), den_out still the
+// denominator; a decay gamma != 1 (intra_mode 2 only) weights the state before
+// the block by gamma^(j + 1) and the intra-block scores by gamma^(t - s).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __restrict__ V,
                 const float* __restrict__ s_mix, const float* __restrict__ z_mix,
                 const float* __restrict__ mixing, T* __restrict__ Y, float* __restrict__ den_out,
-                int H, int N, int block, int tile, float eps, int intra_mode, TokMap map) {
+                int H, int N, int block, int tile, float eps, int intra_mode, TokMap map, int phi_kind,
+                int normalise, float gamma) {
   constexpr int ROWS = kThreads / D;
   constexpr int PASSES = (kOutTile + ROWS - 1) / ROWS;
   extern __shared__ float smem[];
@@ -184,7 +196,7 @@ simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
   for (int i = threadIdx.x; i < D; i += kThreads) sz[i] = z_mix[((size_t)head * M + blk) * D + i];
   const int j0 = t0 - blk * block;
   for (int i = threadIdx.x; i < tile * D; i += kThreads)
-    sq[i] = phi(to_f(Q[hbase + (size_t)map.tok(blk, j0 + i / D) * D + i % D]));
+    sq[i] = phi_k(to_f(Q[hbase + (size_t)map.tok(blk, j0 + i / D) * D + i % D]), phi_kind);
   __syncthreads();
   const int e = threadIdx.x % D, r = threadIdx.x / D;
   float num[PASSES], nin[PASSES], rs[PASSES];
@@ -202,7 +214,7 @@ simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
     for (int s0 = blk * block; s0 <= last; s0 += kTokTile) {
       const int ns = min(kTokTile, last + 1 - s0);
       for (int i = threadIdx.x; i < ns * D; i += kThreads) {
-        sk[i] = phi(to_f(K[hbase + (size_t)s0 * D + i]));
+        sk[i] = phi_k(to_f(K[hbase + (size_t)s0 * D + i]), phi_kind);
         sv[i] = to_f(V[hbase + (size_t)s0 * D + i]);
       }
       __syncthreads();
@@ -210,7 +222,9 @@ simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
         const int t = idx / ns, s = idx % ns;
         float dot = 0.f;
         for (int c = 0; c < D; ++c) dot = fmaf(sq[t * D + c], sk[s * D + c], dot);
-        ssc[t * kTokTile + s] = (s0 + s <= t0 + t) ? dot : 0.f;  // causal mask keeps s <= t
+        const int lag = (t0 + t) - (s0 + s);
+        if (gamma != 1.f) dot *= powf(gamma, (float)lag);
+        ssc[t * kTokTile + s] = lag >= 0 ? dot : 0.f;  // causal mask keeps s <= t
       }
       __syncthreads();
 #pragma unroll
@@ -232,8 +246,10 @@ simt_out_kernel(const T* __restrict__ Q, const T* __restrict__ K, const T* __res
     if (t < tile) {
       float den = 0.f;
       for (int c = 0; c < D; ++c) den = fmaf(sq[t * D + c], sz[c], den);
-      den = den + w_ii * rs[p] + eps;
-      const float y = (num[p] + w_ii * nin[p]) / den;
+      const float gd = gamma == 1.f ? 1.f : powf(gamma, (float)(j0 + t + 1));  // state before the block
+      den = fmaf(gd, den, w_ii * rs[p]) + eps;
+      const float n = fmaf(gd, num[p], w_ii * nin[p]);
+      const float y = normalise ? n / den : n;
       const int tok = map.tok(blk, j0 + t);
       Y[hbase + (size_t)tok * D + e] = from_f<T>(y);
       if (den_out != nullptr && e == 0) den_out[(size_t)head * N + tok] = den;
@@ -277,11 +293,13 @@ cudaError_t mhla_launch_t(const MhlaShape& s, const SimtPlan& pl, const void* q,
   const int heads = s.heads(), M = s.M();
   const TokMap map = tok_map(s);
   simt_summary_kernel<T, D><<<dim3(pl.parts, heads), kThreads, 0, st>>>(
-      static_cast<const T*>(k), static_cast<const T*>(v), s_part, z_part, s.N, pl.chunk, pl.P, map);
+      static_cast<const T*>(k), static_cast<const T*>(v), s_part, z_part, s.N, pl.chunk, pl.P, map, s.phi_kind,
+      s.gamma, s.block);
   note_launch();
   const int ents = D * D + D;
   simt_mix_kernel<<<dim3((ents + kThreads - 1) / kThreads, heads), kThreads, 0, st>>>(
-      s_part, z_part, mixing, s_mix, z_mix, s.H, M, pl.P, D, (int)mode);
+      s_part, z_part, mixing, s_mix, z_mix, s.H, M, pl.P, D, (int)mode,
+      s.gamma == 1.f ? 1.f : std::pow(s.gamma, (float)s.block));
   note_launch();
   const int tile = divisor_at_most(s.block, kOutTile);
   const size_t smem = out_smem_bytes(D);
@@ -291,7 +309,8 @@ cudaError_t mhla_launch_t(const MhlaShape& s, const SimtPlan& pl, const void* q,
   const int intra = mode == MIX_FULL ? 0 : (mode == MIX_STRICT_LOWER ? 1 : 2);
   simt_out_kernel<T, D><<<dim3(s.N / tile, heads), kThreads, smem, st>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), s_mix, z_mix,
-      mixing, static_cast<T*>(y), den_out, s.H, s.N, s.block, tile, eps, intra, map);
+      mixing, static_cast<T*>(y), den_out, s.H, s.N, s.block, tile, eps, intra, map, s.phi_kind,
+      s.normalise ? 1 : 0, s.gamma);
   note_launch();
   return cudaGetLastError();
 }

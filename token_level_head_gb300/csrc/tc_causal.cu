@@ -113,6 +113,7 @@ struct CParams {
   float* den_out;                // [T * 128] or null
   unsigned* status;
   int T, CH, G;                  // chunks in all, chunks per head, CTAs
+  int normalise;                 // 0: Y is the numerator alone (den_out still the denominator)
   float eps;
 };
 
@@ -566,7 +567,7 @@ __device__ bool out_store(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
   }
   const size_t row = (size_t)(lo + i) * kTile + t;
   if (p.den_out != nullptr) p.den_out[row] = dn;
-  const float r = 1.f / dn;
+  const float r = p.normalise ? 1.f / dn : 1.f;
 #pragma unroll
   for (int x = 0; x < 64; ++x) v[x] *= r;
   if (lane == 0 && nst >= 1) tma_store_wait_read1();  // the store of two chunks ago has read yb
@@ -803,6 +804,7 @@ int sm_count() {
 }  // namespace
 
 bool tc_causal_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
+  if (!s.plain_phi()) return false;  // ELU + 1 without decay only
   if (dt != MHLA_BF16 || s.d != kD || mode != MIX_PREFIX) return false;
   if (s.N % kTile != 0) return false;
   return (long long)s.heads() * s.N < (1ll << 31);
@@ -825,6 +827,7 @@ cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, c
   p.T = s.heads() * (s.N / kTile);
   p.CH = s.N / kTile;
   p.eps = eps;
+  p.normalise = s.normalise ? 1 : 0;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   p.G = std::min(max_ctas(s), sms);

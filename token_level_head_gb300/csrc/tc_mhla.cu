@@ -121,6 +121,7 @@ struct Params {
   int mix_n;                     // transposed MIX: N of its MMAs, M rounded up to 16
   int zx;                        // 1: the CTAs with a z row take no MIX units (C > 64, heads <= grid / 4)
   int grid2d;                    // 1: 2-D blocks (tokens on a gw-wide grid, blocks th x tw tiles)
+  int normalise;                 // 0: Y is the numerator alone (den_out still the denominator)
   int gw, gh, tw, th, bpr;       // grid width / height, tile width / height, tiles per grid row
   float eps;
 };
@@ -926,7 +927,7 @@ __device__ void epi_pass(const Params& p, uint8_t* sm, Small* sh, uint32_t tmem,
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
         if (p.den_out != nullptr) p.den_out[chunk_token(p, g, row)] = dn;
-        const float r = 1.f / dn;
+        const float r = p.normalise ? 1.f / dn : 1.f;
         // Y staging: two 4 KB buffers per warp (the whole 32 KB area is free
         // after the MIX phase); the store of two chunks ago has read this one
         uint8_t* yo = sm + L::kOffY + qd * 8192 + (nst & 1) * 4096;
@@ -1468,6 +1469,7 @@ cudaError_t launch_t(const Params& p, int grid, cudaStream_t st) {
 }  // namespace
 
 bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
+  if (!s.plain_phi()) return false;  // ELU + 1 without decay only
   if (dt != MHLA_BF16 || s.d != kD || mode != MIX_FULL) return false;
   if (s.block % kTile != 0 || s.N % kTile != 0) return false;
   // 2-D blocks: a 128-token chunk is whole tile rows (tw divides 128) or part of one
@@ -1533,6 +1535,7 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   p.tc_mix = pl.tc_mix ? 1 : 0;
   p.XS = pl.tc_mix ? s.heads() * kD : 0;
   p.eps = eps;
+  p.normalise = s.normalise ? 1 : 0;
   cudaError_t e;
   if (p.M <= 16)
     e = launch_t<16>(p, grid, st);

@@ -131,6 +131,7 @@ struct Params {
   int heads, H, N, M, C, cpb, cpad, T, I, nmix;
   int E, Dx, Do;
   int NS, stage, off_w, off_ones, off_small;
+  int normalise;                 // 0: Y is the numerator alone (den_out still the denominator)
   float eps;
 };
 
@@ -451,7 +452,7 @@ __device__ void worker(const Params& p, const Sched& sc, uint8_t* sm, Small* sh,
         // two halves of 32 columns: Y row r = D / den (bf16), or the chunk's
         // partial S^T row e = r (qd 0, 1; bf16), or its z (qd 2: TMEM rows
         // 64.. all hold it; lane 0 writes it, fp32)
-        const float rd = it.kind == kOut ? 1.f / dn : 1.f;
+        const float rd = it.kind == kOut && p.normalise ? 1.f / dn : 1.f;
         const size_t g_chunk = (size_t)it.h * p.C + it.j;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -770,6 +771,7 @@ void tc_stream_set_wait_limit(unsigned long long ns) { g_wait_ns = ns == 0 ? kDe
 // the three-pass kernel is faster (DiT-like B8 H6 N4096: 32 us against 57 us,
 // L2-warm) and keeps those shapes.
 bool tc_stream_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
+  if (!s.plain_phi()) return false;  // ELU + 1 without decay only
   if (s.grid()) return false;  // contiguous blocks only
   if (dt != MHLA_BF16 || s.d != kD || mode != MIX_FULL) return false;
   if (s.block % kTile != 0 || s.N % kTile != 0 || s.N / kTile > 64 || (s.N / kTile) % 16 == 0) return false;
@@ -834,6 +836,7 @@ cudaError_t tc_stream_launch(const MhlaShape& s, const void* q, const void* k, c
   p.status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
   p.wait_ns = g_wait_ns;
   p.eps = eps;
+  p.normalise = s.normalise ? 1 : 0;
 
   static SmemOptIn opt_in;
   if ((e = opt_in.ensure((const void*)mhla_stream_kernel, kSmemLimit)) != cudaSuccess) return e;
