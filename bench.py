@@ -117,8 +117,18 @@ def job_value(tokens_per_rank_step, steps, world, ms):
     return world * tokens_per_rank_step * steps / (ms / 1e3)
 
 
+VARIANT_KEYS = ("feature", "normalise", "gamma")
+
+
+def variant_kwargs(wl):
+    """The mhla_forward_ex options a workload asks for ({} = the plain forward)."""
+    return {key: wl.extra[key] for key in VARIANT_KEYS if key in wl.extra}
+
+
 def describe(wl):
     s = f"{wl.name}: B{wl.B} H{wl.H} N{wl.N} d{wl.d} {wl.dtype}"
+    for key, val in variant_kwargs(wl).items():
+        s += f" {key}={val}"
     if wl.kind == "mhla" and "grid" in wl.extra:
         gh, gw, th, tw = wl.extra["grid"]
         s += f" M{wl.M} (2-D blocks: {gh}x{gw} grid, {th}x{tw} tiles)"
@@ -321,6 +331,9 @@ class Runner:
         if wl.kind == "mhla" and "grid" in wl.extra:
             gh, gw, th, tw = wl.extra["grid"]
             b.mhla_forward_grid(s["q"], s["k"], s["v"], s["mixing"], s["y"], (gh, gw), (th, tw), workspace=self.ws)
+        elif variant_kwargs(wl):
+            b.mhla_forward_ex(s["q"], s["k"], s["v"], s.get("mixing") if wl.kind == "mhla" else None, s["y"],
+                              wl.block, causal=int(wl.kind == "causal"), workspace=self.ws, **variant_kwargs(wl))
         elif wl.kind == "mhla":
             b.mhla_forward(s["q"], s["k"], s["v"], s["mixing"], s["y"], wl.block, workspace=self.ws)
         elif wl.kind == "causal":
@@ -474,6 +487,10 @@ def kernel_path(binding, wl):
         return "simt"
     if "grid" in wl.extra:
         return binding.mhla_forward_grid_path(wl.B, wl.H, *wl.extra["grid"], wl.d, tdt)
+    if variant_kwargs(wl):
+        causal = int(wl.kind == "causal")
+        return binding.mhla_forward_ex_path(wl.B, wl.H, wl.N, wl.d, wl.block, causal, 1 - causal, tdt,
+                                            **variant_kwargs(wl))
     return binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
 
 
@@ -540,9 +557,16 @@ def parity_of_timed_output(runner, n_slices=4):
         pick = sorted({0, units - 1} | {(units * i) // n_slices for i in range(n_slices)})[:n_slices]
         heads = [(u // wl.H, u % wl.H) for u in pick]
         x = workloads.mhla_host(wl, heads=heads)
+        vk = variant_kwargs(wl)
         if wl.kind == "mhla" and "grid" in wl.extra:
             ids = oracle.grid_block_ids(*wl.extra["grid"])
             ref, _ = oracle.mhla_block_form_ids(x["q64"], x["k64"], x["v64"], x["mixing64"], ids)
+        elif wl.kind == "mhla" and vk:
+            ref, _ = oracle.mhla_block_form_feature(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block,
+                                                    vk.get("feature", "elu1"), 1e-6, vk.get("normalise", True))
+        elif wl.kind == "causal" and vk:
+            ref, _ = oracle.causal_variant_recurrent(x["q64"], x["k64"], x["v64"], vk.get("feature", "elu1"),
+                                                     vk.get("gamma", 1.0), 1e-6, vk.get("normalise", True))
         elif wl.kind == "mhla":
             ref, _ = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
         else:
@@ -758,12 +782,14 @@ def run_ours(args, wl, rank, world, local_rank):
         del runner
         torch.cuda.empty_cache()
         extra = {}
-        for name in ("dit_grid", "hires", "hires_m1", "causal", "rala", "decode", "decode_fused", "stream"):
+        for name in ("dit_grid", "dit_unnormalised", "dit_relu", "hires", "hires_m1", "causal", "causal_decay",
+                     "rala", "decode", "decode_fused", "stream"):
             if name == wl.name:
                 continue
             try:
                 wl_x = workloads_mod().WORKLOADS[name]
-                n_x = min(args.steps, 20 if wl_x.kind in ("decode_steps", "stream") else 200)
+                slow = wl_x.kind in ("decode_steps", "stream") or bench_path_is_simt(binding, wl_x)
+                n_x = min(args.steps, 20 if slow else 200)
                 extra[name] = workload_line(torch, binding, wl_x, device, l2, n_x, args.warmup)
             except Exception as e:  # report, do not lose the metric line
                 extra[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
@@ -771,6 +797,10 @@ def run_ours(args, wl, rank, world, local_rank):
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(wl, budget_s=args.cpu_seconds)
     return line
+
+
+def bench_path_is_simt(binding, wl):
+    return kernel_path(binding, wl) == "simt"
 
 
 def workloads_mod():

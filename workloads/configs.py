@@ -60,11 +60,19 @@ WORKLOADS = {
     # the same DiT-S/2-like inputs with 2-D blocks: the 64x64 grid cut into 4 x 4 tiles of 16x16
     "dit_grid": Workload("dit_grid", 2, "mhla", 8, 6, 4096, 64, 256, "bf16", 0.125, "softmax_diag2",
                          extra={"grid": (64, 64, 16, 16)}),
+    # variants on the same inputs: no normaliser (MHLA §4.1), the ReLU feature map (notes §二)
+    "dit_unnormalised": Workload("dit_unnormalised", 2, "mhla", 8, 6, 4096, 64, 256, "bf16", 0.125,
+                                 "softmax_diag2", extra={"normalise": False}),
+    "dit_relu": Workload("dit_relu", 2, "mhla", 8, 6, 4096, 64, 256, "bf16", 0.125, "softmax_diag2",
+                         extra={"feature": "relu"}),
     # 256x256 token grid, M = 64 blocks of 1024, and the same inputs with M = 1
     "hires": Workload("hires", 3, "mhla", 1, 6, 65536, 64, 1024, "bf16", 0.125, "softmax"),
     "hires_m1": Workload("hires_m1", 3, "mhla", 1, 6, 65536, 64, 65536, "bf16", 0.125, "ones"),
     # long causal sequences, chunk 128
     "causal": Workload("causal", 4, "causal", 4, 16, 8192, 64, 128, "bf16", 0.125),
+    # the causal inputs with RetNet decay gamma = 0.99 (notes §七)
+    "causal_decay": Workload("causal_decay", 4, "causal", 4, 16, 8192, 64, 128, "bf16", 0.125,
+                             extra={"gamma": 0.99}),
     # recurrent decode: batch 256 x 16 heads, 1024 steps after a 2048-token prefix
     "decode": Workload("decode", 4, "decode", 256, 16, 1024, 64, 0, "bf16", 0.125,
                        extra={"prefix": 2048}),
