@@ -62,7 +62,7 @@ def workload_bytes(wl):
     eb = 2 if wl.dtype == "bf16" else 4
     t = wl.B * wl.H * wl.N * wl.d * eb
     if wl.kind in ("mhla", "causal"):
-        mix = wl.H * wl.M * wl.M * 4 if wl.kind == "mhla" else 0
+        mix = wl.H * wl.M * wl.M * 4 if wl.mixing != "none" else 0
         return 4 * t + mix
     if wl.kind == "decode":
         units = wl.B * wl.H
@@ -155,6 +155,7 @@ KERNEL_SOURCES = {
     "mhla_tcgen05": ["tc_mhla.cu"],
     "mhla_tcgen05_stream": ["tc_stream.cu", "stream_sched.h"],
     "causal_tcgen05": ["tc_causal.cu"],
+    "causal_mhla_tcgen05": ["tc_causal.cu", "tc_mhla.cu"],
     "rala_tcgen05": ["tc_rala.cu"],
     "decode_steps_simt": ["decode_steps.cu"],
 }
@@ -337,7 +338,7 @@ class Runner:
         elif wl.kind == "mhla":
             b.mhla_forward(s["q"], s["k"], s["v"], s["mixing"], s["y"], wl.block, workspace=self.ws)
         elif wl.kind == "causal":
-            b.mhla_forward_causal(s["q"], s["k"], s["v"], None, s["y"], wl.block, workspace=self.ws)
+            b.mhla_forward_causal(s["q"], s["k"], s["v"], s.get("mixing"), s["y"], wl.block, workspace=self.ws)
         elif wl.kind == "rala":
             b.rala_forward(s["q"], s["k"], s["v"], s["x"], s["w"], s["y"], workspace=self.ws)
         elif wl.kind == "decode":
@@ -487,11 +488,19 @@ def kernel_path(binding, wl):
         return "simt"
     if "grid" in wl.extra:
         return binding.mhla_forward_grid_path(wl.B, wl.H, *wl.extra["grid"], wl.d, tdt)
-    if variant_kwargs(wl):
+    if variant_kwargs(wl) or (wl.kind == "causal" and wl.mixing != "none"):
         causal = int(wl.kind == "causal")
-        return binding.mhla_forward_ex_path(wl.B, wl.H, wl.N, wl.d, wl.block, causal, 1 - causal, tdt,
+        with_mixing = int(wl.mixing != "none")
+        return binding.mhla_forward_ex_path(wl.B, wl.H, wl.N, wl.d, wl.block, causal, with_mixing, tdt,
                                             **variant_kwargs(wl))
     return binding.mhla_forward_path(wl.B, wl.H, wl.N, wl.d, wl.block or 1, int(wl.kind == "causal"), tdt)
+
+
+def kernel_family(wl, path):
+    """Name of the kernel family a workload runs (keys the traffic records in profiles/)."""
+    if wl.kind == "causal" and wl.mixing != "none":
+        return f"causal_mhla_{path}"
+    return f"{wl.kind}_{path}"
 
 
 def time_steps(torch, binding, runner, steps, warmup, world=1, sampler=None):
@@ -569,6 +578,8 @@ def parity_of_timed_output(runner, n_slices=4):
                                                      vk.get("gamma", 1.0), 1e-6, vk.get("normalise", True))
         elif wl.kind == "mhla":
             ref, _ = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
+        elif wl.mixing != "none":
+            ref, _ = oracle.causal_mhla_chunked(x["q64"], x["k64"], x["v64"], x["mixing64"], wl.block)
         else:
             ref, _ = oracle.causal_chunked(x["q64"], x["k64"], x["v64"], wl.block)
         got = np.stack([s["y"][b, h].float().cpu().numpy() for b, h in heads]).astype(np.float64)
@@ -673,7 +684,7 @@ def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
     kernel_ms = step_ms if step_ms is not None else elapsed_ms / steps
     achieved = alg / (kernel_ms / 1e3) / 1e9
     path = kernel_path(binding, wl)
-    kname = f"{wl.kind}_{path}"
+    kname = kernel_family(wl, path)
     out = {"workload": describe(wl), "value": tokens_per_step(wl) * steps / (elapsed_ms / 1e3),
            "unit": "tokens/s" if wl.kind != "decode" else "units/s", "steps": steps,
            "ms_per_step": elapsed_ms / steps, "launch_ms": kernel_ms, "kernels_per_step": kernels,
@@ -741,7 +752,7 @@ def run_ours(args, wl, rank, world, local_rank):
     kernel_ms = step_ms if step_ms is not None else elapsed_ms / args.steps
     achieved = alg / (kernel_ms / 1e3) / 1e9
     path = kernel_path(binding, wl)
-    kernel_name = f"{wl.kind}_{path}"
+    kernel_name = kernel_family(wl, path)
     value = job_value(tokens_per_step(wl), args.steps, world, elapsed_ms)
     line = {
         "metric": METRIC if wl.name == "dit" else f"{wl.name} tokens/s",
@@ -782,7 +793,7 @@ def run_ours(args, wl, rank, world, local_rank):
         del runner
         torch.cuda.empty_cache()
         extra = {}
-        for name in ("dit_grid", "dit_unnormalised", "dit_relu", "hires", "hires_m1", "causal", "causal_decay",
+        for name in ("dit_grid", "dit_unnormalised", "dit_relu", "hires", "hires_m1", "causal", "causal_mhla", "causal_decay",
                      "rala", "decode", "decode_fused", "stream"):
             if name == wl.name:
                 continue

@@ -427,6 +427,53 @@ def test_causal_mhla_with_mixing(dtype):
     assert np.array_equal(y2, y) and np.array_equal(den2, den)
 
 
+CAUSAL_MHLA_TC = [  # B, H, N (d = 64, chunk = block = 128, bf16)
+    (1, 2, 1024),   # M = 8
+    (2, 3, 2048),   # M = 16
+    (2, 2, 4096),   # M = 32
+    (1, 4, 8192),   # M = 64
+    (3, 1, 384),    # M = 3
+]
+
+
+@pytest.mark.parametrize("shape", CAUSAL_MHLA_TC, ids=lambda s: "x".join(map(str, s)))
+def test_causal_mhla_tcgen05(shape):
+    """Causal MHLA with a lower-triangular mixing on the tensor cores (the MHLA kernel's prefix
+    pass, then the causal output kernel) against the oracle's chunk form; entries above the
+    diagonal are large and must not reach the result."""
+    B, H, N = shape
+    d, chunk = 64, 128
+    assert binding.mhla_forward_ex_path(B, H, N, d, chunk, 1, 1, torch.bfloat16) == "tcgen05"
+    x = rand_inputs(780 + N, (B, H, N, d), "bf16")
+    M = N // chunk
+    u = np.tril(uniform(781, 9, (H, M, M)) + 0.05)
+    mix = u / u.sum(axis=-1, keepdims=True) + np.triu(np.full((M, M), 5.0), 1)
+    mix_t = torch.from_numpy(mix.astype(np.float32)).cuda()
+    y, den = forward_causal(x["q"], x["k"], x["v"], mix_t, chunk)
+    ref, dref = oracle.causal_mhla_chunked(x["q64"], x["k64"], x["v64"], np.tril(mix.astype(np.float32)), chunk)
+    assert_close_y(y, ref, "bf16")
+    assert_close_den(den, dref, "bf16")
+
+
+def test_causal_mhla_tcgen05_full_size_sampled_heads():
+    """The causal workload's shape (B4 H16 N8192, M = 64) with a causal mixing, 8 heads against
+    the oracle; every output finite."""
+    wl = WORKLOADS["causal"]
+    dev = mhla_device(wl)
+    M = wl.N // wl.block
+    u = np.tril(uniform(790, 9, (wl.H, M, M)) + 0.05)
+    mix = (u / u.sum(axis=-1, keepdims=True)).astype(np.float32)
+    y, den = forward_causal(dev["q"], dev["k"], dev["v"], torch.from_numpy(mix).cuda(), wl.block)
+    assert np.all(np.isfinite(y)) and np.all(den > 0)
+    heads = [(0, 0), (0, 15), (1, 3), (1, 8), (2, 11), (2, 6), (3, 1), (3, 15)]
+    x = mhla_host(wl, heads=heads)
+    mixh = mix[[h for _, h in heads]].astype(np.float64)
+    ref, dref = oracle.causal_mhla_chunked(x["q64"], x["k64"], x["v64"], mixh, wl.block)
+    for i, (b, h) in enumerate(heads):
+        assert_close_y(y[b, h][None, None], ref[0, i][None, None], wl.dtype, what=f"Y[{b},{h}]")
+        assert_close_den(den[b, h], dref[0, i], wl.dtype, what=f"den[{b},{h}]")
+
+
 def test_causal_full_workload_every_head():
     wl = WORKLOADS["causal"]
     dev = mhla_device(wl)
@@ -506,6 +553,73 @@ def test_decode_full_workload_sampled_units():
     assert_close_y(to_f64(outs).transpose(1, 0, 2)[:, None], ref.transpose(1, 0, 2)[:, None], "bf16")
     assert_close_den(to_f64(dens), dref, "bf16")
     assert_close_y(to_f64(Sf[sel])[:, None], s_t[:, None], "f32", what="state S")
+
+
+# ------------------------------------------------ phi on the tensor-core paths
+def bf16_grid_values(lo=-20.0, hi=20.0, tiny=1e-3):
+    """Every bf16 value x with tiny <= |x| <= 20 in [lo, hi], and 0 (about 3.9 thousand), as float64."""
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    bits = bits[(bits & 0x7F80) != 0x7F80]  # finite patterns only
+    x = bf16_bits_to_f64(bits)
+    keep = (x >= lo) & (x <= hi) & ((np.abs(x) >= tiny) | (x == 0))
+    return np.unique(x[keep])
+
+
+def phi_bound(x):
+    """|phi_gpu - phi| / phi the kernels must meet: the base-2 exponential (2^-21 relative, with
+    margin) plus the rounding of x log2 e (|x| 2^-24 relative in the exponent) and of the fp32
+    sums around it (2^-23)."""
+    return 2.0 ** -21 + np.abs(x) * 2.0 ** -23
+
+
+@pytest.mark.parametrize("path", ["tcgen05", "tcgen05_stream", "causal_tcgen05"])
+def test_phi_on_the_tensor_core_paths(path):
+    """phi(x) for every bf16 x with 1e-3 <= |x| <= 20 (and 0), read back through the fp32
+    denominator: Q = 0 (phi = 1), identity mixing, eps = 0, and in each block one key element x
+    with every other key element -100 (phi flushes to 0), so den = phi(x) up to the bound above."""
+    xs = bf16_grid_values()
+    if path == "causal_tcgen05":
+        N, block, per = 128, 128, 1          # one value per head, at its first token
+    elif path == "tcgen05":
+        N, block, per = 2048, 128, 16        # C = 16: the three-pass kernel
+    else:
+        N, block, per = 1152, 128, 9         # C = 9: the stream kernel
+    heads = -(-len(xs) // per)
+    vals = np.resize(xs, heads * per)        # pad by repeating
+    d = 64
+    k = np.full((1, heads, N, d), -100.0)
+    for j in range(per):
+        k[0, :, j * block, 0] = vals[j::per]
+    kt = to_device(bf16_bits(k))
+    q = torch.zeros(1, heads, N, d, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros_like(q)
+    y = torch.empty_like(q)
+    den = torch.empty(1, heads, N, dtype=torch.float32, device="cuda")
+    eps = 0.0
+    if path == "causal_tcgen05":
+        assert binding.mhla_forward_path(1, heads, N, d, block, 1, torch.bfloat16) == "tcgen05"
+        binding.mhla_forward_causal(q, kt, v, None, y, block, eps=eps, den_out=den)
+        got = to_f64(den)[0, :, 0]
+    else:
+        assert binding.mhla_forward_path(1, heads, N, d, block, 0, torch.bfloat16) == path
+        mix = torch.eye(N // block, dtype=torch.float32, device="cuda").expand(heads, -1, -1).contiguous()
+        binding.mhla_forward(q, kt, v, mix, y, block, eps=eps, den_out=den)
+        got = to_f64(den)[0][:, ::block].reshape(-1)
+    torch.cuda.synchronize()
+    ref = oracle.phi(vals)
+    err = np.abs(got - ref) / ref
+    if path == "causal_tcgen05":
+        # the causal denominator sums fp32 phi(K) (an in-chunk prefix beside the MMAs)
+        bound = phi_bound(vals)
+    else:
+        # z comes out of the summary MMA, whose B operand is phi(K) rounded to bf16: den is
+        # that rounding of the fp32 phi, so |error| <= half a bf16 ulp (2^-8 relative) + the above,
+        # and it equals the bf16 rounding of the exact phi except within 2^-21 of a tie
+        bound = 2.0 ** -8 + phi_bound(vals)
+        exact = bf16_bits_to_f64(bf16_bits(ref))
+        assert np.mean(got == exact) > 0.999, f"{np.mean(got == exact):.4f} equal to the rounded phi"
+    worst = int(np.argmax(err / bound))
+    assert np.all(err <= bound), f"x = {vals[worst]}: relative error {err[worst]:.3e}"
 
 
 # ------------------------------------------ variants: phi, normaliser, decay

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdint.h>
 
 #include "mhla.h"
 
@@ -43,6 +44,14 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
                            const float* mixing, void* y, float* den_out, float eps, MixMode mode,
                            void* ws, cudaStream_t st);
 
+// The SUM and MIX passes of the tcgen05 kernel alone, with the weights m_ib for b < i only
+// (causal MHLA's mixed prefix P_i = sum_{b<i} m_ib S_b, zeta_i likewise), into the workspace:
+// S~_i^T as bf16 8 KB K-major 128-byte-swizzled tiles [heads * M], z~ [heads * M][64] fp32.
+bool tc_mhla_prefix_supported(const MhlaShape& s, mhla_dtype dt);
+cudaError_t tc_mhla_prefix_launch(const MhlaShape& s, const void* k, const void* v, const float* mixing, void* ws,
+                                  cudaStream_t st);
+void tc_mhla_mixed_summaries(const MhlaShape& s, void* ws, const uint8_t** smix, const float** zmix);
+
 // ---- tcgen05 stream path (bf16, d = 64, blocks of whole 128-token tiles, at most 64 tiles a head):
 // summaries, mixing and output as one ordered list of items with per-head readiness counters
 bool tc_stream_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
@@ -58,6 +67,14 @@ bool tc_causal_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
 size_t tc_causal_workspace(const MhlaShape& s);
 cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, const void* v, void* y,
                              float* den_out, float eps, void* ws, cudaStream_t st);
+
+// ---- tcgen05 causal MHLA (mixing, chunk = block = 128, M <= 64): the prefix pass of the MHLA
+// kernel, then the causal output kernel on its mixed prefixes
+bool tc_causal_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode);
+size_t tc_causal_mhla_workspace(const MhlaShape& s);
+cudaError_t tc_causal_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
+                                  const float* mixing, void* y, float* den_out, float eps, void* ws,
+                                  cudaStream_t st);
 
 // ---- tcgen05 RALA path (bf16, d = 32, Cx = 64, H <= 2, N a multiple of 64)
 bool tc_rala_supported(int B, int H, int N, int d, int cx, mhla_dtype dt);

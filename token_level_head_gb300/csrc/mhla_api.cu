@@ -36,8 +36,10 @@ mhla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MHLA_OK : MHLA_
 size_t mhla_ws(int B, int H, int N, int d, int block, int causal) {
   MhlaShape s{B, H, N, d, block};
   const size_t a = simt_mhla_workspace(s);
-  const size_t b = causal ? (tc_causal_supported(s, MHLA_BF16, MIX_PREFIX) ? tc_causal_workspace(s) : 0)
-                          : (tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0);
+  size_t b = causal ? (tc_causal_supported(s, MHLA_BF16, MIX_PREFIX) ? tc_causal_workspace(s) : 0)
+                    : (tc_mhla_supported(s, MHLA_BF16, MIX_FULL) ? tc_mhla_workspace(s) : 0);
+  if (causal && tc_causal_mhla_supported(s, MHLA_BF16, MIX_STRICT_LOWER))
+    b = std::max(b, tc_causal_mhla_workspace(s));
   const size_t c = !causal && tc_stream_supported(s, MHLA_BF16, MIX_FULL) ? tc_stream_workspace(s) : 0;
   return std::max(a, std::max(b, c));
 }
@@ -86,7 +88,7 @@ mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int caus
       (dt != MHLA_F32 && dt != MHLA_BF16) || (causal != 0 && causal != 1))
     return MHLA_PATH_NONE;
   const MhlaShape s{B, H, N, d, block_size};
-  if (causal) return tc_causal_supported(s, dt, MIX_PREFIX) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+  if (causal) return tc_causal_supported(s, dt, MIX_PREFIX) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;  // no mixing
   if (tc_stream_supported(s, dt, MIX_FULL)) return MHLA_PATH_TCGEN05_STREAM;
   return tc_mhla_supported(s, dt, MIX_FULL) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }
@@ -127,6 +129,8 @@ static mhla_status run_mhla(const void* q, const void* k, const void* v, const f
   }
   if (tc_causal_supported(s, dt, mode))
     return from_cuda(tc_causal_launch(s, q, k, v, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
+  if (tc_causal_mhla_supported(s, dt, mode))
+    return from_cuda(tc_causal_mhla_launch(s, q, k, v, mixing, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
   if (tc_stream_supported(s, dt, mode))
     return from_cuda(tc_stream_launch(s, q, k, v, mixing, y, den_out, eps, ws, static_cast<cudaStream_t>(stream)));
   if (tc_mhla_supported(s, dt, mode))
@@ -168,7 +172,8 @@ mhla_path mhla_forward_ex_path(int B, int H, int N, int d, int block_size, int c
   const MixMode mode = !causal ? MIX_FULL : with_mixing ? MIX_STRICT_LOWER : MIX_PREFIX;
   MhlaShape s{B, H, N, d, block_size};
   if (!apply_options(s, opt, mode)) return MHLA_PATH_NONE;
-  if (tc_causal_supported(s, dt, mode)) return MHLA_PATH_TCGEN05;  // the order of run_mhla
+  if (tc_causal_supported(s, dt, mode) || tc_causal_mhla_supported(s, dt, mode))
+    return MHLA_PATH_TCGEN05;  // the order of run_mhla
   if (tc_stream_supported(s, dt, mode)) return MHLA_PATH_TCGEN05_STREAM;
   return tc_mhla_supported(s, dt, mode) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
 }

@@ -112,10 +112,22 @@ struct CParams {
   float* agg_z;                  // [G][64]: sum of phi(K)[t][c] over the same tokens
   float* den_out;                // [T * 128] or null
   unsigned* status;
+  // causal MHLA (mixing, chunk = block): the mixed prefixes P_i^T (bf16 tiles in the output
+  // MMA's B layout) and zeta_i (fp32) of every (head, block), and the mixing matrix for m_ii
+  const uint8_t* smix;
+  const float* zmix;
+  const float* mixing;
+  int mix, H;                    // mix: 1 for causal MHLA; H: heads of the mixing matrix
   int T, CH, G;                  // chunks in all, chunks per head, CTAs
   int normalise;                 // 0: Y is the numerator alone (den_out still the denominator)
   float eps;
 };
+
+// m_ii of chunk c (causal MHLA: chunk = block, CH blocks a head).
+__device__ __forceinline__ float self_weight(const CParams& p, int c) {
+  const int hd = c / p.CH, b = c - hd * p.CH;
+  return __ldg(p.mixing + ((size_t)(hd % p.H) * p.CH + b) * p.CH + b);
+}
 
 // First chunk of segment j (j = G gives T).
 __device__ __forceinline__ int seg_lo(const CParams& p, int j) { return (int)(((long long)j * p.T) / p.G); }
@@ -365,7 +377,7 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
   float* zb = reinterpret_cast<float*>(sm + kOffZ);
   int* ab = &sh->abort;
   const int r0 = lane >> 3, j = lane & 7;
-  if (w == 0 && r0 == 0) {
+  if (w == 0 && r0 == 0 && !p.mix) {
     // zeta of the first chunk: the predecessors' phi(K) sums in this head
     float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     const int h0 = lo - lo % p.CH;
@@ -413,12 +425,25 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
     if (!group_and(kBarPhi, kPhiWarps * 32, ok && !ab_get(ab))) return;
     // zeta_c plus the rows of the warps before this one (all warps' totals are
     // read at once, 16-byte loads; warp 0 also forms zeta of the next chunk)
-    float off[8], tot[8];
-    {
+    float off[8], tot[8], zeta[8];
+    float mii = 1.f;
+    if (p.mix) {
+      // causal MHLA: zeta_i = sum_{b<i} m_ib z_b from the MIX pass; the in-chunk terms
+      // are weighted by m_ii
+      const float4* z4 = reinterpret_cast<const float4*>(p.zmix + (size_t)c * kD + 8 * j);
+      const float4 z0 = __ldcg(z4), z1 = __ldcg(z4 + 1);
+      zeta[0] = z0.x; zeta[1] = z0.y; zeta[2] = z0.z; zeta[3] = z0.w;
+      zeta[4] = z1.x; zeta[5] = z1.y; zeta[6] = z1.z; zeta[7] = z1.w;
+      mii = self_weight(p, c);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) off[x] = 0.f;
+    } else {
       const float4* z4 = reinterpret_cast<const float4*>(zb + a * kD + 8 * j);
       const float4 z0 = z4[0], z1 = z4[1];
       off[0] = z0.x; off[1] = z0.y; off[2] = z0.z; off[3] = z0.w;
       off[4] = z1.x; off[5] = z1.y; off[6] = z1.z; off[7] = z1.w;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) zeta[x] = 0.f;
     }
 #pragma unroll
     for (int x = 0; x < 8; ++x) tot[x] = off[x];
@@ -433,7 +458,7 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
         if (ww < w) off[x] += u[x];
       }
     }
-    if (w == 0 && r0 == 0 && i + 1 < n) {
+    if (w == 0 && r0 == 0 && i + 1 < n && !p.mix) {
       // zeta of the next chunk (zero when it starts a new head)
       const bool fresh = (c + 1) % p.CH == 0;
       float4* zn = reinterpret_cast<float4*>(zb + (a ^ 1) * kD + 8 * j);
@@ -446,7 +471,7 @@ __device__ __noinline__ void out_phi(const CParams& p, uint8_t* sm, OSmall* sh, 
     for (int i4 = 0; i4 < 4; ++i4) {
       float d = 0.f;
 #pragma unroll
-      for (int x = 0; x < 8; ++x) d = fmaf(qf[i4][x], off[x] + kf[i4][x], d);
+      for (int x = 0; x < 8; ++x) d = fmaf(qf[i4][x], fmaf(mii, off[x] + kf[i4][x], zeta[x]), d);
       d += __shfl_xor_sync(0xffffffffu, d, 1);
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       d += __shfl_xor_sync(0xffffffffu, d, 4);
@@ -482,7 +507,7 @@ __device__ void out_start(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
   const uint32_t ones = smem_u32(sm + kOffOnesB);
   const uint32_t st = smem_u32(sm + kOffStages + s * kStageB);
   const uint32_t q0 = st, k0 = st + kTileBytes, v0 = st + 2 * kTileBytes;
-  {
+  if (!p.mix) {
     // D = [1 ; V^T] phi(K) (M 128, MN-major A: the ones tile, then V, v0 - ones
     // bytes apart): rows 64 + e hold P^T[e][c] += sum_t V[t][e] phi(K)[t][c];
     // a chunk that starts a head starts from zero
@@ -492,8 +517,8 @@ __device__ void out_start(const CParams& p, uint8_t* sm, OSmall* sh, uint32_t tm
 #pragma unroll
     for (int k = 0; k < kTile / 16; ++k)
       mma_bf16(tmem + kColP, da + k * (2048 >> 4), db + k * (2048 >> 4), idesc, cont || k > 0);
+    mma_commit(&sh->p_full);
   }
-  mma_commit(&sh->p_full);
   {
     const uint64_t da = smem_desc(q0, 16, 1024), db = smem_desc(k0, 16, 1024);
     const uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
@@ -592,6 +617,25 @@ __device__ __noinline__ void out_pchain(const CParams& p, uint8_t* sm, OSmall* s
   uint8_t* ptile = sm + kOffP;
   const uint32_t lq = (uint32_t)(64 + 32 * wq) << 16;
   const int e = 32 * wq + lane;
+  if (p.mix) {
+    // causal MHLA: the P tile of chunk i is the MIX pass's P_i^T tile, copied as it is (the
+    // same swizzled image); tile i % 2 was last read by the MMAs of chunk i - 2
+    for (int i = 0; i < n; ++i) {
+      const int a = i & 1;
+      if (i >= 2 && !cwait(&sh->sc_full[a], ((i - 2) >> 1) & 1, ab)) return;
+      const uint4* src = reinterpret_cast<const uint4*>(p.smix + (size_t)(lo + i) * kPTile) + 8 * e;
+      uint4* dst = reinterpret_cast<uint4*>(ptile + a * kPTile) + 8 * e;
+      uint4 u[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) u[jj] = __ldcg(src + jj);
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) dst[jj] = u[jj];
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->ptile_full[a]);
+    }
+    return;
+  }
   {
     float v[64];
 #pragma unroll
@@ -655,6 +699,7 @@ __device__ __noinline__ void out_epi(const CParams& p, uint8_t* sm, OSmall* sh, 
     tc_fence_after();
     uint8_t* st = sm + kOffStages + (i % kNSB) * kStageB;
     const int t = 32 * qd + lane;
+    const float mii = p.mix ? self_weight(p, lo + i) : 1.f;  // causal MHLA: the in-chunk scores times m_ii
     // 32 columns s0 = 32 qr at a time: below this quadrant's rows they are kept
     // whole, beyond them they are zero, on the diagonal (qr = qd) masked
     for (int qr = 0; qr < 4; ++qr) {
@@ -674,6 +719,8 @@ __device__ __noinline__ void out_epi(const CParams& p, uint8_t* sm, OSmall* sh, 
         for (int x = 0; x < 32; ++x)
           if (x > lane) v[x] = 0.f;
       }
+#pragma unroll
+      for (int x = 0; x < 32; ++x) v[x] *= mii;
 #pragma unroll
       for (int jj = 0; jj < 4; ++jj) *swz_piece(tile, t, j0 + jj) = pack8(v + 8 * jj);
     }
@@ -828,6 +875,11 @@ cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, c
   p.CH = s.N / kTile;
   p.eps = eps;
   p.normalise = s.normalise ? 1 : 0;
+  p.smix = nullptr;
+  p.zmix = nullptr;
+  p.mixing = nullptr;
+  p.mix = 0;
+  p.H = s.H;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   p.G = std::min(max_ctas(s), sms);
@@ -839,6 +891,53 @@ cudaError_t tc_causal_launch(const MhlaShape& s, const void* q, const void* k, c
     causal_agg_kernel<<<p.G, kThreads, kAggSmem, st>>>(p);
     note_launch();
   }
+  causal_out_kernel<<<p.G, kThreads, kOutSmem, st>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// Causal MHLA with a mixing matrix, chunk = block = 128 tokens ("MHLA" paper §4.2 / App. C chunk
+// form): the tcgen05 MHLA kernel's SUM and MIX passes with the weights m_ib for b < i give P_i
+// and zeta_i of every (head, block); the output kernel reads them instead of carrying a prefix
+// and weights its in-chunk terms by m_ii.
+bool tc_causal_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
+  if (!s.plain_phi() || s.grid() || mode != MIX_STRICT_LOWER) return false;
+  if (dt != MHLA_BF16 || s.d != kD || s.block != kTile || s.N % kTile != 0) return false;
+  if ((long long)s.heads() * s.N >= (1ll << 31)) return false;
+  return tc_mhla_prefix_supported(s, dt);
+}
+
+size_t tc_causal_mhla_workspace(const MhlaShape& s) { return tc_mhla_workspace(s); }
+
+cudaError_t tc_causal_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
+                                  const float* mixing, void* y, float* den_out, float eps, void* ws,
+                                  cudaStream_t st) {
+  cudaError_t e = tc_mhla_prefix_launch(s, k, v, mixing, ws, st);
+  if (e != cudaSuccess) return e;
+  char* w = static_cast<char*>(ws);
+  CParams p;
+  const uint64_t rows = (uint64_t)s.heads() * s.N;
+  if (!make_map(&p.tm_q, q, rows, kTile) || !make_map(&p.tm_k, k, rows, kTile) || !make_map(&p.tm_v, v, rows, kTile) ||
+      !make_map(&p.tm_y, y, rows, 32))
+    return cudaErrorInvalidValue;
+  p.agg_s = nullptr;
+  p.agg_z = nullptr;
+  p.den_out = den_out;
+  p.status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
+  p.T = s.heads() * (s.N / kTile);
+  p.CH = s.N / kTile;
+  p.eps = eps;
+  p.normalise = s.normalise ? 1 : 0;
+  tc_mhla_mixed_summaries(s, ws, &p.smix, &p.zmix);
+  p.mixing = mixing;
+  p.mix = 1;
+  p.H = s.H;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  p.G = std::min(max_ctas(s), sms);
+  static SmemOptIn opt_out;
+  e = opt_out.ensure((const void*)causal_out_kernel, (int)kOutSmem);
+  if (e != cudaSuccess) return e;
   causal_out_kernel<<<p.G, kThreads, kOutSmem, st>>>(p);
   note_launch();
   return cudaGetLastError();

@@ -195,6 +195,22 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, i
 }
 
 // L2 cache policy for data that is read or written once (evicted first).
+// L2 policy for data read again soon (kept ahead of evict-normal lines).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 16-byte global load with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_global_hint(const uint4* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

@@ -122,6 +122,8 @@ struct Params {
   int zx;                        // 1: the CTAs with a z row take no MIX units (C > 64, heads <= grid / 4)
   int grid2d;                    // 1: 2-D blocks (tokens on a gw-wide grid, blocks th x tw tiles)
   int normalise;                 // 0: Y is the numerator alone (den_out still the denominator)
+  int strict;                    // 1: weights m_ib for b < i only (causal MHLA's mixed prefix)
+  int mix_only;                  // 1: SUM and MIX only (S~, z~ left in the workspace), no OUT pass
   int gw, gh, tw, th, bpr;       // grid width / height, tile width / height, tiles per grid row
   float eps;
 };
@@ -390,6 +392,7 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
       u += n;
     }
   }
+  if (p.mix_only) return q;
   // OUT pass, on the OUT ring over the same memory: every SUM / MIX stage must
   // have been consumed first.  qm = first OUT stage without its S~ / z~ loads.
   for (int qq = q > kNS ? q - kNS : 0; qq < q; ++qq)
@@ -529,7 +532,8 @@ __device__ __forceinline__ void mix_weight_values(const Params& p, int hh, int k
     const int i = (t >> 3) + 32 * kk;
     float w[8];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) w[c] = (i < p.M && x0 + c < ks) ? __ldg(m + i * p.M + bc[c]) : 0.f;
+    for (int c = 0; c < 8; ++c)
+      w[c] = (i < p.M && x0 + c < ks && !(p.strict && bc[c] >= i)) ? __ldg(m + i * p.M + bc[c]) : 0.f;
     v[kk] = make_uint4(pack_bf16(w[0], w[1]), pack_bf16(w[2], w[3]), pack_bf16(w[4], w[5]), pack_bf16(w[6], w[7]));
     if (mix_rep(p.M)) break;
   }
@@ -665,7 +669,7 @@ __device__ __forceinline__ void mix_t_weights_load(const Params& p, int w, int l
     int b = (8 * pc) / p.cpb, rr = 8 * pc - b * p.cpb;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      v[c] = (i < p.M && 8 * pc + c < p.C) ? __ldg(m + b) : 0.f;
+      v[c] = (i < p.M && 8 * pc + c < p.C && !(p.strict && b >= i)) ? __ldg(m + b) : 0.f;
       if (++rr == p.cpb) {
         rr = 0;
         ++b;
@@ -1063,7 +1067,7 @@ __device__ void stage_weights(const Params& p, float* wt, int hh, int t, int n, 
     for (int k = 0; k < 16; ++k) {
       const int j = j0 + k * n + t;
       const int b = j / MAXM, i = j % MAXM;
-      v[k] = (j < MAXM * MAXM && b < p.M && i < p.M) ? __ldcg(mw + i * p.M + b) : 0.f;
+      v[k] = (j < MAXM * MAXM && b < p.M && i < p.M && !(p.strict && b >= i)) ? __ldcg(mw + i * p.M + b) : 0.f;
     }
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
@@ -1271,7 +1275,7 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
     __syncwarp();
   } else if (warp == kWarpMma) {
     if (lane == 0) {
-      mma_issuer<L>(p, sm, sh, tmem, 0, 0, 2);
+      mma_issuer<L>(p, sm, sh, tmem, 0, 0, p.mix_only ? 1 : 2);
       mma_commit(&sh->fin);  // arrives once this thread's MMAs have all completed
     }
     __syncwarp();
@@ -1309,9 +1313,14 @@ __global__ void __launch_bounds__(kThreads, 1) mhla_tc_kernel(const __grid_const
         mix_rows_all<MAXM>(p, sm, t, false);
       }
       mix_end(p, t);
-      if (warp >= kWarpPhi) phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, qs, q);
-      else if (warp >= kWarpEpi) epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 1, q, nst);
-      else if (warp == kWarpMix && lane == 0) mma_issuer<L>(p, sm, sh, tmem, 1, 2, 2);  // odd OUT chunks
+      if (p.mix_only) {
+      } else if (warp >= kWarpPhi) {
+        phi_pass<L>(p, sm, sh, warp - kWarpPhi, lane, 1, qs, q);
+      } else if (warp >= kWarpEpi) {
+        epi_pass<L>(p, sm, sh, tmem, warp - kWarpEpi, lane, 1, q, nst);
+      } else if (warp == kWarpMix && lane == 0) {
+        mma_issuer<L>(p, sm, sh, tmem, 1, 2, 2);  // odd OUT chunks
+      }
     }
     if (warp == kWarpMix && lane == 0) mma_commit(&sh->fin);
     __syncwarp();
@@ -1482,10 +1491,9 @@ bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
 
 size_t tc_mhla_workspace(const MhlaShape& s) { return tc_plan(s).total; }
 
-cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
-                           const float* mixing, void* y, float* den_out, float eps, MixMode mode,
-                           void* ws, cudaStream_t st) {
-  (void)mode;
+namespace {
+cudaError_t tc_mhla_run(const MhlaShape& s, const void* q, const void* k, const void* v, const float* mixing,
+                        void* y, float* den_out, float eps, bool strict, bool mix_only, void* ws, cudaStream_t st) {
   const TcPlan pl = tc_plan(s);
   char* w = static_cast<char*>(ws);
   Params p;
@@ -1536,6 +1544,8 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
   p.XS = pl.tc_mix ? s.heads() * kD : 0;
   p.eps = eps;
   p.normalise = s.normalise ? 1 : 0;
+  p.strict = strict ? 1 : 0;
+  p.mix_only = mix_only ? 1 : 0;
   cudaError_t e;
   if (p.M <= 16)
     e = launch_t<16>(p, grid, st);
@@ -1545,6 +1555,33 @@ cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, con
     e = launch_t<64>(p, grid, st);
   note_launch();
   return e;
+}
+}  // namespace
+
+cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
+                           const float* mixing, void* y, float* den_out, float eps, MixMode mode,
+                           void* ws, cudaStream_t st) {
+  (void)mode;
+  return tc_mhla_run(s, q, k, v, mixing, y, den_out, eps, false, false, ws, st);
+}
+
+bool tc_mhla_prefix_supported(const MhlaShape& s, mhla_dtype dt) {
+  MhlaShape f = s;
+  f.gh = f.gw = f.th = f.tw = 0;
+  return !s.grid() && tc_mhla_supported(f, dt, MIX_FULL);
+}
+
+cudaError_t tc_mhla_prefix_launch(const MhlaShape& s, const void* k, const void* v, const float* mixing, void* ws,
+                                  cudaStream_t st) {
+  // Q and Y are not touched in this mode: their tensor maps take K's and V's addresses
+  return tc_mhla_run(s, k, k, v, mixing, const_cast<void*>(v), nullptr, 0.f, true, true, ws, st);
+}
+
+void tc_mhla_mixed_summaries(const MhlaShape& s, void* ws, const uint8_t** smix, const float** zmix) {
+  const TcPlan pl = tc_plan(s);
+  char* w = static_cast<char*>(ws);
+  *smix = reinterpret_cast<const uint8_t*>(w + pl.off_smix);
+  *zmix = reinterpret_cast<const float*>(w + pl.off_zmix);
 }
 
 }  // namespace mhla

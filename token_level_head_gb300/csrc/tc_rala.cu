@@ -116,11 +116,14 @@ __global__ void __launch_bounds__(256) rala_qsum_kernel(const __nv_bfloat16* __r
   const int r0 = (int)((long long)s * NP / kSlices), r1 = (int)((long long)(s + 1) * NP / kSlices);
   const int p = threadIdx.x & 7, rr = threadIdx.x >> 3;  // 32 rows at a time
   const uint4* src = reinterpret_cast<const uint4*>(q) + ((size_t)u * NP) * 8;
+  // the output kernel reads Q again: keep it in L2 (evict-last) across the B^T kernel
+  const uint64_t keep = policy_evict_last();
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int r = r0 + rr; r < r1; r += 4 * 32) {  // four 16-byte loads in flight
     uint4 u[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) u[k] = r + 32 * k < r1 ? __ldcs(src + (size_t)(r + 32 * k) * 8 + p) : make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 4; ++k)
+      u[k] = r + 32 * k < r1 ? ld_global_hint(src + (size_t)(r + 32 * k) * 8 + p, keep) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float f[8];

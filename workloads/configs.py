@@ -70,6 +70,9 @@ WORKLOADS = {
     "hires_m1": Workload("hires_m1", 3, "mhla", 1, 6, 65536, 64, 65536, "bf16", 0.125, "ones"),
     # long causal sequences, chunk 128
     "causal": Workload("causal", 4, "causal", 4, 16, 8192, 64, 128, "bf16", 0.125),
+    # the causal inputs as causal MHLA: blocks of 128 (M = 64), a causal mixing matrix
+    "causal_mhla": Workload("causal_mhla", 4, "causal", 4, 16, 8192, 64, 128, "bf16", 0.125,
+                            "lower_uniform_rows"),
     # the causal inputs with RetNet decay gamma = 0.99 (notes §七)
     "causal_decay": Workload("causal_decay", 4, "causal", 4, 16, 8192, 64, 128, "bf16", 0.125,
                              extra={"gamma": 0.99}),
