@@ -297,7 +297,10 @@ mhla_status mhla_forward_noalloc(const void* q, const void* k, const void* v, co
 
 /* Kernel family mhla_forward would use for these arguments (no launch).
  * With causal = 1 the answer is for plain causal linear attention (mixing
- * NULL); causal MHLA with a mixing matrix always runs the SIMT kernels. */
+ * NULL); mhla_forward_ex_path answers for causal MHLA with a mixing matrix,
+ * which runs on the tensor cores for bf16, d = 64, chunk = 128 and
+ * N / 128 <= 64 (the MHLA kernel's summary and mixing passes with the weights
+ * below the diagonal, then the causal output kernel), else on the SIMT kernels. */
 mhla_path mhla_forward_path(int B, int H, int N, int d, int block_size, int causal,
                             mhla_dtype dt);
 
