@@ -81,3 +81,85 @@ def test_block_offset_error_is_caught(monkeypatch):
     x = mhla_host(wl)
     monkeypatch.setattr(om, "block_of", lambda n, bs: np.minimum((np.arange(n) + 1) // bs, n // bs - 1))
     _fails(pins.test_block_form_equals_token_expansion_tiny, (wl, x))
+
+
+# ------------------------------------------------------------- newer forms
+def _causal_small():
+    return pins.causal_small.__wrapped__() if hasattr(pins.causal_small, "__wrapped__") else (
+        pins.normal(11, 1, (2, 2, 96, 8), 0.4), pins.normal(11, 2, (2, 2, 96, 8), 0.4),
+        pins.normal(11, 3, (2, 2, 96, 8)))
+
+
+def test_column_major_tile_numbering_is_caught(monkeypatch):
+    def column_major(gh, gw, th, tw):
+        r, c = np.divmod(np.arange(gh * gw), gw)
+        return (c // tw) * (gh // th) + (r // th)
+    monkeypatch.setattr(oracle, "grid_block_ids", column_major)
+    _fails(pins.test_grid_block_ids_by_hand)
+
+
+def test_manhattan_locality_is_caught(monkeypatch):
+    def manhattan(bh, bw):
+        r, c = np.divmod(np.arange(bh * bw), bw)
+        dist = np.abs(r[:, None] - r[None, :]) + np.abs(c[:, None] - c[None, :]) + 0.0
+        far = dist.max(axis=1, keepdims=True)
+        m0 = np.where(far > 0, 1.0 - dist / np.where(far > 0, far, 1.0), 1.0)
+        return m0 / m0.sum(axis=1, keepdims=True)
+    monkeypatch.setattr(oracle, "locality_mixing_init", manhattan)
+    _fails(pins.test_locality_init_by_hand)
+
+
+def test_decay_of_the_state_only_is_caught(monkeypatch):
+    """Decaying S but not z (the notes write only S) must disagree with the explicit weights."""
+    def s_only(s0, z0, qs, ks, vs, eps=1e-6, gamma=1.0):
+        s, z = np.asarray(s0, np.float64).copy(), np.asarray(z0, np.float64).copy()
+        qs, ks, vs = (np.asarray(a, np.float64) for a in (qs, ks, vs))
+        outs, dens = np.empty_like(vs), np.empty(vs.shape[:-1])
+        for t in range(qs.shape[0]):
+            qt, kt = om.phi(qs[t]), om.phi(ks[t])
+            s = gamma * s + kt[..., :, None] * vs[t][..., None, :]
+            z = z + kt
+            dn = np.einsum("...c,...c->...", qt, z) + eps
+            outs[t] = np.einsum("...c,...ce->...e", qt, s) / dn[..., None]
+            dens[t] = dn
+        return outs, dens, s, z
+    monkeypatch.setattr(oracle, "decode_steps", s_only)
+    _fails(pins.test_decode_with_decay_equals_decayed_bruteforce, _causal_small())
+
+
+def test_stream_without_self_weight_is_caught(monkeypatch):
+    """The running summary entering the output with weight 1 instead of m_ii."""
+    real = om.causal_mhla_stream
+
+    def no_mii(q, k, v, mixing, block_size, eps=1e-6):
+        mix = np.array(mixing, dtype=np.float64)
+        m = mix.shape[-1]
+        mix[:, np.arange(m), np.arange(m)] = 1.0
+        return real(q, k, v, mix, block_size, eps)
+    monkeypatch.setattr(oracle, "causal_mhla_stream", no_mii)
+    _fails(pins.test_causal_mhla_stream_equals_bruteforce, _causal_small())
+
+
+def test_swapped_feature_maps_are_caught(monkeypatch):
+    monkeypatch.setitem(om.FEATURE_MAPS, "relu", om.phi_exp)
+    _fails(pins.test_relu_features_of_nonpositive_queries_give_zero)
+
+
+def test_undecayed_normaliser_in_the_variant_recurrence_is_caught(monkeypatch):
+    def z_undecayed(q, k, v, feature="elu1", gamma=1.0, eps=1e-6, normalise=True):
+        f = om.FEATURE_MAPS[feature]
+        q, k, v = (np.asarray(a, np.float64) for a in (q, k, v))
+        *lead, n, d = q.shape
+        s, z = np.zeros((*lead, d, d)), np.zeros((*lead, d))
+        y, den = np.empty_like(v), np.empty((*lead, n))
+        for t in range(n):
+            qt, kt = f(q[..., t, :]), f(k[..., t, :])
+            s = gamma * s + kt[..., :, None] * v[..., t, None, :]
+            z = z + kt
+            dn = np.einsum("...c,...c->...", qt, z) + eps
+            num = np.einsum("...c,...ce->...e", qt, s)
+            y[..., t, :] = num / dn[..., None] if normalise else num
+            den[..., t] = dn
+        return y, den
+    monkeypatch.setattr(oracle, "causal_variant_recurrent", z_undecayed)
+    _fails(pins.test_causal_variant_recurrence_equals_bruteforce, _causal_small(), "elu1", 0.9)
