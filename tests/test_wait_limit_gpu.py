@@ -1,7 +1,8 @@
 """A device-side wait that gives up: the failure path of the bounded waits.
 
-The bf16 tensor-core forward waits on other CTAs (per-head counters) and on
-its own pipeline (mbarriers); every such wait has a time limit, after which
+The bf16 tensor-core forwards wait on other CTAs (per-head counters, grid
+barriers) and on their own pipelines (mbarriers); every such wait has a time
+limit, after which
 the kernel lets its copies and MMAs in flight finish, raises the call's abort
 flag, leaves the workspace counters at zero and latches MHLA_ERR_TIMEOUT in
 the workspace.  ``mhla_debug_set_wait_limit_ns`` shortens the limit so that a
@@ -29,9 +30,13 @@ def lib():
     return binding.load()
 
 
-def test_wait_limit_gives_up_then_next_call_is_correct():
-    B, H, N, d, block = 2, 3, 1152, 64, 128  # C = 9 chunks a head: the stream kernel
-    assert binding.mhla_forward_path(B, H, N, d, block, 0, torch.bfloat16) == "tcgen05_stream"
+@pytest.mark.parametrize("shape,path", [
+    ((2, 3, 1152, 64, 128), "tcgen05_stream"),  # C = 9 chunks a head: per-head counters
+    ((2, 2, 2048, 64, 256), "tcgen05"),         # C = 16: the three-pass kernel and its grid barriers
+], ids=["stream", "three_pass"])
+def test_wait_limit_gives_up_then_next_call_is_correct(shape, path):
+    B, H, N, d, block = shape
+    assert binding.mhla_forward_path(B, H, N, d, block, 0, torch.bfloat16) == path
     x = rand_inputs(700, (B, H, N, d), "bf16")
     mix_t, mix64 = rand_mixing(31, H, N // block)
     ws = binding.new_workspace(binding.mhla_workspace_bytes(B, H, N, d, block), "cuda")

@@ -51,6 +51,8 @@ bool tc_mhla_prefix_supported(const MhlaShape& s, mhla_dtype dt);
 cudaError_t tc_mhla_prefix_launch(const MhlaShape& s, const void* k, const void* v, const float* mixing, void* ws,
                                   cudaStream_t st);
 void tc_mhla_mixed_summaries(const MhlaShape& s, void* ws, const uint8_t** smix, const float** zmix);
+// Limit of every bounded device-side wait of the three-pass kernel (0 restores the default 0.5 s).
+void tc_mhla_set_wait_limit(unsigned long long ns);
 
 // ---- tcgen05 stream path (bf16, d = 64, blocks of whole 128-token tiles, at most 64 tiles a head):
 // summaries, mixing and output as one ordered list of items with per-head readiness counters

@@ -381,6 +381,9 @@ const char* mhla_status_string(mhla_status s) {
 
 unsigned long long mhla_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-void mhla_debug_set_wait_limit_ns(unsigned long long ns) { tc_stream_set_wait_limit(ns); }
+void mhla_debug_set_wait_limit_ns(unsigned long long ns) {
+  tc_stream_set_wait_limit(ns);
+  tc_mhla_set_wait_limit(ns);
+}
 
 }  // extern "C"

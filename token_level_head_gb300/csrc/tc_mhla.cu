@@ -53,7 +53,7 @@ constexpr int kSTile = kD * kD * 2;         // 8 KB S~^T tile
 constexpr int kNA = 4;                      // TMEM accumulators, 64 columns each
 constexpr uint32_t kTmemCols = 512;         // SUM / OUT use the first kNA x 64 columns, MIX all
 constexpr int kMixRows = kD + 1;            // MIX rows per head: 64 of S^T, then z
-constexpr uint64_t kWaitLimitNs = 500000000ull;  // a wait gives up after 0.5 s
+constexpr uint64_t kWaitLimitNs = 500000000ull;  // a wait gives up after 0.5 s (the default)
 
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpMix = 2, kWarpEpi = 4, kWarpPhi = 8;
 constexpr int kMixThreads = (16 - kWarpMix) * 32;  // warps 2-15 run the MIX phase
@@ -125,6 +125,8 @@ struct Params {
   int strict;                    // 1: weights m_ib for b < i only (causal MHLA's mixed prefix)
   int mix_only;                  // 1: SUM and MIX only (S~, z~ left in the workspace), no OUT pass
   int gw, gh, tw, th, bpr;       // grid width / height, tile width / height, tiles per grid row
+  unsigned long long wait_ns;    // limit of the producer's waits for the mixed summaries (kWaitLimitNs
+                                 // unless a diagnostic shortened it)
   float eps;
 };
 
@@ -177,7 +179,7 @@ __device__ __forceinline__ int aborted(Small* sh) { return *reinterpret_cast<vol
 __device__ __forceinline__ void set_abort(Small* sh) { *reinterpret_cast<volatile int*>(&sh->abort) = 1; }
 
 // mbarrier phase wait.  The waiting thread sleeps in the barrier unit (it
-// issues nothing while suspended); false once kWaitLimitNs has passed (and
+// issues nothing while suspended); false once the wait limit has passed (and
 // then the CTA aborts) or as soon as another role has aborted.
 __device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, Small* sh) {
   // A few polls, then suspended waits with a short limit: a waiter is not
@@ -208,7 +210,7 @@ __device__ __noinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > 10000000ull) return;
 }
 
-// Global counter wait (acquire): false after kWaitLimitNs or on abort.
+// Global counter wait (acquire): false after the wait limit or on abort.
 __device__ __noinline__ bool gwait(const unsigned* p, unsigned target, Small* sh) {
   if (ld_acquire(p) >= target) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -411,7 +413,7 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
           for (; qm < qo; ++qm, gm += gridDim.x) issue_mix_loads(p, sm, sh, qm, gm);
         }
         if (aborted(sh)) break;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > p.wait_ns) {
           set_abort(sh);
           break;
         }
@@ -433,7 +435,7 @@ __device__ int producer(const Params& p, uint8_t* sm, Small* sh) {
       for (; qm < qo; ++qm, gm += gridDim.x) issue_mix_loads(p, sm, sh, qm, gm);
       break;
     }
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > p.wait_ns) {
       set_abort(sh);
       break;
     }
@@ -1492,6 +1494,8 @@ bool tc_mhla_supported(const MhlaShape& s, mhla_dtype dt, MixMode mode) {
 size_t tc_mhla_workspace(const MhlaShape& s) { return tc_plan(s).total; }
 
 namespace {
+unsigned long long g_wait_ns = kWaitLimitNs;
+
 cudaError_t tc_mhla_run(const MhlaShape& s, const void* q, const void* k, const void* v, const float* mixing,
                         void* y, float* den_out, float eps, bool strict, bool mix_only, void* ws, cudaStream_t st) {
   const TcPlan pl = tc_plan(s);
@@ -1546,6 +1550,7 @@ cudaError_t tc_mhla_run(const MhlaShape& s, const void* q, const void* k, const 
   p.normalise = s.normalise ? 1 : 0;
   p.strict = strict ? 1 : 0;
   p.mix_only = mix_only ? 1 : 0;
+  p.wait_ns = g_wait_ns;
   cudaError_t e;
   if (p.M <= 16)
     e = launch_t<16>(p, grid, st);
@@ -1557,6 +1562,8 @@ cudaError_t tc_mhla_run(const MhlaShape& s, const void* q, const void* k, const 
   return e;
 }
 }  // namespace
+
+void tc_mhla_set_wait_limit(unsigned long long ns) { g_wait_ns = ns == 0 ? kWaitLimitNs : ns; }
 
 cudaError_t tc_mhla_launch(const MhlaShape& s, const void* q, const void* k, const void* v,
                            const float* mixing, void* y, float* den_out, float eps, MixMode mode,
