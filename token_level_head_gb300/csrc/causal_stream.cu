@@ -8,7 +8,7 @@
 //   den = phi(q) . (sum_{b<i} m_ib z_b + m_ii z_i) + eps,   out = num / den,
 // the chunk form of the causal MHLA forward evaluated at one token.
 //
-// One CTA per (batch, head) unit walks the call's tokens in order (their rows
+// d = 128: one CTA per (batch, head) unit walks the call's tokens in order (their rows
 // arrive through a cp.async ring several tokens ahead; phi of token n + 1 is
 // taken while token n is computed).  Its
 // threads hold the unit's running summary S_i and the mixed state
@@ -17,11 +17,15 @@
 // summaries in memory when block i starts, so a token costs three d^2 FMAs
 // (S_i, R, and the output) whatever i is.  A finished block's summary is
 // written back to its slot.
+//
+// d <= 64: a warp per (unit, 32-column slab) instead (below), with the same registers
+// per column and no barrier wider than the warp.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace mhla {
 namespace {
@@ -174,13 +178,205 @@ causal_stream_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
   cp_async_wait<0>();
 }
 
+// ------------------------------------------------------------------------------------------
+// d <= 64: a warp per (unit, 32-column slab).  Lane e holds column e of both the running summary
+// S_i and the mixed state R = P_i + m_ii S_i, as row pairs (packed fp32x2 FMAs update two rows
+// at once), so a warp needs nothing from any other warp: each slab warp also keeps the whole z
+// (rows lane + 32 j) and its own denominator.  The step's rows come through a per-warp cp.async
+// ring; phi of token n + 1 is taken while token n is computed (within a block).
+template <int D> struct WarpGeom {
+  static constexpr int LA = D < 32 ? D : 32;   // lanes holding a column
+  static constexpr int SL = D / LA;            // slab warps per unit
+  static constexpr int RZ = (D + 31) / 32;     // z rows per lane
+  static constexpr int WARPS = 4;              // warps per CTA
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(WarpGeom<D>::WARPS * 32, 12 / WarpGeom<D>::WARPS)
+causal_stream_warp_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                          const float* __restrict__ mixing, float* __restrict__ S, float* __restrict__ z,
+                          T* __restrict__ out, float* __restrict__ den_out, int t0, int T_steps, int units, int H,
+                          int block, int M, float eps) {
+  using G = WarpGeom<D>;
+  constexpr int LA = G::LA, SL = G::SL, RZ = G::RZ, WARPS = G::WARPS;
+  constexpr int QC = D * (int)sizeof(T) / 16;   // 16-byte chunks of a q or k row
+  constexpr int VCH = LA * (int)sizeof(T) / 16; // 16-byte chunks of the slab's v columns
+  constexpr int NCH = 2 * QC + VCH;
+  constexpr int NI = (NCH + 31) / 32;
+  constexpr int STAGE = 2 * D + LA;
+  static_assert(QC >= 1 && VCH >= 1 && D % 4 == 0, "whole 16-byte chunks");
+
+  __shared__ __align__(16) T ring[WARPS][kPipe][STAGE];
+  __shared__ __align__(16) float phq[WARPS][2][D];
+  __shared__ __align__(16) float phk[WARPS][2][D];
+
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const long long task = (long long)blockIdx.x * WARPS + wid;
+  if (T_steps <= 0 || task >= (long long)units * SL) return;  // no block-wide barrier in this kernel
+  const int u = (int)(task / SL), slab = (int)(task % SL);
+  const int e = slab * LA + lane;             // this lane's column
+  const bool owns = LA == 32 || lane < LA;
+  const int ec = owns ? e : 0;                // a valid column for the idle lanes' dummy loads
+  const float* mh = mixing + (size_t)(u % H) * M * M;
+  float* Su = S + (size_t)u * M * D * D;
+  float* zu = z + (size_t)u * M * D;
+
+  // ---- ring of the call's tokens: token n at stage n % kPipe (past the end: the last token again)
+  const size_t tstride = (size_t)units * D * sizeof(T);
+  const char* src[NI];
+  uint32_t dst_off[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int c = lane + 32 * i;
+    const size_t row = (size_t)u * D;
+    const T* base = c < QC ? q + row : c < 2 * QC ? k + row : v + row + slab * LA;
+    const int cc = c < QC ? c : c < 2 * QC ? c - QC : c - 2 * QC;
+    src[i] = reinterpret_cast<const char*>(base) + cc * 16;
+    dst_off[i] = (uint32_t)(c * 16);
+  }
+  char* ring_w = reinterpret_cast<char*>(ring[wid][0]);
+  auto issue = [&](int n) {
+    const int nn = n < T_steps ? n : T_steps - 1;
+    char* dst = ring_w + (n % kPipe) * (STAGE * (int)sizeof(T));
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (lane + 32 * i < NCH) cp_async16(dst + dst_off[i], src[i] + (size_t)nn * tstride);
+    cp_async_commit();
+  };
+
+  float2 rp[D / 2], sp[D / 2];  // R and S_i of column e, rows (2p, 2p + 1)
+  float zr[RZ], zc[RZ];          // rows lane + 32 j: zeta_i + m_ii z_i, and z_i
+  float mii = 0.f;
+  int cur = -1;
+
+  // phi of token n, its v and the denominator with this block's weights
+  auto prep = [&](int n, float& vv, float& den) {
+    const T* rq = ring[wid][n % kPipe];
+    const T* rk = rq + D;
+    const T* rv = rq + 2 * D;
+    float part = 0.f;
+#pragma unroll
+    for (int j = 0; j < RZ; ++j) {
+      const int c = lane + 32 * j;
+      if (c < D) {
+        const float fq = tc::phi_f(to_f(rq[c])), fk = tc::phi_f(to_f(rk[c]));
+        phq[wid][n & 1][c] = fq;
+        phk[wid][n & 1][c] = fk;
+        zc[j] += fk;
+        zr[j] = fmaf(mii, fk, zr[j]);
+        part = fmaf(fq, zr[j], part);
+      }
+    }
+    vv = owns ? to_f(rv[lane]) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    den = part + eps;
+  };
+
+  for (int n = 0; n < kPipe - 1; ++n) issue(n);
+  cp_async_wait<kPipe - 2>();  // token 0
+  __syncwarp();
+
+  bool have = false;  // token n's prep done (in the previous iteration)
+  float vv = 0.f, den = 1.f;
+  for (int n = 0; n < T_steps; ++n) {
+    const int t = t0 + n, bi = t / block;
+    if (bi != cur) {
+      // block bi starts (or the call starts inside it): S_i from its slot (zero at its first
+      // token), R = sum_{b<i} m_ib S_b + m_ii S_i from the frozen slots, z likewise
+      const bool fresh = t % block == 0;
+      mii = __ldg(mh + (size_t)bi * M + bi);
+#pragma unroll
+      for (int pp = 0; pp < D / 2; ++pp) {
+        sp[pp] = fresh ? make_float2(0.f, 0.f)
+                       : make_float2(Su[((size_t)bi * D + 2 * pp) * D + ec], Su[((size_t)bi * D + 2 * pp + 1) * D + ec]);
+        rp[pp] = make_float2(mii * sp[pp].x, mii * sp[pp].y);
+      }
+#pragma unroll
+      for (int j = 0; j < RZ; ++j) {
+        const int c = lane + 32 * j;
+        zc[j] = (fresh || c >= D) ? 0.f : zu[(size_t)bi * D + c];
+        zr[j] = mii * zc[j];
+      }
+      for (int b = 0; b < bi; ++b) {
+        const float w = __ldg(mh + (size_t)bi * M + b);
+        const float* sb = Su + (size_t)b * D * D + ec;
+#pragma unroll
+        for (int pp = 0; pp < D / 2; ++pp) {
+          rp[pp].x = fmaf(w, __ldcg(sb + (size_t)(2 * pp) * D), rp[pp].x);
+          rp[pp].y = fmaf(w, __ldcg(sb + (size_t)(2 * pp + 1) * D), rp[pp].y);
+        }
+#pragma unroll
+        for (int j = 0; j < RZ; ++j) {
+          const int c = lane + 32 * j;
+          if (c < D) zr[j] = fmaf(w, __ldcg(zu + (size_t)b * D + c), zr[j]);
+        }
+      }
+      cur = bi;
+      have = false;
+    }
+    if (!have) prep(n, vv, den);  // its rows have landed (the previous wait) and are visible
+    const float v0 = vv, d0 = den;
+    issue(n + kPipe - 1);          // into token n - 1's stage (read before the last barrier)
+    cp_async_wait<kPipe - 2>();    // token n + 1 copied (this lane's chunks)
+    __syncwarp();                  // every lane's copies and phi writes visible; token n - 1's reads done
+    have = n + 1 < T_steps && (t + 1) / block == bi;
+    if (have) prep(n + 1, vv, den);
+
+    const float* pq = phq[wid][n & 1];
+    const float* pk = phk[wid][n & 1];
+    const float2 v2 = make_float2(v0, v0), m2 = make_float2(mii, mii);
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c4 = 0; c4 < D; c4 += 4) {
+      const float4 k4 = *reinterpret_cast<const float4*>(pk + c4);
+      const float4 q4 = *reinterpret_cast<const float4*>(pq + c4);
+      const float2 ka = make_float2(k4.x, k4.y), kb = make_float2(k4.z, k4.w);
+      sp[c4 / 2] = __ffma2_rn(ka, v2, sp[c4 / 2]);
+      sp[c4 / 2 + 1] = __ffma2_rn(kb, v2, sp[c4 / 2 + 1]);
+      rp[c4 / 2] = __ffma2_rn(__fmul2_rn(ka, m2), v2, rp[c4 / 2]);
+      rp[c4 / 2 + 1] = __ffma2_rn(__fmul2_rn(kb, m2), v2, rp[c4 / 2 + 1]);
+      acc0 = __ffma2_rn(make_float2(q4.x, q4.y), rp[c4 / 2], acc0);
+      acc1 = __ffma2_rn(make_float2(q4.z, q4.w), rp[c4 / 2 + 1], acc1);
+    }
+    const size_t row = (size_t)n * units + u;
+    if (owns) out[row * D + e] = from_f<T>(__fdividef((acc0.x + acc0.y) + (acc1.x + acc1.y), d0));
+    if (den_out != nullptr && slab == 0 && lane == 0) den_out[row] = d0;
+    if (t % block == block - 1 || n == T_steps - 1) {
+      // the block is finished (frozen from now on) or the call ends inside it: its slot (every
+      // slab writes the same z, so that each reads back only values it wrote)
+      if (owns) {
+#pragma unroll
+        for (int pp = 0; pp < D / 2; ++pp) {
+          Su[((size_t)bi * D + 2 * pp) * D + e] = sp[pp].x;
+          Su[((size_t)bi * D + 2 * pp + 1) * D + e] = sp[pp].y;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < RZ; ++j) {
+        const int c = lane + 32 * j;
+        if (c < D) zu[(size_t)bi * D + c] = zc[j];
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
 template <typename T, int D>
 cudaError_t stream_t(const void* q, const void* k, const void* v, const float* mixing, float* S, float* z,
                      void* out, float* den_out, int t0, int T_steps, int units, int H, int block, int M, float eps,
                      cudaStream_t st) {
-  causal_stream_kernel<T, D><<<units, StreamGeom<D>::NT, 0, st>>>(
-      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), mixing, S, z,
-      static_cast<T*>(out), den_out, t0, T_steps, units, H, block, M, eps);
+  if constexpr (D <= 64) {
+    using G = WarpGeom<D>;
+    const long long blocks = ((long long)units * G::SL + G::WARPS - 1) / G::WARPS;
+    causal_stream_warp_kernel<T, D><<<(unsigned)blocks, G::WARPS * 32, 0, st>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), mixing, S, z,
+        static_cast<T*>(out), den_out, t0, T_steps, units, H, block, M, eps);
+  } else {
+    causal_stream_kernel<T, D><<<units, StreamGeom<D>::NT, 0, st>>>(
+        static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), mixing, S, z,
+        static_cast<T*>(out), den_out, t0, T_steps, units, H, block, M, eps);
+  }
   note_launch();
   return cudaGetLastError();
 }
