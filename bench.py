@@ -71,12 +71,12 @@ def workload_bytes(wl):
         units = wl.B * wl.H
         return units * (2 * (wl.d * wl.d + wl.d) * 4 + wl.N * (4 * wl.d * eb + 4))
     if wl.kind == "stream":
-        # each token's q, k, v, out, den; at each block start the frozen summaries of the
-        # blocks before it (to mix them); each block's summary written once
+        # each token's q, k, v, out, den; the summaries frozen before the call read once (and the
+        # running summary of a block the call starts inside); each touched block's summary written once
         units, P, blk = wl.B * wl.H, wl.extra["prefix"], wl.block
         first, last = P // blk, (P + wl.N - 1) // blk
         slot = (wl.d * wl.d + wl.d) * 4
-        reads = sum(range(first, last + 1)) * slot + (slot if P % blk else 0)
+        reads = first * slot + (slot if P % blk else 0)
         return units * (wl.N * (4 * wl.d * eb + 4) + reads + (last - first + 1) * slot)
     if wl.kind == "rala":
         cx = wl.extra["cx"]
@@ -89,10 +89,20 @@ def tokens_per_step(wl):
 
 
 def workload_flops(wl):
-    """fp32 operations of one fused decode call (an FMA counts 2): per unit and step the state
-    update and the output read 2 d^2 FMAs, the denominator d FMAs, z d adds."""
-    assert wl.kind == "decode_steps"
-    return wl.B * wl.H * wl.N * (4 * wl.d * wl.d + 3 * wl.d)
+    """fp32 operations of one call (an FMA counts 2).
+    Fused decode, per unit and step: the state update and the output read 2 d^2 FMAs, the
+    denominator d FMAs, z d adds.
+    Causal MHLA inference, per unit and token: S_i += phi(k) v^T, R += m_ii phi(k) v^T and the
+    output phi(q) R are 3 d^2 FMAs, z_i d adds, the mixed z and the denominator 2 d FMAs; per block
+    that starts in the call, sum_{b<i} m_ib (S_b, z_b) is i (d^2 + d) FMAs."""
+    d = wl.d
+    if wl.kind == "decode_steps":
+        return wl.B * wl.H * wl.N * (4 * d * d + 3 * d)
+    assert wl.kind == "stream"
+    P, blk = wl.extra["prefix"], wl.block
+    starts = range(-(-P // blk), (P + wl.N - 1) // blk + 1)  # blocks starting inside the call
+    mixed = sum(starts) + (P // blk if P % blk else 0)     # slots mixed at their starts
+    return wl.B * wl.H * (wl.N * (6 * d * d + 5 * d) + mixed * 2 * (d * d + d))
 
 
 def fp32_peak_tflops(sm_count, sm_mhz=2070.0):
@@ -665,8 +675,9 @@ def parity_of_stream(runner):
 
 
 def alu_roofline(torch, wl, device, launch_ms):
-    """The fused decode's roofline: fp32 FMA issue (its loop is bound by it), against the FP32
-    peak at the maximum SM clock (152 SMs x 128 lanes x 2 x 2070 MHz on GB300)."""
+    """The roofline of the token-sequential recurrences (fused decode, causal MHLA inference):
+    fp32 FMA issue, which binds them (their minimal HBM time is well below their minimal FMA
+    time), against the FP32 peak at the maximum SM clock (152 SMs x 128 lanes x 2 x 2070 MHz)."""
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     peak = fp32_peak_tflops(sms)
     achieved = workload_flops(wl) / (launch_ms / 1e3) / 1e12
@@ -695,6 +706,9 @@ def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
                        "the next, so this is not a DRAM figure")
     elif wl.kind == "decode_steps":
         out["unit"] = "unit-steps/s"
+        out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
+        out["parity"] = parity_of_timed_output(runner)
+    elif wl.kind == "stream":
         out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
         out["parity"] = parity_of_timed_output(runner)
     else:
@@ -782,7 +796,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "clocks": sampler.summary(t_wall0, t_wall1),
         "parity": parity,
     }
-    if wl.kind == "decode_steps":  # bound by fp32 FMA issue, not by HBM
+    if wl.kind in ("decode_steps", "stream"):  # bound by fp32 FMA issue, not by HBM
         line["roofline"] = dict(alu_roofline(torch, wl, device, kernel_ms), kernel=kernel_name,
                                 traffic=line["roofline"]["traffic"], kernels_per_step=per_step_kernels,
                                 launch_ms=kernel_ms, effective_GBps=achieved)

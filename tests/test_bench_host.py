@@ -34,6 +34,14 @@ def test_algorithmic_bytes_of_the_workloads():
     assert bench.workload_bytes(fused) == 4096 * (2 * (64 * 64 + 64) * 4 + 1024 * (4 * 64 * 2 + 4))
     assert bench.workload_flops(fused) == 4096 * 1024 * (4 * 64 * 64 + 3 * 64)
     assert abs(bench.fp32_peak_tflops(152) - 80.548) < 0.001
+    # causal MHLA inference of 1024 tokens after 2048 (16 frozen blocks of 128, 8 blocks touched):
+    # tokens' q, k, v, out and den; the 16 frozen slots read once; the 8 touched slots written once;
+    # 3 d^2 + 3 d FMAs a token, and blocks 16 .. 23 each mix the i slots before them
+    st = W["stream"]
+    slot = (64 * 64 + 64) * 4
+    assert bench.tokens_per_step(st) == 4096 * 1024
+    assert bench.workload_bytes(st) == 4096 * (1024 * (4 * 64 * 2 + 4) + 16 * slot + 8 * slot)
+    assert bench.workload_flops(st) == 4096 * (1024 * (6 * 64 * 64 + 5 * 64) + 156 * 2 * (64 * 64 + 64))
 
 
 def test_traffic_record_needs_matching_sources(monkeypatch):

@@ -812,12 +812,34 @@ STREAM = [  # B, H, N, d, block, dtype
 def test_causal_stream_against_the_oracle(shape):
     """Whole sequences token by token, in three calls cut inside blocks."""
     B, H, N, d, block, dtype = shape
+    check_stream_calls(shape, [0, block // 2 + 1, N - block - 3, N])
+
+
+# many blocks: calls that start on a block boundary and inside a block after 10 to 18 frozen
+# blocks, with 1, 9, 13 and 14 blocks starting inside one call (the kernels mix the frozen
+# slots of up to 8 later blocks per pass)
+STREAM_MANY = [  # shape, cuts
+    ((1, 2, 200, 16, 8, "f32"), [0, 80, 81, 200]),
+    ((1, 2, 512, 64, 16, "bf16"), [0, 160, 300, 512]),
+    ((2, 1, 384, 32, 16, "f32"), [0, 160, 163, 384]),
+    ((1, 1, 256, 128, 16, "bf16"), [0, 160, 170, 256]),
+]
+
+
+@pytest.mark.parametrize("case", STREAM_MANY, ids=lambda c: "x".join(map(str, c[0])))
+def test_causal_stream_many_blocks(case):
+    check_stream_calls(*case)
+
+
+def check_stream_calls(shape, cuts):
+    """The sequence through one mhla_causal_stream call per range of cuts, against the oracle's
+    token-by-token causal MHLA (outputs, denominators, and every block's summary slot)."""
+    B, H, N, d, block, dtype = shape
     M = N // block
     x = rand_inputs(600 + N + d, (B, H, N, d), dtype)
     mix_t, mix64 = lower_mixing(601 + d, H, M)
     S = torch.full((B, H, M, d, d), float("nan"), device="cuda")  # every slot is written before it is read
     z = torch.full((B, H, M, d), float("nan"), device="cuda")
-    cuts = [0, block // 2 + 1, N - block - 3, N]
     outs, dens = [], []
     for a, b in zip(cuts[:-1], cuts[1:]):
         o, dn = stream_run(x, mix_t, S, z, block, a, b - a, dtype)

@@ -36,7 +36,9 @@ template <int D> struct StreamGeom {
   static constexpr int RPT = D / G;                // rows per thread
 };
 
-constexpr int kPipe = 8;  // tokens in flight in the cp.async ring
+constexpr int kPipe = 8;      // tokens in flight in the cp.async ring
+constexpr int kMixGroup = 8;  // premix: blocks accumulated per pass over the frozen slots
+constexpr int kMixRows = 8;   // premix: rows of a lane's column per accumulator
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
@@ -183,7 +185,9 @@ causal_stream_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 // S_i and the mixed state R = P_i + m_ii S_i, as row pairs (packed fp32x2 FMAs update two rows
 // at once), so a warp needs nothing from any other warp: each slab warp also keeps the whole z
 // (rows lane + 32 j) and its own denominator.  The step's rows come through a per-warp cp.async
-// ring; phi of token n + 1 is taken while token n is computed (within a block).
+// ring; phi of token n + 1 is taken while token n is computed (within a block).  At call start
+// the frozen part of the mixed state of every block starting inside the call is premixed into that
+// block's slot, so each frozen slot is read once per call.
 template <int D> struct WarpGeom {
   static constexpr int LA = D < 32 ? D : 32;   // lanes holding a column
   static constexpr int SL = D / LA;            // slab warps per unit
@@ -205,6 +209,7 @@ causal_stream_warp_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
   constexpr int NI = (NCH + 31) / 32;
   constexpr int STAGE = 2 * D + LA;
   static_assert(QC >= 1 && VCH >= 1 && D % 4 == 0, "whole 16-byte chunks");
+  static_assert(D % kMixRows == 0, "premix row chunks");
 
   __shared__ __align__(16) T ring[WARPS][kPipe][STAGE];
   __shared__ __align__(16) float phq[WARPS][2][D];
@@ -277,28 +282,96 @@ causal_stream_warp_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
   cp_async_wait<kPipe - 2>();  // token 0
   __syncwarp();
 
+  // ---- the frozen part of the mixed state of every block that starts inside the call,
+  // sum_{b<F} m_ib S_b over the F slots frozen before it, into that block's own slot (free until
+  // the block ends): each frozen slot is read once per call instead of once per block start.
+  // A lane reads and writes only its own column, so no other lane is involved.
+  const int F = t0 / block;
+  const int first_fresh = t0 % block == 0 ? F : F + 1;
+  const int last_blk = (t0 + T_steps - 1) / block;
+  const bool premix = F > 0 && first_fresh <= last_blk;
+  if (premix) {
+    for (int i0 = first_fresh; i0 <= last_blk; i0 += kMixGroup) {
+      const int ni = min(kMixGroup, last_blk + 1 - i0);
+      const float* wrow = mh + (size_t)i0 * M;
+      for (int r0 = 0; r0 < D; r0 += kMixRows) {
+        float acc[kMixGroup][kMixRows];
+#pragma unroll
+        for (int ii = 0; ii < kMixGroup; ++ii)
+#pragma unroll
+          for (int rr = 0; rr < kMixRows; ++rr) acc[ii][rr] = 0.f;
+#pragma unroll 2
+        for (int b = 0; b < F; ++b) {
+          const float* sb = Su + ((size_t)b * D + r0) * D + ec;
+          float val[kMixRows];
+#pragma unroll
+          for (int rr = 0; rr < kMixRows; ++rr) val[rr] = __ldcg(sb + (size_t)rr * D);
+#pragma unroll
+          for (int ii = 0; ii < kMixGroup; ++ii) {
+            const float w = ii < ni ? __ldg(wrow + (size_t)ii * M + b) : 0.f;
+#pragma unroll
+            for (int rr = 0; rr < kMixRows; ++rr) acc[ii][rr] = fmaf(w, val[rr], acc[ii][rr]);
+          }
+        }
+        if (owns) {
+#pragma unroll
+          for (int ii = 0; ii < kMixGroup; ++ii)
+            if (ii < ni) {
+#pragma unroll
+              for (int rr = 0; rr < kMixRows; ++rr) Su[((size_t)(i0 + ii) * D + r0 + rr) * D + e] = acc[ii][rr];
+            }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < RZ; ++j) {
+        const int c = lane + 32 * j;
+        if (c < D) {
+          float az[kMixGroup];
+#pragma unroll
+          for (int ii = 0; ii < kMixGroup; ++ii) az[ii] = 0.f;
+          for (int b = 0; b < F; ++b) {
+            const float zb = __ldcg(zu + (size_t)b * D + c);
+#pragma unroll
+            for (int ii = 0; ii < kMixGroup; ++ii)
+              az[ii] = fmaf(ii < ni ? __ldg(wrow + (size_t)ii * M + b) : 0.f, zb, az[ii]);
+          }
+          // every slab warp writes the same values (each reads back only what it wrote)
+#pragma unroll
+          for (int ii = 0; ii < kMixGroup; ++ii)
+            if (ii < ni) zu[(size_t)(i0 + ii) * D + c] = az[ii];
+        }
+      }
+    }
+  }
+
   bool have = false;  // token n's prep done (in the previous iteration)
   float vv = 0.f, den = 1.f;
   for (int n = 0; n < T_steps; ++n) {
     const int t = t0 + n, bi = t / block;
     if (bi != cur) {
       // block bi starts (or the call starts inside it): S_i from its slot (zero at its first
-      // token), R = sum_{b<i} m_ib S_b + m_ii S_i from the frozen slots, z likewise
+      // token), R = sum_{b<i} m_ib S_b + m_ii S_i, z likewise.  A block that starts inside the
+      // call finds the frozen part of its sum in its slot when the call premixed it, and adds
+      // the blocks finished during the call; otherwise every earlier slot is mixed here.
       const bool fresh = t % block == 0;
+      const bool pre = fresh && premix;
       mii = __ldg(mh + (size_t)bi * M + bi);
 #pragma unroll
       for (int pp = 0; pp < D / 2; ++pp) {
-        sp[pp] = fresh ? make_float2(0.f, 0.f)
-                       : make_float2(Su[((size_t)bi * D + 2 * pp) * D + ec], Su[((size_t)bi * D + 2 * pp + 1) * D + ec]);
-        rp[pp] = make_float2(mii * sp[pp].x, mii * sp[pp].y);
+        const float2 slot = (fresh && !pre) ? make_float2(0.f, 0.f)
+                                            : make_float2(Su[((size_t)bi * D + 2 * pp) * D + ec],
+                                                          Su[((size_t)bi * D + 2 * pp + 1) * D + ec]);
+        sp[pp] = fresh ? make_float2(0.f, 0.f) : slot;
+        rp[pp] = pre ? slot : make_float2(mii * slot.x, mii * slot.y);
       }
 #pragma unroll
       for (int j = 0; j < RZ; ++j) {
         const int c = lane + 32 * j;
-        zc[j] = (fresh || c >= D) ? 0.f : zu[(size_t)bi * D + c];
-        zr[j] = mii * zc[j];
+        const float zs = ((fresh && !pre) || c >= D) ? 0.f : zu[(size_t)bi * D + c];
+        zc[j] = fresh ? 0.f : zs;
+        zr[j] = pre ? zs : mii * zs;
       }
-      for (int b = 0; b < bi; ++b) {
+      for (int b = pre ? F : 0; b < bi; ++b) {
         const float w = __ldg(mh + (size_t)bi * M + b);
         const float* sb = Su + (size_t)b * D * D + ec;
 #pragma unroll
@@ -325,7 +398,8 @@ causal_stream_warp_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
 
     const float* pq = phq[wid][n & 1];
     const float* pk = phk[wid][n & 1];
-    const float2 v2 = make_float2(v0, v0), m2 = make_float2(mii, mii);
+    const float mv = mii * v0;
+    const float2 v2 = make_float2(v0, v0), mv2 = make_float2(mv, mv);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c4 = 0; c4 < D; c4 += 4) {
@@ -334,8 +408,8 @@ causal_stream_warp_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
       const float2 ka = make_float2(k4.x, k4.y), kb = make_float2(k4.z, k4.w);
       sp[c4 / 2] = __ffma2_rn(ka, v2, sp[c4 / 2]);
       sp[c4 / 2 + 1] = __ffma2_rn(kb, v2, sp[c4 / 2 + 1]);
-      rp[c4 / 2] = __ffma2_rn(__fmul2_rn(ka, m2), v2, rp[c4 / 2]);
-      rp[c4 / 2 + 1] = __ffma2_rn(__fmul2_rn(kb, m2), v2, rp[c4 / 2 + 1]);
+      rp[c4 / 2] = __ffma2_rn(ka, mv2, rp[c4 / 2]);
+      rp[c4 / 2 + 1] = __ffma2_rn(kb, mv2, rp[c4 / 2 + 1]);
       acc0 = __ffma2_rn(make_float2(q4.x, q4.y), rp[c4 / 2], acc0);
       acc1 = __ffma2_rn(make_float2(q4.z, q4.w), rp[c4 / 2 + 1], acc1);
     }
