@@ -54,4 +54,6 @@ from .mhla_oracle import (  # noqa: F401
     rala_forward,
     rala_bruteforce,
     numerical_rank,
+    phi_grad,
+    mhla_block_form_backward,
 )

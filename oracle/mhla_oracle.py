@@ -63,6 +63,11 @@ PIN_STATUS = {
     "rala_forward": "brute form; closed forms at Q=0 and K=0; softmax weights sum to 1",
     "rala_bruteforce": "closed forms at Q=0 and K=0; hand-derived golden fixture",
     "numerical_rank": "diagonal matrices of known rank",
+    "phi_grad": "closed-form values at 0, +1, -1; central differences of phi",
+    "mhla_block_form_backward": "central differences of mhla_block_form for every entry of q, k, v and the "
+                                "mixing; Euler identities: <dV, V> = <dY, Y> (Y linear in V), and with "
+                                "eps = 0 <dM, M> = 0 and <dphi(q_t), phi(q_t)> = 0 per token, "
+                                "sum_j <dphi(k_j), phi(k_j)> = 0 per slice (Y of degree 0 in each)",
 }
 
 
@@ -618,6 +623,67 @@ def causal_mhla_stream(q, k, v, mixing, block_size, eps=1e-6):
             frozen_s[:, :, i] = s_cur
             frozen_z[:, :, i] = z_cur
     return y, den
+
+
+def phi_grad(x):
+    """Derivative of phi = ELU + 1: 1 for x > 0, exp(x) for x <= 0.
+
+    Both one-sided derivatives at 0 equal 1, so phi is continuously
+    differentiable (Linear Attention notes §二 feature map, ELU with alpha = 1).
+    """
+    x = _f64(x)
+    return np.where(x > 0.0, 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def mhla_block_form_backward(q, k, v, mixing, block_size, dy, eps=1e-6):
+    """Gradients of the scalar sum(dy * Y), Y = mhla_block_form(q, k, v, mixing, block_size, eps)[0].
+    Returns ``(dq, dk, dv, dmixing)``; ``dmixing`` is [H, M, M] and sums over the batch, since the
+    mixing of head h is shared by every sample.
+
+    MHLA paper §4.2 learns the mixing coefficients end to end but gives no backward formulas;
+    these are the chain rule through the forward steps of §4.1, taken in reverse order
+    (block i holds the query token t, block b the key token j):
+      Y_t = num_t / den_t           -> dnum_t = dY_t / den_t,   dden_t = -(dY_t . Y_t) / den_t
+      num_t = phi(q_t)^T S~_i       -> dS~_i = sum_t phi(q_t) dnum_t^T,   dphi(q_t) = S~_i dnum_t
+      den_t = phi(q_t) . z~_i + eps -> dz~_i = sum_t phi(q_t) dden_t,     dphi(q_t) += dden_t z~_i
+      S~_i = sum_b m_ib S_b (z too) -> dS_b = sum_i m_ib dS~_i,  dz_b = sum_i m_ib dz~_i,
+                                       dm_ib = <dS~_i, S_b> + dz~_i . z_b   (summed over samples)
+      S_b = sum_j phi(k_j) v_j^T    -> dphi(k_j) = dS_b v_j + dz_b,   dv_j = dS_b^T phi(k_j)
+      z_b = sum_j phi(k_j)
+      dq = phi'(q) dphi(q),  dk = phi'(k) dphi(k).
+    """
+    q, k, v, dy = _f64(q), _f64(k), _f64(v), _f64(dy)
+    bsz, nh, n, d = q.shape
+    m, mix = _check_blocks(n, block_size, mixing)
+    # the forward's intermediate values (block summaries, mixed summaries, num, den)
+    kf = phi(k).reshape(bsz, nh, m, block_size, d)
+    vb = v.reshape(bsz, nh, m, block_size, d)
+    s = np.einsum("bhmjc,bhmje->bhmce", kf, vb)
+    z = kf.sum(axis=3)
+    s_mix = np.einsum("hib,zhbce->zhice", mix, s)
+    z_mix = np.einsum("hib,zhbc->zhic", mix, z)
+    qf = phi(q).reshape(bsz, nh, m, block_size, d)
+    num = np.einsum("bhitc,bhice->bhite", qf, s_mix)
+    den = np.einsum("bhitc,bhic->bhit", qf, z_mix) + eps
+    y = num / den[..., None]
+    # Y = num / den
+    g = dy.reshape(bsz, nh, m, block_size, d)
+    dnum = g / den[..., None]
+    dden = -np.einsum("bhite,bhite->bhit", g, y) / den
+    # num and den
+    ds_mix = np.einsum("bhitc,bhite->bhice", qf, dnum)
+    dz_mix = np.einsum("bhitc,bhit->bhic", qf, dden)
+    dqf = np.einsum("bhice,bhite->bhitc", s_mix, dnum) + dden[..., None] * z_mix[:, :, :, None, :]
+    # mixing
+    ds = np.einsum("hib,zhice->zhbce", mix, ds_mix)
+    dz = np.einsum("hib,zhic->zhbc", mix, dz_mix)
+    dmix = np.einsum("zhice,zhbce->hib", ds_mix, s) + np.einsum("zhic,zhbc->hib", dz_mix, z)
+    # block summaries
+    dkf = np.einsum("bhmce,bhmje->bhmjc", ds, vb) + dz[:, :, :, None, :]
+    dv = np.einsum("bhmce,bhmjc->bhmje", ds, kf)
+    dq = phi_grad(q) * dqf.reshape(bsz, nh, n, d)
+    dk = phi_grad(k) * dkf.reshape(bsz, nh, n, d)
+    return dq, dk, dv.reshape(bsz, nh, n, d), dmix
 
 
 def numerical_rank(a, rtol=None):

@@ -163,3 +163,45 @@ def test_undecayed_normaliser_in_the_variant_recurrence_is_caught(monkeypatch):
         return y, den
     monkeypatch.setattr(oracle, "causal_variant_recurrent", z_undecayed)
     _fails(pins.test_causal_variant_recurrence_equals_bruteforce, _causal_small(), "elu1", 0.9)
+
+
+# ------------------------------------------------------------ backward
+bwd_small = pins.bwd_small  # the pins' fixture
+
+
+def _mutated_backward(old, new):
+    """The oracle's backward with one expression replaced (the text must occur exactly once)."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(om.mhla_block_form_backward))
+    assert src.count(old) == 1, old
+    ns = dict(vars(om))
+    exec(compile(src.replace(old, new), "<mutated backward>", "exec"), ns)
+    return ns["mhla_block_form_backward"]
+
+
+BACKWARD_MUTATIONS = {
+    # the denominator's path dropped from dphi(q)
+    "no_dden_in_dq": ("+ dden[..., None] * z_mix[:, :, :, None, :]", ""),
+    # dden without its minus sign
+    "dden_sign": ("dden = -np.einsum", "dden = np.einsum"),
+    # the mixing not transposed on the way back (m_bi instead of m_ib)
+    "untransposed_mixing": ('np.einsum("hib,zhice->zhbce", mix, ds_mix)', 'np.einsum("hbi,zhice->zhbce", mix, ds_mix)'),
+    # dV from dS instead of dS^T
+    "dv_untransposed": ('np.einsum("bhmce,bhmjc->bhmje", ds, kf)', 'np.einsum("bhmec,bhmjc->bhmje", ds, kf)'),
+    # z's gradient left out of dphi(k)
+    "no_dz_in_dk": ("+ dz[:, :, :, None, :]", ""),
+    # dM of the first sample only instead of the sum over the batch
+    "dm_one_sample": ('np.einsum("zhice,zhbce->hib", ds_mix, s)', 'np.einsum("hice,hbce->hib", ds_mix[0], s[0])'),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BACKWARD_MUTATIONS))
+def test_backward_mutation_is_caught(monkeypatch, bwd_small, name):
+    monkeypatch.setattr(oracle, "mhla_block_form_backward", _mutated_backward(*BACKWARD_MUTATIONS[name]))
+    _fails(pins.test_backward_equals_central_differences, bwd_small, 1e-6)
+
+
+def test_backward_with_phi_prime_one_is_caught(monkeypatch, bwd_small):
+    monkeypatch.setattr(om, "phi_grad", lambda x: np.ones_like(np.asarray(x, dtype=np.float64)))
+    _fails(pins.test_backward_equals_central_differences, bwd_small, 1e-6)

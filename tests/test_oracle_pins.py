@@ -499,3 +499,63 @@ def test_causal_variants_reduce_to_the_pinned_forms(causal_small):
     y, d = oracle.causal_variant_recurrent(q, k, v, "elu1", 0.0)
     a = np.einsum("bhtc,bhtc->bht", oracle.phi(q), oracle.phi(k))
     assert close(y, a[..., None] * v / (a + 1e-6)[..., None], 1e-12)
+
+
+# ---------------------------------------------------------------- backward (dQ, dK, dV, dM)
+def test_phi_grad_closed_forms_and_differences():
+    assert close(oracle.phi_grad([0.0, 1.0, -1.0, 3.5]), [1.0, 1.0, math.exp(-1.0), 1.0], 1e-15)
+    x = np.linspace(-3.0, 3.0, 61) + 0.013  # away from the kink at 0
+    h = 1e-6
+    fd = (oracle.phi(x + h) - oracle.phi(x - h)) / (2 * h)
+    assert close(oracle.phi_grad(x), fd, 1e-8)
+
+
+@pytest.fixture
+def bwd_small():
+    """B2 H2 N6 d3, blocks of 2 (M = 3): inputs, a positive mixing (den stays away from 0) and dY."""
+    shape = (2, 2, 6, 3)
+    q, k, v, dy = (normal(700 + i, 1, shape, 0.8) for i in range(4))
+    mix = uniform(704, 2, (2, 3, 3)) + 0.1
+    return q, k, v, mix, dy
+
+
+def _loss(q, k, v, mix, dy, eps):
+    return float(np.sum(dy * oracle.mhla_block_form(q, k, v, mix, 2, eps)[0]))
+
+
+@pytest.mark.parametrize("eps", [1e-6, 0.3])
+def test_backward_equals_central_differences(bwd_small, eps):
+    """Every entry of dq, dk, dv and dmixing against (L(x + h) - L(x - h)) / 2h of the forward."""
+    q, k, v, mix, dy = bwd_small
+    grads = oracle.mhla_block_form_backward(q, k, v, mix, 2, dy, eps)
+    h = 1e-6
+    for which, (x, g) in enumerate(zip((q, k, v, mix), grads)):
+        assert g.shape == x.shape
+        fd = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            args = [q, k, v, mix]
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args[which] = xp
+            lp = _loss(*args, dy, eps)
+            args[which] = xm
+            fd[idx] = (lp - _loss(*args, dy, eps)) / (2 * h)
+        assert close(g, fd, 1e-7), ("q", "k", "v", "mixing")[which]
+
+
+def test_backward_euler_identities(bwd_small):
+    """Y is linear in V: <dV, V> = <dY, Y> for any eps.  With eps = 0, Y is of degree 0 in the
+    mixing, in phi(q_t) of each token and in phi(K) of each (b, h) slice, so the matching inner
+    products vanish (phi(x) = x + 1 and phi' = 1 on positive inputs)."""
+    q, k, v, mix, dy = bwd_small
+    y = oracle.mhla_block_form(q, k, v, mix, 2, 0.25)[0]
+    dv = oracle.mhla_block_form_backward(q, k, v, mix, 2, dy, 0.25)[2]
+    assert close(np.sum(dv * v), np.sum(dy * y), 1e-12)
+    qp, kp = np.abs(q) + 0.1, np.abs(k) + 0.1
+    dq, dk, _, dm = oracle.mhla_block_form_backward(qp, kp, v, mix, 2, dy, 0.0)
+    assert abs(np.sum(dm * mix)) < 1e-12 * np.sum(np.abs(dm * mix))
+    per_token = np.einsum("bhtc,bhtc->bht", dq, qp + 1.0)
+    assert np.max(np.abs(per_token)) < 1e-12 * np.max(np.abs(dq))
+    per_slice = np.einsum("bhtc,bhtc->bh", dk, kp + 1.0)
+    assert np.max(np.abs(per_slice)) < 1e-12 * np.sum(np.abs(dk))
