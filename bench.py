@@ -81,6 +81,8 @@ def workload_bytes(wl):
     if wl.kind == "rala":
         cx = wl.extra["cx"]
         return 4 * t + wl.B * wl.N * cx * eb + cx * wl.d * eb
+    if wl.kind == "backward":  # Q, K, V, dY read once, dQ, dK, dV written once; the mixing in, dM out
+        return 7 * t + 2 * wl.H * wl.M * wl.M * 4
     raise ValueError(wl.kind)
 
 
@@ -92,12 +94,19 @@ def workload_flops(wl):
     """fp32 operations of one call (an FMA counts 2).
     Fused decode, per unit and step: the state update and the output read 2 d^2 FMAs, the
     denominator d FMAs, z d adds.
+    MHLA backward: see the per-head-token count below.
     Causal MHLA inference, per unit and token: S_i += phi(k) v^T, R += m_ii phi(k) v^T and the
     output phi(q) R are 3 d^2 FMAs, z_i d adds, the mixed z and the denominator 2 d FMAs; per block
     that starts in the call, sum_{b<i} m_ib (S_b, z_b) is i (d^2 + d) FMAs."""
     d = wl.d
     if wl.kind == "decode_steps":
         return wl.B * wl.H * wl.N * (4 * d * d + 3 * d)
+    if wl.kind == "backward":
+        # per head-token: S_b, num, dphi(q), dS~, dphi(k), dv are 6 d^2 FMAs; z, den, dden, dnum,
+        # dden z~, dz~, dq, dz, dk another 4 d FMAs and 5 d adds / multiplies; per unit the mixing,
+        # its transpose and dM are 3 M^2 (d^2 + d) FMAs
+        M = wl.M
+        return wl.B * wl.H * (wl.N * (12 * d * d + 13 * d) + 6 * M * M * (d * d + d))
     assert wl.kind == "stream"
     P, blk = wl.extra["prefix"], wl.block
     starts = range(-(-P // blk), (P + wl.N - 1) // blk + 1)  # blocks starting inside the call
@@ -168,6 +177,7 @@ KERNEL_SOURCES = {
     "causal_mhla_tcgen05": ["tc_causal.cu", "tc_mhla.cu"],
     "rala_tcgen05": ["tc_rala.cu"],
     "decode_steps_simt": ["decode_steps.cu"],
+    "backward_simt": ["mhla_backward.cu"],
 }
 SHARED_SOURCES = ["tc_common.cuh", "common.cuh"]
 
@@ -288,6 +298,16 @@ class Runner:
                 s = {k: (v if r == 0 else v.clone()) for k, v in base.items()}
                 s["y"] = torch.empty_like(s["q"])
                 self.sets.append(s)
+        elif wl.kind == "backward":
+            base = workloads.mhla_device(wl, device)
+            self.ws = binding.new_workspace(binding.mhla_backward_workspace_bytes(wl.B, wl.H, wl.N, wl.d, wl.block),
+                                            device)
+            for r in range(self.R):
+                s = {k: (v if r == 0 else v.clone()) for k, v in base.items()}
+                for g in ("dq", "dk", "dv"):
+                    s[g] = torch.empty_like(s["q"])
+                s["dm"] = torch.empty_like(s["mixing"])
+                self.sets.append(s)
         elif wl.kind == "rala":
             base = workloads.rala_device(wl, device)
             cx = wl.extra["cx"]
@@ -351,6 +371,9 @@ class Runner:
             b.mhla_forward_causal(s["q"], s["k"], s["v"], s.get("mixing"), s["y"], wl.block, workspace=self.ws)
         elif wl.kind == "rala":
             b.rala_forward(s["q"], s["k"], s["v"], s["x"], s["w"], s["y"], workspace=self.ws)
+        elif wl.kind == "backward":
+            b.mhla_backward(s["q"], s["k"], s["v"], s["mixing"], s["dy"], s["dq"], s["dk"], s["dv"], s["dm"],
+                            wl.block, workspace=self.ws)
         elif wl.kind == "decode":
             st = s["steps"]
             t = i % st["step_q"].shape[0]
@@ -494,7 +517,7 @@ def kernel_path(binding, wl):
         return binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
     if wl.kind == "decode":
         return "simt"
-    if wl.kind in ("decode_steps", "stream"):
+    if wl.kind in ("decode_steps", "stream", "backward"):
         return "simt"
     if "grid" in wl.extra:
         return binding.mhla_forward_grid_path(wl.B, wl.H, *wl.extra["grid"], wl.d, tdt)
@@ -599,6 +622,8 @@ def parity_of_timed_output(runner, n_slices=4):
         return parity_of_decode_steps(runner)
     elif wl.kind == "stream":
         return parity_of_stream(runner)
+    elif wl.kind == "backward":
+        return parity_of_backward(runner)
     elif wl.kind == "rala":
         batches = [0, wl.B - 1][:n_slices]
         host = workloads.rala_host(wl, batches)
@@ -674,8 +699,28 @@ def parity_of_stream(runner):
             "sample": f"2 of {U} units, all {T} tokens of the timed call (graph replay)"}
 
 
+def parity_of_backward(runner):
+    """All eight samples of head 0 of the timed backward (dQ, dK, dV and the head's dM) against the
+    oracle's backward."""
+    import numpy as np
+    import oracle
+    import workloads
+    wl, s = runner.wl, runner.sets[0]
+    host = workloads.mhla_host(wl, heads=[(b, 0) for b in range(wl.B)])
+    shp = (wl.B, 1, wl.N, wl.d)
+    ref = oracle.mhla_block_form_backward(host["q64"].reshape(shp), host["k64"].reshape(shp), host["v64"].reshape(shp),
+                                          host["mixing64"][:1], wl.block, host["dy64"].reshape(shp))
+    got = [s[g][:, :1].float().cpu().numpy().astype(np.float64) for g in ("dq", "dk", "dv")]
+    got.append(s["dm"][:1].cpu().numpy().astype(np.float64))
+    errs = [float(np.max(np.abs(g - r)) / np.max(np.abs(r))) for g, r in zip(got, ref)]
+    tol = 2e-2 if wl.dtype == "bf16" else 1e-4
+    return {"max_rel_err": {"dq": errs[0], "dk": errs[1], "dv": errs[2], "dmixing": errs[3]}, "tol": tol,
+            "ok": bool(max(errs) <= tol),
+            "sample": f"head 0 of {wl.H}, all {wl.B} samples, of the timed call (graph replay)"}
+
+
 def alu_roofline(torch, wl, device, launch_ms):
-    """The roofline of the token-sequential recurrences (fused decode, causal MHLA inference):
+    """The roofline of the fp32 SIMT paths (fused decode, causal MHLA inference, the backward):
     fp32 FMA issue, which binds them (their minimal HBM time is well below their minimal FMA
     time), against the FP32 peak at the maximum SM clock (152 SMs x 128 lanes x 2 x 2070 MHz)."""
     sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -708,7 +753,7 @@ def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
         out["unit"] = "unit-steps/s"
         out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
         out["parity"] = parity_of_timed_output(runner)
-    elif wl.kind == "stream":
+    elif wl.kind in ("stream", "backward"):
         out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
         out["parity"] = parity_of_timed_output(runner)
     else:
@@ -743,7 +788,7 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # end to end through host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and wl.kind != "backward":  # the end-to-end form covers the forward workloads
         runner.e2e_setup()
         k_e2e = max(3, min(args.steps, 50))
         runner.e2e_run(2)
@@ -796,7 +841,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "clocks": sampler.summary(t_wall0, t_wall1),
         "parity": parity,
     }
-    if wl.kind in ("decode_steps", "stream"):  # bound by fp32 FMA issue, not by HBM
+    if wl.kind in ("decode_steps", "stream", "backward"):  # bound by fp32 FMA issue, not by HBM
         line["roofline"] = dict(alu_roofline(torch, wl, device, kernel_ms), kernel=kernel_name,
                                 traffic=line["roofline"]["traffic"], kernels_per_step=per_step_kernels,
                                 launch_ms=kernel_ms, effective_GBps=achieved)
@@ -808,7 +853,7 @@ def run_ours(args, wl, rank, world, local_rank):
         torch.cuda.empty_cache()
         extra = {}
         for name in ("dit_grid", "dit_unnormalised", "dit_relu", "hires", "hires_m1", "causal", "causal_mhla", "causal_decay",
-                     "rala", "decode", "decode_fused", "stream"):
+                     "rala", "decode", "decode_fused", "stream", "dit_backward"):
             if name == wl.name:
                 continue
             try:

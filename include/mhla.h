@@ -245,6 +245,37 @@ mhla_status mhla_causal_stream(const void* q, const void* k, const void* v, cons
                                float* z, void* out, float* den_out, int t0, int T, int B, int H, int d,
                                int block, int M, mhla_dtype dt, float eps, void* stream);
 
+/* Workspace bytes for mhla_backward; 0 if the sizes are invalid or unsupported
+ * (N / block_size above 64). */
+size_t mhla_backward_workspace_bytes(int B, int H, int N, int d, int block_size);
+
+/* Backward of the non-causal MHLA forward (mhla_forward with causal = 0:
+ * contiguous blocks, phi = ELU + 1, with the normaliser) for training the
+ * mixing end to end ([MHLA] §4.2; the pages give no backward formulas, these
+ * are the chain rule through the steps of [MHLA] §4.1):
+ *   dnum_t = dY_t / den_t,  dden_t = -(dY_t . Y_t) / den_t
+ *   dS~_i = sum_{t in i} phi(q_t) dnum_t^T,  dz~_i = sum_{t in i} phi(q_t) dden_t
+ *   dq_t = phi'(q_t) * (S~_i dnum_t + dden_t z~_i)
+ *   dS_b = sum_i m_ib dS~_i,  dz_b = sum_i m_ib dz~_i
+ *   dm[h][i][b] = sum over the samples of <dS~_i, S_b> + dz~_i . z_b
+ *   dk_j = phi'(k_j) * (dS_b v_j + dz_b),  dv_j = dS_b^T phi(k_j)
+ * with phi'(x) = 1 for x > 0 and exp(x) otherwise.  S, z, S~, z~, Y and den
+ * are recomputed from q, k, v and the mixing (the forward saves nothing).
+ *   q, k, v, dy     : [B, H, N, d] (dtype dt), as given to the forward; dy = dL/dY
+ *   mixing          : [H, M, M] fp32, M = N / block_size <= 64
+ *   dq, dk, dv      : [B, H, N, d] (dtype dt), written (not accumulated)
+ *   dmixing         : [H, M, M] fp32, written (not accumulated); sums over the B samples
+ *   workspace       : >= mhla_backward_workspace_bytes(...) device bytes,
+ *                     256-byte aligned, contents ignored; must not overlap any argument
+ * All arithmetic is fp32 (bf16 values are widened at the loads, gradients
+ * rounded at the stores).  Outputs must not overlap the inputs or each other
+ * (MHLA_ERR_INVALID_ARG).  M above 64 returns MHLA_ERR_UNSUPPORTED.
+ * B*H*N = 0 returns MHLA_OK without a launch.  Deterministic: every sum has a
+ * fixed order. */
+mhla_status mhla_backward(const void* q, const void* k, const void* v, const float* mixing, const void* dy,
+                          void* dq, void* dk, void* dv, float* dmixing, int B, int H, int N, int d, int block_size,
+                          mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes for rala_forward; 0 if the sizes are invalid. */
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx);
 

@@ -180,6 +180,31 @@ def test_causal_stream_argument_errors(lib):
                                   1e-6, None) == OK        # no units
 
 
+def test_backward_argument_errors(lib):
+    def bw(q=P, mix=4 * P, dy=5 * P, dq=6 * P, dk=7 * P, dv=8 * P, dm=9 * P, B=1, H=1, N=256, d=64, block=64,
+           dt=BF16, eps=1e-6, ws=16 * P, wsb=1 << 30):
+        return lib.mhla_backward(q, 2 * P, 3 * P, mix, dy, dq, dk, dv, dm, B, H, N, d, block, dt, eps, ws, wsb, None)
+    assert binding.mhla_backward_workspace_bytes(1, 1, 256, 64, 64) > 0
+    assert binding.mhla_backward_workspace_bytes(1, 1, 4096, 64, 32) == 0   # M = 128 blocks
+    assert binding.mhla_backward_workspace_bytes(1, 1, 256, 48, 64) == 0    # d not supported
+    assert bw(d=48) == INVALID
+    assert bw(block=0) == INVALID
+    assert bw(N=250) == INVALID                           # block does not divide N
+    assert bw(N=4096, block=32) == UNSUPPORTED            # M = 128 > 64
+    assert bw(mix=None) == INVALID
+    assert bw(dq=P) == INVALID                            # dq aliases q
+    assert bw(dk=6 * P) == INVALID                        # dk aliases dq
+    assert bw(dm=4 * P + 16) == INVALID                   # dmixing inside the mixing
+    assert bw(ws=None) == INVALID
+    assert bw(ws=16 * P + 16) == INVALID                  # not 256-byte aligned
+    assert bw(wsb=1024) == INVALID                        # too small
+    assert bw(ws=6 * P) == INVALID                        # workspace over dq
+    assert bw(eps=-1.0) == INVALID
+    assert bw(dt=7) == INVALID
+    assert bw(B=0, q=None, dq=None) == OK                 # nothing to do, no launch
+    assert bw(N=0) == OK
+
+
 def test_options_argument_errors(lib):
     import ctypes
     def ex(feature=0, normalise=1, gamma=1.0, causal=0, mix=4 * P, B=2):

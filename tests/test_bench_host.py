@@ -42,6 +42,10 @@ def test_algorithmic_bytes_of_the_workloads():
     assert bench.tokens_per_step(st) == 4096 * 1024
     assert bench.workload_bytes(st) == 4096 * (1024 * (4 * 64 * 2 + 4) + 16 * slot + 8 * slot)
     assert bench.workload_flops(st) == 4096 * (1024 * (6 * 64 * 64 + 5 * 64) + 156 * 2 * (64 * 64 + 64))
+    # backward on the DiT inputs: Q, K, V, dY in, dQ, dK, dV out (bf16), the mixing in and dM out (fp32)
+    bw = W["dit_backward"]
+    assert bench.workload_bytes(bw) == 196_608 * 64 * 2 * 7 + 2 * 6 * 16 * 16 * 4
+    assert bench.workload_flops(bw) == 48 * (4096 * (12 * 64 * 64 + 13 * 64) + 6 * 16 * 16 * (64 * 64 + 64))
 
 
 def test_traffic_record_needs_matching_sources(monkeypatch):

@@ -24,6 +24,8 @@ from .binding import (  # noqa: F401
     mhla_launch_count,
     mhla_query_status,
     mhla_workspace_bytes,
+    mhla_backward,
+    mhla_backward_workspace_bytes,
     new_workspace,
     rala_forward,
     rala_workspace_bytes,

@@ -45,6 +45,8 @@ _SIGNATURES = {
     "mhla_launch_count": (ctypes.c_ulonglong, []),
     "mhla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "mhla_debug_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
+    "mhla_backward_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "mhla_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
 }
 
 EXPORTED = tuple(_SIGNATURES)
@@ -138,6 +140,10 @@ def _mhla_args(q, k, v, mixing, y, den_out, block, mixing_required=True):
 
 def mhla_workspace_bytes(B: int, H: int, N: int, d: int, block_size: int, causal: int = 0) -> int:
     return int(load().mhla_workspace_bytes(B, H, N, d, block_size, causal))
+
+
+def mhla_backward_workspace_bytes(B: int, H: int, N: int, d: int, block_size: int) -> int:
+    return int(load().mhla_backward_workspace_bytes(B, H, N, d, block_size))
 
 
 def rala_workspace_bytes(B: int, H: int, N: int, d: int, cx: int) -> int:
@@ -294,6 +300,24 @@ def mhla_forward_causal(q, k, v, mixing, y, chunk, *, eps=1e-6, den_out=None, wo
                                         workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward_causal", st)
     return y
+
+
+def mhla_backward(q, k, v, mixing, dy, dq, dk, dv, dmixing, block_size, *, eps=1e-6, workspace=None, stream=None):
+    """Gradients of the non-causal MHLA forward: dq, dk, dv [B, H, N, d] (q's dtype) and dmixing
+    [H, M, M] fp32 from dy = dL/dY; all four are written."""
+    B, H, N, d = _mhla_args(q, k, v, mixing, dy, None, block_size)
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _expect(t, name, q.shape, q.dtype)
+    _expect(dmixing, "dmixing", mixing.shape, torch.float32)
+    dev = _same_device(q, k, v, mixing, dy, dq, dk, dv, dmixing, workspace)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            workspace = new_workspace(mhla_backward_workspace_bytes(B, H, N, d, block_size), dev)
+        st = load().mhla_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(mixing), _ptr(dy), _ptr(dq), _ptr(dk), _ptr(dv),
+                                  _ptr(dmixing), B, H, N, d, block_size, _dtype(q), eps, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream, dev))
+    _check("mhla_backward", st)
+    return dq, dk, dv, dmixing
 
 
 def linattn_decode_step(q, k, v, S, z, out, *, eps=1e-6, den_out=None, stream=None):

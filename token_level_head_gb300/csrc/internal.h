@@ -100,6 +100,12 @@ cudaError_t decode_steps_launch(int T_steps, int units, int d, mhla_dtype dt, co
 cudaError_t causal_stream_launch(int t0, int T_steps, int units, int H, int d, int block, int M, mhla_dtype dt,
                                  const void* q, const void* k, const void* v, const float* mixing, float* S,
                                  float* z, void* out, float* den_out, float eps, cudaStream_t st);
+// ---- backward of the non-causal block form (SIMT, any dtype, d in {16, 32, 64, 128}, M <= 64)
+size_t mhla_backward_workspace(int B, int H, int N, int d, int block);
+int mhla_backward_max_blocks();
+cudaError_t mhla_backward_launch(int B, int H, int N, int d, int block, mhla_dtype dt, const void* q, const void* k,
+                                 const void* v, const float* mixing, const void* dy, void* dq, void* dk, void* dv,
+                                 float* dm, float eps, void* ws, cudaStream_t st);
 size_t simt_rala_workspace(int B, int H, int N, int d, int cx);
 cudaError_t simt_rala_launch(int B, int H, int N, int d, int cx, mhla_dtype dt, const void* q,
                              const void* k, const void* v, const void* x, const void* w, void* y,

@@ -314,6 +314,48 @@ mhla_status mhla_causal_stream(const void* q, const void* k, const void* v, cons
                                         eps, static_cast<cudaStream_t>(stream)));
 }
 
+size_t mhla_backward_workspace_bytes(int B, int H, int N, int d, int block_size) {
+  if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0)) return 0;
+  if (N > 0 && N / block_size > mhla_backward_max_blocks()) return 0;
+  return mhla_backward_workspace(B, H, N, d, block_size);
+}
+
+mhla_status mhla_backward(const void* q, const void* k, const void* v, const float* mixing, const void* dy,
+                          void* dq, void* dk, void* dv, float* dmixing, int B, int H, int N, int d, int block_size,
+                          mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, H, N) || !valid_d(d)) return MHLA_ERR_INVALID_ARG;
+  if (dt != MHLA_F32 && dt != MHLA_BF16) return MHLA_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return MHLA_ERR_INVALID_ARG;
+  if (block_size <= 0 || (N > 0 && N % block_size != 0)) return MHLA_ERR_INVALID_ARG;
+  if ((size_t)B * H * N == 0) return MHLA_OK;
+  const int M = N / block_size;
+  if (M > mhla_backward_max_blocks()) return MHLA_ERR_UNSUPPORTED;
+  if ((size_t)B * H * M > 0x7fffffffu) return MHLA_ERR_UNSUPPORTED;
+  const void* bufs[] = {q, k, v, mixing, dy, dq, dk, dv, dmixing};
+  for (const void* b : bufs)
+    if (!b || !aligned16(b)) return MHLA_ERR_INVALID_ARG;
+  const size_t tb = elems(B, H, N, d) * dtype_bytes(dt), mb = (size_t)H * M * M * sizeof(float);
+  const void* ins[] = {q, k, v, dy, mixing};
+  const size_t inb[] = {tb, tb, tb, tb, mb};
+  void* outs[] = {dq, dk, dv, dmixing};
+  const size_t outb[] = {tb, tb, tb, mb};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 5; ++i)
+      if (overlap(outs[o], outb[o], ins[i], inb[i])) return MHLA_ERR_INVALID_ARG;
+    for (int j = o + 1; j < 4; ++j)
+      if (overlap(outs[o], outb[o], outs[j], outb[j])) return MHLA_ERR_INVALID_ARG;
+  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHLA_ERR_INVALID_ARG;
+  const size_t need = mhla_backward_workspace(B, H, N, d, block_size);
+  if (workspace_bytes < need) return MHLA_ERR_INVALID_ARG;
+  for (int o = 0; o < 4; ++o)
+    if (overlap(outs[o], outb[o], workspace, need)) return MHLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i)
+    if (overlap(ins[i], inb[i], workspace, need)) return MHLA_ERR_INVALID_ARG;
+  return from_cuda(mhla_backward_launch(B, H, N, d, block_size, dt, q, k, v, mixing, dy, dq, dk, dv, dmixing, eps,
+                                        workspace, static_cast<cudaStream_t>(stream)));
+}
+
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx) {
   if (!dims_ok(B, H, N) || !valid_d(d) || cx <= 0 || cx % 16 != 0 || cx > 256) return 0;
   const size_t a = simt_rala_workspace(B, H, N, d, cx);

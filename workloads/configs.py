@@ -26,7 +26,7 @@ from .gen import (SEED_BASE, TID, bf16_bits, bf16_bits_to_f64, lower_row_normali
 class Workload:
     name: str
     index: int              # seed = SEED_BASE + index
-    kind: str               # "mhla" | "causal" | "decode" | "decode_steps" | "stream" | "rala"
+    kind: str               # "mhla" | "causal" | "decode" | "decode_steps" | "stream" | "rala" | "backward"
     B: int
     H: int
     N: int                  # tokens (decode: number of steps)
@@ -65,6 +65,8 @@ WORKLOADS = {
                                  "softmax_diag2", extra={"normalise": False}),
     "dit_relu": Workload("dit_relu", 2, "mhla", 8, 6, 4096, 64, 256, "bf16", 0.125, "softmax_diag2",
                          extra={"feature": "relu"}),
+    # the backward of the DiT forward (dQ, dK, dV, dM) on the same inputs, dY ~ N(0, 1)
+    "dit_backward": Workload("dit_backward", 2, "backward", 8, 6, 4096, 64, 256, "bf16", 0.125, "softmax_diag2"),
     # 256x256 token grid, M = 64 blocks of 1024, and the same inputs with M = 1
     "hires": Workload("hires", 3, "mhla", 1, 6, 65536, 64, 1024, "bf16", 0.125, "softmax"),
     "hires_m1": Workload("hires_m1", 3, "mhla", 1, 6, 65536, 64, 65536, "bf16", 0.125, "ones"),
@@ -135,11 +137,12 @@ def mhla_host(wl: Workload, heads=None) -> dict:
     """
     out = {}
     per = wl.N * wl.d
-    for name in ("q", "k", "v"):
+    for name in ("q", "k", "v") + (("dy",) if wl.kind == "backward" else ()):
+        scale = 1.0 if name == "dy" else wl.scale
         if heads is None:
-            x = normal(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), wl.scale)
+            x = normal(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), scale)
         else:
-            x = np.stack([normal(wl.seed, TID[name], (wl.N, wl.d), wl.scale, offset=(b * wl.H + h) * per)
+            x = np.stack([normal(wl.seed, TID[name], (wl.N, wl.d), scale, offset=(b * wl.H + h) * per)
                           for b, h in heads])[None]
         out[name], out[name + "64"] = _as_dtype(x, wl.dtype)
     if wl.mixing != "none":
@@ -155,8 +158,10 @@ def mhla_device(wl: Workload, device="cuda") -> dict:
     """The full MHLA / causal workload as device tensors (same values as :func:`mhla_host`)."""
     import torch
     dt = _torch_dtype(wl.dtype)
-    out = {name: normal_device(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), wl.scale, device=device, dtype=dt)
-           for name in ("q", "k", "v")}
+    names = ("q", "k", "v") + (("dy",) if wl.kind == "backward" else ())
+    out = {name: normal_device(wl.seed, TID[name], (wl.B, wl.H, wl.N, wl.d), 1.0 if name == "dy" else wl.scale,
+                               device=device, dtype=dt)
+           for name in names}
     if wl.mixing != "none":
         out["mixing"] = torch.from_numpy(make_mixing(wl).astype(np.float32)).to(device)
     return out

@@ -27,6 +27,7 @@ TID = {
     "q": 1, "k": 2, "v": 3, "mix": 4, "x": 5, "w": 6,
     "prefix_k": 7, "prefix_v": 8,
     "step_q": 100, "step_k": 101, "step_v": 102,
+    "dy": 9,
 }
 
 GOLDEN_INT = 0x9E3779B97F4A7C15
