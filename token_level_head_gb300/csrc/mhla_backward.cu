@@ -42,8 +42,8 @@ namespace {
 
 constexpr int kBT = 256;     // threads of every backward kernel
 constexpr int kMaxMixM = 64; // blocks per sequence the mixing kernels stage
-constexpr int kMixCols = 32; // slot entries per mixing CTA
-constexpr int kDmK = 32;     // slot entries per stage of the dM kernel
+constexpr int kDmK = 64;     // slot entries per stage of the dM kernel
+constexpr int kDmRange = 128; // slot entries of one sample per dM CTA (many short CTAs hide the load latency)
 
 template <int D>
 struct BwdGeom {
@@ -56,9 +56,44 @@ struct BwdGeom {
   static constexpr int LT = TC + 4;              // row of a feature-major tile
   static constexpr int TPT = kBT / TC;           // threads per token in the denominator sums
   static constexpr int X = D * D + D;            // floats of a slot
+  static constexpr int NL = TC * D / 4 / kBT;    // quads of a chunk staged per thread
   static_assert(TG * NQ == kBT && TT >= 1 && (TT & (TT - 1)) == 0, "chunk product layout");
   static_assert(16 * R == D, "reduction layout");
+  static_assert(NL >= 1 && TC % 16 == 0, "chunk staging layout");
 };
+
+// CTAs per SM each token pass is compiled for (its register budget): d = 128 tiles and fp32
+// prefetch registers need more per thread; the query pass's 105 KB tiles allow two CTAs anyway.
+template <typename T, int D>
+struct BwdOcc {
+  static constexpr int SUMMARY = D == 128 ? (sizeof(T) == 4 ? 1 : 2) : (sizeof(T) == 4 ? 3 : 4);
+  static constexpr int QUERY = D == 128 ? 1 : 2;
+  static constexpr int KEY = D == 128 ? 1 : (sizeof(T) == 4 ? 2 : 3);
+};
+
+// Four consecutive elements as stored (8 bytes of bf16, 16 bytes of fp32), and their fp32 values.
+template <typename T> struct Quad;
+template <> struct Quad<float> { float4 v; };
+template <> struct Quad<__nv_bfloat16> { uint2 v; };
+
+__device__ __forceinline__ Quad<float> ldq(const float* p) { return {*reinterpret_cast<const float4*>(p)}; }
+__device__ __forceinline__ Quad<__nv_bfloat16> ldq(const __nv_bfloat16* p) {
+  return {*reinterpret_cast<const uint2*>(p)};
+}
+__device__ __forceinline__ float4 to_f4(const Quad<float>& q) { return q.v; }
+__device__ __forceinline__ float4 to_f4(const Quad<__nv_bfloat16>& q) {
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.v.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void stq(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+__device__ __forceinline__ void stq(__nv_bfloat16* p, float4 x) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
 
 // n consecutive floats of shared memory (n = 1, 2, 4 or 8; 8 as two float4)
 template <int N>
@@ -77,23 +112,56 @@ __device__ __forceinline__ void lds(float (&r)[N], const float* p) {
   }
 }
 
-// Stage a chunk of TC tokens (rows t0 .. t0 + TC - 1 of a [L][D] block, `valid` of them real) into
-// shared memory: token-major tok[t][c] and / or feature-major fea[c][t], through f (phi or identity);
-// rows past `valid` are zero.
-template <typename T, int D, typename F>
-__device__ __forceinline__ void stage_chunk(const T* __restrict__ src, int valid, float* tok, float* fea, F f) {
-  using G = BwdGeom<D>;
-  for (int e = threadIdx.x; e < G::TC * D; e += kBT) {
-    const int t = e / D, c = e - t * D;
-    const float raw = to_f(src[(size_t)min(t, valid - 1) * D + c]);  // rows past the block: not read
-    const float x = t < valid ? f(raw) : 0.f;
-    if (tok) tok[t * G::LD + c] = x;
-    if (fea) fea[c * G::LT + t] = x;
-  }
-}
-
 struct PhiOp { __device__ float operator()(float x) const { return phi(x); } };
 struct IdOp { __device__ float operator()(float x) const { return x; } };
+
+// A chunk of TC tokens of a [L][D] block held in registers between its global loads and its
+// shared-memory stores, so that the next chunk's loads are in flight while this one is computed.
+// Quad j of a thread: a warp covers 8 tokens x 4 column quads (full 32-byte sectors per token of
+// bf16, two-way bank conflicts at most in the feature-major stores).
+template <typename T, int D>
+struct ChunkRegs {
+  using G = BwdGeom<D>;
+  Quad<T> q[G::NL];
+
+  __device__ __forceinline__ static void where(int j, int& t, int& c) {
+    const int qi = threadIdx.x + kBT * j, lane = qi % 32, w = qi / 32;
+    constexpr int TB = G::TC / 8;
+    t = (w % TB) * 8 + lane % 8;
+    c = ((w / TB) * 4 + lane / 8) * 4;
+  }
+  // rows at and past `valid` are not read (their addresses are clamped to the last real row)
+  __device__ __forceinline__ void load(const T* __restrict__ src, int valid) {
+#pragma unroll
+    for (int j = 0; j < G::NL; ++j) {
+      int t, c;
+      where(j, t, c);
+      q[j] = ldq(src + (size_t)min(t, valid - 1) * D + c);
+    }
+  }
+  // token-major tok[t][c] and / or feature-major fea[c][t], through f; rows past `valid` are zero
+  template <typename F>
+  __device__ __forceinline__ void store(int valid, float* tok, float* fea, F f) const {
+#pragma unroll
+    for (int j = 0; j < G::NL; ++j) {
+      int t, c;
+      where(j, t, c);
+      float4 x = to_f4(q[j]);
+      if (t < valid) {
+        x = make_float4(f(x.x), f(x.y), f(x.z), f(x.w));
+      } else {
+        x = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (tok) *reinterpret_cast<float4*>(tok + t * G::LD + c) = x;
+      if (fea) {
+        fea[(c + 0) * G::LT + t] = x.x;
+        fea[(c + 1) * G::LT + t] = x.y;
+        fea[(c + 2) * G::LT + t] = x.z;
+        fea[(c + 3) * G::LT + t] = x.w;
+      }
+    }
+  }
+};
 
 // out[t][n] (+)= sum_{k < D} X[k][t] W[k][n]: this thread's TT tokens x 4 columns
 template <int D>
@@ -132,10 +200,32 @@ __device__ __forceinline__ void reduce_tokens(float (&acc)[BwdGeom<D>::R][BwdGeo
   }
 }
 
+// acc[c] += sum over this thread's tokens t = re, re + 16, ... of A[t][c0 + c] w(t); the sixteen
+// threads sharing c0 (lanes 16 r .. 16 r + 15 of a warp) together cover the chunk
+template <int D, typename W>
+__device__ __forceinline__ void reduce_rows(float (&acc)[BwdGeom<D>::R], const float* A, int c0, int re, W w) {
+  using G = BwdGeom<D>;
+#pragma unroll
+  for (int t = re; t < G::TC; t += 16) {
+    float a[G::R];
+    lds<G::R>(a, A + t * G::LD + c0);
+    const float wt = w(t);
+#pragma unroll
+    for (int i = 0; i < G::R; ++i) acc[i] = fmaf(a[i], wt, acc[i]);
+  }
+}
+template <int R>
+__device__ __forceinline__ void sum16(float (&acc)[R]) {
+#pragma unroll
+  for (int i = 0; i < R; ++i)
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+}
+
 // ------------------------------------------------------------------ S_b, z_b
 template <typename T, int D>
-__global__ void __launch_bounds__(kBT) bwd_summary_kernel(const T* __restrict__ k, const T* __restrict__ v,
-                                                          float* __restrict__ slots, int N, int L, int M) {
+__global__ void __launch_bounds__(kBT, BwdOcc<T, D>::SUMMARY) bwd_summary_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                             float* __restrict__ slots, int N, int L, int M) {
   using G = BwdGeom<D>;
   extern __shared__ __align__(16) float sm[];
   float* Kt = sm;                 // [TC][LD] phi(K)
@@ -145,22 +235,24 @@ __global__ void __launch_bounds__(kBT) bwd_summary_kernel(const T* __restrict__ 
   const int rc = threadIdx.x / 16, re = threadIdx.x % 16, c0 = rc * G::R, e0 = re * G::R;
   float acc[G::R][G::R] = {};
   float zacc[G::R] = {};
+  ChunkRegs<T, D> rk, rv;
+  rk.load(k + base, min(G::TC, L));
+  rv.load(v + base, min(G::TC, L));
   for (int t0 = 0; t0 < L; t0 += G::TC) {
     const int valid = min(G::TC, L - t0);
+    __syncthreads();  // the previous chunk is no longer read
+    rk.store(valid, Kt, nullptr, PhiOp{});
+    rv.store(valid, Vt, nullptr, IdOp{});
     __syncthreads();
-    stage_chunk<T, D>(k + base + (size_t)t0 * D, valid, Kt, nullptr, PhiOp{});
-    stage_chunk<T, D>(v + base + (size_t)t0 * D, valid, Vt, nullptr, IdOp{});
-    __syncthreads();
-    reduce_tokens<D>(acc, Kt, Vt, c0, e0);
-    if (re == 0) {
-      for (int t = 0; t < G::TC; ++t) {
-        float a[G::R];
-        lds<G::R>(a, Kt + t * G::LD + c0);
-#pragma unroll
-        for (int i = 0; i < G::R; ++i) zacc[i] += a[i];
-      }
+    if (t0 + G::TC < L) {  // the next chunk's loads fly while this one is summed
+      const int nv = min(G::TC, L - t0 - G::TC);
+      rk.load(k + base + (size_t)(t0 + G::TC) * D, nv);
+      rv.load(v + base + (size_t)(t0 + G::TC) * D, nv);
     }
+    reduce_tokens<D>(acc, Kt, Vt, c0, e0);
+    reduce_rows<D>(zacc, Kt, c0, re, [](int) { return 1.f; });
   }
+  sum16<G::R>(zacc);
   float* slot = slots + ((size_t)u * M + b) * G::X;
 #pragma unroll
   for (int i = 0; i < G::R; ++i)
@@ -172,38 +264,50 @@ __global__ void __launch_bounds__(kBT) bwd_summary_kernel(const T* __restrict__ 
 }
 
 // ------------------------------------------------- out_i = sum_b w_ib in_b over the slots
-// w_ib = m[h][i][b] (transpose = 0) or m[h][b][i] (transpose = 1); a CTA takes kMixCols entries
-// of every slot of one unit.
+// w_ib = m[h][i][b] (transpose = 0) or m[h][b][i] (transpose = 1); a thread takes one entry x of
+// every slot of one unit (a CTA kBT consecutive entries) and all M outputs, 16 at a time.
 __global__ void __launch_bounds__(kBT) bwd_mix_kernel(const float* __restrict__ in, const float* __restrict__ mixing,
                                                       float* __restrict__ out, int H, int M, int X, int transpose) {
   __shared__ float sw[kMaxMixM * kMaxMixM];
-  __shared__ float sin_[kMaxMixM][kMixCols];
-  const int cols = (X + kMixCols - 1) / kMixCols;
-  const int u = blockIdx.x / cols, x0 = (blockIdx.x % cols) * kMixCols;
+  const int cols = (X + kBT - 1) / kBT;
+  const int u = blockIdx.x / cols, x = (blockIdx.x % cols) * kBT + threadIdx.x;
   const float* mh = mixing + (size_t)(u % H) * M * M;
   for (int e = threadIdx.x; e < M * M; e += kBT) {
     const int i = e / M, b = e % M;
     sw[i * M + b] = transpose ? mh[(size_t)b * M + i] : mh[(size_t)i * M + b];
   }
-  const int lane = threadIdx.x % 32, g = threadIdx.x / 32;
-  const int x = x0 + lane;
-  const float* ib = in + (size_t)u * M * X;
-  for (int b = g; b < M; b += kBT / 32) sin_[b][lane] = x < X ? ib[(size_t)b * X + x] : 0.f;
   __syncthreads();
   if (x >= X) return;
-  float* ob = out + (size_t)u * M * X;
-  for (int i = g; i < M; i += kBT / 32) {
-    float acc = 0.f;
-    for (int b = 0; b < M; ++b) acc = fmaf(sw[i * M + b], sin_[b][lane], acc);
-    ob[(size_t)i * X + x] = acc;
+  const float* ib = in + (size_t)u * M * X + x;
+  float* ob = out + (size_t)u * M * X + x;
+  for (int i0 = 0; i0 < M; i0 += 16) {
+    float acc[16];
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii) acc[ii] = 0.f;
+    for (int b0 = 0; b0 < M; b0 += 8) {  // eight independent loads in flight, then their FMAs
+      float val[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) val[j] = b0 + j < M ? ib[(size_t)min(b0 + j, M - 1) * X] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) {
+          const float w = (i0 + ii < M && b0 + j < M) ? sw[(i0 + ii) * M + b0 + j] : 0.f;
+          acc[ii] = fmaf(w, val[j], acc[ii]);
+        }
+    }
+#pragma unroll
+    for (int ii = 0; ii < 16; ++ii)
+      if (i0 + ii < M) ob[(size_t)(i0 + ii) * X] = acc[ii];
   }
 }
 
 // ------------------------------------------------------------------ query pass
 template <typename T, int D>
-__global__ void __launch_bounds__(kBT) bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ dy,
-                                                        const float* __restrict__ mixed, float* __restrict__ dmixed,
-                                                        T* __restrict__ dq, int N, int L, int M, float eps) {
+__global__ void __launch_bounds__(kBT, BwdOcc<T, D>::QUERY) bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ dy,
+                                                           const float* __restrict__ mixed,
+                                                           float* __restrict__ dmixed, T* __restrict__ dq, int N,
+                                                           int L, int M, float eps) {
   using G = BwdGeom<D>;
   extern __shared__ __align__(16) float sm[];
   float* St = sm;                    // [D][LD]  S~_i (row c, column e)
@@ -217,6 +321,21 @@ __global__ void __launch_bounds__(kBT) bwd_query_kernel(const T* __restrict__ q,
   float* dd = den + G::TC;           // [TC]     dden
   const int u = blockIdx.x / M, i = blockIdx.x % M;
   const size_t base = ((size_t)u * N + (size_t)i * L) * D;
+  const int tg = threadIdx.x / G::NQ, nq = threadIdx.x % G::NQ;  // chunk products
+  const int tp0 = tg * G::TT, n0 = nq * 4;
+  const int rc = threadIdx.x / 16, re = threadIdx.x % 16, c0 = rc * G::R, e0 = re * G::R;  // dS~
+
+  // first chunk's loads, then S~_i, z~_i into shared memory while they fly
+  ChunkRegs<T, D> rq;
+  Quad<T> ry[G::TT];  // this thread's dY quads of the chunk
+  auto load_chunk = [&](int t0) {
+    const int valid = min(G::TC, L - t0);
+    rq.load(q + base + (size_t)t0 * D, valid);
+#pragma unroll
+    for (int a = 0; a < G::TT; ++a)
+      ry[a] = ldq(dy + base + (size_t)(t0 + min(tp0 + a, valid - 1)) * D + n0);
+  };
+  load_chunk(0);
   const float* slot = mixed + ((size_t)u * M + i) * G::X;
   for (int e = threadIdx.x; e < D * D; e += kBT) {
     const int c = e / D, n = e % D;
@@ -226,16 +345,21 @@ __global__ void __launch_bounds__(kBT) bwd_query_kernel(const T* __restrict__ q,
   }
   for (int c = threadIdx.x; c < D; c += kBT) zt[c] = slot[D * D + c];
 
-  const int tg = threadIdx.x / G::NQ, nq = threadIdx.x % G::NQ;  // chunk products
-  const int tp0 = tg * G::TT, n0 = nq * 4;
-  const int rc = threadIdx.x / 16, re = threadIdx.x % 16, c0 = rc * G::R, e0 = re * G::R;  // dS~
   float ds[G::R][G::R] = {};
   float dz[G::R] = {};
   for (int t0 = 0; t0 < L; t0 += G::TC) {
     const int valid = min(G::TC, L - t0);
     __syncthreads();  // the previous chunk's tiles are no longer read
-    stage_chunk<T, D>(q + base + (size_t)t0 * D, valid, Qk, Qf, PhiOp{});
+    rq.store(valid, Qk, Qf, PhiOp{});
+    float g[G::TT][4];
+#pragma unroll
+    for (int a = 0; a < G::TT; ++a) {
+      const float4 x = to_f4(ry[a]);
+      const bool ok = tp0 + a < valid;
+      g[a][0] = ok ? x.x : 0.f; g[a][1] = ok ? x.y : 0.f; g[a][2] = ok ? x.z : 0.f; g[a][3] = ok ? x.w : 0.f;
+    }
     __syncthreads();
+    if (t0 + G::TC < L) load_chunk(t0 + G::TC);  // in flight during this chunk
     {  // den[t] = phi(q_t) . z~ + eps, G::TPT threads a token
       const int t = threadIdx.x / G::TPT, part = threadIdx.x % G::TPT;
       float s = 0.f;
@@ -248,19 +372,12 @@ __global__ void __launch_bounds__(kBT) bwd_query_kernel(const T* __restrict__ q,
     chunk_product<D>(num, Qf, St, tp0, n0);
     __syncthreads();  // den
     // dnum = dY / den, dden = -(dY . num) / den^2 (dY . Y = dY . num / den)
-    float g[G::TT][4];
     float part[G::TT];
 #pragma unroll
     for (int a = 0; a < G::TT; ++a) {
-      const int t = tp0 + a;
-      const bool ok = t < valid;
-      const T* row = dy + base + (size_t)(t0 + (ok ? t : 0)) * D + n0;  // rows past the block: not read
       part[a] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        g[a][j] = ok ? to_f(row[j]) : 0.f;
-        part[a] = fmaf(g[a][j], num[a][j], part[a]);
-      }
+      for (int j = 0; j < 4; ++j) part[a] = fmaf(g[a][j], num[a][j], part[a]);
     }
 #pragma unroll
     for (int a = 0; a < G::TT; ++a) {
@@ -269,41 +386,34 @@ __global__ void __launch_bounds__(kBT) bwd_query_kernel(const T* __restrict__ q,
       const int t = tp0 + a;
       const float inv = t < valid ? 1.f / den[t] : 0.f;  // rows past the block: no contribution
       if (nq == 0) dd[t] = -part[a] * inv * inv;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float dn = g[a][j] * inv;
-        Nk[t * G::LD + n0 + j] = dn;
-        Nf[(n0 + j) * G::LT + t] = dn;
-      }
+      const float4 dn = make_float4(g[a][0] * inv, g[a][1] * inv, g[a][2] * inv, g[a][3] * inv);
+      *reinterpret_cast<float4*>(Nk + t * G::LD + n0) = dn;
+      Nf[(n0 + 0) * G::LT + t] = dn.x;
+      Nf[(n0 + 1) * G::LT + t] = dn.y;
+      Nf[(n0 + 2) * G::LT + t] = dn.z;
+      Nf[(n0 + 3) * G::LT + t] = dn.w;
     }
     __syncthreads();
-    // dphi(q) = S~ dnum + dden z~ (as dnum^T S~^T); dq = phi'(q) dphi(q)
+    // dphi(q) = S~ dnum + dden z~ (as dnum^T S~^T); dq = phi'(q) dphi(q), phi' = min(1, phi)
     float dqf[G::TT][4] = {};
     chunk_product<D>(dqf, Nf, Stt, tp0, n0);
+    const float4 z4 = *reinterpret_cast<const float4*>(zt + n0);
 #pragma unroll
     for (int a = 0; a < G::TT; ++a) {
       const int t = tp0 + a;
       if (t < valid) {
-        T* row = dq + base + (size_t)(t0 + t) * D + n0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float gq = fmaf(dd[t], zt[n0 + j], dqf[a][j]);
-          row[j] = from_f<T>(fminf(1.f, Qk[t * G::LD + n0 + j]) * gq);
-        }
+        const float4 qf = *reinterpret_cast<const float4*>(Qk + t * G::LD + n0);
+        const float w = dd[t];
+        stq(dq + base + (size_t)(t0 + t) * D + n0,
+            make_float4(fminf(1.f, qf.x) * fmaf(w, z4.x, dqf[a][0]), fminf(1.f, qf.y) * fmaf(w, z4.y, dqf[a][1]),
+                        fminf(1.f, qf.z) * fmaf(w, z4.z, dqf[a][2]), fminf(1.f, qf.w) * fmaf(w, z4.w, dqf[a][3])));
       }
     }
     // dS~ += phi(Q)^T dnum, dz~ += phi(Q)^T dden
     reduce_tokens<D>(ds, Qk, Nk, c0, e0);
-    if (re == 0) {
-      for (int t = 0; t < G::TC; ++t) {
-        float a[G::R];
-        lds<G::R>(a, Qk + t * G::LD + c0);
-        const float w = dd[t];
-#pragma unroll
-        for (int r = 0; r < G::R; ++r) dz[r] = fmaf(a[r], w, dz[r]);
-      }
-    }
+    reduce_rows<D>(dz, Qk, c0, re, [&](int t) { return dd[t]; });
   }
+  sum16<G::R>(dz);
   float* out = dmixed + ((size_t)u * M + i) * G::X;
 #pragma unroll
   for (int a = 0; a < G::R; ++a)
@@ -315,70 +425,78 @@ __global__ void __launch_bounds__(kBT) bwd_query_kernel(const T* __restrict__ q,
 }
 
 // ------------------------------------------------------------------ dM partials
-// part[h][p][i][b] = sum over entries x of range p of the head's slots (sample-major) of
-// dS~[u][i][x] * S[u][b][x]; a thread owns a 4 x 4 tile of (i, b) in [0, 64)^2.
+// part[h][smp][p][i][b] = sum over the entries x of range p of sample smp's slots of head h of
+// dS~[u][i][x] * S[u][b][x]; a thread owns outputs (i, b) = (ti + 16 r, tb + 16 c), r, c < RI,
+// RI = ceil(M / 16).
+template <int RI>
 __global__ void __launch_bounds__(kBT) bwd_dm_kernel(const float* __restrict__ dmixed, const float* __restrict__ slots,
-                                                     float* __restrict__ part, int B, int H, int M, int X, int P,
-                                                     long long per) {
-  __shared__ __align__(16) float sa[kDmK][kMaxMixM + 4];  // padded rows: fewer bank conflicts in the staging
-  __shared__ __align__(16) float sb[kDmK][kMaxMixM + 4];
-  const int h = blockIdx.x / P, p = blockIdx.x % P;
-  const long long total = (long long)B * X;
-  const long long x_begin = (long long)p * per, x_end = min(total, x_begin + per);
+                                                     float* __restrict__ part, int B, int H, int M, int X, int XP) {
+  __shared__ float sa[kDmK][kMaxMixM + 1];  // [entry][block]; odd rows: conflict-free stores and loads
+  __shared__ float sb[kDmK][kMaxMixM + 1];
+  const int p = blockIdx.x % XP, smp = (blockIdx.x / XP) % B, h = blockIdx.x / (XP * B);
+  const size_t u = (size_t)smp * H + h;
+  const int x_begin = p * kDmRange, x_end = min(X, x_begin + kDmRange);
   const int ti = threadIdx.x / 16, tb = threadIdx.x % 16;
-  float acc[4][4] = {};
-  for (long long xs = x_begin; xs < x_end; xs += kDmK) {
+  const float* A = dmixed + u * M * X;
+  const float* S = slots + u * M * X;
+  float acc[RI][RI] = {};
+  for (int xs = x_begin; xs < x_end; xs += kDmK) {
     __syncthreads();
-    for (int e = threadIdx.x; e < kDmK * kMaxMixM; e += kBT) {
-      const int kk = e % kDmK, r = e / kDmK;  // consecutive threads: consecutive entries of one slot
-      const long long xg = xs + kk;
-      float a = 0.f, s = 0.f;
-      if (r < M && xg < x_end) {
-        const long long smp = xg / X, x = xg - smp * X;
-        const size_t u = (size_t)smp * H + h;
-        a = dmixed[(u * M + r) * X + x];
-        s = slots[(u * M + r) * X + x];
-      }
-      sa[kk][r] = a;
-      sb[kk][r] = s;
+#pragma unroll 8
+    for (int e = threadIdx.x; e < kMaxMixM * kDmK; e += kBT) {  // constant trip count: loads in flight
+      const int r = e / kDmK, kk = e % kDmK, x = xs + kk;
+      if (r >= M) break;  // rows grow with e
+      const bool ok = x < x_end;
+      const size_t at = (size_t)r * X + min(x, x_end - 1);  // past the range: not read
+      sa[kk][r] = ok ? A[at] : 0.f;
+      sb[kk][r] = ok ? S[at] : 0.f;
     }
     __syncthreads();
-#pragma unroll 4
+#pragma unroll 8
     for (int kk = 0; kk < kDmK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&sa[kk][ti * 4]);
-      const float4 s = *reinterpret_cast<const float4*>(&sb[kk][tb * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, sv[4] = {s.x, s.y, s.z, s.w};
+      float a[RI], s[RI];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < RI; ++r) {
+        a[r] = sa[kk][ti + 16 * r];  // rows at and past M are never staged: their stale values
+        s[r] = sb[kk][tb + 16 * r];  // reach only outputs (i or b >= M) that are not written
+      }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], sv[c], acc[r][c]);
+      for (int r = 0; r < RI; ++r)
+#pragma unroll
+        for (int c = 0; c < RI; ++c) acc[r][c] = fmaf(a[r], s[c], acc[r][c]);
     }
   }
-  float* out = part + ((size_t)h * P + p) * M * M;
+  float* out = part + (((size_t)h * B + smp) * XP + p) * M * M;
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < RI; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int i = ti * 4 + r, b = tb * 4 + c;
+    for (int c = 0; c < RI; ++c) {
+      const int i = ti + 16 * r, b = tb + 16 * c;
       if (i < M && b < M) out[i * M + b] = acc[r][c];
     }
 }
 
+// dM[h] = the head's B * XP partials summed in a fixed order: a warp per output, lane l taking
+// partials l, l + 32, ..., then a fixed shuffle tree
 __global__ void __launch_bounds__(kBT) bwd_dm_sum_kernel(const float* __restrict__ part, float* __restrict__ dm,
                                                          int H, int M, int P) {
-  const int e = blockIdx.x * kBT + threadIdx.x;
-  if (e >= H * M * M) return;
+  const int e = blockIdx.x * (kBT / 32) + threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (e >= H * M * M) return;  // whole warps leave together
   const int h = e / (M * M), ib = e % (M * M);
+  const float* src = part + (size_t)h * P * M * M + ib;
   float s = 0.f;
-  for (int p = 0; p < P; ++p) s += part[((size_t)h * P + p) * M * M + ib];
-  dm[e] = s;
+#pragma unroll 4
+  for (int p = lane; p < P; p += 32) s += src[(size_t)p * M * M];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) dm[e] = s;
 }
 
 // ------------------------------------------------------------------ key pass
 template <typename T, int D>
-__global__ void __launch_bounds__(kBT) bwd_key_kernel(const T* __restrict__ k, const T* __restrict__ v,
-                                                      const float* __restrict__ dslots, T* __restrict__ dk,
-                                                      T* __restrict__ dv, int N, int L, int M) {
+__global__ void __launch_bounds__(kBT, BwdOcc<T, D>::KEY) bwd_key_kernel(const T* __restrict__ k, const T* __restrict__ v,
+                                                         const float* __restrict__ dslots, T* __restrict__ dk,
+                                                         T* __restrict__ dv, int N, int L, int M) {
   using G = BwdGeom<D>;
   extern __shared__ __align__(16) float sm[];
   float* dS = sm;                 // [D][LD] dS_b (row c, column e)
@@ -388,6 +506,9 @@ __global__ void __launch_bounds__(kBT) bwd_key_kernel(const T* __restrict__ k, c
   float* Vf = Kf + D * G::LT;     // [D][LT] V, feature-major
   const int u = blockIdx.x / M, b = blockIdx.x % M;
   const size_t base = ((size_t)u * N + (size_t)b * L) * D;
+  ChunkRegs<T, D> rk, rv;
+  rk.load(k + base, min(G::TC, L));
+  rv.load(v + base, min(G::TC, L));
   const float* slot = dslots + ((size_t)u * M + b) * G::X;
   for (int e = threadIdx.x; e < D * D; e += kBT) {
     const int c = e / D, n = e % D;
@@ -401,23 +522,28 @@ __global__ void __launch_bounds__(kBT) bwd_key_kernel(const T* __restrict__ k, c
   for (int t0 = 0; t0 < L; t0 += G::TC) {
     const int valid = min(G::TC, L - t0);
     __syncthreads();
-    stage_chunk<T, D>(k + base + (size_t)t0 * D, valid, nullptr, Kf, PhiOp{});
-    stage_chunk<T, D>(v + base + (size_t)t0 * D, valid, nullptr, Vf, IdOp{});
+    rk.store(valid, nullptr, Kf, PhiOp{});
+    rv.store(valid, nullptr, Vf, IdOp{});
     __syncthreads();
+    if (t0 + G::TC < L) {
+      const int nv = min(G::TC, L - t0 - G::TC);
+      rk.load(k + base + (size_t)(t0 + G::TC) * D, nv);
+      rv.load(v + base + (size_t)(t0 + G::TC) * D, nv);
+    }
     float gv[G::TT][4] = {}, gk[G::TT][4] = {};
     chunk_product<D>(gv, Kf, dS, tp0, n0);   // dv_t = dS^T phi(k_t):  sum_c phi(k)[c][t] dS[c][e]
     chunk_product<D>(gk, Vf, dSt, tp0, n0);  // dphi(k_t) = dS v_t:    sum_e v[e][t] dS^T[e][c]
+    const float4 z4 = *reinterpret_cast<const float4*>(dzb + n0);
 #pragma unroll
     for (int a = 0; a < G::TT; ++a) {
       const int t = tp0 + a;
       if (t < valid) {
-        T* rv = dv + base + (size_t)(t0 + t) * D + n0;
-        T* rk = dk + base + (size_t)(t0 + t) * D + n0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          rv[j] = from_f<T>(gv[a][j]);
-          rk[j] = from_f<T>(fminf(1.f, Kf[(n0 + j) * G::LT + t]) * (gk[a][j] + dzb[n0 + j]));
-        }
+        const size_t row = base + (size_t)(t0 + t) * D + n0;
+        stq(dv + row, make_float4(gv[a][0], gv[a][1], gv[a][2], gv[a][3]));
+        stq(dk + row, make_float4(fminf(1.f, Kf[(n0 + 0) * G::LT + t]) * (gk[a][0] + z4.x),
+                                  fminf(1.f, Kf[(n0 + 1) * G::LT + t]) * (gk[a][1] + z4.y),
+                                  fminf(1.f, Kf[(n0 + 2) * G::LT + t]) * (gk[a][2] + z4.z),
+                                  fminf(1.f, Kf[(n0 + 3) * G::LT + t]) * (gk[a][3] + z4.w)));
       }
     }
   }
@@ -425,24 +551,19 @@ __global__ void __launch_bounds__(kBT) bwd_key_kernel(const T* __restrict__ k, c
 
 // ------------------------------------------------------------------ plan and launch
 struct BwdPlan {
-  int M, X, P;
-  long long per;
-  size_t slots, dm_part, total;  // byte offsets / sizes
+  int M, X, XP, P;  // XP: dM ranges per slot, P = B * XP partials per head
+  size_t slots, dm_part, total;  // byte sizes
 };
 
 BwdPlan bwd_plan(int B, int H, int N, int d, int block) {
   BwdPlan p{};
   p.M = N / block;
   p.X = d * d + d;
-  const long long total = (long long)B * p.X;
-  const long long want = std::max<long long>(1, (2 * 152 + H - 1) / std::max(H, 1));  // ~2 CTAs per SM
-  p.P = (int)std::min<long long>(want, (total + kDmK - 1) / kDmK);
-  p.per = ((total + p.P - 1) / p.P + kDmK - 1) / kDmK * kDmK;
-  p.P = (int)((total + p.per - 1) / p.per);
-  const size_t arr = ((size_t)B * H * p.M * p.X * sizeof(float) + 255) & ~size_t(255);
-  p.slots = arr;  // one slot array
+  p.XP = (p.X + kDmRange - 1) / kDmRange;
+  p.P = B * p.XP;
+  p.slots = ((size_t)B * H * p.M * p.X * sizeof(float) + 255) & ~size_t(255);  // one slot array
   p.dm_part = ((size_t)H * p.P * p.M * p.M * sizeof(float) + 255) & ~size_t(255);
-  p.total = 3 * arr + p.dm_part;
+  p.total = 3 * p.slots + p.dm_part;
   return p;
 }
 
@@ -482,14 +603,20 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
   if ((e = opt_q.ensure((const void*)bwd_query_kernel<T, D>, (int)query_smem<D>())) != cudaSuccess) return e;
   if ((e = opt_k.ensure((const void*)bwd_key_kernel<T, D>, (int)key_smem<D>())) != cudaSuccess) return e;
   const unsigned units_blocks = (unsigned)((size_t)U * M);
-  const unsigned mix_grid = (unsigned)((size_t)U * ((X + kMixCols - 1) / kMixCols));
+  const unsigned mix_grid = (unsigned)((size_t)U * ((X + kBT - 1) / kBT));
   bwd_summary_kernel<T, D><<<units_blocks, kBT, summary_smem<D>(), st>>>(tk, tv, slots, N, block, M);
   bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(slots, mixing, mixed, H, M, X, 0);
   bwd_query_kernel<T, D><<<units_blocks, kBT, query_smem<D>(), st>>>(tq, static_cast<const T*>(dy), mixed, dmixed,
                                                                    static_cast<T*>(dq), N, block, M, eps);
   bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(dmixed, mixing, mixed, H, M, X, 1);
-  bwd_dm_kernel<<<(unsigned)(H * p.P), kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.P, p.per);
-  bwd_dm_sum_kernel<<<(unsigned)((H * M * M + kBT - 1) / kBT), kBT, 0, st>>>(dm_part, dm, H, M, p.P);
+  const unsigned dm_grid = (unsigned)((size_t)H * p.P);
+  switch ((M + 15) / 16) {
+    case 1: bwd_dm_kernel<1><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;
+    case 2: bwd_dm_kernel<2><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;
+    case 3: bwd_dm_kernel<3><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;
+    default: bwd_dm_kernel<4><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;
+  }
+  bwd_dm_sum_kernel<<<(unsigned)((H * M * M + kBT / 32 - 1) / (kBT / 32)), kBT, 0, st>>>(dm_part, dm, H, M, p.P);
   bwd_key_kernel<T, D><<<units_blocks, kBT, key_smem<D>(), st>>>(tk, tv, mixed, static_cast<T*>(dk),
                                                                static_cast<T*>(dv), N, block, M);
   note_launch(7);
