@@ -66,7 +66,7 @@ struct BwdGeom {
 // prefetch registers need more per thread; the query pass's 105 KB tiles allow two CTAs anyway.
 template <typename T, int D>
 struct BwdOcc {
-  static constexpr int SUMMARY = D == 128 ? (sizeof(T) == 4 ? 1 : 2) : (sizeof(T) == 4 ? 3 : 4);
+  static constexpr int SUMMARY = D == 128 ? 1 : 3;
   static constexpr int QUERY = D == 128 ? 1 : 2;
   static constexpr int KEY = D == 128 ? 1 : (sizeof(T) == 4 ? 2 : 3);
 };
@@ -163,40 +163,79 @@ struct ChunkRegs {
   }
 };
 
-// out[t][n] (+)= sum_{k < D} X[k][t] W[k][n]: this thread's TT tokens x 4 columns
+// out[t][n] (+)= sum_{k < D} X[k][t] W[k][n]: this thread's TT tokens x 4 columns.  The next k's
+// operands are loaded before this k's FMAs; with two or more tokens the FMAs are packed fp32x2
+// (two tokens against one column value).
 template <int D>
 __device__ __forceinline__ void chunk_product(float (&acc)[BwdGeom<D>::TT][4], const float* Xf, const float* W,
                                               int t0, int n0) {
   using G = BwdGeom<D>;
-#pragma unroll 8
+  float xn[G::TT];
+  lds<G::TT>(xn, Xf + t0);
+  float4 wn = *reinterpret_cast<const float4*>(W + n0);
+#pragma unroll 4
   for (int k = 0; k < D; ++k) {
     float x[G::TT];
-    lds<G::TT>(x, Xf + k * G::LT + t0);
-    const float4 w = *reinterpret_cast<const float4*>(W + k * G::LD + n0);
 #pragma unroll
-    for (int i = 0; i < G::TT; ++i) {
-      acc[i][0] = fmaf(x[i], w.x, acc[i][0]);
-      acc[i][1] = fmaf(x[i], w.y, acc[i][1]);
-      acc[i][2] = fmaf(x[i], w.z, acc[i][2]);
-      acc[i][3] = fmaf(x[i], w.w, acc[i][3]);
+    for (int i = 0; i < G::TT; ++i) x[i] = xn[i];
+    const float4 w = wn;
+    if (k + 1 < D) {
+      lds<G::TT>(xn, Xf + (k + 1) * G::LT + t0);
+      wn = *reinterpret_cast<const float4*>(W + (k + 1) * G::LD + n0);
+    }
+    if constexpr (G::TT >= 2) {
+#pragma unroll
+      for (int i = 0; i < G::TT; i += 2) {
+        const float2 xx = make_float2(x[i], x[i + 1]);
+        float2 a0 = make_float2(acc[i][0], acc[i + 1][0]), a1 = make_float2(acc[i][1], acc[i + 1][1]);
+        float2 a2 = make_float2(acc[i][2], acc[i + 1][2]), a3 = make_float2(acc[i][3], acc[i + 1][3]);
+        a0 = __ffma2_rn(xx, make_float2(w.x, w.x), a0);
+        a1 = __ffma2_rn(xx, make_float2(w.y, w.y), a1);
+        a2 = __ffma2_rn(xx, make_float2(w.z, w.z), a2);
+        a3 = __ffma2_rn(xx, make_float2(w.w, w.w), a3);
+        acc[i][0] = a0.x; acc[i + 1][0] = a0.y; acc[i][1] = a1.x; acc[i + 1][1] = a1.y;
+        acc[i][2] = a2.x; acc[i + 1][2] = a2.y; acc[i][3] = a3.x; acc[i + 1][3] = a3.y;
+      }
+    } else {
+      acc[0][0] = fmaf(x[0], w.x, acc[0][0]);
+      acc[0][1] = fmaf(x[0], w.y, acc[0][1]);
+      acc[0][2] = fmaf(x[0], w.z, acc[0][2]);
+      acc[0][3] = fmaf(x[0], w.w, acc[0][3]);
     }
   }
 }
 
-// acc[c][e] += sum_{t < TC} A[t][c0 + c] B[t][e0 + e]  (token-major tiles)
+// acc[c][e] += sum_{t < TC} A[t][c0 + c] B[t][e0 + e]  (token-major tiles); the next token's
+// operands are loaded before this token's FMAs, packed fp32x2 over pairs of e when R >= 2
 template <int D>
 __device__ __forceinline__ void reduce_tokens(float (&acc)[BwdGeom<D>::R][BwdGeom<D>::R], const float* A,
                                               const float* B, int c0, int e0) {
   using G = BwdGeom<D>;
+  float an[G::R], bn[G::R];
+  lds<G::R>(an, A + c0);
+  lds<G::R>(bn, B + e0);
 #pragma unroll 4
   for (int t = 0; t < G::TC; ++t) {
     float a[G::R], b[G::R];
-    lds<G::R>(a, A + t * G::LD + c0);
-    lds<G::R>(b, B + t * G::LD + e0);
 #pragma unroll
-    for (int i = 0; i < G::R; ++i)
+    for (int i = 0; i < G::R; ++i) { a[i] = an[i]; b[i] = bn[i]; }
+    if (t + 1 < G::TC) {
+      lds<G::R>(an, A + (t + 1) * G::LD + c0);
+      lds<G::R>(bn, B + (t + 1) * G::LD + e0);
+    }
+    if constexpr (G::R >= 2) {
 #pragma unroll
-      for (int j = 0; j < G::R; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      for (int i = 0; i < G::R; ++i)
+#pragma unroll
+        for (int j = 0; j < G::R; j += 2) {
+          float2 c = make_float2(acc[i][j], acc[i][j + 1]);
+          c = __ffma2_rn(make_float2(a[i], a[i]), make_float2(b[j], b[j + 1]), c);
+          acc[i][j] = c.x;
+          acc[i][j + 1] = c.y;
+        }
+    } else {
+      acc[0][0] = fmaf(a[0], b[0], acc[0][0]);
+    }
   }
 }
 
