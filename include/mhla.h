@@ -266,15 +266,28 @@ size_t mhla_backward_workspace_bytes(int B, int H, int N, int d, int block_size)
  *   dq, dk, dv      : [B, H, N, d] (dtype dt), written (not accumulated)
  *   dmixing         : [H, M, M] fp32, written (not accumulated); sums over the B samples
  *   workspace       : >= mhla_backward_workspace_bytes(...) device bytes,
- *                     256-byte aligned, contents ignored; must not overlap any argument
- * All arithmetic is fp32 (bf16 values are widened at the loads, gradients
- * rounded at the stores).  Outputs must not overlap the inputs or each other
+ *                     256-byte aligned; must not overlap any argument
+ *   workspace       : zero-filled before its first use (a status word at its
+ *                     start, as for mhla_forward; the library leaves it zero
+ *                     unless a device wait gave up, which mhla_query_status
+ *                     reports as MHLA_ERR_TIMEOUT and clears)
+ * Paths (mhla_backward_path): bf16 with d = 64 and block_size a multiple of
+ * 128 runs the token passes on the tensor cores (bf16 operands: phi(Q),
+ * phi(K), V, dY, dnum, dden and the bf16-rounded S~ and dS; fp32
+ * accumulation); everything else, and the summaries, mixing and dM, run on
+ * the SIMT cores in fp32 (bf16 values widened at the loads, gradients rounded
+ * at the stores).  Outputs must not overlap the inputs or each other
  * (MHLA_ERR_INVALID_ARG).  M above 64 returns MHLA_ERR_UNSUPPORTED.
  * B*H*N = 0 returns MHLA_OK without a launch.  Deterministic: every sum has a
  * fixed order. */
 mhla_status mhla_backward(const void* q, const void* k, const void* v, const float* mixing, const void* dy,
                           void* dq, void* dk, void* dv, float* dmixing, int B, int H, int N, int d, int block_size,
                           mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Kernel family mhla_backward would use for these arguments (no launch):
+ * MHLA_PATH_TCGEN05 for the tensor-core token passes, MHLA_PATH_SIMT
+ * otherwise, MHLA_PATH_NONE for invalid or unsupported sizes. */
+mhla_path mhla_backward_path(int B, int H, int N, int d, int block_size, mhla_dtype dt);
 
 /* Workspace bytes for rala_forward; 0 if the sizes are invalid. */
 size_t rala_workspace_bytes(int B, int H, int N, int d, int cx);

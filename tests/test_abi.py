@@ -9,6 +9,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from token_level_head_gb300 import binding
 from token_level_head_gb300.build import INCLUDE, build_library
@@ -203,6 +204,11 @@ def test_backward_argument_errors(lib):
     assert bw(dt=7) == INVALID
     assert bw(B=0, q=None, dq=None) == OK                 # nothing to do, no launch
     assert bw(N=0) == OK
+    assert binding.mhla_backward_path(8, 6, 4096, 64, 256, torch.bfloat16) == "tcgen05"
+    assert binding.mhla_backward_path(8, 6, 4096, 64, 256, torch.float32) == "simt"
+    assert binding.mhla_backward_path(8, 6, 4096, 64, 64, torch.bfloat16) == "simt"   # blocks of half a chunk
+    assert binding.mhla_backward_path(8, 6, 4096, 32, 256, torch.bfloat16) == "simt"
+    assert binding.mhla_backward_path(1, 1, 4096, 64, 32, torch.bfloat16) == "none"   # M = 128
 
 
 def test_options_argument_errors(lib):

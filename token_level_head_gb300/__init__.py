@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     mhla_query_status,
     mhla_workspace_bytes,
     mhla_backward,
+    mhla_backward_path,
     mhla_backward_workspace_bytes,
     new_workspace,
     rala_forward,

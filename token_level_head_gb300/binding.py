@@ -46,6 +46,7 @@ _SIGNATURES = {
     "mhla_forward_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "mhla_debug_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
     "mhla_backward_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "mhla_backward_path": (_i, [_i, _i, _i, _i, _i, _i]),
     "mhla_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
 }
 
@@ -300,6 +301,11 @@ def mhla_forward_causal(q, k, v, mixing, y, chunk, *, eps=1e-6, den_out=None, wo
                                         workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check("mhla_forward_causal", st)
     return y
+
+
+def mhla_backward_path(B, H, N, d, block_size, dtype) -> str:
+    dt = MHLA_BF16 if dtype == torch.bfloat16 else MHLA_F32
+    return PATH_NAMES[int(load().mhla_backward_path(B, H, N, d, block_size, dt))]
 
 
 def mhla_backward(q, k, v, mixing, dy, dq, dk, dv, dmixing, block_size, *, eps=1e-6, workspace=None, stream=None):

@@ -106,6 +106,16 @@ int mhla_backward_max_blocks();
 cudaError_t mhla_backward_launch(int B, int H, int N, int d, int block, mhla_dtype dt, const void* q, const void* k,
                                  const void* v, const float* mixing, const void* dy, void* dq, void* dk, void* dv,
                                  float* dm, float eps, void* ws, cudaStream_t st);
+// tensor-core token passes of the backward (bf16, d = 64, blocks of whole 128-token chunks)
+bool tc_backward_supported(int B, int H, int N, int d, int block, mhla_dtype dt);
+cudaError_t tc_backward_query_launch(int units, int N, int block, const void* q, const void* dy,
+                                     const uint8_t* tiles_t, const uint8_t* tiles_n, const float* mu,
+                                     const float* mixed, void* dq, float* dmixed, float eps, unsigned* status,
+                                     cudaStream_t st);
+cudaError_t tc_backward_key_launch(int units, int N, int block, const void* k, const void* v,
+                                   const uint8_t* tiles_t, const uint8_t* tiles_n, const float* dslots, void* dk,
+                                   void* dv, unsigned* status, cudaStream_t st);
+mhla_path mhla_backward_kernel_path(int B, int H, int N, int d, int block, mhla_dtype dt);
 size_t simt_rala_workspace(int B, int H, int N, int d, int cx);
 cudaError_t simt_rala_launch(int B, int H, int N, int d, int cx, mhla_dtype dt, const void* q,
                              const void* k, const void* v, const void* x, const void* w, void* y,

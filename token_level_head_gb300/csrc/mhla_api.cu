@@ -320,6 +320,13 @@ size_t mhla_backward_workspace_bytes(int B, int H, int N, int d, int block_size)
   return mhla_backward_workspace(B, H, N, d, block_size);
 }
 
+mhla_path mhla_backward_path(int B, int H, int N, int d, int block_size, mhla_dtype dt) {
+  if (!dims_ok(B, H, N) || !valid_d(d) || block_size <= 0 || (N > 0 && N % block_size != 0) ||
+      (dt != MHLA_F32 && dt != MHLA_BF16) || (N > 0 && N / block_size > mhla_backward_max_blocks()))
+    return MHLA_PATH_NONE;
+  return mhla_backward_kernel_path(B, H, N, d, block_size, dt);
+}
+
 mhla_status mhla_backward(const void* q, const void* k, const void* v, const float* mixing, const void* dy,
                           void* dq, void* dk, void* dv, float* dmixing, int B, int H, int N, int d, int block_size,
                           mhla_dtype dt, float eps, void* workspace, size_t workspace_bytes, void* stream) {

@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -304,9 +305,15 @@ __global__ void __launch_bounds__(kBT, BwdOcc<T, D>::SUMMARY) bwd_summary_kernel
 
 // ------------------------------------------------- out_i = sum_b w_ib in_b over the slots
 // w_ib = m[h][i][b] (transpose = 0) or m[h][b][i] (transpose = 1); a thread takes one entry x of
-// every slot of one unit (a CTA kBT consecutive entries) and all M outputs, 16 at a time.
+// every slot of one unit (a CTA kBT consecutive entries) and all M outputs, 16 at a time.  With
+// tile outputs (d = 64) each d x d result also goes out in bf16 as two 8 KB 128-byte-swizzled
+// tiles, the tensor-core key pass's B operands: rows e / columns c, and rows c / columns e.
+__device__ __forceinline__ size_t swz64(int row, int col) {  // byte of (row, col) in a [64][64] bf16 tile
+  return (size_t)row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1));
+}
 __global__ void __launch_bounds__(kBT) bwd_mix_kernel(const float* __restrict__ in, const float* __restrict__ mixing,
-                                                      float* __restrict__ out, int H, int M, int X, int transpose) {
+                                                      float* __restrict__ out, int H, int M, int X, int transpose,
+                                                      uint8_t* __restrict__ tiles_t, uint8_t* __restrict__ tiles_n) {
   __shared__ float sw[kMaxMixM * kMaxMixM];
   const int cols = (X + kBT - 1) / kBT;
   const int u = blockIdx.x / cols, x = (blockIdx.x % cols) * kBT + threadIdx.x;
@@ -338,6 +345,51 @@ __global__ void __launch_bounds__(kBT) bwd_mix_kernel(const float* __restrict__ 
 #pragma unroll
     for (int ii = 0; ii < 16; ++ii)
       if (i0 + ii < M) ob[(size_t)(i0 + ii) * X] = acc[ii];
+    if (tiles_t != nullptr && x < 64 * 64) {
+      const int c = x >> 6, e = x & 63;
+#pragma unroll
+      for (int ii = 0; ii < 16; ++ii)
+        if (i0 + ii < M) {
+          const size_t tile = ((size_t)u * M + i0 + ii) * 8192;
+          const __nv_bfloat16 v = __float2bfloat16_rn(acc[ii]);
+          *reinterpret_cast<__nv_bfloat16*>(tiles_t + tile + swz64(e, c)) = v;
+          *reinterpret_cast<__nv_bfloat16*>(tiles_n + tile + swz64(c, e)) = v;
+        }
+    }
+  }
+}
+
+// ------------------------------------------------- S~_i = z~_i mu_i^T + S'_i (d = 64)
+// mu_i = S~_i^T z~_i / |z~_i|^2 (the least-squares rank-one part; zero when z~_i = 0); mu in fp32,
+// S' as the two bf16 tiles of the tensor-core query pass.  phi is near 1, so S~'s rows are near
+// multiples of one vector: S' is small and its bf16 rounding costs little, while the rank-one part
+// stays in fp32.  A CTA per slot.
+__global__ void __launch_bounds__(kBT) bwd_center_kernel(const float* __restrict__ mixed, float* __restrict__ mu,
+                                                         uint8_t* __restrict__ tiles_t, uint8_t* __restrict__ tiles_n) {
+  constexpr int D = 64, X = D * D + D;
+  __shared__ float zz[D], sm_mu[D];
+  const size_t slot = blockIdx.x;
+  const float* sl = mixed + slot * X;
+  if (threadIdx.x < D) zz[threadIdx.x] = sl[D * D + threadIdx.x];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float z2 = 0.f, a = 0.f;
+    for (int c = 0; c < D; ++c) {
+      z2 = fmaf(zz[c], zz[c], z2);
+      a = fmaf(zz[c], sl[c * D + threadIdx.x], a);
+    }
+    const float m = z2 > 0.f ? a / z2 : 0.f;
+    sm_mu[threadIdx.x] = m;
+    mu[slot * D + threadIdx.x] = m;
+  }
+  __syncthreads();
+  uint8_t* tt = tiles_t + slot * 8192;
+  uint8_t* tn = tiles_n + slot * 8192;
+  for (int x = threadIdx.x; x < D * D; x += kBT) {
+    const int c = x >> 6, e = x & 63;
+    const __nv_bfloat16 v = __float2bfloat16_rn(sl[x] - zz[c] * sm_mu[e]);
+    *reinterpret_cast<__nv_bfloat16*>(tt + swz64(e, c)) = v;
+    *reinterpret_cast<__nv_bfloat16*>(tn + swz64(c, e)) = v;
   }
 }
 
@@ -589,20 +641,33 @@ __global__ void __launch_bounds__(kBT, BwdOcc<T, D>::KEY) bwd_key_kernel(const T
 }
 
 // ------------------------------------------------------------------ plan and launch
+// Workspace: a 256-byte header (its status word is set when a tensor-core pass gives up a wait),
+// the three slot arrays, the dM partials and, for shapes the tensor-core passes can take (d = 64,
+// blocks of whole 128-token chunks), two arrays of bf16 d x d tiles and the rank-one parts mu.
 struct BwdPlan {
   int M, X, XP, P;  // XP: dM ranges per slot, P = B * XP partials per head
-  size_t slots, dm_part, total;  // byte sizes
+  size_t slots, dm_part, tiles;  // byte sizes (tiles: one array, 0 without the tensor-core passes)
+  size_t off_slots, off_mixed, off_dmixed, off_dm, off_tt, off_tn, off_mu, total;
 };
 
 BwdPlan bwd_plan(int B, int H, int N, int d, int block) {
+  auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
   BwdPlan p{};
   p.M = N / block;
   p.X = d * d + d;
   p.XP = (p.X + kDmRange - 1) / kDmRange;
   p.P = B * p.XP;
-  p.slots = ((size_t)B * H * p.M * p.X * sizeof(float) + 255) & ~size_t(255);  // one slot array
-  p.dm_part = ((size_t)H * p.P * p.M * p.M * sizeof(float) + 255) & ~size_t(255);
-  p.total = 3 * p.slots + p.dm_part;
+  p.slots = a256((size_t)B * H * p.M * p.X * sizeof(float));
+  p.dm_part = a256((size_t)H * p.P * p.M * p.M * sizeof(float));
+  p.tiles = tc_backward_supported(B, H, N, d, block, MHLA_BF16) ? (size_t)B * H * p.M * 8192 : 0;
+  p.off_slots = sizeof(WorkspaceHeader);
+  p.off_mixed = p.off_slots + p.slots;
+  p.off_dmixed = p.off_mixed + p.slots;
+  p.off_dm = p.off_dmixed + p.slots;
+  p.off_tt = p.off_dm + p.dm_part;
+  p.off_tn = p.off_tt + p.tiles;
+  p.off_mu = p.off_tn + p.tiles;
+  p.total = p.off_mu + (p.tiles ? (size_t)B * H * p.M * 64 * sizeof(float) : 0);
   return p;
 }
 
@@ -630,10 +695,16 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
   const BwdPlan p = bwd_plan(B, H, N, D, block);
   const int U = B * H, M = p.M, X = p.X;
   char* w = static_cast<char*>(ws);
-  float* slots = reinterpret_cast<float*>(w);                 // S_b, z_b
-  float* mixed = reinterpret_cast<float*>(w + p.slots);       // S~, z~; then dS, dz
-  float* dmixed = reinterpret_cast<float*>(w + 2 * p.slots);  // dS~, dz~
-  float* dm_part = reinterpret_cast<float*>(w + 3 * p.slots);
+  float* slots = reinterpret_cast<float*>(w + p.off_slots);    // S_b, z_b
+  float* mixed = reinterpret_cast<float*>(w + p.off_mixed);    // S~, z~; then dS, dz
+  float* dmixed = reinterpret_cast<float*>(w + p.off_dmixed);  // dS~, dz~
+  float* dm_part = reinterpret_cast<float*>(w + p.off_dm);
+  // the tensor-core token passes (bf16, d = 64, blocks of whole 128-token chunks)
+  const bool tc = std::is_same<T, __nv_bfloat16>::value && tc_backward_supported(B, H, N, D, block, MHLA_BF16);
+  uint8_t* tt = tc ? reinterpret_cast<uint8_t*>(w + p.off_tt) : nullptr;
+  uint8_t* tn = tc ? reinterpret_cast<uint8_t*>(w + p.off_tn) : nullptr;
+  float* mu = tc ? reinterpret_cast<float*>(w + p.off_mu) : nullptr;
+  unsigned* status = &reinterpret_cast<WorkspaceHeader*>(w)->status;
   const T* tq = static_cast<const T*>(q);
   const T* tk = static_cast<const T*>(k);
   const T* tv = static_cast<const T*>(v);
@@ -644,10 +715,17 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
   const unsigned units_blocks = (unsigned)((size_t)U * M);
   const unsigned mix_grid = (unsigned)((size_t)U * ((X + kBT - 1) / kBT));
   bwd_summary_kernel<T, D><<<units_blocks, kBT, summary_smem<D>(), st>>>(tk, tv, slots, N, block, M);
-  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(slots, mixing, mixed, H, M, X, 0);
-  bwd_query_kernel<T, D><<<units_blocks, kBT, query_smem<D>(), st>>>(tq, static_cast<const T*>(dy), mixed, dmixed,
-                                                                   static_cast<T*>(dq), N, block, M, eps);
-  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(dmixed, mixing, mixed, H, M, X, 1);
+  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(slots, mixing, mixed, H, M, X, 0, nullptr, nullptr);
+  if (tc) {
+    bwd_center_kernel<<<units_blocks, kBT, 0, st>>>(mixed, mu, tt, tn);
+    if ((e = tc_backward_query_launch(U, N, block, q, dy, tt, tn, mu, mixed, dq, dmixed, eps, status, st)) !=
+        cudaSuccess)
+      return e;
+  } else {
+    bwd_query_kernel<T, D><<<units_blocks, kBT, query_smem<D>(), st>>>(tq, static_cast<const T*>(dy), mixed, dmixed,
+                                                                     static_cast<T*>(dq), N, block, M, eps);
+  }
+  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(dmixed, mixing, mixed, H, M, X, 1, tt, tn);
   const unsigned dm_grid = (unsigned)((size_t)H * p.P);
   switch ((M + 15) / 16) {
     case 1: bwd_dm_kernel<1><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;
@@ -656,6 +734,10 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
     default: bwd_dm_kernel<4><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;
   }
   bwd_dm_sum_kernel<<<(unsigned)((H * M * M + kBT / 32 - 1) / (kBT / 32)), kBT, 0, st>>>(dm_part, dm, H, M, p.P);
+  if (tc) {
+    note_launch(6);  // the SIMT launches; the tensor-core passes count their own
+    return tc_backward_key_launch(U, N, block, k, v, tt, tn, mixed, dk, dv, status, st);
+  }
   bwd_key_kernel<T, D><<<units_blocks, kBT, key_smem<D>(), st>>>(tk, tv, mixed, static_cast<T*>(dk),
                                                                static_cast<T*>(dv), N, block, M);
   note_launch(7);
@@ -665,6 +747,10 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
 }  // namespace
 
 size_t mhla_backward_workspace(int B, int H, int N, int d, int block) { return bwd_plan(B, H, N, d, block).total; }
+
+mhla_path mhla_backward_kernel_path(int B, int H, int N, int d, int block, mhla_dtype dt) {
+  return tc_backward_supported(B, H, N, d, block, dt) ? MHLA_PATH_TCGEN05 : MHLA_PATH_SIMT;
+}
 
 int mhla_backward_max_blocks() { return kMaxMixM; }
 
