@@ -178,6 +178,7 @@ KERNEL_SOURCES = {
     "rala_tcgen05": ["tc_rala.cu"],
     "decode_steps_simt": ["decode_steps.cu"],
     "backward_simt": ["mhla_backward.cu"],
+    "backward_tcgen05": ["mhla_backward.cu", "tc_backward.cu"],
 }
 SHARED_SOURCES = ["tc_common.cuh", "common.cuh"]
 
@@ -517,8 +518,10 @@ def kernel_path(binding, wl):
         return binding.rala_forward_path(wl.B, wl.H, wl.N, wl.d, wl.extra["cx"], tdt)
     if wl.kind == "decode":
         return "simt"
-    if wl.kind in ("decode_steps", "stream", "backward"):
+    if wl.kind in ("decode_steps", "stream"):
         return "simt"
+    if wl.kind == "backward":
+        return binding.mhla_backward_path(wl.B, wl.H, wl.N, wl.d, wl.block, tdt)
     if "grid" in wl.extra:
         return binding.mhla_forward_grid_path(wl.B, wl.H, *wl.extra["grid"], wl.d, tdt)
     if variant_kwargs(wl) or (wl.kind == "causal" and wl.mixing != "none"):
@@ -753,8 +756,10 @@ def workload_line(torch, binding, wl, device, l2, steps, warmup, sets=0):
         out["unit"] = "unit-steps/s"
         out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
         out["parity"] = parity_of_timed_output(runner)
-    elif wl.kind in ("stream", "backward"):
+    elif wl.kind == "stream" or (wl.kind == "backward" and path == "simt"):
         out["roofline"] = alu_roofline(torch, wl, device, kernel_ms)
+        out["parity"] = parity_of_timed_output(runner)
+    elif wl.kind == "backward":  # tensor-core token passes: bound by HBM like the forward
         out["parity"] = parity_of_timed_output(runner)
     else:
         out["parity"] = parity_of_timed_output(runner, n_slices=2)
@@ -841,7 +846,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "clocks": sampler.summary(t_wall0, t_wall1),
         "parity": parity,
     }
-    if wl.kind in ("decode_steps", "stream", "backward"):  # bound by fp32 FMA issue, not by HBM
+    if wl.kind in ("decode_steps", "stream") or (wl.kind == "backward" and path == "simt"):  # fp32 FMA issue
         line["roofline"] = dict(alu_roofline(torch, wl, device, kernel_ms), kernel=kernel_name,
                                 traffic=line["roofline"]["traffic"], kernels_per_step=per_step_kernels,
                                 launch_ms=kernel_ms, effective_GBps=achieved)

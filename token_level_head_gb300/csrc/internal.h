@@ -112,6 +112,8 @@ cudaError_t tc_backward_query_launch(int units, int N, int block, const void* q,
                                      const uint8_t* tiles_t, const uint8_t* tiles_n, const float* mu,
                                      const float* mixed, void* dq, float* dmixed, float eps, unsigned* status,
                                      cudaStream_t st);
+cudaError_t tc_backward_summary_launch(int units, int N, int block, const void* k, const void* v, float* slots,
+                                       unsigned* status, cudaStream_t st);
 cudaError_t tc_backward_key_launch(int units, int N, int block, const void* k, const void* v,
                                    const uint8_t* tiles_t, const uint8_t* tiles_n, const float* dslots, void* dk,
                                    void* dv, unsigned* status, cudaStream_t st);

@@ -14,8 +14,8 @@
 //   dphi(k_j) = dS_b v_j + dz_b,  dv_j = dS_b^T phi(k_j),
 //   dq = phi'(q) dphi(q),  dk = phi'(k) dphi(k),  phi'(x) = min(1, phi(x)).
 //
-// Seven launches, everything in fp32 (bf16 inputs and gradients are converted
-// at the loads and stores):
+// SIMT path, seven launches, everything in fp32 (bf16 inputs and gradients are
+// converted at the loads and stores):
 //   bwd_summary  (unit, block)   S_b, z_b                      from K, V
 //   bwd_mix      (unit, columns) S~, z~  = M  applied to the slots
 //   bwd_query    (unit, block)   dQ, dS~_i, dz~_i              from Q, dY, S~_i, z~_i
@@ -23,6 +23,9 @@
 //   bwd_dm       (head, range)   partial sums of dM over a range of the head's slot entries
 //   bwd_dm_sum   (head)          dM = the partials summed in a fixed order (deterministic)
 //   bwd_key      (unit, block)   dK, dV                        from K, V, dS_b, dz_b
+// bf16 with d = 64 and blocks of whole 128-token chunks: the summary, query and
+// key passes run on the tensor cores (tc_backward.cu), fed by bwd_tiles (the
+// bf16 operand tiles of S~ - z~ mu^T and of dS); mixing and dM stay here.
 // A slot is the d^2 + d floats (S then z) of one (unit, block).  The token
 // passes walk a block in chunks of TC tokens staged in shared memory, both
 // token-major ([t][c]) and feature-major ([c][t]), so that every product
@@ -305,15 +308,12 @@ __global__ void __launch_bounds__(kBT, BwdOcc<T, D>::SUMMARY) bwd_summary_kernel
 
 // ------------------------------------------------- out_i = sum_b w_ib in_b over the slots
 // w_ib = m[h][i][b] (transpose = 0) or m[h][b][i] (transpose = 1); a thread takes one entry x of
-// every slot of one unit (a CTA kBT consecutive entries) and all M outputs, 16 at a time.  With
-// tile outputs (d = 64) each d x d result also goes out in bf16 as two 8 KB 128-byte-swizzled
-// tiles, the tensor-core key pass's B operands: rows e / columns c, and rows c / columns e.
+// every slot of one unit (a CTA kBT consecutive entries) and all M outputs, 16 at a time.
 __device__ __forceinline__ size_t swz64(int row, int col) {  // byte of (row, col) in a [64][64] bf16 tile
   return (size_t)row * 128 + ((((col >> 3) ^ (row & 7)) << 4) | ((col & 7) << 1));
 }
 __global__ void __launch_bounds__(kBT) bwd_mix_kernel(const float* __restrict__ in, const float* __restrict__ mixing,
-                                                      float* __restrict__ out, int H, int M, int X, int transpose,
-                                                      uint8_t* __restrict__ tiles_t, uint8_t* __restrict__ tiles_n) {
+                                                      float* __restrict__ out, int H, int M, int X, int transpose) {
   __shared__ float sw[kMaxMixM * kMaxMixM];
   const int cols = (X + kBT - 1) / kBT;
   const int u = blockIdx.x / cols, x = (blockIdx.x % cols) * kBT + threadIdx.x;
@@ -345,51 +345,57 @@ __global__ void __launch_bounds__(kBT) bwd_mix_kernel(const float* __restrict__ 
 #pragma unroll
     for (int ii = 0; ii < 16; ++ii)
       if (i0 + ii < M) ob[(size_t)(i0 + ii) * X] = acc[ii];
-    if (tiles_t != nullptr && x < 64 * 64) {
-      const int c = x >> 6, e = x & 63;
-#pragma unroll
-      for (int ii = 0; ii < 16; ++ii)
-        if (i0 + ii < M) {
-          const size_t tile = ((size_t)u * M + i0 + ii) * 8192;
-          const __nv_bfloat16 v = __float2bfloat16_rn(acc[ii]);
-          *reinterpret_cast<__nv_bfloat16*>(tiles_t + tile + swz64(e, c)) = v;
-          *reinterpret_cast<__nv_bfloat16*>(tiles_n + tile + swz64(c, e)) = v;
-        }
-    }
   }
 }
 
-// ------------------------------------------------- S~_i = z~_i mu_i^T + S'_i (d = 64)
-// mu_i = S~_i^T z~_i / |z~_i|^2 (the least-squares rank-one part; zero when z~_i = 0); mu in fp32,
-// S' as the two bf16 tiles of the tensor-core query pass.  phi is near 1, so S~'s rows are near
-// multiples of one vector: S' is small and its bf16 rounding costs little, while the rank-one part
-// stays in fp32.  A CTA per slot.
-__global__ void __launch_bounds__(kBT) bwd_center_kernel(const float* __restrict__ mixed, float* __restrict__ mu,
-                                                         uint8_t* __restrict__ tiles_t, uint8_t* __restrict__ tiles_n) {
+// ------------------------------------------------- bf16 tiles of the slots (d = 64)
+// The two 8 KB 128-byte-swizzled bf16 tiles of each slot's d x d matrix A (rows e / columns c and
+// rows c / columns e), the tensor-core passes' B operands, built in shared memory and written
+// with 16-byte stores.  With mu: A = S~_i - z~_i mu_i^T, mu_i = S~_i^T z~_i / |z~_i|^2 (the
+// least-squares rank-one part, zero when z~_i = 0; written in fp32): phi is near 1, so S~'s rows
+// are near multiples of one vector; the remainder is small and its bf16 rounding costs little,
+// while the rank-one part stays in fp32.  A CTA per slot.
+__global__ void __launch_bounds__(kBT) bwd_tiles_kernel(const float* __restrict__ slots, float* __restrict__ mu,
+                                                        uint8_t* __restrict__ tiles_t, uint8_t* __restrict__ tiles_n) {
   constexpr int D = 64, X = D * D + D;
-  __shared__ float zz[D], sm_mu[D];
+  __shared__ __align__(16) uint8_t st[8192], sn[8192];
+  __shared__ float zz[D], smu[D], part[4][D], z2p[4];
   const size_t slot = blockIdx.x;
-  const float* sl = mixed + slot * X;
-  if (threadIdx.x < D) zz[threadIdx.x] = sl[D * D + threadIdx.x];
-  __syncthreads();
-  if (threadIdx.x < D) {
-    float z2 = 0.f, a = 0.f;
-    for (int c = 0; c < D; ++c) {
+  const float* sl = slots + slot * X;
+  const int tid = threadIdx.x;
+  if (mu != nullptr) {
+    if (tid < D) zz[tid] = sl[D * D + tid];
+    __syncthreads();
+    const int e = tid & 63, pc = tid >> 6;  // 4 threads an e, 16 c's each
+    float a = 0.f, z2 = 0.f;
+#pragma unroll
+    for (int c = 16 * pc; c < 16 * pc + 16; ++c) {
+      a = fmaf(zz[c], sl[c * D + e], a);
       z2 = fmaf(zz[c], zz[c], z2);
-      a = fmaf(zz[c], sl[c * D + threadIdx.x], a);
     }
-    const float m = z2 > 0.f ? a / z2 : 0.f;
-    sm_mu[threadIdx.x] = m;
-    mu[slot * D + threadIdx.x] = m;
+    part[pc][e] = a;
+    if (e == 0) z2p[pc] = z2;
+    __syncthreads();
+    if (tid < D) {
+      const float zt = (z2p[0] + z2p[1]) + (z2p[2] + z2p[3]);
+      const float m = zt > 0.f ? ((part[0][tid] + part[1][tid]) + (part[2][tid] + part[3][tid])) / zt : 0.f;
+      smu[tid] = m;
+      mu[slot * D + tid] = m;
+    }
+    __syncthreads();
+  }
+  for (int x = tid; x < D * D; x += kBT) {
+    const int c = x >> 6, e = x & 63;
+    const __nv_bfloat16 v = __float2bfloat16_rn(mu != nullptr ? sl[x] - zz[c] * smu[e] : sl[x]);
+    *reinterpret_cast<__nv_bfloat16*>(st + swz64(e, c)) = v;
+    *reinterpret_cast<__nv_bfloat16*>(sn + swz64(c, e)) = v;
   }
   __syncthreads();
-  uint8_t* tt = tiles_t + slot * 8192;
-  uint8_t* tn = tiles_n + slot * 8192;
-  for (int x = threadIdx.x; x < D * D; x += kBT) {
-    const int c = x >> 6, e = x & 63;
-    const __nv_bfloat16 v = __float2bfloat16_rn(sl[x] - zz[c] * sm_mu[e]);
-    *reinterpret_cast<__nv_bfloat16*>(tt + swz64(e, c)) = v;
-    *reinterpret_cast<__nv_bfloat16*>(tn + swz64(c, e)) = v;
+  uint4* gt = reinterpret_cast<uint4*>(tiles_t + slot * 8192);
+  uint4* gn = reinterpret_cast<uint4*>(tiles_n + slot * 8192);
+  for (int i = tid; i < 512; i += kBT) {
+    gt[i] = reinterpret_cast<const uint4*>(st)[i];
+    gn[i] = reinterpret_cast<const uint4*>(sn)[i];
   }
 }
 
@@ -714,10 +720,14 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
   if ((e = opt_k.ensure((const void*)bwd_key_kernel<T, D>, (int)key_smem<D>())) != cudaSuccess) return e;
   const unsigned units_blocks = (unsigned)((size_t)U * M);
   const unsigned mix_grid = (unsigned)((size_t)U * ((X + kBT - 1) / kBT));
-  bwd_summary_kernel<T, D><<<units_blocks, kBT, summary_smem<D>(), st>>>(tk, tv, slots, N, block, M);
-  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(slots, mixing, mixed, H, M, X, 0, nullptr, nullptr);
   if (tc) {
-    bwd_center_kernel<<<units_blocks, kBT, 0, st>>>(mixed, mu, tt, tn);
+    if ((e = tc_backward_summary_launch(U, N, block, k, v, slots, status, st)) != cudaSuccess) return e;
+  } else {
+    bwd_summary_kernel<T, D><<<units_blocks, kBT, summary_smem<D>(), st>>>(tk, tv, slots, N, block, M);
+  }
+  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(slots, mixing, mixed, H, M, X, 0);
+  if (tc) {
+    bwd_tiles_kernel<<<units_blocks, kBT, 0, st>>>(mixed, mu, tt, tn);
     if ((e = tc_backward_query_launch(U, N, block, q, dy, tt, tn, mu, mixed, dq, dmixed, eps, status, st)) !=
         cudaSuccess)
       return e;
@@ -725,7 +735,8 @@ cudaError_t backward_t(int B, int H, int N, int block, const void* q, const void
     bwd_query_kernel<T, D><<<units_blocks, kBT, query_smem<D>(), st>>>(tq, static_cast<const T*>(dy), mixed, dmixed,
                                                                      static_cast<T*>(dq), N, block, M, eps);
   }
-  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(dmixed, mixing, mixed, H, M, X, 1, tt, tn);
+  bwd_mix_kernel<<<mix_grid, kBT, 0, st>>>(dmixed, mixing, mixed, H, M, X, 1);
+  if (tc) bwd_tiles_kernel<<<units_blocks, kBT, 0, st>>>(mixed, nullptr, tt, tn);
   const unsigned dm_grid = (unsigned)((size_t)H * p.P);
   switch ((M + 15) / 16) {
     case 1: bwd_dm_kernel<1><<<dm_grid, kBT, 0, st>>>(dmixed, slots, dm_part, B, H, M, X, p.XP); break;

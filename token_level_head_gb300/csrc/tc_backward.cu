@@ -17,7 +17,8 @@
 // with phi'(x) = min(1, phi(x)).  S'_i and dS_b arrive as bf16 tiles in both orientations (K-major
 // B operands, 128-byte swizzle), written by the centring and mixing kernels.
 //
-// One CTA per (unit, block), 6 warps: warp 0 TMA producer (the block's d x d tiles, then each
+// The block summaries S_b, z_b come from a third pass of the same shape ([V^T ; 1] phi(K), as the
+// forward's summary pass).  One CTA per (unit, block), 6 warps: warp 0 TMA producer (the block's d x d tiles, then each
 // chunk's two 128 x 64 tiles), warp 1 MMA issuer (one thread), warps 2-5 epilogue (TMEM lane
 // quadrant = warp % 4, one token row a thread: phi in place, the fp32 denominator, the dnum and
 // dden tiles, the gradients).  Every hand-over is an mbarrier; every wait is bounded (on time-out
@@ -127,8 +128,9 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
 }
 
-// phi in place (bf16) on row r of a chunk tile; returns phi(row) . z + eps (fp32 phi) when z is given
-__device__ __forceinline__ float phi_row(uint8_t* tile, int r, const float* z, float eps) {
+// phi in place (bf16) on row r of a chunk tile, and phi - bf16(phi) at the same place of `lo` when
+// given; returns phi(row) . z + eps (fp32 phi) when z is given
+__device__ __forceinline__ float phi_row(uint8_t* tile, int r, const float* z, float eps, uint8_t* lo = nullptr) {
   float den = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -140,7 +142,15 @@ __device__ __forceinline__ float phi_row(uint8_t* tile, int r, const float* z, f
       f[x] = phi_f(f[x]);
       if (z) den = fmaf(f[x], z[8 * j + x], den);
     }
-    *p = pack8(f);
+    const uint4 hi = pack8(f);
+    *p = hi;
+    if (lo) {
+      float h[8];
+      unpack8(hi, h);
+#pragma unroll
+      for (int x = 0; x < 8; ++x) h[x] = f[x] - h[x];
+      *piece(lo, r, j) = pack8(h);
+    }
   }
   return den + eps;
 }
@@ -426,6 +436,99 @@ __global__ void __launch_bounds__(kThreads, 4) tc_bwd_key_kernel(const __grid_co
   finish(p, b, tmem, kKCols, warp);
 }
 
+// ================================================================ summaries
+// S_b^T and z_b in one M = 128 accumulator, as the forward's summary pass:
+// D[m][c] += sum_t [V^T ; 1][m][t] phi(K)[t][c] (A: the V tile, then a tile of ones, 16 KB on;
+// B = phi(K); both MN-major), with phi(K) as its bf16 high part plus its bf16 low part (two
+// products; V and the ones are exact in bf16), so S and z are those of fp32 phi: dq depends on
+// the small part of S~ that is not a multiple of z~, where bf16 phi(K) alone would cost ~1.5%.
+constexpr int kS_K = 0, kS_V = kTile, kS_ONE = 2 * kTile, kS_LO = 3 * kTile, kS_BAR = 4 * kTile;
+constexpr uint32_t kSCols = 64;
+constexpr size_t kSSmem = 1024 + kS_BAR + sizeof(Bars);
+static_assert(kSSmem <= 232448 / 3, "three summary CTAs per SM");
+
+__global__ void __launch_bounds__(kThreads, 3) tc_bwd_summary_kernel(const __grid_constant__ BParams p) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  Bars* b = reinterpret_cast<Bars*>(sm + kS_BAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u = blockIdx.x / p.M, bb = blockIdx.x % p.M, nch = p.L / kT;
+  const size_t slot = (size_t)u * p.M + bb;
+  const int row0 = u * p.N + bb * p.L;
+  setup(b, kSCols, p, warp, lane);
+  const uint32_t tmem = b->tbase;
+  int* ab = &b->abort;
+
+  if (warp == kWarpProd) {
+    if (lane == 0) {
+      int j = 0;
+      for (; j < nch; ++j) {
+        if (j > 0 && !bwait(&b->acc1, (j - 1) & 1, ab)) break;  // chunk j - 1's MMAs have read the tiles
+        mbar_arrive_expect_tx(&b->full, 2 * kTile);
+        tma_load_2d(sm + kS_K, &p.tm_a, 0, row0 + j * kT, &b->full);
+        tma_load_2d(sm + kS_V, &p.tm_b, 0, row0 + j * kT, &b->full);
+      }
+      b->issued = j;
+    }
+    __syncwarp();
+  } else if (warp == kWarpMma) {
+    if (lane == 0) {
+      const uint32_t v = smem_u32(sm + kS_V), one = smem_u32(sm + kS_ONE);
+      const uint64_t da = smem_desc(v, one - v, 1024), db = smem_desc(smem_u32(sm + kS_K), 8192, 1024);
+      const uint64_t dbl = smem_desc(smem_u32(sm + kS_LO), 8192, 1024);
+      const uint32_t id = idesc_bf16_f32(128, 64, 1, 1);
+      for (int j = 0; j < nch; ++j) {
+        if (!bwait(&b->phi, j & 1, ab)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kT / 16; ++k) mma_bf16(tmem, da + k * (2048 >> 4), db + k * (2048 >> 4), id, j > 0 || k > 0);
+#pragma unroll
+        for (int k = 0; k < kT / 16; ++k) mma_bf16(tmem, da + k * (2048 >> 4), dbl + k * (2048 >> 4), id, true);
+        mma_commit(&b->acc1);
+      }
+      mma_commit(&b->fin);
+    }
+    __syncwarp();
+  } else {
+    const int qd = warp & 3, t = qd * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
+    const uint32_t one2 = pack_bf16(1.f, 1.f);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) *piece(sm + kS_ONE, t, jj) = make_uint4(one2, one2, one2, one2);
+    bool ok = true;
+    for (int j = 0; ok && j < nch; ++j) {
+      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab));
+      if (!ok) break;
+      phi_row(sm + kS_K, t, nullptr, 0.f, sm + kS_LO);
+      fence_proxy_async_smem();  // phi (and, the first time, the ones tile) -> tensor core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&b->phi);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, bwait(&b->acc1, (nch - 1) & 1, ab));
+    if (ok && !ab_get(ab)) {
+      tc_fence_after();
+      // lanes 0-63: S^T[e][c] -> the slot's S[c][e]; lane 64: z[c]  (whole warps load)
+      float* out = p.out_slots + slot * kX;
+      if (qd < 3) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float v[16];
+          tmem_ld16(trow + 16 * g, v);
+          tmem_ld_wait();
+          if (qd < 2) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) out[(16 * g + x) * kD + t] = v[x];
+          } else if (lane == 0) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) out[kD * kD + 16 * g + x] = v[x];
+          }
+        }
+      }
+    }
+  }
+  finish(p, b, tmem, kSCols, warp);
+}
+
 // ================================================================ host
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -484,6 +587,31 @@ cudaError_t tc_backward_query_launch(int units, int N, int block, const void* q,
   cudaError_t e = opt.ensure((const void*)tc_bwd_query_kernel, (int)kQSmem);
   if (e != cudaSuccess) return e;
   tc_bwd_query_kernel<<<(unsigned)((size_t)units * p.M), kThreads, kQSmem, st>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t tc_backward_summary_launch(int units, int N, int block, const void* k, const void* v, float* slots,
+                                       unsigned* status, cudaStream_t st) {
+  BParams p;
+  const uint64_t rows = (uint64_t)units * N;
+  if (!make_map(&p.tm_a, k, rows) || !make_map(&p.tm_b, v, rows)) return cudaErrorInvalidValue;
+  p.tiles_t = nullptr;
+  p.tiles_n = nullptr;
+  p.mu = nullptr;
+  p.zslots = nullptr;
+  p.g0 = nullptr;
+  p.g1 = nullptr;
+  p.out_slots = slots;
+  p.status = status;
+  p.N = N;
+  p.L = block;
+  p.M = N / block;
+  p.eps = 0.f;
+  static SmemOptIn opt;
+  cudaError_t e = opt.ensure((const void*)tc_bwd_summary_kernel, (int)kSSmem);
+  if (e != cudaSuccess) return e;
+  tc_bwd_summary_kernel<<<(unsigned)((size_t)units * p.M), kThreads, kSSmem, st>>>(p);
   note_launch();
   return cudaGetLastError();
 }
