@@ -362,8 +362,9 @@ unsigned long long mhla_launch_count(void);
 
 /* Diagnostic: sets the limit, in nanoseconds, of the bounded device-side
  * waits of the non-causal bf16 tensor-core kernels (every wait of the stream
- * path; the waits for the mixed summaries of the three-pass path) for calls
- * launched after it (process
+ * path; the waits for the mixed summaries of the three-pass path) and of the
+ * tensor-core passes of mhla_backward (every wait) for calls launched after it
+ * (process
  * wide; 0 restores the default of 0.5 s).  With a limit too short for the
  * work in flight a call gives up: its output is incomplete, the kernel lets
  * its copies and MMAs in flight finish, leaves the workspace counters at

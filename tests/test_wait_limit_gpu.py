@@ -56,3 +56,31 @@ def test_wait_limit_gives_up_then_next_call_is_correct(shape, path):
     ref, dref = oracle.mhla_block_form(x["q64"], x["k64"], x["v64"], mix64, block)
     assert_close_y(to_f64(y), ref, "bf16")
     assert_close_den(to_f64(den), dref, "bf16")
+
+
+def test_backward_wait_limit_gives_up_then_next_call_is_correct():
+    """The tensor-core passes of the backward: with every wait at its shortest the call gives up,
+    latches MHLA_ERR_TIMEOUT in its workspace, and the next call on the same workspace is right."""
+    from test_backward_gpu import check, dm_term_magnitudes
+    from test_parity_gpu import rounded
+    from workloads import normal
+    B, H, N, d, block = 2, 2, 512, 64, 128
+    assert binding.mhla_backward_path(B, H, N, d, block, torch.bfloat16) == "tcgen05"
+    x = rand_inputs(710, (B, H, N, d), "bf16")
+    dy, dy64 = rounded(normal(711, 4, (B, H, N, d)), "bf16")
+    mix_t, mix64 = rand_mixing(712, H, N // block)
+    ws = binding.new_workspace(binding.mhla_backward_workspace_bytes(B, H, N, d, block), "cuda")
+    grads = [torch.empty_like(x[n]) for n in "qkv"] + [torch.empty_like(mix_t)]
+    binding.mhla_debug_set_wait_limit_ns(1)
+    try:
+        binding.mhla_backward(x["q"], x["k"], x["v"], mix_t, dy, *grads, block, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        binding.mhla_debug_set_wait_limit_ns(0)
+    assert binding.mhla_query_status(ws) == binding.MHLA_ERR_TIMEOUT
+    assert binding.mhla_query_status(ws) == binding.MHLA_OK
+    binding.mhla_backward(x["q"], x["k"], x["v"], mix_t, dy, *grads, block, workspace=ws)
+    assert binding.mhla_query_status(ws) == binding.MHLA_OK
+    args = (x["q64"], x["k64"], x["v64"], mix64, block, dy64, 1e-6)
+    check(tuple(to_f64(g) for g in grads), oracle.mhla_block_form_backward(*args), "bf16",
+          dm_term_magnitudes(*args, absolute=True), "tcgen05")

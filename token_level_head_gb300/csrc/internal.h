@@ -108,6 +108,7 @@ cudaError_t mhla_backward_launch(int B, int H, int N, int d, int block, mhla_dty
                                  float* dm, float eps, void* ws, cudaStream_t st);
 // tensor-core token passes of the backward (bf16, d = 64, blocks of whole 128-token chunks)
 bool tc_backward_supported(int B, int H, int N, int d, int block, mhla_dtype dt);
+void tc_backward_set_wait_limit(unsigned long long ns);
 cudaError_t tc_backward_query_launch(int units, int N, int block, const void* q, const void* dy,
                                      const uint8_t* tiles_t, const uint8_t* tiles_n, const float* mu,
                                      const float* mixed, void* dq, float* dmixed, float eps, unsigned* status,

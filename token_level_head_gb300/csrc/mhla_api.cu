@@ -433,6 +433,7 @@ unsigned long long mhla_launch_count(void) { return g_launches.load(std::memory_
 void mhla_debug_set_wait_limit_ns(unsigned long long ns) {
   tc_stream_set_wait_limit(ns);
   tc_mhla_set_wait_limit(ns);
+  tc_backward_set_wait_limit(ns);
 }
 
 }  // extern "C"

@@ -44,7 +44,7 @@ constexpr int kSTile = kD * kD * 2;     // 8 KB bf16 d x d tile
 constexpr int kX = kD * kD + kD;        // floats of a slot (S then z)
 constexpr int kThreads = 192;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpEpi = 2, kEpiWarps = 4;
-constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s
+constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s: a wait's default limit
 
 // query pass: Q (phi in place), dY, dnum, dden repeated (right after dnum: the LBO of the stacked
 // A operand), S'^T, S', z~ then mu (fp32)
@@ -65,6 +65,7 @@ struct Bars {
   uint64_t acc2;   // query: dphi(Q) and the dS~ accumulation done (MMA commit)
   uint64_t free_;  // the chunk's tiles may be overwritten (4 epilogue warps)
   uint64_t fin;    // every MMA of the CTA has completed (MMA commit)
+  unsigned long long wait_ns;  // a wait's limit
   uint32_t tbase;
   int abort;
   int issued;      // chunks whose loads the producer issued
@@ -86,24 +87,26 @@ struct BParams {
   __nv_bfloat16* g1;        // key: dv
   float* out_slots;         // query: dS~ [c][e] and dz~ per slot
   unsigned* status;
+  unsigned long long wait_ns;  // the limit of every wait (the default, or a diagnostic's shorter one)
   int N, L, M;
   float eps;
 };
 
 __device__ __forceinline__ bool ab_get(const int* ab) { return *reinterpret_cast<const volatile int*>(ab) != 0; }
 
-__device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, int* ab) {
+__device__ __noinline__ bool bwait_slow(uint64_t* bar, uint32_t parity, int* ab, unsigned long long limit) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_ns(bar, parity, 256)) return true;
     if (ab_get(ab)) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) break;
+    if (globaltimer_ns() - t0 > limit) break;
   }
   *reinterpret_cast<volatile int*>(ab) = 1;
   return false;
 }
-__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, int* ab) {
-  return mbar_test(bar, parity) || bwait_slow(bar, parity, ab);
+// ab: the CTA's abort flag; limit: the wait's limit in ns
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, int* ab, unsigned long long limit) {
+  return mbar_test(bar, parity) || bwait_slow(bar, parity, ab, limit);
 }
 // Short wait (10 ms at most), only while winding down after an abort.
 __device__ __noinline__ void drain(uint64_t* bar, uint32_t parity) {
@@ -168,6 +171,7 @@ __device__ __forceinline__ void setup(Bars* b, uint32_t cols, const BParams& p, 
     mbar_init(&b->fin, 1);
     b->abort = 0;
     b->issued = 0;
+    b->wait_ns = p.wait_ns;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -194,7 +198,7 @@ __device__ __forceinline__ void produce(const BParams& p, uint8_t* sm, Bars* b, 
   bulk_load_1d(sm + z_off, p.zslots + slot * kX + kD * kD, kD * 4, &b->sfull);
   int j = 0;
   for (; j < nch; ++j) {
-    if (j > 0 && !bwait(&b->free_, (j - 1) & 1, ab)) break;
+    if (j > 0 && !bwait(&b->free_, (j - 1) & 1, ab, b->wait_ns)) break;
     mbar_arrive_expect_tx(&b->full, 2 * kTile);
     tma_load_2d(sm + a_off, &p.tm_a, 0, row0 + j * kT, &b->full);
     tma_load_2d(sm + b_off, &p.tm_b, 0, row0 + j * kT, &b->full);
@@ -242,15 +246,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       const uint64_t a1 = smem_desc(q, 16, 1024), b1 = smem_desc(smem_u32(sm + kQ_ST), 16, 1024);
       const uint64_t a2 = smem_desc(n, 16, 1024), b2 = smem_desc(smem_u32(sm + kQ_SN), 16, 1024);
       const uint64_t a3 = smem_desc(n, r - n, 1024), b3 = smem_desc(q, 8192, 1024);
-      if (bwait(&b->sfull, 0, ab)) {
+      if (bwait(&b->sfull, 0, ab, b->wait_ns)) {
         for (int j = 0; j < nch; ++j) {
-          if (!bwait(&b->phi, j & 1, ab)) break;
+          if (!bwait(&b->phi, j & 1, ab, b->wait_ns)) break;
           tc_fence_after();
           // phi(Q) S'[t][e] = sum_c phi(Q)[t][c] S'[c][e]: A = phi(Q) (K-major), B = S'^T tile (K-major)
 #pragma unroll
           for (int k = 0; k < kD / 16; ++k) mma_bf16(tmem, a1 + k * 2, b1 + k * 2, id_k, k > 0);
           mma_commit(&b->acc1);
-          if (!bwait(&b->mid, j & 1, ab)) break;
+          if (!bwait(&b->mid, j & 1, ab, b->wait_ns)) break;
           tc_fence_after();
           // dnum S'^T[t][c] = sum_e dnum[t][e] S'[c][e]: A = dnum (K-major), B = S' tile (K-major)
 #pragma unroll
@@ -271,15 +275,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     const float* z = reinterpret_cast<const float*>(sm + kQ_Z);
     uint8_t* qt = sm + kQ_Q;
-    bool ok = bwait(&b->sfull, 0, ab);
+    bool ok = bwait(&b->sfull, 0, ab, b->wait_ns);
     for (int j = 0; ok && j < nch; ++j) {
-      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab));
+      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab, b->wait_ns));
       if (!ok) break;
       const float den = phi_row(qt, t, z, p.eps);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&b->phi);
-      ok = __all_sync(0xffffffffu, bwait(&b->acc1, j & 1, ab));
+      ok = __all_sync(0xffffffffu, bwait(&b->acc1, j & 1, ab, b->wait_ns));
       if (!ok) break;
       tc_fence_after();
       // num = (den - eps) mu + phi(Q) S';  dnum = dY / den (bf16 tile), mu . dnum (fp32),
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&b->mid);
-      ok = __all_sync(0xffffffffu, bwait(&b->acc2, j & 1, ab));
+      ok = __all_sync(0xffffffffu, bwait(&b->acc2, j & 1, ab, b->wait_ns));
       if (!ok) break;
       tc_fence_after();
       // dq = min(1, phi(q)) (dnum S'^T + (mu . dnum + dden) z~)
@@ -379,9 +383,9 @@ __global__ void __launch_bounds__(kThreads, 4) tc_bwd_key_kernel(const __grid_co
       const uint32_t id_k = idesc_bf16_f32(128, 64, 0, 0);
       const uint64_t ak = smem_desc(smem_u32(sm + kK_K), 16, 1024), av = smem_desc(smem_u32(sm + kK_V), 16, 1024);
       const uint64_t bt = smem_desc(smem_u32(sm + kK_ST), 16, 1024), bn = smem_desc(smem_u32(sm + kK_SN), 16, 1024);
-      if (bwait(&b->sfull, 0, ab)) {
+      if (bwait(&b->sfull, 0, ab, b->wait_ns)) {
         for (int j = 0; j < nch; ++j) {
-          if (!bwait(&b->phi, j & 1, ab)) break;
+          if (!bwait(&b->phi, j & 1, ab, b->wait_ns)) break;
           tc_fence_after();
           // dv[t][e] = sum_c phi(K)[t][c] dS[c][e]: B = dS^T tile;  dphi(K)[t][c] = sum_e V[t][e] dS[c][e]: B = dS tile
 #pragma unroll
@@ -399,15 +403,15 @@ __global__ void __launch_bounds__(kThreads, 4) tc_bwd_key_kernel(const __grid_co
     const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
     const float* z = reinterpret_cast<const float*>(sm + kK_Z);
     uint8_t* kt = sm + kK_K;
-    bool ok = bwait(&b->sfull, 0, ab);
+    bool ok = bwait(&b->sfull, 0, ab, b->wait_ns);
     for (int j = 0; ok && j < nch; ++j) {
-      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab));
+      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab, b->wait_ns));
       if (!ok) break;
       phi_row(kt, t, nullptr, 0.f);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&b->phi);
-      ok = __all_sync(0xffffffffu, bwait(&b->acc1, j & 1, ab));
+      ok = __all_sync(0xffffffffu, bwait(&b->acc1, j & 1, ab, b->wait_ns));
       if (!ok) break;
       tc_fence_after();
       const size_t row = (size_t)(row0 + j * kT + t) * kD;
@@ -463,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 3) tc_bwd_summary_kernel(const __gri
     if (lane == 0) {
       int j = 0;
       for (; j < nch; ++j) {
-        if (j > 0 && !bwait(&b->acc1, (j - 1) & 1, ab)) break;  // chunk j - 1's MMAs have read the tiles
+        if (j > 0 && !bwait(&b->acc1, (j - 1) & 1, ab, b->wait_ns)) break;  // chunk j - 1's MMAs have read the tiles
         mbar_arrive_expect_tx(&b->full, 2 * kTile);
         tma_load_2d(sm + kS_K, &p.tm_a, 0, row0 + j * kT, &b->full);
         tma_load_2d(sm + kS_V, &p.tm_b, 0, row0 + j * kT, &b->full);
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 3) tc_bwd_summary_kernel(const __gri
       const uint64_t dbl = smem_desc(smem_u32(sm + kS_LO), 8192, 1024);
       const uint32_t id = idesc_bf16_f32(128, 64, 1, 1);
       for (int j = 0; j < nch; ++j) {
-        if (!bwait(&b->phi, j & 1, ab)) break;
+        if (!bwait(&b->phi, j & 1, ab, b->wait_ns)) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kT / 16; ++k) mma_bf16(tmem, da + k * (2048 >> 4), db + k * (2048 >> 4), id, j > 0 || k > 0);
@@ -497,14 +501,14 @@ __global__ void __launch_bounds__(kThreads, 3) tc_bwd_summary_kernel(const __gri
     for (int jj = 0; jj < 8; ++jj) *piece(sm + kS_ONE, t, jj) = make_uint4(one2, one2, one2, one2);
     bool ok = true;
     for (int j = 0; ok && j < nch; ++j) {
-      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab));
+      ok = __all_sync(0xffffffffu, bwait(&b->full, j & 1, ab, b->wait_ns));
       if (!ok) break;
       phi_row(sm + kS_K, t, nullptr, 0.f, sm + kS_LO);
       fence_proxy_async_smem();  // phi (and, the first time, the ones tile) -> tensor core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(&b->phi);
     }
-    if (ok) ok = __all_sync(0xffffffffu, bwait(&b->acc1, (nch - 1) & 1, ab));
+    if (ok) ok = __all_sync(0xffffffffu, bwait(&b->acc1, (nch - 1) & 1, ab, b->wait_ns));
     if (ok && !ab_get(ab)) {
       tc_fence_after();
       // lanes 0-63: S^T[e][c] -> the slot's S[c][e]; lane 64: z[c]  (whole warps load)
@@ -557,7 +561,11 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+unsigned long long g_wait_ns = kWaitNs;
+
 }  // namespace
+
+void tc_backward_set_wait_limit(unsigned long long ns) { g_wait_ns = ns == 0 ? kWaitNs : ns; }
 
 bool tc_backward_supported(int B, int H, int N, int d, int block, mhla_dtype dt) {
   if (dt != MHLA_BF16 || d != kD || block <= 0 || block % kT != 0 || N % block != 0) return false;
@@ -579,6 +587,7 @@ cudaError_t tc_backward_query_launch(int units, int N, int block, const void* q,
   p.g1 = nullptr;
   p.out_slots = dmixed;
   p.status = status;
+  p.wait_ns = g_wait_ns;
   p.N = N;
   p.L = block;
   p.M = N / block;
@@ -604,6 +613,7 @@ cudaError_t tc_backward_summary_launch(int units, int N, int block, const void* 
   p.g1 = nullptr;
   p.out_slots = slots;
   p.status = status;
+  p.wait_ns = g_wait_ns;
   p.N = N;
   p.L = block;
   p.M = N / block;
@@ -630,6 +640,7 @@ cudaError_t tc_backward_key_launch(int units, int N, int block, const void* k, c
   p.g1 = static_cast<__nv_bfloat16*>(dv);
   p.out_slots = nullptr;
   p.status = status;
+  p.wait_ns = g_wait_ns;
   p.N = N;
   p.L = block;
   p.M = N / block;
