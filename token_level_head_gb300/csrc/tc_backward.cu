@@ -291,16 +291,18 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       const float inv = 1.f / den, dz0 = den - p.eps;
       const float* mu = z + kD;
       float s = 0.f, mdn = 0.f;
+      float nm[64];  // the row's four 16-column loads in flight together, one wait
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tmem_ld16(trow + 16 * g, nm + 16 * g);
+      tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float nm[16], dy[16];
-        tmem_ld16(trow + 16 * g, nm);
+        float dy[16];
         unpack8(*piece(sm + kQ_Y, t, 2 * g), dy);
         unpack8(*piece(sm + kQ_Y, t, 2 * g + 1), dy + 8);
-        tmem_ld_wait();
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          s = fmaf(dy[x], fmaf(dz0, mu[16 * g + x], nm[x]), s);
+          s = fmaf(dy[x], fmaf(dz0, mu[16 * g + x], nm[16 * g + x]), s);
           dy[x] *= inv;
           mdn = fmaf(mu[16 * g + x], dy[x], mdn);
         }
@@ -322,17 +324,19 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       // dq = min(1, phi(q)) (dnum S'^T + (mu . dnum + dden) z~)
       const float zc = mdn + dd;
       uint4* dst = reinterpret_cast<uint4*>(p.g0 + (size_t)(row0 + j * kT + t) * kD);
+      float gq[64];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tmem_ld16(trow + 64 + 16 * g, gq + 16 * g);
+      tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float gq[16], qf[16];
-        tmem_ld16(trow + 64 + 16 * g, gq);
+        float qf[16];
         unpack8(*piece(qt, t, 2 * g), qf);
         unpack8(*piece(qt, t, 2 * g + 1), qf + 8);
-        tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) gq[x] = fminf(1.f, qf[x]) * fmaf(zc, z[16 * g + x], gq[x]);
-        dst[2 * g] = pack8(gq);
-        dst[2 * g + 1] = pack8(gq + 8);
+        for (int x = 0; x < 16; ++x) qf[x] = fminf(1.f, qf[x]) * fmaf(zc, z[16 * g + x], gq[16 * g + x]);
+        dst[2 * g] = pack8(qf);
+        dst[2 * g + 1] = pack8(qf + 8);
       }
       tc_fence_before();
       __syncwarp();
@@ -343,18 +347,16 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       // (tcgen05.ld is warp-collective: whole warps load, then the owning lanes store)
       float* out = p.out_slots + slot * kX;
       if (qd < 3) {
+        float v[64];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float v[16];
-          tmem_ld16(trow + 128 + 16 * g, v);
-          tmem_ld_wait();
-          if (qd < 2) {
+        for (int g = 0; g < 4; ++g) tmem_ld16(trow + 128 + 16 * g, v + 16 * g);
+        tmem_ld_wait();
+        if (qd < 2) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) out[(16 * g + x) * kD + t] = v[x];
-          } else if (lane == 0) {
+          for (int x = 0; x < 64; ++x) out[x * kD + t] = v[x];
+        } else if (lane == 0) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) out[kD * kD + 16 * g + x] = v[x];
-          }
+          for (int x = 0; x < 64; ++x) out[kD * kD + x] = v[x];
         }
       }
     }
@@ -418,19 +420,26 @@ __global__ void __launch_bounds__(kThreads, 4) tc_bwd_key_kernel(const __grid_co
       uint4* dv = reinterpret_cast<uint4*>(p.g1 + row);
       uint4* dk = reinterpret_cast<uint4*>(p.g0 + row);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        float gv[16], gk[16], kf[16];
-        tmem_ld16(trow + 16 * g, gv);
-        tmem_ld16(trow + 64 + 16 * g, gk);
-        unpack8(*piece(kt, t, 2 * g), kf);
-        unpack8(*piece(kt, t, 2 * g + 1), kf + 8);
+      for (int hh = 0; hh < 2; ++hh) {  // 32 columns at a time: four loads in flight, one wait
+        float gv[32], gk[32];
+        tmem_ld16(trow + 32 * hh, gv);
+        tmem_ld16(trow + 32 * hh + 16, gv + 16);
+        tmem_ld16(trow + 64 + 32 * hh, gk);
+        tmem_ld16(trow + 64 + 32 * hh + 16, gk + 16);
         tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) gk[x] = fminf(1.f, kf[x]) * (gk[x] + z[16 * g + x]);
-        dv[2 * g] = pack8(gv);
-        dv[2 * g + 1] = pack8(gv + 8);
-        dk[2 * g] = pack8(gk);
-        dk[2 * g + 1] = pack8(gk + 8);
+        for (int g = 0; g < 2; ++g) {
+          const int gg = 2 * hh + g;
+          float kf[16];
+          unpack8(*piece(kt, t, 2 * gg), kf);
+          unpack8(*piece(kt, t, 2 * gg + 1), kf + 8);
+#pragma unroll
+          for (int x = 0; x < 16; ++x) kf[x] = fminf(1.f, kf[x]) * (gk[16 * g + x] + z[16 * gg + x]);
+          dv[2 * gg] = pack8(gv + 16 * g);
+          dv[2 * gg + 1] = pack8(gv + 16 * g + 8);
+          dk[2 * gg] = pack8(kf);
+          dk[2 * gg + 1] = pack8(kf + 8);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -514,18 +523,16 @@ __global__ void __launch_bounds__(kThreads, 3) tc_bwd_summary_kernel(const __gri
       // lanes 0-63: S^T[e][c] -> the slot's S[c][e]; lane 64: z[c]  (whole warps load)
       float* out = p.out_slots + slot * kX;
       if (qd < 3) {
+        float v[64];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float v[16];
-          tmem_ld16(trow + 16 * g, v);
-          tmem_ld_wait();
-          if (qd < 2) {
+        for (int g = 0; g < 4; ++g) tmem_ld16(trow + 16 * g, v + 16 * g);
+        tmem_ld_wait();
+        if (qd < 2) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) out[(16 * g + x) * kD + t] = v[x];
-          } else if (lane == 0) {
+          for (int x = 0; x < 64; ++x) out[x * kD + t] = v[x];
+        } else if (lane == 0) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) out[kD * kD + 16 * g + x] = v[x];
-          }
+          for (int x = 0; x < 64; ++x) out[kD * kD + x] = v[x];
         }
       }
     }
