@@ -177,6 +177,7 @@ KERNEL_SOURCES = {
     "causal_mhla_tcgen05": ["tc_causal.cu", "tc_mhla.cu"],
     "rala_tcgen05": ["tc_rala.cu"],
     "decode_steps_simt": ["decode_steps.cu"],
+    "stream_simt": ["causal_stream.cu"],
     "backward_simt": ["mhla_backward.cu"],
     "backward_tcgen05": ["mhla_backward.cu", "tc_backward.cu"],
 }
