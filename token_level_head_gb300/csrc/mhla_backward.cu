@@ -318,24 +318,29 @@ __global__ void __launch_bounds__(kBT) bwd_mix_kernel(const float* __restrict__ 
   const int cols = (X + kBT - 1) / kBT;
   const int u = blockIdx.x / cols, x = (blockIdx.x % cols) * kBT + threadIdx.x;
   const float* mh = mixing + (size_t)(u % H) * M * M;
+  const int xc = min(x, X - 1);  // threads past the slot load a valid entry and store nothing
+  const float* ib = in + (size_t)u * M * X + xc;
+  float* ob = out + (size_t)u * M * X + x;
+  float pre[16];  // the first 16 inputs, in flight while the weights are staged
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pre[j] = ib[(size_t)min(j, M - 1) * X];
   for (int e = threadIdx.x; e < M * M; e += kBT) {
     const int i = e / M, b = e % M;
     sw[i * M + b] = transpose ? mh[(size_t)b * M + i] : mh[(size_t)i * M + b];
   }
   __syncthreads();
   if (x >= X) return;
-  const float* ib = in + (size_t)u * M * X + x;
-  float* ob = out + (size_t)u * M * X + x;
   for (int i0 = 0; i0 < M; i0 += 16) {
     float acc[16];
 #pragma unroll
     for (int ii = 0; ii < 16; ++ii) acc[ii] = 0.f;
-    for (int b0 = 0; b0 < M; b0 += 8) {  // eight independent loads in flight, then their FMAs
-      float val[8];
+    for (int b0 = 0; b0 < M; b0 += 16) {  // sixteen independent loads in flight, then their FMAs
+      float val[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) val[j] = b0 + j < M ? ib[(size_t)min(b0 + j, M - 1) * X] : 0.f;
+      for (int j = 0; j < 16; ++j)
+        val[j] = b0 + j < M ? (b0 == 0 ? pre[j] : ib[(size_t)min(b0 + j, M - 1) * X]) : 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 16; ++j)
 #pragma unroll
         for (int ii = 0; ii < 16; ++ii) {
           const float w = (i0 + ii < M && b0 + j < M) ? sw[(i0 + ii) * M + b0 + j] : 0.f;
@@ -359,10 +364,25 @@ __global__ void __launch_bounds__(kBT) bwd_tiles_kernel(const float* __restrict_
                                                         uint8_t* __restrict__ tiles_t, uint8_t* __restrict__ tiles_n) {
   constexpr int D = 64, X = D * D + D;
   __shared__ __align__(16) uint8_t st[8192], sn[8192];
+  __shared__ __align__(16) float sl[X];  // the slot, staged with all of a thread's loads in flight
   __shared__ float zz[D], smu[D], part[4][D], z2p[4];
   const size_t slot = blockIdx.x;
-  const float* sl = slots + slot * X;
   const int tid = threadIdx.x;
+  {
+    const float4* g = reinterpret_cast<const float4*>(slots + slot * X);  // X * 4 bytes: 16-byte aligned slots
+    float4 v[(X / 4 + kBT - 1) / kBT];
+#pragma unroll
+    for (int j = 0; j < (X / 4 + kBT - 1) / kBT; ++j) {
+      const int q = tid + j * kBT;
+      v[j] = q < X / 4 ? g[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < (X / 4 + kBT - 1) / kBT; ++j) {
+      const int q = tid + j * kBT;
+      if (q < X / 4) reinterpret_cast<float4*>(sl)[q] = v[j];
+    }
+    __syncthreads();
+  }
   if (mu != nullptr) {
     if (tid < D) zz[tid] = sl[D * D + tid];
     __syncthreads();
