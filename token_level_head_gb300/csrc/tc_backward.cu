@@ -46,11 +46,13 @@ constexpr int kThreads = 192;
 constexpr int kWarpProd = 0, kWarpMma = 1, kWarpEpi = 2, kEpiWarps = 4;
 constexpr uint64_t kWaitNs = 500000000ull;  // 0.5 s: a wait's default limit
 
-// query pass: Q (phi in place), dY, dnum, dden repeated (right after dnum: the LBO of the stacked
-// A operand), S'^T, S', z~ then mu (fp32)
-constexpr int kQ_Q = 0, kQ_Y = kTile, kQ_N = 2 * kTile, kQ_R = 3 * kTile, kQ_ST = 4 * kTile,
-              kQ_SN = kQ_ST + kSTile, kQ_Z = kQ_SN + kSTile, kQ_BAR = kQ_Z + 512;
-constexpr uint32_t kQCols = 256;        // num [0, 64), dphi(Q) [64, 128), [dS~^T ; dz~] [128, 192)
+// query pass: Q (phi in place), dY (dnum is written over it, row by row), dden repeated (right
+// after dnum: the LBO of the stacked A operand), S'^T, S', z~ then mu (fp32).  65 KB and 128 TMEM
+// columns: three CTAs an SM, so three chunk chains in flight (a chunk is a serial chain of phi,
+// MMA, dnum/dden, MMAs, dq; the chains in flight set the pass's rate).
+constexpr int kQ_Q = 0, kQ_Y = kTile, kQ_R = 2 * kTile, kQ_ST = 3 * kTile, kQ_SN = kQ_ST + kSTile,
+              kQ_Z = kQ_SN + kSTile, kQ_BAR = kQ_Z + 512;
+constexpr uint32_t kQCols = 128;        // phi(Q) S', then dnum S'^T, in [0, 64); [dS~^T ; dz~] [64, 128)
 // key pass: K (phi in place), V, dS^T, dS, dz
 constexpr int kK_K = 0, kK_V = kTile, kK_ST = 2 * kTile, kK_SN = kK_ST + kSTile, kK_Z = kK_SN + kSTile,
               kK_BAR = kK_Z + 256;
@@ -73,8 +75,8 @@ struct Bars {
 
 constexpr size_t kQSmem = 1024 + kQ_BAR + sizeof(Bars);
 constexpr size_t kKSmem = 1024 + kK_BAR + sizeof(Bars);
-static_assert(kQSmem <= 232448 / 2, "two query CTAs per SM (their TMEM columns fit too)");
-static_assert(kQ_R - kQ_N == kTile, "the stacked A operand: dden right after dnum");
+static_assert(kQSmem <= 232448 / 3, "three query CTAs per SM (their TMEM columns fit too)");
+static_assert(kQ_R - kQ_Y == kTile, "the stacked A operand: dden right after dnum");
 static_assert(kKSmem <= 232448 / 4, "four key CTAs per SM");
 
 struct BParams {
@@ -224,7 +226,7 @@ __device__ __forceinline__ void finish(const BParams& p, Bars* b, uint32_t tmem,
 }
 
 // ================================================================ query pass
-__global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_constant__ BParams p) {
+__global__ void __launch_bounds__(kThreads, 3) tc_bwd_query_kernel(const __grid_constant__ BParams p) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   Bars* b = reinterpret_cast<Bars*>(sm + kQ_BAR);
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
     __syncwarp();
   } else if (warp == kWarpMma) {
     if (lane == 0) {
-      const uint32_t q = smem_u32(sm + kQ_Q), n = smem_u32(sm + kQ_N), r = smem_u32(sm + kQ_R);
+      const uint32_t q = smem_u32(sm + kQ_Q), n = smem_u32(sm + kQ_Y), r = smem_u32(sm + kQ_R);
       const uint32_t id_k = idesc_bf16_f32(128, 64, 0, 0), id_mn = idesc_bf16_f32(128, 64, 1, 1);
       const uint64_t a1 = smem_desc(q, 16, 1024), b1 = smem_desc(smem_u32(sm + kQ_ST), 16, 1024);
       const uint64_t a2 = smem_desc(n, 16, 1024), b2 = smem_desc(smem_u32(sm + kQ_SN), 16, 1024);
@@ -256,14 +258,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
           mma_commit(&b->acc1);
           if (!bwait(&b->mid, j & 1, ab, b->wait_ns)) break;
           tc_fence_after();
-          // dnum S'^T[t][c] = sum_e dnum[t][e] S'[c][e]: A = dnum (K-major), B = S' tile (K-major)
+          // dnum S'^T[t][c] = sum_e dnum[t][e] S'[c][e]: A = dnum (K-major, over dY), B = S' tile
+          // (K-major); into the columns of phi(Q) S', which the epilogue read before releasing dnum
 #pragma unroll
-          for (int k = 0; k < kD / 16; ++k) mma_bf16(tmem + 64, a2 + k * 2, b2 + k * 2, id_k, k > 0);
+          for (int k = 0; k < kD / 16; ++k) mma_bf16(tmem, a2 + k * 2, b2 + k * 2, id_k, k > 0);
           // [dS~^T ; dz~][m][c] += sum_t [dnum^T ; dden][m][t] phi(Q)[t][c]: A MN-major (the dnum
           // tile, then the dden tile r - n bytes on), B = phi(Q) (MN-major)
 #pragma unroll
           for (int k = 0; k < kT / 16; ++k)
-            mma_bf16(tmem + 128, a3 + k * (2048 >> 4), b3 + k * (2048 >> 4), id_mn, j > 0 || k > 0);
+            mma_bf16(tmem + 64, a3 + k * (2048 >> 4), b3 + k * (2048 >> 4), id_mn, j > 0 || k > 0);
           mma_commit(&b->acc2);
         }
       }
@@ -291,23 +294,21 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       const float inv = 1.f / den, dz0 = den - p.eps;
       const float* mu = z + kD;
       float s = 0.f, mdn = 0.f;
-      float nm[64];  // the row's four 16-column loads in flight together, one wait
-#pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld16(trow + 16 * g, nm + 16 * g);
-      tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float dy[16];
+        float nm[16], dy[16];
+        tmem_ld16(trow + 16 * g, nm);
         unpack8(*piece(sm + kQ_Y, t, 2 * g), dy);
         unpack8(*piece(sm + kQ_Y, t, 2 * g + 1), dy + 8);
+        tmem_ld_wait();
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          s = fmaf(dy[x], fmaf(dz0, mu[16 * g + x], nm[16 * g + x]), s);
+          s = fmaf(dy[x], fmaf(dz0, mu[16 * g + x], nm[x]), s);
           dy[x] *= inv;
           mdn = fmaf(mu[16 * g + x], dy[x], mdn);
         }
-        *piece(sm + kQ_N, t, 2 * g) = pack8(dy);
-        *piece(sm + kQ_N, t, 2 * g + 1) = pack8(dy + 8);
+        *piece(sm + kQ_Y, t, 2 * g) = pack8(dy);  // dnum over the row's dY
+        *piece(sm + kQ_Y, t, 2 * g + 1) = pack8(dy + 8);
       }
       const float dd = -s * inv * inv;
       const uint32_t ddw = pack_bf16(dd, dd);
@@ -324,17 +325,15 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       // dq = min(1, phi(q)) (dnum S'^T + (mu . dnum + dden) z~)
       const float zc = mdn + dd;
       uint4* dst = reinterpret_cast<uint4*>(p.g0 + (size_t)(row0 + j * kT + t) * kD);
-      float gq[64];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) tmem_ld16(trow + 64 + 16 * g, gq + 16 * g);
-      tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float qf[16];
+        float gq[16], qf[16];
+        tmem_ld16(trow + 16 * g, gq);
         unpack8(*piece(qt, t, 2 * g), qf);
         unpack8(*piece(qt, t, 2 * g + 1), qf + 8);
+        tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 16; ++x) qf[x] = fminf(1.f, qf[x]) * fmaf(zc, z[16 * g + x], gq[16 * g + x]);
+        for (int x = 0; x < 16; ++x) qf[x] = fminf(1.f, qf[x]) * fmaf(zc, z[16 * g + x], gq[x]);
         dst[2 * g] = pack8(qf);
         dst[2 * g + 1] = pack8(qf + 8);
       }
@@ -347,16 +346,18 @@ __global__ void __launch_bounds__(kThreads, 2) tc_bwd_query_kernel(const __grid_
       // (tcgen05.ld is warp-collective: whole warps load, then the owning lanes store)
       float* out = p.out_slots + slot * kX;
       if (qd < 3) {
-        float v[64];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) tmem_ld16(trow + 128 + 16 * g, v + 16 * g);
-        tmem_ld_wait();
-        if (qd < 2) {
+        for (int g = 0; g < 4; ++g) {
+          float v[16];
+          tmem_ld16(trow + 64 + 16 * g, v);
+          tmem_ld_wait();
+          if (qd < 2) {
 #pragma unroll
-          for (int x = 0; x < 64; ++x) out[x * kD + t] = v[x];
-        } else if (lane == 0) {
+            for (int x = 0; x < 16; ++x) out[(16 * g + x) * kD + t] = v[x];
+          } else if (lane == 0) {
 #pragma unroll
-          for (int x = 0; x < 64; ++x) out[kD * kD + x] = v[x];
+            for (int x = 0; x < 16; ++x) out[kD * kD + 16 * g + x] = v[x];
+          }
         }
       }
     }
